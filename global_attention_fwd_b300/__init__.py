@@ -1,0 +1,182 @@
+"""Python binding of libzgattn.so, the ZGCM-1 attention hot path for B300.
+
+Argument marshalling only: tensors are checked for device, dtype and
+contiguity, and their pointers and the current CUDA stream are passed to the
+C ABI declared in ``include/zg_attn.h``.  Every step of the computation runs
+in the library's CUDA kernels; there is no CPU or PyTorch fallback, and
+importing this package fails if the library cannot be loaded.
+
+Entry points (same names as the C ABI without the ``zg_`` prefix):
+``swa_prefill``, ``global_prefill``, ``hybrid_decode``,
+``hybrid_decode_workspace_bytes``, ``device_status``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libzgattn.so")
+
+STATUS = {
+    0: "ZG_OK", -1: "ZG_ERR_NULL", -2: "ZG_ERR_ALIGN", -3: "ZG_ERR_SHAPE", -4: "ZG_ERR_UNSUPPORTED",
+    -5: "ZG_ERR_POSITION", -6: "ZG_ERR_WORKSPACE", -7: "ZG_ERR_CUDA", -8: "ZG_ERR_DEVICE_TIMEOUT",
+    -9: "ZG_ERR_UNIMPLEMENTED",
+}
+EXPORTS = ("zg_swa_prefill", "zg_global_prefill", "zg_hybrid_decode_workspace_bytes", "zg_hybrid_decode",
+           "zg_device_status", "zg_selftest_bounded_wait", "zg_status_string")
+
+
+class ZgError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS.get(status, status)} ({_lib.zg_status_string(status).decode()})")
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with `python -m global_attention_fwd_b300._build`")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I, I64, D, F, SZ, U64 = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_double, ctypes.c_float,
+                                ctypes.c_size_t, ctypes.c_uint64)
+    lib.zg_swa_prefill.argtypes = [P] * 8 + [I] * 7 + [D, F, P]
+    lib.zg_swa_prefill.restype = I
+    lib.zg_global_prefill.argtypes = [P] * 7 + [I] * 6 + [D, F, P]
+    lib.zg_global_prefill.restype = I
+    lib.zg_hybrid_decode_workspace_bytes.argtypes = [I, I, I, I, I64]
+    lib.zg_hybrid_decode_workspace_bytes.restype = SZ
+    lib.zg_hybrid_decode.argtypes = [P] * 13 + [I] * 5 + [I64, I, I, D, F, P, SZ, P]
+    lib.zg_hybrid_decode.restype = I
+    lib.zg_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+    lib.zg_device_status.restype = I
+    lib.zg_selftest_bounded_wait.argtypes = [U64, P]
+    lib.zg_selftest_bounded_wait.restype = I
+    lib.zg_status_string.argtypes = [I]
+    lib.zg_status_string.restype = ctypes.c_char_p
+    return lib
+
+
+_lib = _load()
+lib = _lib  # raw ctypes handle: the C ABI itself
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(t, name, dtype, ndim=None):
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {t.dim()}")
+
+
+def _raise(st, what):
+    if st != 0:
+        raise ZgError(st, what)
+
+
+def swa_prefill(q, k, v, gate, pos, wq, wk, *, window=128, rotary_dim, theta, eps=1e-6, out=None, stream=None):
+    """Gated sliding-window GQA prefill.  q, gate [B,L,Hq,d] bf16; k, v [B,L,Hkv,d] bf16;
+    pos [B,L] int32; wq, wk [d] float32.  Returns out [B,L,Hq,d] bf16."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (gate, "gate")):
+        _check(t, n, torch.bfloat16, 4)
+    _check(pos, "pos", torch.int32, 2)
+    _check(wq, "wq", torch.float32)
+    _check(wk, "wk", torch.float32)
+    B, L, Hq, d = q.shape
+    Hkv = k.shape[2]
+    if out is None:
+        out = torch.empty_like(q)
+    _check(out, "out", torch.bfloat16, 4)
+    st = _lib.zg_swa_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(gate), _ptr(pos), _ptr(wq), _ptr(wk), _ptr(out),
+                             B, L, Hq, Hkv, d, int(window), int(rotary_dim), float(theta), float(eps), _stream(stream))
+    _raise(st, "zg_swa_prefill")
+    return out
+
+
+def global_prefill(q, k, v, pos, wq, wk, *, rotary_dim, theta, eps=1e-6, out=None, stream=None):
+    """Global (full causal, ungated) GQA prefill.  Same layouts as swa_prefill without gate."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, n, torch.bfloat16, 4)
+    _check(pos, "pos", torch.int32, 2)
+    _check(wq, "wq", torch.float32)
+    _check(wk, "wk", torch.float32)
+    B, L, Hq, d = q.shape
+    Hkv = k.shape[2]
+    if out is None:
+        out = torch.empty_like(q)
+    _check(out, "out", torch.bfloat16, 4)
+    st = _lib.zg_global_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(pos), _ptr(wq), _ptr(wk), _ptr(out),
+                                B, L, Hq, Hkv, d, int(rotary_dim), float(theta), float(eps), _stream(stream))
+    _raise(st, "zg_global_prefill")
+    return out
+
+
+def hybrid_decode_workspace_bytes(NG, B, Hq, d, S_max) -> int:
+    return int(_lib.zg_hybrid_decode_workspace_bytes(int(NG), int(B), int(Hq), int(d), int(S_max)))
+
+
+def hybrid_decode(q, k_new, v_new, gate, pos, wq, wk, is_global, k_glob, v_glob, k_ring, v_ring, *,
+                  rotary_dim, theta, eps=1e-6, out=None, workspace=None, stream=None):
+    """One decode step through the hybrid layer stack (caches updated in place).
+    q, gate [NL,B,Hq,d]; k_new, v_new [NL,B,Hkv,d]; pos [B] int32 (device); wq, wk [NL,d];
+    is_global: sequence of NL flags (host); k_glob, v_glob [NG,B,Hkv,S,d]; k_ring, v_ring [NS,B,Hkv,W,d]."""
+    for t, n in ((q, "q"), (k_new, "k_new"), (v_new, "v_new"), (gate, "gate")):
+        _check(t, n, torch.bfloat16)
+    _check(pos, "pos", torch.int32, 1)
+    _check(wq, "wq", torch.float32, 2)
+    _check(wk, "wk", torch.float32, 2)
+    NL, B, Hq, d = q.shape
+    Hkv = k_new.shape[2]
+    flags = bytes(1 if int(x) else 0 for x in (is_global.tolist() if hasattr(is_global, "tolist") else is_global))
+    NG = sum(flags)
+    S = 0
+    W = 0
+    if NG:
+        _check(k_glob, "k_glob", torch.bfloat16, 5)
+        _check(v_glob, "v_glob", torch.bfloat16, 5)
+        S = k_glob.shape[3]
+    if NL - NG:
+        _check(k_ring, "k_ring", torch.bfloat16, 5)
+        _check(v_ring, "v_ring", torch.bfloat16, 5)
+        W = k_ring.shape[3]
+    else:
+        W = 128
+    if out is None:
+        out = torch.empty_like(q)
+    need = hybrid_decode_workspace_bytes(NG, B, Hq, d, S)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    flag_buf = ctypes.create_string_buffer(flags, len(flags))
+    st = _lib.zg_hybrid_decode(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(gate), _ptr(pos), _ptr(wq), _ptr(wk),
+                               ctypes.cast(flag_buf, ctypes.c_void_p), _ptr(k_glob), _ptr(v_glob), _ptr(k_ring),
+                               _ptr(v_ring), _ptr(out), NL, B, Hq, Hkv, d, int(S), int(W), int(rotary_dim),
+                               float(theta), float(eps), _ptr(workspace), ws_bytes, _stream(stream))
+    _raise(st, "zg_hybrid_decode")
+    return out
+
+
+def device_status():
+    """(status, detail): synchronises and reads/clears the device error word."""
+    detail = ctypes.c_uint32(0)
+    st = _lib.zg_device_status(ctypes.byref(detail))
+    return st, detail.value
+
+
+def selftest_bounded_wait(limit_ns: int, stream=None):
+    _raise(_lib.zg_selftest_bounded_wait(int(limit_ns), _stream(stream)), "zg_selftest_bounded_wait")

@@ -1,0 +1,197 @@
+// api.cu -- the C ABI declared in include/zg_attn.h: argument checks, TMA
+// descriptors, RoPE constants, launches.  No device memory is allocated here.
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/zg_attn.h"
+#include "zg_kernels.cuh"
+
+namespace zg {
+
+// device error word (bounded waits record themselves here)
+__device__ uint32_t g_err_word = 0;
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    });
+    return fn;
+}
+
+unsigned long long wait_limit_ns() {
+    static unsigned long long lim = [] {
+        const char* e = std::getenv("ZG_WAIT_LIMIT_NS");
+        unsigned long long v = e ? std::strtoull(e, nullptr, 10) : 0ull;
+        return v ? v : 4000000000ull;
+    }();
+    return lim;
+}
+
+bool dev_ctl(DevCtl& ctl) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_err_word) != cudaSuccess) return false;
+    ctl.err_word = static_cast<uint32_t*>(p);
+    ctl.wait_limit_ns = wait_limit_ns();
+    return true;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// 4-D bf16 tensor map over [outer][L][heads][d] with a {64, box_heads, box_rows, 1} box, 128-byte swizzle
+bool make_map(CUtensorMap* m, const void* base, int d, int heads, int L, int B, int box_heads, int box_rows) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)L, (cuuint64_t)B};
+    cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)heads * d * 2, (cuuint64_t)L * heads * d * 2};
+    cuuint32_t box[4] = {64, (cuuint32_t)box_heads, (cuuint32_t)box_rows, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// theta^(-2j/r) in double, split into float head + float tail
+bool rope_consts(RopeConsts& rc, int rotary_dim, double theta) {
+    if (rotary_dim < 0 || (rotary_dim & 1) || rotary_dim / 2 > kMaxRotHalf) return false;
+    rc.half = rotary_dim / 2;
+    for (int j = 0; j < kMaxRotHalf; ++j) {
+        double f = j < rc.half ? std::pow(theta, -2.0 * j / rotary_dim) : 0.0;
+        float hi = static_cast<float>(f);
+        rc.f_hi[j] = hi;
+        rc.f_lo[j] = static_cast<float>(f - static_cast<double>(hi));
+    }
+    return true;
+}
+
+zg_status check_prefill(const void* q, const void* k, const void* v, const void* gate, bool gated, const void* pos,
+                        const void* wq, const void* wk, const void* out, int B, int L, int Hq, int Hkv, int d,
+                        int rotary_dim, double theta, float eps) {
+    if (!q || !k || !v || (gated && !gate) || !pos || !wq || !wk || !out) return ZG_ERR_NULL;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || (gated && !aligned16(gate)) || !aligned16(pos) ||
+        !aligned16(wq) || !aligned16(wk) || !aligned16(out))
+        return ZG_ERR_ALIGN;
+    if (B < 0 || L < 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || Hq % Hkv) return ZG_ERR_SHAPE;
+    if (rotary_dim < 0 || rotary_dim > d || (rotary_dim & 1)) return ZG_ERR_SHAPE;
+    if (!(theta > 0.0) || !(eps >= 0.0f)) return ZG_ERR_SHAPE;
+    return ZG_OK;
+}
+
+}  // namespace
+}  // namespace zg
+
+using namespace zg;
+
+extern "C" {
+
+zg_status zg_swa_prefill(const zg_bf16* q, const zg_bf16* k, const zg_bf16* v, const zg_bf16* gate,
+                         const int32_t* pos, const float* wq, const float* wk, zg_bf16* out, int B, int L, int Hq,
+                         int Hkv, int d, int window, int rotary_dim, double theta, float eps, zg_stream stream) {
+    zg_status st = check_prefill(q, k, v, gate, true, pos, wq, wk, out, B, L, Hq, Hkv, d, rotary_dim, theta, eps);
+    if (st != ZG_OK) return st;
+    if (window < 1) return ZG_ERR_SHAPE;
+    const int G = Hq / Hkv;
+    if ((d != 64 && d != 128) || (G != 1 && G != 2 && G != 4 && G != 8) || window > 128 || Hkv > 65535)
+        return ZG_ERR_UNSUPPORTED;
+    if (B == 0 || L == 0) return ZG_OK;
+    const int T = 128 / G;
+    const long long n_lt = (L + T - 1) / T;
+    if (n_lt * Hkv * B >= (1ll << 31)) return ZG_ERR_UNSUPPORTED;
+    const int NK = ((T + 127) + 31) / 32 * 32;
+
+    PrefillParams p;
+    std::memset(&p, 0, sizeof(p));
+    if (!dev_ctl(p.ctl)) return ZG_ERR_CUDA;
+    if (!make_map(&p.tm_q, q, d, Hq, L, B, G, T) || !make_map(&p.tm_gate, gate, d, Hq, L, B, G, T) ||
+        !make_map(&p.tm_out, out, d, Hq, L, B, G, T) || !make_map(&p.tm_k, k, d, Hkv, L, B, 1, NK) ||
+        !make_map(&p.tm_v, v, d, Hkv, L, B, 1, NK))
+        return ZG_ERR_CUDA;
+    p.pos = pos;
+    p.wq = wq;
+    p.wk = wk;
+    p.B = B;
+    p.L = L;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.window = window;
+    p.n_ltiles = static_cast<int>(n_lt);
+    p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
+    p.eps = eps;
+    if (!rope_consts(p.rope, rotary_dim, theta)) return ZG_ERR_SHAPE;
+    return launch_swa_prefill(p, d, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? ZG_OK : ZG_ERR_CUDA;
+}
+
+zg_status zg_global_prefill(const zg_bf16* q, const zg_bf16* k, const zg_bf16* v, const int32_t* pos,
+                            const float* wq, const float* wk, zg_bf16* out, int B, int L, int Hq, int Hkv, int d,
+                            int rotary_dim, double theta, float eps, zg_stream stream) {
+    zg_status st = check_prefill(q, k, v, nullptr, false, pos, wq, wk, out, B, L, Hq, Hkv, d, rotary_dim, theta, eps);
+    if (st != ZG_OK) return st;
+    if (d != 128 || Hq / Hkv != 4 || Hkv > 65535) return ZG_ERR_UNSUPPORTED;
+    if (B == 0 || L == 0) return ZG_OK;
+    return ZG_ERR_UNIMPLEMENTED;
+}
+
+size_t zg_hybrid_decode_workspace_bytes(int NG, int B, int Hq, int d, int64_t S_max) {
+    if (NG <= 0 || B <= 0 || Hq <= 0 || d <= 0 || S_max <= 0) return 0;
+    return 0;
+}
+
+zg_status zg_hybrid_decode(const zg_bf16* q, const zg_bf16* k_new, const zg_bf16* v_new, const zg_bf16* gate,
+                           const int32_t* pos, const float* wq, const float* wk, const uint8_t* is_global,
+                           zg_bf16* k_glob, zg_bf16* v_glob, zg_bf16* k_ring, zg_bf16* v_ring, zg_bf16* out, int NL,
+                           int B, int Hq, int Hkv, int d, int64_t S_max, int window, int rotary_dim, double theta,
+                           float eps, void* workspace, size_t workspace_bytes, zg_stream stream) {
+    (void)q; (void)k_new; (void)v_new; (void)gate; (void)pos; (void)wq; (void)wk; (void)is_global;
+    (void)k_glob; (void)v_glob; (void)k_ring; (void)v_ring; (void)out; (void)NL; (void)B; (void)Hq; (void)Hkv;
+    (void)d; (void)S_max; (void)window; (void)rotary_dim; (void)theta; (void)eps; (void)workspace;
+    (void)workspace_bytes; (void)stream;
+    return ZG_ERR_UNIMPLEMENTED;
+}
+
+zg_status zg_device_status(uint32_t* detail) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return ZG_ERR_CUDA;
+    uint32_t w = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&w, g_err_word, sizeof(w)) != cudaSuccess) return ZG_ERR_CUDA;
+    if (w && cudaMemcpyToSymbol(g_err_word, &zero, sizeof(zero)) != cudaSuccess) return ZG_ERR_CUDA;
+    if (detail) *detail = w;
+    return w ? ZG_ERR_DEVICE_TIMEOUT : ZG_OK;
+}
+
+zg_status zg_selftest_bounded_wait(uint64_t limit_ns, zg_stream stream) {
+    DevCtl ctl;
+    if (!dev_ctl(ctl)) return ZG_ERR_CUDA;
+    ctl.wait_limit_ns = limit_ns;
+    return launch_wait_selftest(ctl, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? ZG_OK : ZG_ERR_CUDA;
+}
+
+const char* zg_status_string(int s) {
+    switch (s) {
+        case ZG_OK: return "ok";
+        case ZG_ERR_NULL: return "null pointer";
+        case ZG_ERR_ALIGN: return "pointer not 16-byte aligned";
+        case ZG_ERR_SHAPE: return "invalid size or parameter";
+        case ZG_ERR_UNSUPPORTED: return "shape not supported by the kernels";
+        case ZG_ERR_POSITION: return "position outside the cache";
+        case ZG_ERR_WORKSPACE: return "workspace missing or too small";
+        case ZG_ERR_CUDA: return "CUDA runtime error";
+        case ZG_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+        case ZG_ERR_UNIMPLEMENTED: return "not implemented";
+        default: return "unknown status";
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,75 @@
+// zg_kernels.cuh -- parameter blocks and launch entry points shared by the
+// CUDA kernels and the C-ABI layer of the library.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "zg_ptx.cuh"
+
+namespace zg {
+
+constexpr int kMaxRotHalf = 64;  // rotary_dim / 2 <= head_dim / 2 <= 64
+
+// Per-call RoPE constants computed on the host in double precision:
+// inverse frequency theta^(-2j/r) split into a float head and a float tail so the
+// device can form pos * f to ~2^-40 relative before reducing it modulo 2*pi.
+struct RopeConsts {
+    int half;  // rotary_dim / 2
+    float f_hi[kMaxRotHalf];
+    float f_lo[kMaxRotHalf];
+};
+
+// ---------------------------------------------------------------- prefill
+struct PrefillParams {
+    CUtensorMap tm_q, tm_k, tm_v, tm_gate, tm_out;  // 4-D maps {d, heads, L, B}
+    const int32_t* pos;                              // [B, L]
+    const float* wq;                                 // [d]
+    const float* wk;                                 // [d]
+    int B, L, Hq, Hkv, window;
+    int n_ltiles;      // query tiles along L per (b, kv head)
+    float scale_log2;  // log2(e) / sqrt(d)
+    float eps;
+    RopeConsts rope;
+    DevCtl ctl;
+};
+
+cudaError_t launch_swa_prefill(const PrefillParams& p, int d, cudaStream_t s);
+cudaError_t launch_global_prefill(const PrefillParams& p, int d, cudaStream_t s);
+
+// ---------------------------------------------------------------- decode
+struct DecodeParams {
+    const __nv_bfloat16* q;      // [NL, B, Hq, d]
+    const __nv_bfloat16* k_new;  // [NL, B, Hkv, d]
+    const __nv_bfloat16* v_new;  // [NL, B, Hkv, d]
+    const __nv_bfloat16* gate;   // [NL, B, Hq, d]
+    const int32_t* pos;          // [B]
+    const float* wq;             // [NL, d]
+    const float* wk;             // [NL, d]
+    __nv_bfloat16* k_glob;       // [NG, B, Hkv, S, d]
+    __nv_bfloat16* v_glob;
+    __nv_bfloat16* k_ring;       // [NS, B, Hkv, W, d]
+    __nv_bfloat16* v_ring;
+    __nv_bfloat16* out;          // [NL, B, Hq, d]
+    float* ws_o;                 // [NG, B, Hq, nsplit, d] partial outputs
+    float* ws_ml;                // [NG, B, Hq, nsplit, 2] partial (max, sum)
+    int NL, NG, NS, B, Hq, Hkv, W;
+    long long S;
+    int split_len;  // keys per split of a global layer
+    int nsplit;     // splits per (global layer, b, kv head)
+    int layer_of_global[32];  // global index -> layer
+    int layer_of_local[64];   // local index -> layer
+    float scale_log2;
+    float eps;
+    RopeConsts rope;
+    DevCtl ctl;
+};
+
+constexpr int kMaxLayers = 96;
+
+cudaError_t launch_hybrid_decode(const DecodeParams& p, int d, cudaStream_t s);
+
+// bounded-wait self test: waits on a barrier nothing arrives on
+cudaError_t launch_wait_selftest(DevCtl ctl, cudaStream_t s);
+
+}  // namespace zg

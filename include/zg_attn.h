@@ -1,0 +1,151 @@
+/*
+ * zg_attn.h -- C ABI of the ZGCM-1 attention hot path for NVIDIA B300 (sm_103a).
+ *
+ * The operation (sources by page title and section):
+ *   "ZGCM-1-7B 完全解説" (gotosocial explainer), section "アーキテクチャ"
+ *   (architecture): 27 of the 32 layers are gated sliding-window GQA attention
+ *   over the most recent 128 tokens, GatedSWA(h) = o_proj(A_SWA(q,k,v) ⊙
+ *   σ(g_proj(h))); the other 5 layers (0-indexed 5, 11, 17, 23, 29) are global
+ *   causal attention without the gate; q and k get QK RMSNorm and partial RoPE
+ *   with rotary ratio 0.33; the decode KV cache keeps 128 tokens for local
+ *   layers and the whole sequence for global layers.
+ *   "ZGCM-1: A Fully Open and Extremely Efficient Foundation Model for Math and
+ *   Agentic Search" (jaehun.me review), section "게이트형 SWA의 동작": a window
+ *   of W tokens includes the query token itself; the gate is element-wise.
+ *   Same review, section "KV 캐시가 6.4배 줄어드는 이유": 20 KiB of cache per
+ *   token for the hybrid stack against 128 KiB for full attention.
+ *   hyper.ai summary of arXiv 2609.13356, section "方法": the GatedSWA equation.
+ *
+ * What every entry point computes, per query token i and query head h, with
+ * KV head g = floor(h * Hkv / Hq) and d = head_dim:
+ *   q_hat = RoPE(RMSNorm(q[i,h]; wq, eps), pos[i])      k_hat_j likewise (wk)
+ *   RMSNorm(x; w, eps) = x * (mean(x^2) + eps)^(-1/2) * w     (over d values)
+ *   RoPE: dims [0, r) rotate in pairs (j, j + r/2) by pos * theta^(-2j/r);
+ *         dims [r, d) pass through.  r = rotary_dim (even).
+ *   A = sum_j softmax_j(q_hat . k_hat_j / sqrt(d)) v[j,g]
+ *   SWA:    j in [max(0, i - window + 1), i]   -> out = A * sigmoid(gate)
+ *   global: j in [0, i]                        -> out = A
+ * Scores, softmax and accumulation run in fp32; q_hat, k_hat and the softmax
+ * weights are rounded to bf16 for the tensor cores; out is rounded to bf16.
+ *
+ * Conventions for every call:
+ *   - All tensors are device memory, row-major and contiguous, owned by the
+ *     caller.  bf16 tensors are passed as zg_bf16 (raw bf16 bits).
+ *   - Every tensor pointer must be 16-byte aligned.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream).  Arguments are checked on the host BEFORE anything is
+ *     launched; a failed check returns a negative zg_status and launches
+ *     nothing.  ZG_ERR_CUDA reports a launch failure.
+ *   - Device-side waits are bounded (ZG_WAIT_LIMIT_NS in the environment,
+ *     default 4 s).  A wait that runs out records itself in a device error
+ *     word; zg_device_status() synchronises the device and returns
+ *     ZG_ERR_DEVICE_TIMEOUT (or ZG_OK) and clears the word.
+ *   - The library allocates no device memory in these calls.
+ */
+#ifndef ZG_ATTN_H
+#define ZG_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t zg_bf16;          /* raw bfloat16 bits */
+typedef struct CUstream_st *zg_stream; /* same type as cudaStream_t */
+
+typedef enum {
+    ZG_OK = 0,
+    ZG_ERR_NULL = -1,           /* a required pointer is NULL */
+    ZG_ERR_ALIGN = -2,          /* a pointer is not 16-byte aligned */
+    ZG_ERR_SHAPE = -3,          /* a size is negative or inconsistent */
+    ZG_ERR_UNSUPPORTED = -4,    /* valid, but not a shape the kernels implement */
+    ZG_ERR_POSITION = -5,       /* decode position outside the cache */
+    ZG_ERR_WORKSPACE = -6,      /* workspace missing or too small */
+    ZG_ERR_CUDA = -7,           /* a CUDA runtime call failed */
+    ZG_ERR_DEVICE_TIMEOUT = -8, /* a device-side wait gave up */
+    ZG_ERR_UNIMPLEMENTED = -9
+} zg_status;
+
+/*
+ * Gated sliding-window GQA attention prefill (the local layers).
+ *   q, gate: [B, L, Hq, d] bf16      k, v: [B, L, Hkv, d] bf16
+ *   pos: [B, L] int32 RoPE positions (0 <= pos < 2^24)
+ *   wq, wk: [d] float32 QK-norm weights (shared by all heads)
+ *   out: [B, L, Hq, d] bf16 (written; must not overlap the inputs)
+ *   window: keys per query including itself, 1 <= window <= 128
+ * Kernel shapes: d in {64, 128}; Hq / Hkv in {1, 2, 4, 8}; Hkv <= 65535.
+ * B == 0 or L == 0 is a no-op returning ZG_OK.
+ */
+zg_status zg_swa_prefill(const zg_bf16 *q, const zg_bf16 *k, const zg_bf16 *v, const zg_bf16 *gate,
+                         const int32_t *pos, const float *wq, const float *wk, zg_bf16 *out,
+                         int B, int L, int Hq, int Hkv, int d, int window, int rotary_dim,
+                         double theta, float eps, zg_stream stream);
+
+/*
+ * Global (full causal, ungated) GQA attention prefill (the global layers).
+ * Same layouts as zg_swa_prefill without gate and window.
+ * Kernel shapes: d == 128; Hq / Hkv == 4.
+ */
+zg_status zg_global_prefill(const zg_bf16 *q, const zg_bf16 *k, const zg_bf16 *v,
+                            const int32_t *pos, const float *wq, const float *wk, zg_bf16 *out,
+                            int B, int L, int Hq, int Hkv, int d, int rotary_dim,
+                            double theta, float eps, zg_stream stream);
+
+/*
+ * Bytes of workspace zg_hybrid_decode needs for these sizes (0 when there is
+ * no global layer).  NG = number of global layers, S_max = global-cache slots.
+ */
+size_t zg_hybrid_decode_workspace_bytes(int NG, int B, int Hq, int d, int64_t S_max);
+
+/*
+ * One decode step through an NL-layer hybrid stack: every layer gets one new
+ * token per sequence.  Layers are independent here (their q/k/v/gate come in
+ * precomputed).  Per layer l and sequence b, at position p = pos[b]:
+ *   k_hat = RoPE(RMSNorm(k_new; wk[l]), p) is written into the layer's cache
+ *   (global layer: slot p of its full cache; local layer: slot p mod W of its
+ *   ring) together with v_new, and the new q attends to
+ *     global: positions 0..p          -> out = A
+ *     local:  positions max(0,p-W+1)..p (min(p+1, W) ring slots)
+ *                                      -> out = A * sigmoid(gate)
+ * Cache slots hold post-norm, post-RoPE keys and raw values.
+ *   q, gate: [NL, B, Hq, d] bf16 (gate rows of global layers are ignored)
+ *   k_new, v_new: [NL, B, Hkv, d] bf16
+ *   pos: [B] int32 device, 0 <= pos[b] < S_max (positions are not checked on
+ *        the host; a position outside the cache makes that sequence's output
+ *        zero and records nothing in the cache)
+ *   wq, wk: [NL, d] float32
+ *   is_global: [NL] uint8, HOST memory; global layers are numbered in order of
+ *        appearance into k_glob/v_glob, local layers into k_ring/v_ring
+ *   k_glob, v_glob: [NG, B, Hkv, S_max, d] bf16 (updated in place)
+ *   k_ring, v_ring: [NS, B, Hkv, W, d] bf16 (updated in place), W = window
+ *   out: [NL, B, Hq, d] bf16
+ *   workspace: device scratch of at least zg_hybrid_decode_workspace_bytes()
+ *        bytes (may be NULL when NG == 0); its contents need no initialisation.
+ * Kernel shapes: d == 128, Hq / Hkv == 4, W == 128, NL <= 96.
+ */
+zg_status zg_hybrid_decode(const zg_bf16 *q, const zg_bf16 *k_new, const zg_bf16 *v_new, const zg_bf16 *gate,
+                           const int32_t *pos, const float *wq, const float *wk, const uint8_t *is_global,
+                           zg_bf16 *k_glob, zg_bf16 *v_glob, zg_bf16 *k_ring, zg_bf16 *v_ring, zg_bf16 *out,
+                           int NL, int B, int Hq, int Hkv, int d, int64_t S_max, int window, int rotary_dim,
+                           double theta, float eps, void *workspace, size_t workspace_bytes, zg_stream stream);
+
+/* Synchronise the current device, return ZG_ERR_DEVICE_TIMEOUT if a device wait
+ * gave up since the last call (and clear that record), ZG_ERR_CUDA if the
+ * device reports an error, else ZG_OK.  *detail (may be NULL) receives the raw
+ * record: (site << 8) | code. */
+zg_status zg_device_status(uint32_t *detail);
+
+/* Launch a kernel whose only work is a bounded wait on a barrier that nothing
+ * completes, with the given limit in ns; used to test the timeout path.  The
+ * caller then reads the outcome with zg_device_status(). */
+zg_status zg_selftest_bounded_wait(uint64_t limit_ns, zg_stream stream);
+
+/* Static text for a status code. */
+const char *zg_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* ZG_ATTN_H */
