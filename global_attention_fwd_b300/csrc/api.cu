@@ -147,7 +147,8 @@ zg_status zg_global_prefill(const zg_bf16* q, const zg_bf16* k, const zg_bf16* v
 
 size_t zg_hybrid_decode_workspace_bytes(int NG, int B, int Hq, int d, int64_t S_max) {
     if (NG <= 0 || B <= 0 || Hq <= 0 || d <= 0 || S_max <= 0) return 0;
-    return 0;
+    (void)d;
+    return decode_workspace_bytes(NG, B, Hq, S_max);
 }
 
 zg_status zg_hybrid_decode(const zg_bf16* q, const zg_bf16* k_new, const zg_bf16* v_new, const zg_bf16* gate,
@@ -155,11 +156,65 @@ zg_status zg_hybrid_decode(const zg_bf16* q, const zg_bf16* k_new, const zg_bf16
                            zg_bf16* k_glob, zg_bf16* v_glob, zg_bf16* k_ring, zg_bf16* v_ring, zg_bf16* out, int NL,
                            int B, int Hq, int Hkv, int d, int64_t S_max, int window, int rotary_dim, double theta,
                            float eps, void* workspace, size_t workspace_bytes, zg_stream stream) {
-    (void)q; (void)k_new; (void)v_new; (void)gate; (void)pos; (void)wq; (void)wk; (void)is_global;
-    (void)k_glob; (void)v_glob; (void)k_ring; (void)v_ring; (void)out; (void)NL; (void)B; (void)Hq; (void)Hkv;
-    (void)d; (void)S_max; (void)window; (void)rotary_dim; (void)theta; (void)eps; (void)workspace;
-    (void)workspace_bytes; (void)stream;
-    return ZG_ERR_UNIMPLEMENTED;
+    if (!q || !k_new || !v_new || !gate || !pos || !wq || !wk || !is_global || !out) return ZG_ERR_NULL;
+    if (NL < 0 || B < 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || Hq % Hkv || window <= 0) return ZG_ERR_SHAPE;
+    if (rotary_dim < 0 || rotary_dim > d || (rotary_dim & 1) || !(theta > 0.0) || !(eps >= 0.0f)) return ZG_ERR_SHAPE;
+    if (NL > kMaxLayers) return ZG_ERR_UNSUPPORTED;
+    int NG = 0, NS = 0;
+    int glob_layers[kMaxLayers], loc_layers[kMaxLayers];
+    for (int l = 0; l < NL; ++l) {
+        if (is_global[l]) glob_layers[NG++] = l;
+        else loc_layers[NS++] = l;
+    }
+    if ((NG && (!k_glob || !v_glob)) || (NS && (!k_ring || !v_ring))) return ZG_ERR_NULL;
+    const void* ptrs[] = {q, k_new, v_new, gate, pos, wq, wk, out};
+    for (const void* x : ptrs)
+        if (!aligned16(x)) return ZG_ERR_ALIGN;
+    if ((NG && (!aligned16(k_glob) || !aligned16(v_glob))) || (NS && (!aligned16(k_ring) || !aligned16(v_ring))))
+        return ZG_ERR_ALIGN;
+    if (NG && S_max <= 0) return ZG_ERR_SHAPE;
+    if (d != 128 || Hq != 4 * Hkv || window > 4096 || S_max >= (1ll << 31)) return ZG_ERR_UNSUPPORTED;
+    if (NL == 0 || B == 0) return ZG_OK;
+    const size_t need = NG ? decode_workspace_bytes(NG, B, Hq, S_max) : 0;
+    if (need && (!workspace || workspace_bytes < need || !aligned16(workspace))) return ZG_ERR_WORKSPACE;
+    const long long nsplit = NG ? (S_max + kDecodeSplitLen - 1) / kDecodeSplitLen : 1;
+    const long long ctas = static_cast<long long>(NG) * B * Hkv * nsplit + static_cast<long long>(NS) * B * Hkv;
+    if (ctas >= (1ll << 31) || static_cast<long long>(NG) * B * Hq >= (1ll << 31)) return ZG_ERR_UNSUPPORTED;
+
+    DecodeParams p;
+    std::memset(&p, 0, sizeof(p));
+    if (!dev_ctl(p.ctl)) return ZG_ERR_CUDA;
+    p.q = reinterpret_cast<const __nv_bfloat16*>(q);
+    p.k_new = reinterpret_cast<const __nv_bfloat16*>(k_new);
+    p.v_new = reinterpret_cast<const __nv_bfloat16*>(v_new);
+    p.gate = reinterpret_cast<const __nv_bfloat16*>(gate);
+    p.pos = pos;
+    p.wq = wq;
+    p.wk = wk;
+    p.k_glob = reinterpret_cast<__nv_bfloat16*>(k_glob);
+    p.v_glob = reinterpret_cast<__nv_bfloat16*>(v_glob);
+    p.k_ring = reinterpret_cast<__nv_bfloat16*>(k_ring);
+    p.v_ring = reinterpret_cast<__nv_bfloat16*>(v_ring);
+    p.out = reinterpret_cast<__nv_bfloat16*>(out);
+    const size_t rows = static_cast<size_t>(NG) * B * Hq * static_cast<size_t>(nsplit);
+    p.ws_o = static_cast<float*>(workspace);
+    p.ws_ml = NG ? static_cast<float*>(workspace) + rows * d : nullptr;
+    p.NL = NL;
+    p.NG = NG;
+    p.NS = NS;
+    p.B = B;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.W = window;
+    p.S = NG ? S_max : (1ll << 31) - 1;  // local-only stacks: any position >= 0 is valid
+    p.split_len = kDecodeSplitLen;
+    p.nsplit = static_cast<int>(nsplit);
+    for (int i = 0; i < NG; ++i) p.layer_of_global[i] = glob_layers[i];
+    for (int i = 0; i < NS; ++i) p.layer_of_local[i] = loc_layers[i];
+    p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
+    p.eps = eps;
+    if (!rope_consts(p.rope, rotary_dim, theta)) return ZG_ERR_SHAPE;
+    return launch_hybrid_decode(p, d, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? ZG_OK : ZG_ERR_CUDA;
 }
 
 zg_status zg_device_status(uint32_t* detail) {

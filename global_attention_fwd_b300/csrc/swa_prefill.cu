@@ -15,7 +15,8 @@
 // keys are the NK = T + 127 (rounded up to 16) tokens j0 = i0-127 .. i0+T-1,
 // one K/V tile.  Four warps; thread t owns tile row t (TMEM lane t).
 //   1. TMA: Q tile and K tile (128-byte swizzle) on one barrier, V on another.
-//   2. every thread normalises + rotates its Q row and its K row(s) in smem.
+//   2. every thread normalises + rotates its Q row and its K row(s) in smem
+//      (bf16 in, fp16 out: the normalised values are bounded, see zg_qk.cuh).
 //   3. one thread issues S = Q K^T (tcgen05, M128 x N=NK, fp32 in TMEM).
 //   4. gate tile is fetched by TMA into the now-free Q buffer.
 //   5. each thread reads its S row, masks it to the window, takes the exact
@@ -148,7 +149,7 @@ __global__ void __launch_bounds__(128, 2) swa_prefill_kernel(const __grid_consta
     // ---- 3. S = Q K^T
     const uint32_t s_base = smem_u32(smem);
     if (t == 0 && *sflag) {
-        constexpr uint32_t idesc = idesc_bf16_f32(128, C::NK, false, false);
+        constexpr uint32_t idesc = idesc_f16_f32(128, C::NK, false, false);  // q_hat, k_hat in fp16
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
             const uint32_t koff = (ks & 3) * 32;

@@ -57,8 +57,8 @@ struct DecodeParams {
     long long S;
     int split_len;  // keys per split of a global layer
     int nsplit;     // splits per (global layer, b, kv head)
-    int layer_of_global[32];  // global index -> layer
-    int layer_of_local[64];   // local index -> layer
+    int layer_of_global[96];  // global-layer index -> layer
+    int layer_of_local[96];   // local-layer index -> layer
     float scale_log2;
     float eps;
     RopeConsts rope;
@@ -66,8 +66,10 @@ struct DecodeParams {
 };
 
 constexpr int kMaxLayers = 96;
+constexpr int kDecodeSplitLen = 4096;  // keys of a global cache per split
 
 cudaError_t launch_hybrid_decode(const DecodeParams& p, int d, cudaStream_t s);
+size_t decode_workspace_bytes(int NG, int B, int Hq, long long S);
 
 // bounded-wait self test: waits on a barrier nothing arrives on
 cudaError_t launch_wait_selftest(DevCtl ctl, cudaStream_t s);

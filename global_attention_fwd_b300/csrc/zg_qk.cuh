@@ -7,6 +7,8 @@
 // Readings used here: x_hat = x * (mean_d x^2 + eps)^(-1/2) * w, then dims
 // [0, r) rotate in pairs (j, j + r/2) by pos * theta^(-2j/r); dims [r, d) pass.
 #pragma once
+#include <cuda_fp16.h>
+
 #include "zg_kernels.cuh"
 
 namespace zg {
@@ -50,6 +52,9 @@ __device__ __forceinline__ uint8_t* sw_elem(uint8_t* base, uint32_t chunk_stride
 }
 
 // In-place RMSNorm + partial RoPE of one D-element row held in a swizzled smem tile.
+// Reads bf16, writes fp16: RMSNorm bounds every element of x_hat by sqrt(D) * max|w|
+// (x_i^2 <= sum x^2 = D * rms^2, and RoPE preserves the norm of each pair), so fp16
+// holds q_hat / k_hat with 3 more mantissa bits than bf16 for any |w| < 4096.
 // Only the calling thread touches this row.  w: [D] float weights (global memory).
 template <int D>
 __device__ __forceinline__ void qk_norm_rope_row(uint8_t* base, uint32_t chunk_stride, int row, const float* __restrict__ w,
@@ -71,34 +76,29 @@ __device__ __forceinline__ void qk_norm_rope_row(uint8_t* base, uint32_t chunk_s
         }
     }
     const float inv = ss > 0.f || eps > 0.f ? rsqrtf(ss * (1.0f / D) + eps) : 0.f;
-    const int r = 2 * rc.half;
-    // pass-through dims [r, D): scale now; dims [0, r) stay raw for the rotation pass
+    // pass 1: y = x * inv * w for every dim, stored as fp16
 #pragma unroll
     for (int c = 0; c < NC; ++c) {
-        if (c * 8 + 8 <= r) continue;
         uint32_t u[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+        const float4 w0 = __ldg(reinterpret_cast<const float4*>(w + c * 8));
+        const float4 w1 = __ldg(reinterpret_cast<const float4*>(w + c * 8 + 4));
+        const float ww[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int e = c * 8 + 2 * k;
-            float a = bf16lo(u[k]), b = bf16hi(u[k]);
-            if (e >= r) a = a * inv * __ldg(w + e);
-            if (e + 1 >= r) b = b * inv * __ldg(w + e + 1);
-            u[k] = pack_bf16x2(a, b);
-        }
+        for (int k = 0; k < 4; ++k)
+            u[k] = pack_half2(bf16lo(u[k]) * inv * ww[2 * k], bf16hi(u[k]) * inv * ww[2 * k + 1]);
         *reinterpret_cast<uint4*>(base + (c >> 3) * chunk_stride + sw128_off(row, c & 7)) =
             make_uint4(u[0], u[1], u[2], u[3]);
     }
-    // rotated dims: pairs (j, j + half)
+    // pass 2: rotate the pairs (j, j + half) of the normalised values
 #pragma unroll 1
     for (int j = 0; j < rc.half; ++j) {
-        uint8_t* p1 = sw_elem(base, chunk_stride, row, j);
-        uint8_t* p2 = sw_elem(base, chunk_stride, row, j + rc.half);
-        const float x1 = ld_bf16(p1) * inv * __ldg(w + j);
-        const float x2 = ld_bf16(p2) * inv * __ldg(w + j + rc.half);
+        __half* p1 = reinterpret_cast<__half*>(sw_elem(base, chunk_stride, row, j));
+        __half* p2 = reinterpret_cast<__half*>(sw_elem(base, chunk_stride, row, j + rc.half));
+        const float x1 = __half2float(*p1), x2 = __half2float(*p2);
         float cs, sn;
         rope_cos_sin(pos, rc.f_hi[j], rc.f_lo[j], cs, sn);
-        st_bf16(p1, x1 * cs - x2 * sn);
-        st_bf16(p2, x2 * cs + x1 * sn);
+        *p1 = __float2half_rn(x1 * cs - x2 * sn);
+        *p2 = __float2half_rn(x2 * cs + x1 * sn);
     }
 }
 

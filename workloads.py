@@ -198,3 +198,52 @@ def decode_caches_cpu(c: DecodeCase, salt: int = 0, batches=None) -> dict:
             t[:, bi] = _randn_bf16((n_l, Hkv, slots, d), g)
         out[name] = t
     return out
+
+
+def decode_caches_device(c: DecodeCase, device, salt: int = 0) -> dict:
+    """Device bf16 caches ~ N(0,1) drawn with a seeded CUDA generator (fast path for the
+    full-size case; the oracle receives host copies of the slices it checks, taken
+    before the decode step runs)."""
+    sh = cache_shapes(c)
+    out = {}
+    for name, stream, shape in (("k_glob", "k", sh["glob"]), ("v_glob", "v", sh["glob"]),
+                                ("k_ring", "k", sh["ring"]), ("v_ring", "v", sh["ring"])):
+        g = torch.Generator(device=device)
+        g.manual_seed(1000 * c.cfg_id + STREAM[stream] + 100000 * salt + (77 if "glob" in name else 99))
+        t = torch.empty(shape, dtype=torch.bfloat16, device=device)
+        flat = t.view(-1)
+        for s in range(0, flat.numel(), 1 << 28):
+            e = min(flat.numel(), s + (1 << 28))
+            flat[s:e] = torch.randn(e - s, generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
+        out[name] = t
+    return out
+
+
+def prefill_inputs_device(c: PrefillCase, device, salt: int = 0) -> dict:
+    """Same recipe as prefill_inputs, drawn on the device with a seeded CUDA generator (used
+    where the values are only timed, e.g. the benchmark; values differ from the CPU draw)."""
+    def draw(shape, stream, outlier_stream=None):
+        g = torch.Generator(device=device)
+        g.manual_seed(1000 * c.cfg_id + STREAM[stream] + 100000 * salt)
+        t = torch.empty(shape, dtype=torch.bfloat16, device=device)
+        flat = t.view(-1)
+        og = None
+        if outlier_stream is not None:
+            og = torch.Generator(device=device)
+            og.manual_seed(1000 * c.cfg_id + STREAM["outlier"] + 100000 * salt + outlier_stream)
+        for s in range(0, flat.numel(), 1 << 28):
+            e = min(flat.numel(), s + (1 << 28))
+            x = torch.randn(e - s, generator=g, device=device, dtype=torch.float32)
+            if og is not None:
+                m = torch.rand(e - s, generator=og, device=device) < 0.01
+                x = torch.where(m, x * 20.0, x)
+            flat[s:e] = x.to(torch.bfloat16)
+        return t
+    q = draw((c.B, c.L, c.Hq, c.d), "q", 0 if c.outliers else None)
+    k = draw((c.B, c.L, c.Hkv, c.d), "k", 7 if c.outliers else None)
+    v = draw((c.B, c.L, c.Hkv, c.d), "v")
+    gate = draw((c.B, c.L, c.Hq, c.d), "gate") if c.gated else None
+    pos = torch.arange(c.L, dtype=torch.int32, device=device).repeat(c.B, 1).contiguous()
+    return dict(q=q, k=k, v=v, gate=gate, pos=pos,
+                wq=norm_weights(c.d, c.cfg_id, "wq", salt=salt).to(device),
+                wk=norm_weights(c.d, c.cfg_id, "wk", salt=salt).to(device))
