@@ -7,8 +7,8 @@ in the library's CUDA kernels; there is no CPU or PyTorch fallback, and
 importing this package fails if the library cannot be loaded.
 
 Entry points (same names as the C ABI without the ``zg_`` prefix):
-``swa_prefill``, ``global_prefill``, ``hybrid_decode``,
-``hybrid_decode_workspace_bytes``, ``device_status``.
+``swa_prefill``, ``global_prefill``, ``global_prefill_workspace_bytes``,
+``hybrid_decode``, ``hybrid_decode_workspace_bytes``, ``device_status``.
 """
 from __future__ import annotations
 
@@ -25,7 +25,8 @@ STATUS = {
     -5: "ZG_ERR_POSITION", -6: "ZG_ERR_WORKSPACE", -7: "ZG_ERR_CUDA", -8: "ZG_ERR_DEVICE_TIMEOUT",
     -9: "ZG_ERR_UNIMPLEMENTED",
 }
-EXPORTS = ("zg_swa_prefill", "zg_global_prefill", "zg_hybrid_decode_workspace_bytes", "zg_hybrid_decode",
+EXPORTS = ("zg_swa_prefill", "zg_global_prefill_workspace_bytes", "zg_global_prefill",
+           "zg_hybrid_decode_workspace_bytes", "zg_hybrid_decode",
            "zg_device_status", "zg_selftest_bounded_wait", "zg_status_string")
 
 
@@ -43,7 +44,9 @@ def _load() -> ctypes.CDLL:
                                 ctypes.c_size_t, ctypes.c_uint64)
     lib.zg_swa_prefill.argtypes = [P] * 8 + [I] * 7 + [D, F, P]
     lib.zg_swa_prefill.restype = I
-    lib.zg_global_prefill.argtypes = [P] * 7 + [I] * 6 + [D, F, P]
+    lib.zg_global_prefill_workspace_bytes.argtypes = [I, I, I, I]
+    lib.zg_global_prefill_workspace_bytes.restype = SZ
+    lib.zg_global_prefill.argtypes = [P] * 7 + [I] * 6 + [D, F, P, SZ, P]
     lib.zg_global_prefill.restype = I
     lib.zg_hybrid_decode_workspace_bytes.argtypes = [I, I, I, I, I64]
     lib.zg_hybrid_decode_workspace_bytes.restype = SZ
@@ -108,8 +111,13 @@ def swa_prefill(q, k, v, gate, pos, wq, wk, *, window=128, rotary_dim, theta, ep
     return out
 
 
-def global_prefill(q, k, v, pos, wq, wk, *, rotary_dim, theta, eps=1e-6, out=None, stream=None):
-    """Global (full causal, ungated) GQA prefill.  Same layouts as swa_prefill without gate."""
+def global_prefill_workspace_bytes(B, L, Hkv, d) -> int:
+    return int(_lib.zg_global_prefill_workspace_bytes(int(B), int(L), int(Hkv), int(d)))
+
+
+def global_prefill(q, k, v, pos, wq, wk, *, rotary_dim, theta, eps=1e-6, out=None, workspace=None, stream=None):
+    """Global (full causal, ungated) GQA prefill.  Same layouts as swa_prefill without gate.
+    workspace: optional uint8 CUDA tensor of >= global_prefill_workspace_bytes() bytes."""
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _check(t, n, torch.bfloat16, 4)
     _check(pos, "pos", torch.int32, 2)
@@ -120,8 +128,13 @@ def global_prefill(q, k, v, pos, wq, wk, *, rotary_dim, theta, eps=1e-6, out=Non
     if out is None:
         out = torch.empty_like(q)
     _check(out, "out", torch.bfloat16, 4)
+    need = global_prefill_workspace_bytes(B, L, Hkv, d)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     st = _lib.zg_global_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(pos), _ptr(wq), _ptr(wk), _ptr(out),
-                                B, L, Hq, Hkv, d, int(rotary_dim), float(theta), float(eps), _stream(stream))
+                                B, L, Hq, Hkv, d, int(rotary_dim), float(theta), float(eps), _ptr(workspace),
+                                ws_bytes, _stream(stream))
     _raise(st, "zg_global_prefill")
     return out
 

@@ -53,14 +53,15 @@ bool dev_ctl(DevCtl& ctl) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // 4-D bf16 tensor map over [outer][L][heads][d] with a {64, box_heads, box_rows, 1} box, 128-byte swizzle
-bool make_map(CUtensorMap* m, const void* base, int d, int heads, int L, int B, int box_heads, int box_rows) {
+bool make_map(CUtensorMap* m, const void* base, int d, int heads, int L, int B, int box_heads, int box_rows,
+              CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
     cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)L, (cuuint64_t)B};
     cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)heads * d * 2, (cuuint64_t)L * heads * d * 2};
     cuuint32_t box[4] = {64, (cuuint32_t)box_heads, (cuuint32_t)box_rows, 1};
     cuuint32_t es[4] = {1, 1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+    return enc(m, dt, 4, const_cast<void*>(base), dims, strides, box, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -135,14 +136,48 @@ zg_status zg_swa_prefill(const zg_bf16* q, const zg_bf16* k, const zg_bf16* v, c
     return launch_swa_prefill(p, d, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? ZG_OK : ZG_ERR_CUDA;
 }
 
+size_t zg_global_prefill_workspace_bytes(int B, int L, int Hkv, int d) {
+    if (B <= 0 || L <= 0 || Hkv <= 0 || d <= 0) return 0;
+    return static_cast<size_t>(B) * L * Hkv * d * 2;  // fp16 normalised + rotated keys
+}
+
 zg_status zg_global_prefill(const zg_bf16* q, const zg_bf16* k, const zg_bf16* v, const int32_t* pos,
                             const float* wq, const float* wk, zg_bf16* out, int B, int L, int Hq, int Hkv, int d,
-                            int rotary_dim, double theta, float eps, zg_stream stream) {
+                            int rotary_dim, double theta, float eps, void* workspace, size_t workspace_bytes,
+                            zg_stream stream) {
     zg_status st = check_prefill(q, k, v, nullptr, false, pos, wq, wk, out, B, L, Hq, Hkv, d, rotary_dim, theta, eps);
     if (st != ZG_OK) return st;
     if (d != 128 || Hq / Hkv != 4 || Hkv > 65535) return ZG_ERR_UNSUPPORTED;
     if (B == 0 || L == 0) return ZG_OK;
-    return ZG_ERR_UNIMPLEMENTED;
+    const size_t need = zg_global_prefill_workspace_bytes(B, L, Hkv, d);
+    if (!workspace || workspace_bytes < need || !aligned16(workspace)) return ZG_ERR_WORKSPACE;
+    const int T = global_q_tile_tokens();
+    const long long n_lt = (L + T - 1) / T;
+    if (n_lt * Hkv * B >= (1ll << 31) || static_cast<long long>(B) * L * Hkv / 8 >= (1ll << 31))
+        return ZG_ERR_UNSUPPORTED;
+
+    PrefillParams p;
+    std::memset(&p, 0, sizeof(p));
+    if (!dev_ctl(p.ctl)) return ZG_ERR_CUDA;
+    if (!make_map(&p.tm_q, q, d, Hq, L, B, 4, T) || !make_map(&p.tm_out, out, d, Hq, L, B, 4, T) ||
+        !make_map(&p.tm_kh, workspace, d, Hkv, L, B, 1, 128, CU_TENSOR_MAP_DATA_TYPE_FLOAT16) ||
+        !make_map(&p.tm_v, v, d, Hkv, L, B, 1, 128))
+        return ZG_ERR_CUDA;
+    p.k_raw = reinterpret_cast<const __nv_bfloat16*>(k);
+    p.khat = static_cast<__half*>(workspace);
+    p.pos = pos;
+    p.wq = wq;
+    p.wk = wk;
+    p.B = B;
+    p.L = L;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.window = L;
+    p.n_ltiles = static_cast<int>(n_lt);
+    p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
+    p.eps = eps;
+    if (!rope_consts(p.rope, rotary_dim, theta)) return ZG_ERR_SHAPE;
+    return launch_global_prefill(p, d, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? ZG_OK : ZG_ERR_CUDA;
 }
 
 size_t zg_hybrid_decode_workspace_bytes(int NG, int B, int Hq, int d, int64_t S_max) {

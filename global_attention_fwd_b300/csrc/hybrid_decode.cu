@@ -63,36 +63,6 @@ __device__ __forceinline__ void ffma2(float2& acc, float2 a, float2 b) {
 }
 __device__ __forceinline__ float2 bf2_to_f2(uint32_t u) { return make_float2(bf16lo(u), bf16hi(u)); }
 
-// RMSNorm + partial RoPE of one head vector with one warp; x is bf16 [128] in global memory.
-// Result (fp32, times `scale`) goes to smem dst[128].
-__device__ void norm_rope_warp(const __nv_bfloat16* x, const float* w, float eps, int pos, const RopeConsts& rc,
-                               float scale, float* dst) {
-    const int lane = threadIdx.x & 31;
-    const uint2 raw = *reinterpret_cast<const uint2*>(x + lane * 4);
-    float v[4] = {bf16lo(raw.x), bf16hi(raw.x), bf16lo(raw.y), bf16hi(raw.y)};
-    float ss = v[0] * v[0] + v[1] * v[1] + v[2] * v[2] + v[3] * v[3];
-#pragma unroll
-    for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    const float inv = ss > 0.f || eps > 0.f ? rsqrtf(ss * (1.0f / D) + eps) : 0.f;
-    const float4 ww = __ldg(reinterpret_cast<const float4*>(w + lane * 4));
-    dst[lane * 4 + 0] = v[0] * inv * ww.x;
-    dst[lane * 4 + 1] = v[1] * inv * ww.y;
-    dst[lane * 4 + 2] = v[2] * inv * ww.z;
-    dst[lane * 4 + 3] = v[3] * inv * ww.w;
-    __syncwarp();
-    for (int j = lane; j < rc.half; j += 32) {
-        const float a = dst[j], b = dst[j + rc.half];
-        float cs, sn;
-        rope_cos_sin(pos, rc.f_hi[j], rc.f_lo[j], cs, sn);
-        dst[j] = a * cs - b * sn;
-        dst[j + rc.half] = b * cs + a * sn;
-    }
-    __syncwarp();
-    if (scale != 1.0f)
-        for (int e = lane; e < D; e += 32) dst[e] *= scale;
-    __syncwarp();
-}
-
 __global__ void __launch_bounds__(NTHR, 2) decode_attn_kernel(const __grid_constant__ DecodeParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + OFF_BAR);

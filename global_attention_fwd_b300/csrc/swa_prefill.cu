@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(128, 2) swa_prefill_kernel(const __grid_consta
     }
 
     // ---- 2. QK-norm + RoPE in place
-    if (ok) ok = mbar_wait(bar_qk, 0, p.ctl, 11);
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_qk, 0, p.ctl, 11));
     if (ok) {
         qk_norm_rope_row<D>(sQ, C::Q_CHUNK, t, p.wq, p.eps, pos_q, p.rope);
 #pragma unroll
@@ -161,7 +161,7 @@ __global__ void __launch_bounds__(128, 2) swa_prefill_kernel(const __grid_consta
     }
     __syncthreads();
     ok = *sflag != 0;
-    if (ok) ok = mbar_wait(bar_mma, 0, p.ctl, 12);
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_mma, 0, p.ctl, 12));
     tc_fence_after();
     __syncthreads();
     if (!ok) *sflag = 0;
@@ -257,9 +257,9 @@ __global__ void __launch_bounds__(128, 2) swa_prefill_kernel(const __grid_consta
     }
     __syncthreads();
     ok = *sflag != 0;
-    if (ok) ok = mbar_wait(bar_mma, 1, p.ctl, 14);
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_mma, 1, p.ctl, 14));
     tc_fence_after();
-    if (ok) ok = mbar_wait(bar_g, 0, p.ctl, 15);
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_g, 0, p.ctl, 15));
 
     // ---- 7. epilogue: out = O / l * sigmoid(gate), in place over the gate tile
     if (ok) {

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <cstdint>
 
+#include <cuda_fp16.h>
+
 #include "zg_ptx.cuh"
 
 namespace zg {
@@ -23,6 +25,9 @@ struct RopeConsts {
 // ---------------------------------------------------------------- prefill
 struct PrefillParams {
     CUtensorMap tm_q, tm_k, tm_v, tm_gate, tm_out;  // 4-D maps {d, heads, L, B}
+    CUtensorMap tm_kh;                               // global prefill: fp16 k_hat workspace
+    const __nv_bfloat16* k_raw;                      // global prefill: raw keys [B, L, Hkv, d]
+    __half* khat;                                    // global prefill: k_hat workspace [B, L, Hkv, d]
     const int32_t* pos;                              // [B, L]
     const float* wq;                                 // [d]
     const float* wk;                                 // [d]
@@ -36,6 +41,7 @@ struct PrefillParams {
 
 cudaError_t launch_swa_prefill(const PrefillParams& p, int d, cudaStream_t s);
 cudaError_t launch_global_prefill(const PrefillParams& p, int d, cudaStream_t s);
+int global_q_tile_tokens();
 
 // ---------------------------------------------------------------- decode
 struct DecodeParams {

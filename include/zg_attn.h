@@ -40,7 +40,8 @@
  *     default 4 s).  A wait that runs out records itself in a device error
  *     word; zg_device_status() synchronises the device and returns
  *     ZG_ERR_DEVICE_TIMEOUT (or ZG_OK) and clears the word.
- *   - The library allocates no device memory in these calls.
+ *   - The library allocates no device memory in these calls; scratch memory
+ *     comes from a caller-provided workspace (global prefill, decode).
  */
 #ifndef ZG_ATTN_H
 #define ZG_ATTN_H
@@ -83,15 +84,22 @@ zg_status zg_swa_prefill(const zg_bf16 *q, const zg_bf16 *k, const zg_bf16 *v, c
                          int B, int L, int Hq, int Hkv, int d, int window, int rotary_dim,
                          double theta, float eps, zg_stream stream);
 
+/* Bytes of workspace zg_global_prefill needs: B * L * Hkv * d * 2 (0 for empty input). */
+size_t zg_global_prefill_workspace_bytes(int B, int L, int Hkv, int d);
+
 /*
  * Global (full causal, ungated) GQA attention prefill (the global layers).
  * Same layouts as zg_swa_prefill without gate and window.
+ *   workspace: device scratch of at least zg_global_prefill_workspace_bytes()
+ *        bytes, 16-byte aligned; it receives the normalised, rotated keys (fp16)
+ *        and needs no initialisation.  ZG_ERR_WORKSPACE if missing or too small.
  * Kernel shapes: d == 128; Hq / Hkv == 4.
  */
 zg_status zg_global_prefill(const zg_bf16 *q, const zg_bf16 *k, const zg_bf16 *v,
                             const int32_t *pos, const float *wq, const float *wk, zg_bf16 *out,
                             int B, int L, int Hq, int Hkv, int d, int rotary_dim,
-                            double theta, float eps, zg_stream stream);
+                            double theta, float eps, void *workspace, size_t workspace_bytes,
+                            zg_stream stream);
 
 /*
  * Bytes of workspace zg_hybrid_decode needs for these sizes (0 when there is

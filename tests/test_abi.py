@@ -71,7 +71,8 @@ def _glob(zg, **kw):
     a = dict(q=A, k=A, v=A, pos=A, wq=A, wk=A, out=A, B=1, L=16, Hq=32, Hkv=8, d=128, rot=42, theta=1e6, eps=1e-6)
     a.update(kw)
     return zg.lib.zg_global_prefill(a["q"], a["k"], a["v"], a["pos"], a["wq"], a["wk"], a["out"], a["B"], a["L"],
-                                    a["Hq"], a["Hkv"], a["d"], a["rot"], a["theta"], a["eps"], None)
+                                    a["Hq"], a["Hkv"], a["d"], a["rot"], a["theta"], a["eps"], a.get("ws", A),
+                                    a.get("ws_bytes", 1 << 40), None)
 
 
 def test_global_rejects_bad_arguments_before_launch(zg):
@@ -81,6 +82,10 @@ def test_global_rejects_bad_arguments_before_launch(zg):
     assert _glob(zg, d=64, rot=20) == -4
     assert _glob(zg, Hq=16) == -4
     assert _glob(zg, L=0) == 0
+    assert _glob(zg, ws=None) == -6
+    assert _glob(zg, ws_bytes=16 * 8 * 128 * 2 - 1) == -6
+    assert _glob(zg, ws=A + 8) == -6
+    assert zg.global_prefill_workspace_bytes(1, 16, 8, 128) == 16 * 8 * 128 * 2
 
 
 def test_status_strings(zg):

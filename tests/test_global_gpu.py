@@ -1,0 +1,61 @@
+"""Global (full causal, ungated) prefill: CUDA path (through the C ABI) against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from parity import assert_close, rows_of
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def zg():
+    import global_attention_fwd_b300 as zg
+    return zg
+
+
+def _synthetic(B, L, Hq, Hkv, d, seed):
+    g = torch.Generator().manual_seed(seed)
+    return dict(q=torch.randn(B, L, Hq, d, generator=g).bfloat16(), k=torch.randn(B, L, Hkv, d, generator=g).bfloat16(),
+                v=torch.randn(B, L, Hkv, d, generator=g).bfloat16(),
+                pos=torch.arange(L, dtype=torch.int32).repeat(B, 1).contiguous(),
+                wq=0.5 + torch.rand(d, generator=g), wk=0.5 + torch.rand(d, generator=g))
+
+
+def _check(zg, inp, rows, rotary_dim, theta, what, eps=1e-6):
+    d = {k: v.cuda() for k, v in inp.items() if v is not None}
+    out = zg.global_prefill(d["q"], d["k"], d["v"], d["pos"], d["wq"], d["wk"], rotary_dim=rotary_dim, theta=theta,
+                            eps=eps)
+    torch.cuda.synchronize()
+    st, detail = zg.device_status()
+    assert st == 0, (st, detail)
+    ref = oracle.prefill_rows(inp["q"], inp["k"], inp["v"], None, inp["pos"], inp["wq"], inp["wk"], window=0,
+                              rotary_dim=rotary_dim, theta=theta, eps=eps, rows=rows)
+    return assert_close(rows_of(out, rows), ref, what), out
+
+
+@pytest.mark.parametrize("B,L", [(1, 1), (1, 31), (2, 33), (1, 128), (1, 129), (2, 300), (1, 1000)])
+def test_small_lengths_all_rows(zg, B, L):
+    inp = _synthetic(B, L, 32, 8, 128, seed=L + B)
+    _check(zg, inp, list(range(B * L)), 42, 1e6, f"global B{B} L{L}")
+
+
+def test_medium_length_sampled(zg):
+    inp = _synthetic(1, 8192, 8, 2, 128, seed=11)
+    rows = sorted(set(range(0, 8192, 37)) | set(workloads.edge_rows(8192)))
+    _check(zg, inp, rows, 42, 1e6, "global L8192")
+
+
+def test_deterministic(zg):
+    inp = {k: v.cuda() for k, v in _synthetic(1, 2000, 32, 8, 128, seed=12).items()}
+    a = zg.global_prefill(inp["q"], inp["k"], inp["v"], inp["pos"], inp["wq"], inp["wk"], rotary_dim=42, theta=1e6)
+    b = zg.global_prefill(inp["q"], inp["k"], inp["v"], inp["pos"], inp["wq"], inp["wk"], rotary_dim=42, theta=1e6)
+    assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("c", [workloads.GLOBAL_64K, workloads.GLOBAL_256K], ids=lambda c: c.name)
+def test_global_config_sampled_rows(zg, c):
+    inp = workloads.prefill_inputs(c)
+    _check(zg, inp, workloads.sample_rows(c), c.rotary_dim, c.theta, c.name)
