@@ -1,0 +1,448 @@
+#!/usr/bin/env python3
+"""Benchmark of the ZGCM-1 attention hot path on B300 (one JSON line on stdout).
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+  1. gated sliding-window prefill, B=1, L=262144, 32/8 heads, d=128, window 128
+     (the headline: tokens/s),
+  2. one hybrid decode step, B=8 sequences at position 262143 through the
+     32-layer stack (5 global layers with 256K caches, 27 local 128-slot rings),
+  3. global (full causal) prefill, B=1, L=65536, 32/8 heads, d=128.
+Inputs are drawn once on the device with seeded generators and stay resident in
+HBM; every input is larger than the 126 MB L2, so no flush is needed between
+steps.  `value` is the gated-SWA prefill throughput (tokens/s summed over all
+ranks, from CUDA events around that call); `parts` reports every call with its
+own roofline.  `e2e` repeats the SWA prefill through the same public API with
+the inputs in pinned host memory, the host->device copies and the device->host
+copy of the output inside the timed region.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+Under torchrun (N > 1) every rank runs the same per-GPU work (replicas, no
+collective on the data path); timing is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "gated-SWA prefill tokens/s @256K; hybrid decode µs/step; % of roofline"
+PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_PATH = os.path.join(ROOT, "profiles", "traffic.json")
+FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+CSRC = os.path.join(ROOT, "global_attention_fwd_b300", "csrc")
+
+
+def _peaks():
+    try:
+        with open(PEAKS_PATH) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in FALLBACK}, "measured"
+    except Exception:
+        return dict(FALLBACK), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(CSRC)):
+        with open(os.path.join(CSRC, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic(kernel: str):
+    """Per-launch DRAM bytes from the committed ncu summary, or None when the kernels changed since."""
+    try:
+        with open(TRAFFIC_PATH) as f:
+            t = json.load(f)
+        if t.get("kernel_source_hash") != kernel_source_hash():
+            return None
+        return t["per_launch_bytes"].get(kernel)
+    except Exception:
+        return None
+
+
+# ------------------------------------------------------------------ workloads
+SWA = workloads.SWA_256K
+DEC = workloads.HYBRID_DECODE
+GLB = workloads.GLOBAL_64K
+
+
+def swa_bytes(c):  # algorithmic HBM bytes: read q, gate, k, v once, write out once
+    return c.B * c.L * (3 * c.Hq * c.d * 2 + 2 * c.Hkv * c.d * 2)
+
+
+def global_flops(c):  # 2 matmuls x 2 flop x d per unmasked (row, key, head)
+    return 4.0 * c.d * c.Hq * c.B * (c.L * (c.L + 1) / 2)
+
+
+def decode_bytes(c):  # caches read once (global 0..p, rings all slots), new-token rows, outputs
+    ng = len(c.global_layers)
+    ns = c.NL - ng
+    cache = 2 * ng * c.B * c.Hkv * (c.pos + 1) * c.d * 2 + 2 * ns * c.B * c.Hkv * c.W * c.d * 2
+    tok = c.NL * c.B * (3 * c.Hq + 2 * c.Hkv) * c.d * 2
+    return cache + tok
+
+
+class Clocks:
+    """Samples SM clocks and throttle reasons with nvidia-smi while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"zg_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx = float(parts[2])
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ---------------------------------------------------------------- oracle arm
+def oracle_sample(rows: int, nthreads=None, seed_salt=0):
+    """Time the fp64 oracle on `rows` consecutive gated-SWA rows (all heads) from the middle of
+    the 256K workload (a slice with the 127-token history each row needs)."""
+    import oracle
+
+    c = SWA
+    start = c.L // 2
+    lo = start - (c.window - 1)
+    sl = workloads.PrefillCase("swa_slice", c.cfg_id, 1, rows + c.window - 1, c.Hq, c.Hkv, c.d, c.window,
+                               c.rotary_dim, c.theta, True, outliers=True)
+    inp = workloads.prefill_inputs(sl, salt=seed_salt)
+    inp["pos"] = inp["pos"] + lo
+    rr = list(range(c.window - 1, c.window - 1 + rows))
+    n = nthreads or oracle.default_threads()
+    t0 = time.perf_counter()
+    oracle.prefill_rows(inp["q"], inp["k"], inp["v"], inp["gate"], inp["pos"], inp["wq"], inp["wk"],
+                        window=c.window, rotary_dim=c.rotary_dim, theta=c.theta, eps=c.eps, rows=rr, nthreads=n)
+    dt = time.perf_counter() - t0
+    return rows / dt, n, dt
+
+
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    rows = args.ref_rows
+    for _ in range(args.warmup):
+        oracle_sample(rows)
+    rates, dts = [], []
+    n = None
+    for _ in range(args.steps):
+        r, n, dt = oracle_sample(rows)
+        rates.append(r)
+        dts.append(dt)
+    value = statistics.median(rates)
+    sample = (f"{rows} consecutive query rows x all 32 heads of the gated-SWA 256K workload per step "
+              f"(rows 131072.., fp64 C oracle); tokens/s = rows/s")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * statistics.median(dts), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": SWA.name, "global_batch": SWA.B, "seq_len": SWA.L, "parallelism": "none (host)"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": n, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_gpu(args):
+    ws, rank, local = _dist()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    import global_attention_fwd_b300 as zg
+
+    peaks, peak_kind = _peaks()
+    # ---- inputs, resident in HBM
+    sx = workloads.prefill_inputs_device(SWA, dev)
+    s_out = torch.empty_like(sx["q"])
+    gx = workloads.prefill_inputs_device(GLB, dev)
+    g_out = torch.empty_like(gx["q"])
+    g_ws = torch.empty(zg.global_prefill_workspace_bytes(GLB.B, GLB.L, GLB.Hkv, GLB.d), dtype=torch.uint8, device=dev)
+    tok = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in workloads.decode_token_inputs(DEC).items()}
+    caches = workloads.decode_caches_device(DEC, dev)
+    d_ws = torch.empty(zg.hybrid_decode_workspace_bytes(len(DEC.global_layers), DEC.B, DEC.Hq, DEC.d, DEC.S),
+                       dtype=torch.uint8, device=dev)
+    d_out = torch.empty_like(tok["q"])
+    flags = DEC.layer_flags()
+
+    def swa():
+        zg.swa_prefill(sx["q"], sx["k"], sx["v"], sx["gate"], sx["pos"], sx["wq"], sx["wk"], window=SWA.window,
+                       rotary_dim=SWA.rotary_dim, theta=SWA.theta, eps=SWA.eps, out=s_out)
+
+    def dec():
+        zg.hybrid_decode(tok["q"], tok["k_new"], tok["v_new"], tok["gate"], tok["pos"], tok["wq"], tok["wk"], flags,
+                         caches["k_glob"], caches["v_glob"], caches["k_ring"], caches["v_ring"],
+                         rotary_dim=DEC.rotary_dim, theta=DEC.theta, eps=DEC.eps, out=d_out, workspace=d_ws)
+
+    def glob():
+        zg.global_prefill(gx["q"], gx["k"], gx["v"], gx["pos"], gx["wq"], gx["wk"], rotary_dim=GLB.rotary_dim,
+                          theta=GLB.theta, eps=GLB.eps, out=g_out, workspace=g_ws)
+
+    parts = [("swa_prefill", swa, 1), ("hybrid_decode", dec, 2), ("global_prefill", glob, 2)]
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        for _, fn, _ in parts:
+            fn()
+    torch.cuda.synchronize()
+    st, detail = zg.device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} detail {detail:#x} after warm-up")
+
+    ev = {name: [] for name, _, _ in parts}
+
+    def barrier():
+        if ws > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    smi_index = vis.split(",")[local] if vis else str(local)
+    with Clocks(smi_index) as clk:
+        barrier()
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for _ in range(args.steps):
+            for name, fn, _ in parts:
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                fn()
+                b.record(stream)
+                ev[name].append((a, b))
+        t_end.record(stream)
+        barrier()
+    clocks = clk.summary()
+    st, detail = zg.device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} detail {detail:#x} after the timed region")
+    total_ms = t_start.elapsed_time(t_end)
+    part_ms = {name: [a.elapsed_time(b) for a, b in ev[name]] for name in ev}
+    swa_ms = sum(part_ms["swa_prefill"])
+    # max over ranks
+    vals = torch.tensor([total_ms, swa_ms], dtype=torch.float64, device=dev)
+    if ws > 1:
+        torch.distributed.all_reduce(vals, op=torch.distributed.ReduceOp.MAX)
+    total_ms, swa_ms = vals.tolist()
+    value = ws * SWA.tokens * args.steps / (swa_ms * 1e-3)
+
+    # ---- rooflines per part (average launch durations on this stream)
+    def avg(name):
+        return statistics.mean(part_ms[name]) * 1e-3
+
+    sw_t, dc_t, gl_t = avg("swa_prefill"), avg("hybrid_decode"), avg("global_prefill")
+    hbm = peaks["hbm_gbs"]
+    rl_swa = {"bound": "hbm", "achieved": swa_bytes(SWA) / sw_t / 1e9, "peak": hbm, "unit": "GB/s",
+              "frac": swa_bytes(SWA) / sw_t / 1e9 / hbm, "traffic": _traffic("swa_prefill_kernel"),
+              "algorithmic_bytes": swa_bytes(SWA)}
+    rl_dec = {"bound": "hbm", "achieved": decode_bytes(DEC) / dc_t / 1e9, "peak": hbm, "unit": "GB/s",
+              "frac": decode_bytes(DEC) / dc_t / 1e9 / hbm, "traffic": _traffic("decode_attn_kernel"),
+              "algorithmic_bytes": decode_bytes(DEC)}
+    gf = global_flops(GLB)
+    rl_glb = {"bound": "tensor", "achieved": gf / gl_t / 1e12, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+              "frac": gf / gl_t / 1e12 / peaks["bf16_tflops"],
+              "frac_of_sustained": gf / gl_t / 1e12 / peaks["bf16_tflops_sustained"],
+              "traffic": _traffic("global_attn_kernel"), "algorithmic_flops": gf}
+    shares = {"swa_prefill": sw_t, "hybrid_decode": dc_t, "global_prefill": gl_t}
+    dominant = max(shares, key=shares.get)
+    top = {"swa_prefill": rl_swa, "hybrid_decode": rl_dec, "global_prefill": rl_glb}[dominant]
+    roofline = dict(top, kernel=dominant, peak_source=f"{peak_kind} (MEASURED_PEAKS.json)" if peak_kind == "measured"
+                    else "fallback")
+
+    # ---- e2e: SWA prefill through the public API with pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        host = {k: v.cpu().pin_memory() for k, v in sx.items()}
+        host_out = torch.empty(s_out.shape, dtype=s_out.dtype).pin_memory()
+        h2d = sum(v.numel() * v.element_size() for v in host.values())
+        d2h = host_out.numel() * host_out.element_size()
+        e_steps = max(1, min(args.steps, 3))
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e_steps):
+            for k in ("q", "k", "v", "gate", "pos", "wq", "wk"):
+                sx[k].copy_(host[k], non_blocking=True)
+            swa()
+            host_out.copy_(s_out, non_blocking=True)
+        e1.record(stream)
+        barrier()
+        e_ms = e0.elapsed_time(e1)
+        ev_ = torch.tensor([e_ms], dtype=torch.float64, device=dev)
+        if ws > 1:
+            torch.distributed.all_reduce(ev_, op=torch.distributed.ReduceOp.MAX)
+        e2e = {"value": ws * SWA.tokens * e_steps / (ev_.item() * 1e-3), "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e_steps}
+
+    # ---- CPU baseline: the oracle on a bounded sample (rank 0, N=1 only)
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu:
+        r, n, dt = oracle_sample(args.cpu_rows)
+        cpu = {"value": r, "unit": "tokens/s", "cores": n, "kind": "oracle",
+               "sample": f"{args.cpu_rows} consecutive query rows x 32 heads of the gated-SWA 256K workload "
+                         f"(rows 131072.., fp64 C oracle, {dt:.1f} s); tokens/s = rows/s"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{SWA.name} + {DEC.name} + {GLB.name}", "global_batch": SWA.B * ws,
+                   "seq_len": SWA.L, "parallelism": "replicas" if ws > 1 else "single GPU",
+                   "l2": "no flush: every input is larger than L2"},
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps * sum(n for _, _, n in parts),
+        "clocks": clocks,
+        "parts": {
+            "swa_prefill": {"workload": SWA.name, "ms": sw_t * 1e3, "tokens_per_s": SWA.tokens / sw_t,
+                            "roofline": rl_swa},
+            "hybrid_decode": {"workload": DEC.name, "us_per_step": dc_t * 1e6, "roofline": rl_dec},
+            "global_prefill": {"workload": GLB.name, "ms": gl_t * 1e3, "tokens_per_s": GLB.tokens / gl_t,
+                               "roofline": rl_glb},
+        },
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def run_profile_case(args):
+    """A small case of one kernel for ncu captures (warm-up launch + `--steps` launches)."""
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    import global_attention_fwd_b300 as zg
+
+    kind = args.profile_case
+    if kind == "swa":
+        c = workloads.PrefillCase("swa_B1_L65536_profile", 3, 1, 65536, 32, 8, 128, 128, 42, 1e6, True, outliers=True)
+        x = workloads.prefill_inputs_device(c, dev)
+        out = torch.empty_like(x["q"])
+
+        def fn():
+            zg.swa_prefill(x["q"], x["k"], x["v"], x["gate"], x["pos"], x["wq"], x["wk"], window=128,
+                           rotary_dim=c.rotary_dim, theta=c.theta, out=out)
+    elif kind == "global":
+        c = workloads.PrefillCase("global_B1_L16384_profile", 4, 1, 16384, 32, 8, 128, 0, 42, 1e6, False)
+        x = workloads.prefill_inputs_device(c, dev)
+        out = torch.empty_like(x["q"])
+        ws = torch.empty(zg.global_prefill_workspace_bytes(1, c.L, 8, 128), dtype=torch.uint8, device=dev)
+
+        def fn():
+            zg.global_prefill(x["q"], x["k"], x["v"], x["pos"], x["wq"], x["wk"], rotary_dim=c.rotary_dim,
+                              theta=c.theta, out=out, workspace=ws)
+    else:
+        c = workloads.DecodeCase("hybrid_decode_B1_p131071_profile", 5, 1, 32, (5, 11, 17, 23, 29), 32, 8, 128,
+                                 131072, 128, 131071, 42, 1e6)
+        tok = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in workloads.decode_token_inputs(c).items()}
+        caches = workloads.decode_caches_device(c, dev)
+        ws = torch.empty(zg.hybrid_decode_workspace_bytes(5, 1, 32, 128, c.S), dtype=torch.uint8, device=dev)
+        flags = c.layer_flags()
+
+        def fn():
+            zg.hybrid_decode(tok["q"], tok["k_new"], tok["v_new"], tok["gate"], tok["pos"], tok["wq"], tok["wk"], flags,
+                             caches["k_glob"], caches["v_glob"], caches["k_ring"], caches["v_ring"],
+                             rotary_dim=c.rotary_dim, theta=c.theta, workspace=ws)
+    for _ in range(1 + args.steps):
+        fn()
+    torch.cuda.synchronize()
+    st, detail = zg.device_status()
+    print(json.dumps({"profile_case": c.name, "status": st, "detail": detail}))
+    return 0 if st == 0 else 1
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--cpu-rows", type=int, default=16384)
+    ap.add_argument("--ref-rows", type=int, default=4096)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--profile-case", choices=["swa", "global", "decode"], default=None,
+                    help="run only a small case of one kernel (for ncu captures)")
+    args = ap.parse_args()
+    if args.profile_case:
+        return run_profile_case(args)
+    if args.warmup < 3:
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
