@@ -26,7 +26,7 @@ STATUS = {
     -9: "ZG_ERR_UNIMPLEMENTED",
 }
 EXPORTS = ("zg_swa_prefill", "zg_global_prefill_workspace_bytes", "zg_global_prefill",
-           "zg_hybrid_decode_workspace_bytes", "zg_hybrid_decode",
+           "zg_hybrid_decode_workspace_bytes", "zg_hybrid_decode", "zg_hybrid_decode_noalloc",
            "zg_device_status", "zg_selftest_bounded_wait", "zg_status_string")
 
 

@@ -139,6 +139,37 @@ zg_status zg_hybrid_decode(const zg_bf16 *q, const zg_bf16 *k_new, const zg_bf16
                            int NL, int B, int Hq, int Hkv, int d, int64_t S_max, int window, int rotary_dim,
                            double theta, float eps, void *workspace, size_t workspace_bytes, zg_stream stream);
 
+/*
+ * zg_hybrid_decode_noalloc -- the same decode step as zg_hybrid_decode, for
+ * callers that cannot allocate device memory (no counterpart in the paper: it
+ * exists for how the library is called, not for what it computes).
+ *
+ * Some callers cannot call cudaMalloc: a plugin inside a host application whose
+ * memory manager owns every device allocation and lends none to plugins, or a
+ * serving loop that must not allocate while answering requests.  They still own
+ * and pass every input and output; only the split-K scratch moves into a fixed
+ * array of ZG_NOALLOC_SCRATCH_BYTES compiled into the library, which each GPU
+ * that loads the library holds until the process exits.  This call allocates
+ * nothing.
+ *   - Arguments, layouts and results are those of zg_hybrid_decode.
+ *   - Sizes whose scratch need (zg_hybrid_decode_workspace_bytes) exceeds
+ *     ZG_NOALLOC_SCRATCH_BYTES are rejected with ZG_ERR_WORKSPACE before any
+ *     launch.  64 MiB covers, e.g., 5 global layers x 8 sequences x 32 query
+ *     heads with 256K-slot caches (42.6 MB).
+ *   - The first call on a device looks up the array's device address on that
+ *     device (the device must be current); make that first call before any
+ *     stream capture begins.
+ *   - All calls share the one array, which keeps the last call's contents; no
+ *     clearing is needed between calls, but calls whose kernels overlap on the
+ *     GPU (unordered streams) race on it.
+ */
+#define ZG_NOALLOC_SCRATCH_BYTES (64u << 20)
+zg_status zg_hybrid_decode_noalloc(const zg_bf16 *q, const zg_bf16 *k_new, const zg_bf16 *v_new, const zg_bf16 *gate,
+                                   const int32_t *pos, const float *wq, const float *wk, const uint8_t *is_global,
+                                   zg_bf16 *k_glob, zg_bf16 *v_glob, zg_bf16 *k_ring, zg_bf16 *v_ring, zg_bf16 *out,
+                                   int NL, int B, int Hq, int Hkv, int d, int64_t S_max, int window, int rotary_dim,
+                                   double theta, float eps, zg_stream stream);
+
 /* Synchronise the current device, return ZG_ERR_DEVICE_TIMEOUT if a device wait
  * gave up since the last call (and clear that record), ZG_ERR_CUDA if the
  * device reports an error, else ZG_OK.  *detail (may be NULL) receives the raw
