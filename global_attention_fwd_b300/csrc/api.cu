@@ -112,7 +112,7 @@ zg_status zg_swa_prefill(const zg_bf16* q, const zg_bf16* k, const zg_bf16* v, c
     const int T = 128 / G;
     const long long n_lt = (L + T - 1) / T;
     if (n_lt * Hkv * B >= (1ll << 31)) return ZG_ERR_UNSUPPORTED;
-    const int NK = ((T + 127) + 31) / 32 * 32;
+    const int NK = swa_kv_box_rows(G);
 
     PrefillParams p;
     std::memset(&p, 0, sizeof(p));

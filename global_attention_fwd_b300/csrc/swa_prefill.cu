@@ -314,10 +314,15 @@ cudaError_t launch_swa_t(const PrefillParams& p, cudaStream_t s) {
 
 }  // namespace
 
-int swa_tokens_per_tile(int Hq, int Hkv) { return 128 / (Hq / Hkv); }
+int swa_kv_box_rows(int G) {
+    const int T = 128 / G;
+    if (swa2_supports(128, G)) return T;  // persistent kernel: one key slot of T tokens per copy
+    return ((T + 127) + 31) / 32 * 32;    // one-tile kernel: the tile's whole key window
+}
 
 cudaError_t launch_swa_prefill(const PrefillParams& p, int d, cudaStream_t s) {
     const int G = p.Hq / p.Hkv;
+    if (swa2_supports(d, G)) return launch_swa2_prefill(p, d, s);
     if (d == 128 && G == 4) return launch_swa_t<128, 4>(p, s);
     if (d == 64 && G == 4) return launch_swa_t<64, 4>(p, s);
     if (d == 128 && G == 8) return launch_swa_t<128, 8>(p, s);

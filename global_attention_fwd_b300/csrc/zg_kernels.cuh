@@ -40,6 +40,9 @@ struct PrefillParams {
 };
 
 cudaError_t launch_swa_prefill(const PrefillParams& p, int d, cudaStream_t s);
+int swa_kv_box_rows(int G);  // rows of the K/V TMA box the SWA kernel for GQA ratio G expects
+bool swa2_supports(int d, int G);
+cudaError_t launch_swa2_prefill(const PrefillParams& p, int d, cudaStream_t s);
 cudaError_t launch_global_prefill(const PrefillParams& p, int d, cudaStream_t s);
 int global_q_tile_tokens();
 

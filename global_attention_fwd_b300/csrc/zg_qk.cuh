@@ -60,14 +60,12 @@ template <int D>
 __device__ __forceinline__ void qk_norm_rope_row(uint8_t* base, uint32_t chunk_stride, int row, const float* __restrict__ w,
                                                  float eps, int pos, const RopeConsts& rc) {
     constexpr int NC = D / 8;  // 16-byte chunks per row
-    uint4 v[NC];
-#pragma unroll
-    for (int c = 0; c < NC; ++c)
-        v[c] = *reinterpret_cast<const uint4*>(base + (c >> 3) * chunk_stride + sw128_off(row, c & 7));
+    // pass 0: sum of squares, streaming the row chunk by chunk (keeps register use low)
     float ss = 0.f;
-#pragma unroll
+#pragma unroll 4
     for (int c = 0; c < NC; ++c) {
-        const uint32_t u[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+        const uint4 v = *reinterpret_cast<const uint4*>(base + (c >> 3) * chunk_stride + sw128_off(row, c & 7));
+        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const float a = bf16lo(u[k]), b = bf16hi(u[k]);
@@ -77,17 +75,18 @@ __device__ __forceinline__ void qk_norm_rope_row(uint8_t* base, uint32_t chunk_s
     }
     const float inv = ss > 0.f || eps > 0.f ? rsqrtf(ss * (1.0f / D) + eps) : 0.f;
     // pass 1: y = x * inv * w for every dim, stored as fp16
-#pragma unroll
+#pragma unroll 4
     for (int c = 0; c < NC; ++c) {
-        uint32_t u[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+        uint8_t* cp = base + (c >> 3) * chunk_stride + sw128_off(row, c & 7);
+        const uint4 v = *reinterpret_cast<const uint4*>(cp);
+        uint32_t u[4] = {v.x, v.y, v.z, v.w};
         const float4 w0 = __ldg(reinterpret_cast<const float4*>(w + c * 8));
         const float4 w1 = __ldg(reinterpret_cast<const float4*>(w + c * 8 + 4));
         const float ww[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
         for (int k = 0; k < 4; ++k)
             u[k] = pack_half2(bf16lo(u[k]) * inv * ww[2 * k], bf16hi(u[k]) * inv * ww[2 * k + 1]);
-        *reinterpret_cast<uint4*>(base + (c >> 3) * chunk_stride + sw128_off(row, c & 7)) =
-            make_uint4(u[0], u[1], u[2], u[3]);
+        *reinterpret_cast<uint4*>(cp) = make_uint4(u[0], u[1], u[2], u[3]);
     }
     // pass 2: rotate the pairs (j, j + half) of the normalised values
 #pragma unroll 1
@@ -99,6 +98,223 @@ __device__ __forceinline__ void qk_norm_rope_row(uint8_t* base, uint32_t chunk_s
         rope_cos_sin(pos, rc.f_hi[j], rc.f_lo[j], cs, sn);
         *p1 = __float2half_rn(x1 * cs - x2 * sn);
         *p2 = __float2half_rn(x2 * cs + x1 * sn);
+    }
+}
+
+// Faster in-place RMSNorm + partial RoPE of one row of a swizzled smem tile, for warps
+// whose 32 lanes hold 32 consecutive rows.  w_s: the D weights in shared memory.
+// SHARE > 1: groups of SHARE consecutive lanes hold rows of the same token (the GQA
+// heads of one query), so each lane evaluates cos/sin for every SHARE-th frequency
+// and the group exchanges them with shuffles.  Every lane of the warp must call this.
+template <int D, int SHARE>
+__device__ __forceinline__ void qk_norm_rope_row_fast(uint8_t* base, uint32_t chunk_stride, int row, const float* w_s,
+                                                      float eps, int pos, const RopeConsts& rc) {
+    constexpr int NC = D / 8;
+    float2 ss2 = make_float2(0.f, 0.f);
+#pragma unroll 4
+    for (int c = 0; c < NC; ++c) {
+        const uint4 v = *reinterpret_cast<const uint4*>(base + (c >> 3) * chunk_stride + sw128_off(row, c & 7));
+        const float2 a = bf2f2(v.x), b = bf2f2(v.y), cc = bf2f2(v.z), d = bf2f2(v.w);
+        ss2 = fma2(a, a, ss2);
+        ss2 = fma2(b, b, ss2);
+        ss2 = fma2(cc, cc, ss2);
+        ss2 = fma2(d, d, ss2);
+    }
+    const float ss = ss2.x + ss2.y;
+    const float inv = ss > 0.f || eps > 0.f ? rsqrtf(ss * (1.0f / D) + eps) : 0.f;
+    const float2 inv2 = make_float2(inv, inv);
+#pragma unroll 4
+    for (int c = 0; c < NC; ++c) {
+        uint8_t* cp = base + (c >> 3) * chunk_stride + sw128_off(row, c & 7);
+        const uint4 v = *reinterpret_cast<const uint4*>(cp);
+        const float4 w0 = *reinterpret_cast<const float4*>(w_s + c * 8);
+        const float4 w1 = *reinterpret_cast<const float4*>(w_s + c * 8 + 4);
+        const float2 y0 = mul2(mul2(bf2f2(v.x), make_float2(w0.x, w0.y)), inv2);
+        const float2 y1 = mul2(mul2(bf2f2(v.y), make_float2(w0.z, w0.w)), inv2);
+        const float2 y2 = mul2(mul2(bf2f2(v.z), make_float2(w1.x, w1.y)), inv2);
+        const float2 y3 = mul2(mul2(bf2f2(v.w), make_float2(w1.z, w1.w)), inv2);
+        *reinterpret_cast<uint4*>(cp) = make_uint4(pack_half2(y0.x, y0.y), pack_half2(y1.x, y1.y),
+                                                   pack_half2(y2.x, y2.y), pack_half2(y3.x, y3.y));
+    }
+    const int half = rc.half;
+    auto rotate = [&](int j, float cs, float sn) {
+        __half* p1 = reinterpret_cast<__half*>(sw_elem(base, chunk_stride, row, j));
+        __half* p2 = reinterpret_cast<__half*>(sw_elem(base, chunk_stride, row, j + half));
+        const float x1 = __half2float(*p1), x2 = __half2float(*p2);
+        *p1 = __float2half_rn(x1 * cs - x2 * sn);
+        *p2 = __float2half_rn(x2 * cs + x1 * sn);
+    };
+    if constexpr (SHARE == 1) {
+#pragma unroll 1
+        for (int j = 0; j < half; ++j) {
+            float cs, sn;
+            rope_cos_sin(pos, rc.f_hi[j], rc.f_lo[j], cs, sn);
+            rotate(j, cs, sn);
+        }
+    } else {
+        const int lane = threadIdx.x & 31;
+        const int mine = lane & (SHARE - 1);
+        const int grp = lane & ~(SHARE - 1);
+        constexpr int NI = (kMaxRotHalf + SHARE - 1) / SHARE;
+#pragma unroll
+        for (int i = 0; i < NI; ++i) {
+            if (i * SHARE >= half) break;  // uniform over the warp
+            const int jm = i * SHARE + mine;
+            float cs = 1.f, sn = 0.f;
+            if (jm < half) rope_cos_sin(pos, rc.f_hi[jm], rc.f_lo[jm], cs, sn);
+#pragma unroll
+            for (int h = 0; h < SHARE; ++h) {
+                const float c2 = __shfl_sync(0xffffffffu, cs, grp | h);
+                const float s2 = __shfl_sync(0xffffffffu, sn, grp | h);
+                if (i * SHARE + h < half) rotate(i * SHARE + h, c2, s2);
+            }
+        }
+    }
+}
+
+// In-place RMSNorm + partial RoPE of one row of a swizzled smem tile with TWO lanes per
+// row: lanes 2i and 2i+1 of the warp own the same row, the even lane the first half of
+// the D values and the odd lane the second half.  SL (a power of two >= 2) consecutive
+// lanes share one RoPE position (SL = 2 for key rows, 2G for the G query heads of a
+// token): each lane evaluates cos/sin for every SL-th frequency and they exchange them
+// with shuffles; the even lane of each row applies the rotations.  Every lane of the
+// warp must call this, with the same rc.half.  w_s: the D weights in shared memory.
+template <int D, int SL>
+__device__ __forceinline__ void qk_norm_rope_row_pair(uint8_t* base, uint32_t chunk_stride, int row, const float* w_s,
+                                                      float eps, int pos, const RopeConsts& rc, bool active = true) {
+    constexpr int NC2 = D / 16;  // 16-byte chunks per half row
+    const int lane = threadIdx.x & 31;
+    const int part = lane & 1;
+    const int c0 = part * NC2;
+    float2 ss2 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int c = c0; c < c0 + NC2; ++c) {
+        const uint4 v = *reinterpret_cast<const uint4*>(base + (c >> 3) * chunk_stride + sw128_off(row, c & 7));
+        const float2 a = bf2f2(v.x), b = bf2f2(v.y), cc = bf2f2(v.z), d = bf2f2(v.w);
+        ss2 = fma2(a, a, ss2);
+        ss2 = fma2(b, b, ss2);
+        ss2 = fma2(cc, cc, ss2);
+        ss2 = fma2(d, d, ss2);
+    }
+    float ss = ss2.x + ss2.y;
+    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+    const float inv = ss > 0.f || eps > 0.f ? rsqrtf(ss * (1.0f / D) + eps) : 0.f;
+    const float2 inv2 = make_float2(inv, inv);
+#pragma unroll
+    for (int c = c0; c < c0 + NC2; ++c) {
+        uint8_t* cp = base + (c >> 3) * chunk_stride + sw128_off(row, c & 7);
+        const uint4 v = *reinterpret_cast<const uint4*>(cp);
+        const float4 w0 = *reinterpret_cast<const float4*>(w_s + c * 8);
+        const float4 w1 = *reinterpret_cast<const float4*>(w_s + c * 8 + 4);
+        const float2 y0 = mul2(mul2(bf2f2(v.x), make_float2(w0.x, w0.y)), inv2);
+        const float2 y1 = mul2(mul2(bf2f2(v.y), make_float2(w0.z, w0.w)), inv2);
+        const float2 y2 = mul2(mul2(bf2f2(v.z), make_float2(w1.x, w1.y)), inv2);
+        const float2 y3 = mul2(mul2(bf2f2(v.w), make_float2(w1.z, w1.w)), inv2);
+        if (active)
+            *reinterpret_cast<uint4*>(cp) = make_uint4(pack_half2(y0.x, y0.y), pack_half2(y1.x, y1.y),
+                                                       pack_half2(y2.x, y2.y), pack_half2(y3.x, y3.y));
+    }
+    __syncwarp();  // the odd lane's half is in shared memory before the even lane rotates
+    const int half = rc.half;
+    const int mine = lane & (SL - 1);
+    const int grp = lane & ~(SL - 1);
+    constexpr int NI = (kMaxRotHalf + SL - 1) / SL;
+#pragma unroll
+    for (int i = 0; i < NI; ++i) {
+        if (i * SL >= half) break;  // uniform over the warp
+        const int jm = i * SL + mine;
+        float cs = 1.f, sn = 0.f;
+        if (jm < half) rope_cos_sin(pos, rc.f_hi[jm], rc.f_lo[jm], cs, sn);
+#pragma unroll
+        for (int h = 0; h < SL; ++h) {
+            const float c2 = __shfl_sync(0xffffffffu, cs, grp | h);
+            const float s2 = __shfl_sync(0xffffffffu, sn, grp | h);
+            const int j = i * SL + h;
+            if (active && part == 0 && j < half) {
+                __half* p1 = reinterpret_cast<__half*>(sw_elem(base, chunk_stride, row, j));
+                __half* p2 = reinterpret_cast<__half*>(sw_elem(base, chunk_stride, row, j + half));
+                const float x1 = __half2float(*p1), x2 = __half2float(*p2);
+                *p1 = __float2half_rn(x1 * c2 - x2 * s2);
+                *p2 = __float2half_rn(x2 * c2 + x1 * s2);
+            }
+        }
+    }
+}
+
+// As qk_norm_rope_row_pair, for a rotary width 2*HALF known at compile time: the even
+// lane keeps the first ceil(2*HALF/8) chunks of its half row in registers and rotates
+// them there, so no per-element shared-memory round trip is needed.
+template <int D, int SL, int HALF>
+__device__ __forceinline__ void qk_norm_rope_row_pair_ct(uint8_t* base, uint32_t chunk_stride, int row,
+                                                         const float* w_s, float eps, int pos, const RopeConsts& rc,
+                                                         bool active = true) {
+    constexpr int NC2 = D / 16;
+    constexpr int NR = (2 * HALF + 7) / 8;  // chunks holding rotated dims
+    static_assert(NR <= NC2, "rotated dims must lie in the first half row");
+    const int lane = threadIdx.x & 31;
+    const int part = lane & 1;
+    const int c0 = part * NC2;
+    float2 ss2 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int c = 0; c < NC2; ++c) {
+        const uint4 v =
+            *reinterpret_cast<const uint4*>(base + ((c0 + c) >> 3) * chunk_stride + sw128_off(row, (c0 + c) & 7));
+        const float2 a = bf2f2(v.x), b = bf2f2(v.y), cc = bf2f2(v.z), d = bf2f2(v.w);
+        ss2 = fma2(a, a, ss2);
+        ss2 = fma2(b, b, ss2);
+        ss2 = fma2(cc, cc, ss2);
+        ss2 = fma2(d, d, ss2);
+    }
+    float ss = ss2.x + ss2.y;
+    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+    const float inv = ss > 0.f || eps > 0.f ? rsqrtf(ss * (1.0f / D) + eps) : 0.f;
+    const float2 inv2 = make_float2(inv, inv);
+    float y[NR * 8];  // even lane: normalised dims [0, 8*NR) before rotation
+#pragma unroll
+    for (int c = 0; c < NC2; ++c) {
+        const int cg = c0 + c;
+        uint8_t* cp = base + (cg >> 3) * chunk_stride + sw128_off(row, cg & 7);
+        const uint4 v = *reinterpret_cast<const uint4*>(cp);
+        const float4 w0 = *reinterpret_cast<const float4*>(w_s + cg * 8);
+        const float4 w1 = *reinterpret_cast<const float4*>(w_s + cg * 8 + 4);
+        const float2 y0 = mul2(mul2(bf2f2(v.x), make_float2(w0.x, w0.y)), inv2);
+        const float2 y1 = mul2(mul2(bf2f2(v.y), make_float2(w0.z, w0.w)), inv2);
+        const float2 y2 = mul2(mul2(bf2f2(v.z), make_float2(w1.x, w1.y)), inv2);
+        const float2 y3 = mul2(mul2(bf2f2(v.w), make_float2(w1.z, w1.w)), inv2);
+        if (c < NR) {  // kept for the rotation (meaningful on the even lane only)
+            y[c * 8 + 0] = y0.x; y[c * 8 + 1] = y0.y; y[c * 8 + 2] = y1.x; y[c * 8 + 3] = y1.y;
+            y[c * 8 + 4] = y2.x; y[c * 8 + 5] = y2.y; y[c * 8 + 6] = y3.x; y[c * 8 + 7] = y3.y;
+        }
+        if (active && (part == 1 || c >= NR))
+            *reinterpret_cast<uint4*>(cp) = make_uint4(pack_half2(y0.x, y0.y), pack_half2(y1.x, y1.y),
+                                                       pack_half2(y2.x, y2.y), pack_half2(y3.x, y3.y));
+    }
+    // cos/sin: lane (grp | h) evaluates frequencies j = i*SL + h; everyone gathers them
+    const int mine = lane & (SL - 1);
+    const int grp = lane & ~(SL - 1);
+    constexpr int NI = (HALF + SL - 1) / SL;
+    float cj[NI], sj[NI];
+#pragma unroll
+    for (int i = 0; i < NI; ++i) {
+        const int jm = i * SL + mine;
+        cj[i] = 1.f;
+        sj[i] = 0.f;
+        if (jm < HALF) rope_cos_sin(pos, rc.f_hi[jm], rc.f_lo[jm], cj[i], sj[i]);
+    }
+#pragma unroll
+    for (int j = 0; j < HALF; ++j) {
+        const float cs = __shfl_sync(0xffffffffu, cj[j / SL], grp | (j % SL));
+        const float sn = __shfl_sync(0xffffffffu, sj[j / SL], grp | (j % SL));
+        const float a = y[j], b = y[j + HALF];
+        y[j] = a * cs - b * sn;
+        y[j + HALF] = b * cs + a * sn;
+    }
+    if (active && part == 0) {
+#pragma unroll
+        for (int c = 0; c < NR; ++c)
+            *reinterpret_cast<uint4*>(base + (c >> 3) * chunk_stride + sw128_off(row, c & 7)) =
+                make_uint4(pack_half2(y[c * 8 + 0], y[c * 8 + 1]), pack_half2(y[c * 8 + 2], y[c * 8 + 3]),
+                           pack_half2(y[c * 8 + 4], y[c * 8 + 5]), pack_half2(y[c * 8 + 6], y[c * 8 + 7]));
     }
 }
 
