@@ -14,23 +14,23 @@
 // of T keys.  Keys and values therefore live in a ring of NS + 1 slots in shared
 // memory and each key is loaded and normalised once per run.
 //
-// Warp roles (22 warps):
-//   warp 0      TMA producer: Q tiles into a 3-deep buffer ring, the gate tile of
-//               tile n-1 into its (freed) Q buffer.
-//   warp 20     TMA producer: K slots into the key ring (a slot is refilled once the
-//               last QK that reads it has completed).
-//   warp 21     TMA producer: V slots into the value ring (refilled after the last PV).
-//   warp 1      MMA issuer (one lane): S = Q K^T (fp16, M128 x N=NK, split in two
-//               when the window wraps around the ring) into one of two TMEM S
-//               buffers; O = P V with P read from TMEM (packed bf16) and V from
-//               the ring (MN-major).  Owns TMEM (512 columns).
+// Warp roles (20 warps):
+//   warp 0      TMA loop (one thread): K slots into the key ring (refilled once the
+//               last QK reading a slot has completed), V slots (after the last PV),
+//               Q tiles into a 3-deep buffer ring, output stores.
+//   warp 1      MMA loop (one thread), QK and PV as soon as each is ready (below).
+//               Warp 1 owns TMEM (512 columns).
 //   warps 4-11  RMSNorm + RoPE of the Q tile rows, in place (bf16 -> fp16), two
-//               lanes per row, cos/sin shared by the lanes of one token.
+//               lanes per row, cos/sin shared by the lanes of one token.  The MMA
+//               loop then issues S = Q K^T (fp16, M128 x N=NK, split in two when
+//               the window wraps around the key ring) into one of two TMEM S buffers.
 //   warps 2-3   the same for the K rows of every new slot.
 //   warps 12-15 softmax: exp2 against a bound on the scores, bf16 P written back
-//               over S in TMEM, row sums handed to the epilogue in shared memory.
-//   warps 16-19 epilogue: O / l * sigmoid(gate), in place over the gate tile,
-//               TMA store, buffer released.
+//               over S in TMEM, after which the MMA loop issues O = P V (P read from
+//               TMEM, V MN-major from the ring) and l = P 1 (row sums); the softmax
+//               also fetches the gate tile into the freed Q buffer.
+//   warps 16-19 epilogue: O / l * sigmoid(gate), in place over the gate tile, which
+//               the TMA loop then stores.
 // Every hand-off is an mbarrier with a bounded wait; a wait that gives up sets
 // the CTA's abort flag and every role winds down.
 #include "zg_qk.cuh"
@@ -45,7 +45,7 @@ struct Swa2 {
     static constexpr int NS = WS + 1;         // slots per tile window
     static constexpr int NK = NS * T;         // keys per tile (N of the QK product)
     static constexpr int SLOT2 = T * 128 * (D / 64) * 2;  // bytes of one K slot + one V slot
-    static constexpr int BASE_SMEM = 3 * 128 * 128 * (D / 64) + 2048 + 2 * D * 4;
+    static constexpr int BASE_SMEM = 3 * 128 * 128 * (D / 64) + 4096 + 2 * D * 4;
     static constexpr int SPARE = (232448 - BASE_SMEM) / SLOT2 - (NS + 1);
     static constexpr int R = NS + 1 + (SPARE > 3 ? 3 : SPARE);  // ring slots
     static constexpr int RR = R * T;          // ring rows
@@ -59,21 +59,22 @@ struct Swa2 {
     static constexpr uint32_t OFF_Q = 0;
     static constexpr uint32_t OFF_K = OFF_Q + NQB * QBUF;
     static constexpr uint32_t OFF_V = OFF_K + RING;
-    static constexpr uint32_t OFF_BAR = OFF_V + RING;
-    static constexpr int NBAR = 4 * NQB + 5 * R + 2 * 3 + 2 + 2 * 2 + 2;
+    static constexpr uint32_t OFF_ONES = OFF_V + RING;  // 2 KB of bf16 1.0: B operand of the row-sum MMA
+    static constexpr uint32_t OFF_BAR = OFF_ONES + 2048;
+    static constexpr int NBAR = 4 * NQB + 5 * R + 2 * 3 + 2 + 3;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
-    static constexpr uint32_t OFF_L = (OFF_MISC + 16 + 15) / 16 * 16;
-    static constexpr uint32_t OFF_W = OFF_L + 2 * 128 * 4;  // wq [D], wk [D] fp32
+    static constexpr uint32_t OFF_W = (OFF_MISC + 16 + 15) / 16 * 16;  // wq [D], wk [D] fp32
     static constexpr uint32_t SMEM = OFF_W + 2 * D * 4;
     static constexpr int SCOLS = (NK + 31) / 32 * 32;  // TMEM columns of one S buffer
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr int O_COL = 2 * SCOLS;
-    static_assert(O_COL + D <= 512, "TMEM budget");
+    static constexpr int L_COL = O_COL + D;  // 16 columns: row sums of P (every column the same)
+    static_assert(L_COL + 16 <= 512, "TMEM budget");
     static_assert(SMEM <= 232448, "shared memory budget");
     static_assert(T % 16 == 0 && NK <= 256, "tile shape");
 };
 
-constexpr int kThreads = 704;  // 22 warps
+constexpr int kThreads = 640;  // 20 warps
 
 struct TileIdx {
     int b, g, lt;
@@ -97,6 +98,32 @@ __device__ __forceinline__ void next_tile(TileIdx& t, int n_lt, int Hkv) {
     }
 }
 
+// Walks the K/V slot stream of a CTA: at the start of a span (first tile of the run,
+// or a sequence start) the WS history slots come first, then one slot per tile.
+struct SlotCursor {
+    TileIdx ti;
+    int it, w, c;
+    __device__ __forceinline__ void init(const TileIdx& first, int WS) {
+        ti = first;
+        it = 0;
+        c = 0;
+        w = WS;  // the run's first tile always starts a span
+    }
+    __device__ __forceinline__ int slot_tile() const { return ti.lt - w; }
+    __device__ __forceinline__ void advance(int n_tiles, int n_lt, int Hkv, int WS) {
+        ++c;
+        if (w > 0) {
+            --w;
+            return;
+        }
+        ++it;
+        if (it < n_tiles) {
+            next_tile(ti, n_lt, Hkv);
+            w = ti.lt == 0 ? WS : 0;
+        }
+    }
+};
+
 // ROT: rotary width compiled in (the dims then stay in registers), or 0 = any width.
 template <int D, int G, int ROT>
 __global__ void __launch_bounds__(kThreads, 1) swa2_kernel(const __grid_constant__ PrefillParams p) {
@@ -106,8 +133,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa2_kernel(const __grid_constant
     uint64_t* q_full = bar;
     uint64_t* q_ready = q_full + C::NQB;
     uint64_t* g_full = q_ready + C::NQB;
-    uint64_t* q_empty = g_full + C::NQB;
-    uint64_t* k_full = q_empty + C::NQB;
+    uint64_t* k_full = g_full + C::NQB;
     uint64_t* v_full = k_full + C::R;
     uint64_t* k_ready = v_full + C::R;
     uint64_t* k_empty = k_ready + C::R;  // K slot free: the last QK reading it has completed
@@ -117,13 +143,11 @@ __global__ void __launch_bounds__(kThreads, 1) swa2_kernel(const __grid_constant
     uint64_t* s_empty = p_ready + 2;
     uint64_t* o_full = s_empty + 2;
     uint64_t* o_empty = o_full + 1;
-    uint64_t* l_full = o_empty + 1;
-    uint64_t* l_empty = l_full + 2;
-    uint64_t* drain = l_empty + 2;
-    uint64_t* epi_bar = drain + 1;  // rendezvous of the 128 epilogue threads before each store
+    uint64_t* drain = o_empty + 1;
+    uint64_t* drain2 = drain + 1;
+    uint64_t* out_ready = drain2 + 1;  // [NQB] the 128 epilogue threads wrote the tile in that buffer
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
-    float* lbuf = reinterpret_cast<float*>(smem + C::OFF_L);
     float* wq_s = reinterpret_cast<float*>(smem + C::OFF_W);
     float* wk_s = wq_s + D;
 
@@ -139,7 +163,6 @@ __global__ void __launch_bounds__(kThreads, 1) swa2_kernel(const __grid_constant
             mbar_init(&q_full[i], 1);
             mbar_init(&q_ready[i], 256);
             mbar_init(&g_full[i], 1);
-            mbar_init(&q_empty[i], 1);
         }
         for (int i = 0; i < C::R; ++i) {
             mbar_init(&k_full[i], 1);
@@ -152,13 +175,12 @@ __global__ void __launch_bounds__(kThreads, 1) swa2_kernel(const __grid_constant
             mbar_init(&s_full[i], 1);
             mbar_init(&p_ready[i], 128);
             mbar_init(&s_empty[i], 1);
-            mbar_init(&l_full[i], 128);
-            mbar_init(&l_empty[i], 128);
         }
         mbar_init(o_full, 1);
         mbar_init(o_empty, 128);
         mbar_init(drain, 1);
-        mbar_init(epi_bar, 128);
+        mbar_init(drain2, 1);
+        for (int i = 0; i < C::NQB; ++i) mbar_init(&out_ready[i], 128);
         fence_barrier_init();
     }
     if (warp == 1) {
@@ -166,6 +188,9 @@ __global__ void __launch_bounds__(kThreads, 1) swa2_kernel(const __grid_constant
         tmem_relinquish();
     }
     for (int e = threadIdx.x; e < 2 * D; e += kThreads) wq_s[e] = e < D ? __ldg(p.wq + e) : __ldg(p.wk + e - D);
+    for (int e = threadIdx.x; e < 512; e += kThreads)
+        reinterpret_cast<uint32_t*>(smem + C::OFF_ONES)[e] = 0x3F803F80u;  // bf16 pair (1.0, 1.0)
+    fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -179,142 +204,191 @@ __global__ void __launch_bounds__(kThreads, 1) swa2_kernel(const __grid_constant
     const TileIdx first = decode_tile(t_begin, p.n_ltiles, p.Hkv);
     const int n_tiles = static_cast<int>(t_end - t_begin);
 
-    if (warp == 0 || warp == 20 || warp == 21) {
-        // ------------------------------------------------------------ producers
-        // warp 0: Q tiles and gate tiles; warp 20: K/V slots (independent, so a full
-        // key ring never holds back the next Q tile)
+    // QK(n) = Q K^T over the tile's key window into S buffer n&1 (fp16, M128 x N=NK, split
+    // in two where the window wraps around the key ring); issued by one thread, which then
+    // commits: S ready, and the K slots no later QK of the span reads (the oldest slot, or
+    // all of them at the span's end).
+    auto issue_qk = [&](int n, int cn, bool span_last) {
+        const int sb = n & 1;
+        const int row0 = ((cn - C::WS) % C::R) * C::T;
+        const int n1 = min(C::NK, C::RR - row0);
+        const int n2 = C::NK - n1;
+        const uint32_t id1 = idesc_f16_f32(128, n1, false, false);
+        const uint32_t id2 = idesc_f16_f32(128, n2 > 0 ? n2 : 16, false, false);
+        const uint32_t qofs = C::OFF_Q + (n % C::NQB) * C::QBUF;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t co = (ks >> 2) * C::QCH + (ks & 3) * 32;
+            const uint32_t cok = (ks >> 2) * C::KCH + (ks & 3) * 32;
+            const uint64_t a = sdesc(sbase + qofs + co, 16, 1024, kSw128);
+            umma_bf16(tbase + sb * C::SCOLS, a, sdesc(sbase + C::OFF_K + row0 * 128 + cok, 16, 1024, kSw128), id1,
+                      ks > 0);
+            if (n2 > 0)
+                umma_bf16(tbase + sb * C::SCOLS + n1, a, sdesc(sbase + C::OFF_K + cok, 16, 1024, kSw128), id2, ks > 0);
+        }
+        umma_commit(&s_full[sb]);
+        for (int j = cn - C::WS; j <= (span_last ? cn : cn - C::WS); ++j) umma_commit(&k_empty[j % C::R]);
+    };
+    // PV(n): O = P V with P read from TMEM (packed bf16, over S buffer n&1) and V from the
+    // ring (MN-major); then l = P 1, the row sums of the very bf16 P the product used.
+    auto issue_pv = [&](int n, int cn, bool span_last) {
+        const int sb = n & 1;
+        const int row0 = ((cn - C::WS) % C::R) * C::T;
+        constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, false, true);
+#pragma unroll
+        for (int ks = 0; ks < C::NK / 16; ++ks) {
+            const int row = (row0 + ks * 16) % C::RR;
+            const uint64_t bd = sdesc(sbase + C::OFF_V + row * 128, C::KCH, 1024, kSw128);
+            umma_tmem_a(tbase + C::O_COL, tbase + sb * C::SCOLS + ks * 8, bd, idesc_pv, ks > 0);
+        }
+        constexpr uint32_t idesc_l = idesc_bf16_f32(128, 16, false, false);
+        const uint64_t ones = sdesc(sbase + C::OFF_ONES, 16, 1024, kSw128);
+#pragma unroll
+        for (int ks = 0; ks < C::NK / 16; ++ks)
+            umma_tmem_a(tbase + C::L_COL, tbase + sb * C::SCOLS + ks * 8, ones, idesc_l, ks > 0);
+        umma_commit(o_full);
+        umma_commit(&s_empty[sb]);
+        for (int j = cn - C::WS; j <= (span_last ? cn : cn - C::WS); ++j) umma_commit(&v_empty[j % C::R]);
+    };
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA loop (one thread)
+        // Four independent streams, each advanced whenever its next step is possible, so
+        // no stream ever waits behind another: K slots (refilled once the last QK reading
+        // them has completed), V slots (after the last PV), Q tiles into the 3-deep buffer
+        // ring, output stores.  A Q buffer takes the next Q tile once the store of the
+        // tile that last held it has been read.
         if (lane == 0 && !aborted()) {
-            const bool kv_role = warp != 0;
-            const bool k_role = warp == 20;
-            if (kv_role) {
-                tma_prefetch_desc(k_role ? &p.tm_k : &p.tm_v);
-            } else {
-                tma_prefetch_desc(&p.tm_q);
-                tma_prefetch_desc(&p.tm_gate);
-                tma_prefetch_desc(&p.tm_out);
-            }
-            int c = 0, n = 0;
-            TileIdx prev{0, 0, 0};
-            bool ok = true;
-            auto load_slot = [&](int cc, const TileIdx& ti, int tile_l) {
-                const int s = cc % C::R;
-                uint64_t* empty = k_role ? &k_empty[s] : &v_empty[s];
-                uint64_t* full = k_role ? &k_full[s] : &v_full[s];
-                uint8_t* ring = k_role ? kring : vring;
-                const CUtensorMap* map = k_role ? &p.tm_k : &p.tm_v;
-                if (!mbar_wait(empty, ((cc / C::R) & 1) ^ 1, p.ctl, 31)) return false;
-                const int tok = tile_l * C::T;
-                mbar_arrive_expect_tx(full, C::SLOT_BYTES);
-#pragma unroll
-                for (int ch = 0; ch < C::NCH; ++ch)
-                    tma_load_4d(ring + ch * C::KCH + s * C::T * 128, map, full, ch * 64, ti.g, tok, ti.b);
-                return true;
-            };
-            auto load_gate = [&](int m, const TileIdx& ti) {
-                if (!mbar_wait(&s_full[m & 1], (m >> 1) & 1, p.ctl, 32)) return false;
-                uint8_t* dst = qbuf0 + (m % C::NQB) * C::QBUF;
-                mbar_arrive_expect_tx(&g_full[m % C::NQB], C::QBUF);
-#pragma unroll
-                for (int ch = 0; ch < C::NCH; ++ch)
-                    tma_load_4d(dst + ch * C::QCH, &p.tm_gate, &g_full[m % C::NQB], ch * 64, ti.g * G, ti.lt * C::T,
-                                ti.b);
-                return true;
-            };
-            TileIdx ti = first;
-            for (int it = 0; it < n_tiles && ok && !aborted(); ++it, next_tile(ti, p.n_ltiles, p.Hkv)) {
-                if (kv_role) {
-                    if (it == 0 || ti.lt == 0)
-                        for (int w = C::WS; w >= 1 && ok; --w) ok = load_slot(c++, ti, ti.lt - w);
-                    ok = ok && load_slot(c++, ti, ti.lt);
-                    continue;
-                }
-                const int qb = n % C::NQB;
-                ok = mbar_wait(&q_empty[qb], ((n / C::NQB) & 1) ^ 1, p.ctl, 33);
-                if (ok) {
-                    uint8_t* dst = qbuf0 + qb * C::QBUF;
-                    mbar_arrive_expect_tx(&q_full[qb], C::QBUF);
+            tma_prefetch_desc(&p.tm_q);
+            tma_prefetch_desc(&p.tm_k);
+            tma_prefetch_desc(&p.tm_v);
+            tma_prefetch_desc(&p.tm_out);
+            SlotCursor kcur, vcur;
+            kcur.init(first, C::WS);
+            vcur.init(first, C::WS);
+            int nq = 0, ns = 0;
+            TileIdx tq = first, ts = first;
+            long long t_prog = clock64();
+            while (!aborted()) {
+                bool prog = false, pending = false;
+                for (int kv = 0; kv < 2; ++kv) {
+                    SlotCursor& cur = kv == 0 ? kcur : vcur;
+                    if (cur.it >= n_tiles) continue;
+                    pending = true;
+                    const int s = cur.c % C::R;
+                    uint64_t* empty = kv == 0 ? &k_empty[s] : &v_empty[s];
+                    if (!mbar_test(empty, ((cur.c / C::R) & 1) ^ 1)) continue;
+                    uint64_t* full = kv == 0 ? &k_full[s] : &v_full[s];
+                    uint8_t* ring = kv == 0 ? kring : vring;
+                    const CUtensorMap* map = kv == 0 ? &p.tm_k : &p.tm_v;
+                    mbar_arrive_expect_tx(full, C::SLOT_BYTES);
 #pragma unroll
                     for (int ch = 0; ch < C::NCH; ++ch)
-                        tma_load_4d(dst + ch * C::QCH, &p.tm_q, &q_full[qb], ch * 64, ti.g * G, ti.lt * C::T, ti.b);
+                        tma_load_4d(ring + ch * C::KCH + s * C::T * 128, map, full, ch * 64, cur.ti.g,
+                                    cur.slot_tile() * C::T, cur.ti.b);
+                    cur.advance(n_tiles, p.n_ltiles, p.Hkv, C::WS);
+                    prog = true;
                 }
-                if (ok && n >= 1) ok = load_gate(n - 1, prev);
-                prev = ti;
-                ++n;
+                if (nq < n_tiles) {
+                    pending = true;
+                    const int prev_user = nq - C::NQB;  // tile whose output last used this buffer
+                    if (prev_user < 0 || ns > prev_user) {
+                        if (prev_user >= 0) bulk_wait_read_at_most(ns - 1 - prev_user);
+                        const int qb = nq % C::NQB;
+                        uint8_t* dst = qbuf0 + qb * C::QBUF;
+                        mbar_arrive_expect_tx(&q_full[qb], C::QBUF);
+#pragma unroll
+                        for (int ch = 0; ch < C::NCH; ++ch)
+                            tma_load_4d(dst + ch * C::QCH, &p.tm_q, &q_full[qb], ch * 64, tq.g * G, tq.lt * C::T, tq.b);
+                        ++nq;
+                        next_tile(tq, p.n_ltiles, p.Hkv);
+                        prog = true;
+                    }
+                }
+                if (ns < n_tiles) {
+                    pending = true;
+                    const int qb = ns % C::NQB;
+                    if (mbar_test(&out_ready[qb], (ns / C::NQB) & 1)) {
+                        uint8_t* buf = qbuf0 + qb * C::QBUF;
+#pragma unroll
+                        for (int ch = 0; ch < C::NCH; ++ch)
+                            tma_store_4d(&p.tm_out, buf + ch * C::QCH, ch * 64, ts.g * G, ts.lt * C::T, ts.b);
+                        bulk_commit();
+                        ++ns;
+                        next_tile(ts, p.n_ltiles, p.Hkv);
+                        prog = true;
+                    }
+                }
+                if (!pending) break;
+                const long long now = clock64();
+                if (prog) {
+                    t_prog = now;
+                } else if (now - t_prog > wait_limit_cycles(p.ctl)) {
+                    report(p.ctl, 31, kErrTimeout);
+                    fail();
+                    break;
+                }
             }
-            if (!kv_role && ok && n >= 1 && !aborted()) ok = load_gate(n - 1, prev);
-            if (!ok) fail();
+            bulk_wait_all();
         }
     } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
+        // ------------------------------------------------------------ MMA loop (one thread)
+        // QK(n) and PV(m) are issued as soon as their inputs are ready, in tile order each.
         if (lane == 0 && !aborted()) {
-            constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, false, true);
-            int n = 0, c = 0, c_prev = 0;
+            int nqk = 0, npv = 0, cqk = 0, cpv = 0, cqk_cur = 0, cpv_cur = 0;
+            TileIdx tqk = first, tpv = first;
+            bool qk_have = false, pv_have = false;
+            long long t_prog = clock64();
             bool ok = true;
-            auto issue_pv = [&](int m, int cm, bool release_all) {
-                const int sb = m & 1;
-                if (!mbar_wait(&p_ready[sb], (m >> 1) & 1, p.ctl, 34)) return false;
-                if (!mbar_wait(o_empty, (m & 1) ^ 1, p.ctl, 35)) return false;
-                for (int j = cm - C::WS; j <= cm; ++j)
-                    if (!mbar_wait(&v_full[j % C::R], (j / C::R) & 1, p.ctl, 36)) return false;
-                tc_fence_after();
-                const int row0 = ((cm - C::WS) % C::R) * C::T;
-#pragma unroll
-                for (int ks = 0; ks < C::NK / 16; ++ks) {
-                    const int row = (row0 + ks * 16) % C::RR;
-                    const uint64_t bd = sdesc(sbase + C::OFF_V + row * 128, C::KCH, 1024, kSw128);
-                    umma_tmem_a(tbase + C::O_COL, tbase + sb * C::SCOLS + ks * 8, bd, idesc_pv, ks > 0);
-                }
-                umma_commit(o_full);
-                umma_commit(&s_empty[sb]);
-                umma_commit(&v_empty[(cm - C::WS) % C::R]);
-                if (release_all)
-                    for (int j = cm - C::WS + 1; j <= cm; ++j) {
-                        umma_commit(&v_empty[j % C::R]);
-                        umma_commit(&k_empty[j % C::R]);  // the span's last QK is done too
+            while (ok && !aborted() && npv < n_tiles) {
+                bool prog = false;
+                if (nqk < n_tiles) {
+                    if (!qk_have) {
+                        if (nqk == 0 || tqk.lt == 0) cqk += C::WS;
+                        cqk_cur = cqk++;
+                        qk_have = true;
                     }
-                return true;
-            };
-            TileIdx ti = first;
-            for (int it = 0; it < n_tiles && ok && !aborted(); ++it, next_tile(ti, p.n_ltiles, p.Hkv)) {
-                const bool span_start = it == 0 || ti.lt == 0;
-                // a new span needs the whole ring for its warm-up slots: finish the previous tile first
-                if (span_start && n >= 1) {
-                    ok = issue_pv(n - 1, c_prev, true);
-                    if (!ok) break;
+                    const int cn = cqk_cur;
+                    const int sb = nqk & 1;
+                    bool ready = mbar_test(&s_empty[sb], ((nqk >> 1) & 1) ^ 1) &&
+                                 mbar_test(&q_ready[nqk % C::NQB], (nqk / C::NQB) & 1);
+                    for (int j = cn - C::WS; j <= cn && ready; ++j) ready = mbar_test(&k_ready[j % C::R], (j / C::R) & 1);
+                    if (ready) {
+                        tc_fence_after();
+                        issue_qk(nqk, cn, nqk + 1 == n_tiles || tqk.lt + 1 == p.n_ltiles);
+                        ++nqk;
+                        next_tile(tqk, p.n_ltiles, p.Hkv);
+                        qk_have = false;
+                        prog = true;
+                    }
                 }
-                if (span_start) c += C::WS;
-                const int cn = c++;
-                const int sb = n & 1;
-                ok = mbar_wait(&s_empty[sb], ((n >> 1) & 1) ^ 1, p.ctl, 37) &&
-                     mbar_wait(&q_ready[n % C::NQB], (n / C::NQB) & 1, p.ctl, 38);
-                for (int j = cn - C::WS; j <= cn && ok; ++j) ok = mbar_wait(&k_ready[j % C::R], (j / C::R) & 1, p.ctl, 39);
-                if (!ok) break;
-                tc_fence_after();
-                // S = Q K^T over the window; split where the window wraps around the ring
-                const int row0 = ((cn - C::WS) % C::R) * C::T;
-                const int n1 = min(C::NK, C::RR - row0);
-                const int n2 = C::NK - n1;
-                const uint32_t id1 = idesc_f16_f32(128, n1, false, false);
-                const uint32_t id2 = idesc_f16_f32(128, n2 > 0 ? n2 : 16, false, false);
-                const uint32_t qofs = C::OFF_Q + (n % C::NQB) * C::QBUF;
-#pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t co = (ks >> 2) * C::QCH + (ks & 3) * 32;
-                    const uint32_t cok = (ks >> 2) * C::KCH + (ks & 3) * 32;
-                    const uint64_t a = sdesc(sbase + qofs + co, 16, 1024, kSw128);
-                    umma_bf16(tbase + sb * C::SCOLS, a, sdesc(sbase + C::OFF_K + row0 * 128 + cok, 16, 1024, kSw128),
-                              id1, ks > 0);
-                    if (n2 > 0)
-                        umma_bf16(tbase + sb * C::SCOLS + n1, a, sdesc(sbase + C::OFF_K + cok, 16, 1024, kSw128), id2,
-                                  ks > 0);
+                if (npv < nqk) {
+                    if (!pv_have) {
+                        if (npv == 0 || tpv.lt == 0) cpv += C::WS;
+                        cpv_cur = cpv++;
+                        pv_have = true;
+                    }
+                    const int cn = cpv_cur;
+                    const int sb = npv & 1;
+                    bool ready = mbar_test(&p_ready[sb], (npv >> 1) & 1) && mbar_test(o_empty, (npv & 1) ^ 1);
+                    for (int j = cn - C::WS; j <= cn && ready; ++j) ready = mbar_test(&v_full[j % C::R], (j / C::R) & 1);
+                    if (ready) {
+                        tc_fence_after();
+                        issue_pv(npv, cn, npv + 1 == n_tiles || tpv.lt + 1 == p.n_ltiles);
+                        ++npv;
+                        next_tile(tpv, p.n_ltiles, p.Hkv);
+                        pv_have = false;
+                        prog = true;
+                    }
                 }
-                umma_commit(&s_full[sb]);
-                umma_commit(&k_empty[(cn - C::WS) % C::R]);  // no later tile of the span reads it
-                if (n >= 1 && !span_start) ok = issue_pv(n - 1, c_prev, false);
-                c_prev = cn;
-                ++n;
+                const long long now = clock64();
+                if (prog) {
+                    t_prog = now;
+                } else if (now - t_prog > wait_limit_cycles(p.ctl)) {
+                    report(p.ctl, 37, kErrTimeout);
+                    ok = false;
+                }
             }
-            if (ok && n >= 1 && !aborted()) ok = issue_pv(n - 1, c_prev, true);
             if (!ok) fail();
             // every MMA issued above has completed before the CTA may release TMEM
             umma_commit(drain);
@@ -325,15 +399,25 @@ __global__ void __launch_bounds__(kThreads, 1) swa2_kernel(const __grid_constant
         const int row = (threadIdx.x - 128) >> 1;
         int n = 0;
         TileIdx ti = first;
+        // position of this row's token, fetched one tile ahead
+        auto qpos = [&](const TileIdx& t) {
+            const int tok = t.lt * C::T + row / G;
+            return tok < p.L ? __ldg(p.pos + static_cast<long long>(t.b) * p.L + tok) : 0;
+        };
+        int pos_next = n_tiles > 0 ? qpos(ti) : 0;
         for (int it = 0; it < n_tiles; ++it, next_tile(ti, p.n_ltiles, p.Hkv)) {
             if (aborted()) break;
+            const int pos = pos_next;
+            if (it + 1 < n_tiles) {
+                TileIdx tn = ti;
+                next_tile(tn, p.n_ltiles, p.Hkv);
+                pos_next = qpos(tn);
+            }
             const int qb = n % C::NQB;
             if (!__all_sync(0xffffffffu, mbar_wait(&q_full[qb], (n / C::NQB) & 1, p.ctl, 41))) {
                 fail();
                 break;
             }
-            const int tok = ti.lt * C::T + row / G;
-            const int pos = tok < p.L ? __ldg(p.pos + static_cast<long long>(ti.b) * p.L + tok) : 0;
             if constexpr (ROT > 0)
                 qk_norm_rope_row_pair_ct<D, 2 * G, ROT / 2>(qbuf0 + qb * C::QBUF, C::QCH, row, wq_s, p.eps, pos, p.rope);
             else
@@ -349,14 +433,22 @@ __global__ void __launch_bounds__(kThreads, 1) swa2_kernel(const __grid_constant
         bool ok = true;
         auto kslot = [&](int cc, const TileIdx& ti, int tile_l) {
             const int s = cc % C::R;
+            // positions first: their latency overlaps the wait for the slot
+            int posr[(C::T + 31) / 32];
+#pragma unroll
+            for (int q = 0; q < (C::T + 31) / 32; ++q) {
+                const int r = min(q * 32 + (kt >> 1), C::T - 1);
+                const int tok = tile_l * C::T + r;
+                posr[q] = (tok >= 0 && tok < p.L) ? __ldg(p.pos + static_cast<long long>(ti.b) * p.L + tok) : 0;
+            }
             if (!__all_sync(0xffffffffu, mbar_wait(&k_full[s], (cc / C::R) & 1, p.ctl, 42))) return false;
+#pragma unroll
             for (int r0 = 0; r0 < C::T; r0 += 32) {
                 // every lane joins (the row transform is warp-collective); lanes past T only
                 // read row T-1 and write nothing
                 const bool active = r0 + (kt >> 1) < C::T;
                 const int r = min(r0 + (kt >> 1), C::T - 1);
-                const int tok = tile_l * C::T + r;
-                const int pos = (tok >= 0 && tok < p.L) ? __ldg(p.pos + static_cast<long long>(ti.b) * p.L + tok) : 0;
+                const int pos = posr[r0 / 32];
                 if constexpr (ROT > 0)
                     qk_norm_rope_row_pair_ct<D, 2, ROT / 2>(kring, C::KCH, s * C::T + r, wk_s, p.eps, pos, p.rope,
                                                             active);
@@ -410,6 +502,15 @@ __global__ void __launch_bounds__(kThreads, 1) swa2_kernel(const __grid_constant
                 break;
             }
             tc_fence_after();
+            if (row == 0) {
+                // QK(n) has completed: the Q buffer is free for the gate tile the epilogue needs
+                const int qb = n % C::NQB;
+                uint8_t* dst = qbuf0 + qb * C::QBUF;
+                mbar_arrive_expect_tx(&g_full[qb], C::QBUF);
+#pragma unroll
+                for (int ch = 0; ch < C::NCH; ++ch)
+                    tma_load_4d(dst + ch * C::QCH, &p.tm_gate, &g_full[qb], ch * 64, ti.g * G, ti.lt * C::T, ti.b);
+            }
             const int i0 = ti.lt * C::T;
             const int tt = row / G;
             // key column kr <-> key i0 - 128 + kr; valid: kr in [max(128 - i0, tt + 129 - W), tt + 128]
@@ -431,46 +532,44 @@ __global__ void __launch_bounds__(kThreads, 1) swa2_kernel(const __grid_constant
                 mb = (m == -INFINITY ? 0.f : m) * p.scale_log2;
             }
             const float2 nm2 = make_float2(-mb, -mb);
-            float2 l2 = make_float2(0.f, 0.f);
-#pragma unroll 1
-            for (int cb = 0; cb < C::NK; cb += 32) {
-                uint32_t r[32];
-                tmem_ld32(s_addr + cb, r);
-                tmem_wait_ld();
-                uint32_t pk[16];
-                const bool full = cb >= kr_lo && cb + 31 <= kr_hi;
-                if (full) {
+            // 16 key columns per step; the load of step c+1 is in flight while step c is computed
+            auto soft16 = [&](const uint32_t* r, int cb) {
+                uint32_t pk[8];
+                if (cb >= kr_lo && cb + 15 <= kr_hi) {
 #pragma unroll
-                    for (int k = 0; k < 32; k += 2) {
+                    for (int k = 0; k < 16; k += 2) {
                         const float2 x = fma2(make_float2(__uint_as_float(r[k]), __uint_as_float(r[k + 1])), sc2, nm2);
-                        const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-                        pk[k / 2] = pack_bf16x2(e.x, e.y);
-                        l2 = add2(l2, bf2f2(pk[k / 2]));  // sum what the MMA will see
+                        pk[k / 2] = pack_bf16x2(ex2_approx(x.x), ex2_approx(x.y));
                     }
                 } else {
 #pragma unroll
-                    for (int k = 0; k < 32; k += 2) {
+                    for (int k = 0; k < 16; k += 2) {
                         const float2 x = fma2(make_float2(__uint_as_float(r[k]), __uint_as_float(r[k + 1])), sc2, nm2);
                         const int kr = cb + k;
                         const float e0 = (kr >= kr_lo && kr <= kr_hi) ? ex2_approx(x.x) : 0.f;
                         const float e1 = (kr + 1 >= kr_lo && kr + 1 <= kr_hi) ? ex2_approx(x.y) : 0.f;
                         pk[k / 2] = pack_bf16x2(e0, e1);
-                        l2 = add2(l2, bf2f2(pk[k / 2]));
                     }
                 }
-                // P (keys cb..cb+31) -> TMEM columns cb/2 .. cb/2+15 of this S buffer (already read)
-                tmem_st16(s_addr + cb / 2, pk);
+                // P (keys cb..cb+15) -> TMEM columns cb/2 .. cb/2+7 of this S buffer (already read)
+                tmem_st8(s_addr + cb / 2, pk);
+            };
+            uint32_t ra[16], rb[16];
+            tmem_ld16(s_addr, ra);
+            tmem_wait_ld();
+#pragma unroll 1
+            for (int cb = 0; cb < C::NK; cb += 32) {
+                if (cb + 16 < C::NK) tmem_ld16(s_addr + cb + 16, rb);
+                soft16(ra, cb);
+                tmem_wait_ld();
+                if (cb + 16 >= C::NK) break;
+                if (cb + 32 < C::NK) tmem_ld16(s_addr + cb + 32, ra);
+                soft16(rb, cb + 16);
+                tmem_wait_ld();
             }
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(&p_ready[sb]);
-            const int lb = n & 1;
-            if (!__all_sync(0xffffffffu, mbar_wait(&l_empty[lb], ((n >> 1) & 1) ^ 1, p.ctl, 44))) {
-                fail();
-                break;
-            }
-            lbuf[lb * 128 + row] = l2.x + l2.y;
-            mbar_arrive(&l_full[lb]);
             ++n;
         }
     } else if (warp >= 16 && warp <= 19) {
@@ -479,66 +578,59 @@ __global__ void __launch_bounds__(kThreads, 1) swa2_kernel(const __grid_constant
         const uint32_t lane_addr = tbase + (static_cast<uint32_t>((warp & 3) * 32) << 16);
         int n = 0;
         TileIdx ti = first;
-        const float2 half2v = make_float2(0.5f, 0.5f);
         for (int it = 0; it < n_tiles; ++it, next_tile(ti, p.n_ltiles, p.Hkv)) {
             if (aborted()) break;
-            const int lb = n & 1, qb = n % C::NQB;
-            bool ok = mbar_wait(o_full, n & 1, p.ctl, 45) && mbar_wait(&l_full[lb], (n >> 1) & 1, p.ctl, 46) &&
-                      mbar_wait(&g_full[qb], (n / C::NQB) & 1, p.ctl, 47);
+            const int qb = n % C::NQB;
+            bool ok = mbar_wait(o_full, n & 1, p.ctl, 45) && mbar_wait(&g_full[qb], (n / C::NQB) & 1, p.ctl, 47);
             if (!__all_sync(0xffffffffu, ok)) {
                 fail();
                 break;
             }
             tc_fence_after();
-            const float lsum = lbuf[lb * 128 + row];
-            mbar_arrive(&l_empty[lb]);
+            uint32_t lraw;
+            tmem_ld1(lane_addr + C::L_COL, lraw);
+            uint32_t ra[16], rb[16];
+            tmem_ld16(lane_addr + C::O_COL, ra);
+            tmem_wait_ld();
+            const float lsum = __uint_as_float(lraw);
             // out = O / l * sigmoid(g) = (O * 0.5/l) * (1 + tanh(g / 2))
             const float c = lsum > 0.f ? 0.5f / lsum : 0.f;
             const float2 c2 = make_float2(c, c);
             uint8_t* buf = qbuf0 + qb * C::QBUF;
-#pragma unroll 1
-            for (int cb = 0; cb < D; cb += 32) {
-                uint32_t r[32];
-                tmem_ld32(lane_addr + C::O_COL + cb, r);
-                tmem_wait_ld();
+            auto epi16 = [&](const uint32_t* r, int cb) {
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    const int e0 = cb + q4 * 8;
+                for (int q2 = 0; q2 < 2; ++q2) {
+                    const int e0 = cb + q2 * 8;
                     uint8_t* gp = buf + (e0 >> 6) * C::QCH + sw128_off(row, (e0 & 63) >> 3);
                     const uint4 gv = *reinterpret_cast<const uint4*>(gp);
                     const uint32_t gu[4] = {gv.x, gv.y, gv.z, gv.w};
                     uint32_t ou[4];
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
-                        const float2 gh = mul2(bf2f2(gu[k]), half2v);
-                        const float2 t = make_float2(tanh_approx(gh.x), tanh_approx(gh.y));
-                        const float2 oc =
-                            mul2(make_float2(__uint_as_float(r[q4 * 8 + 2 * k]), __uint_as_float(r[q4 * 8 + 2 * k + 1])), c2);
+                        const float2 t = bf2f2(tanh_bf16x2(mul_bf16x2(gu[k], 0x3F003F00u)));  // tanh(g/2)
+                        const float2 oc = mul2(
+                            make_float2(__uint_as_float(r[q2 * 8 + 2 * k]), __uint_as_float(r[q2 * 8 + 2 * k + 1])), c2);
                         const float2 o = fma2(oc, t, oc);
                         ou[k] = pack_bf16x2(o.x, o.y);
                     }
                     *reinterpret_cast<uint4*>(gp) = make_uint4(ou[0], ou[1], ou[2], ou[3]);
                 }
+            };
+#pragma unroll 1
+            for (int cb = 0; cb < D; cb += 32) {
+                tmem_ld16(lane_addr + C::O_COL + cb + 16, rb);
+                epi16(ra, cb);
+                tmem_wait_ld();
+                if (cb + 32 < D) tmem_ld16(lane_addr + C::O_COL + cb + 32, ra);
+                epi16(rb, cb + 16);
+                tmem_wait_ld();
             }
             tc_fence_before();
             mbar_arrive(o_empty);
-            fence_async_smem();
-            mbar_arrive(epi_bar);
-            if (!__all_sync(0xffffffffu, mbar_wait(epi_bar, n & 1, p.ctl, 48))) {
-                fail();
-                break;
-            }
-            if (row == 0) {
-#pragma unroll
-                for (int ch = 0; ch < C::NCH; ++ch)
-                    tma_store_4d(&p.tm_out, buf + ch * C::QCH, ch * 64, ti.g * G, ti.lt * C::T, ti.b);
-                bulk_commit();
-                bulk_wait_read_all();
-                mbar_arrive(&q_empty[qb]);
-            }
+            fence_async_smem();  // output visible to the TMA store issued by the TMA loop
+            mbar_arrive(&out_ready[qb]);
             ++n;
         }
-        if (row == 0) bulk_wait_all();
     }
     __syncthreads();
     if (aborted() && threadIdx.x == 0) {
@@ -569,7 +661,9 @@ cudaError_t launch_t(const PrefillParams& p, cudaStream_t s) {
 
 }  // namespace
 
-bool swa2_supports(int d, int G) { return (d == 64 || d == 128) && (G == 2 || G == 4 || G == 8); }
+// GQA 4 and 8; GQA 1 and 2 (whose score tiles leave no TMEM for double buffering)
+// take the one-tile kernel in swa_prefill.cu.
+bool swa2_supports(int d, int G) { return (d == 64 || d == 128) && (G == 4 || G == 8); }
 
 // The rotary widths of rotary ratio 0.33 (2 * floor(0.33 * d / 2)) get kernels with the
 // width compiled in; any other width takes the general kernel.
@@ -586,8 +680,6 @@ cudaError_t launch_swa2_prefill(const PrefillParams& p, int d, cudaStream_t s) {
     if (d == 64 && G == 4) return launch_rot<64, 4>(p, s);
     if (d == 128 && G == 8) return launch_rot<128, 8>(p, s);
     if (d == 64 && G == 8) return launch_rot<64, 8>(p, s);
-    if (d == 128 && G == 2) return launch_rot<128, 2>(p, s);
-    if (d == 64 && G == 2) return launch_rot<64, 2>(p, s);
     return cudaErrorInvalidValue;
 }
 

@@ -60,15 +60,32 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// Non-blocking test of phase `parity` of `bar`.
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Wait limits are kept in SM clock cycles: reading %globaltimer costs microseconds, the
+// cycle counter a few cycles.  2 cycles per ns bounds every clock this part runs at.
+__device__ __forceinline__ long long wait_limit_cycles(const DevCtl& ctl) {
+    return static_cast<long long>(ctl.wait_limit_ns) * 2;
+}
 // Bounded wait for phase `parity` of `bar`.  false = gave up (error recorded).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const DevCtl& ctl, uint32_t site) {
     if (mbar_try_wait(bar, parity)) return true;
-    const unsigned long long t0 = globaltimer_ns();
+    const long long t0 = clock64();
     while (true) {
 #pragma unroll 1
         for (int i = 0; i < 32; ++i)
             if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer_ns() - t0 > ctl.wait_limit_ns) {
+        if (clock64() - t0 > wait_limit_cycles(ctl)) {
             report(ctl, site, kErrTimeout);
             return false;
         }
@@ -95,6 +112,17 @@ __device__ __forceinline__ void tma_store_4d(const CUtensorMap* m, const void* s
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// wait until at most `pending` committed bulk groups of this thread still read shared memory
+__device__ __forceinline__ void bulk_wait_read_at_most(int pending) {
+    if (pending <= 0)
+        asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+    else if (pending == 1)
+        asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+    else if (pending == 2)
+        asm volatile("cp.async.bulk.wait_group.read 2;" ::: "memory");
+    else
+        asm volatile("cp.async.bulk.wait_group.read 3;" ::: "memory");
+}
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 // generic-proxy smem writes -> visible to the async proxy (TMA store, tcgen05.mma)
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
@@ -181,6 +209,14 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
         : "memory");
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_ld1(uint32_t taddr, uint32_t& r) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* r) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
+                 "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // Instruction descriptor, kind::f16 with fp16 A/B and fp32 D (format code 0 for A and B).
@@ -237,6 +273,18 @@ __device__ __forceinline__ float2 add2(float2 a, float2 b) {
     return bits_f2(d);
 }
 __device__ __forceinline__ float2 bf2f2(uint32_t u) { return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u)); }
+
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t y;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(y) : "r"(a), "r"(b));
+    return y;
+}
+// hardware tanh on a packed bf16 pair
+__device__ __forceinline__ uint32_t tanh_bf16x2(uint32_t x) {
+    uint32_t y;
+    asm("tanh.approx.bf16x2 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
 
 // logistic function through tanh: sigma(x) = 0.5 + 0.5 * tanh(x / 2)
 __device__ __forceinline__ float sigmoid_fast(float x) { return fmaf(0.5f, tanh_approx(0.5f * x), 0.5f); }
