@@ -9,16 +9,24 @@
 // Kernel 1 normalises and rotates every key once (one warp per key row) into
 // an fp16 workspace, so the quadratic loop below never repeats that work.
 //
-// Kernel 2: one CTA per 128-row GQA tile (32 tokens x 4 heads of one KV
-// head), heaviest tiles first.  Keys are consumed in blocks of 128:
-//   S(kb) = Q K^T (fp16 tcgen05, TMEM, double-buffered so QK(kb+1) runs during
-//   the softmax of block kb); each thread owns one row: online softmax with the
-//   running max raised only when a block maximum exceeds it by 8 (log2 units),
-//   then the O accumulator in TMEM is rescaled in place (rare); P (bf16) goes
-//   to shared memory and O += P V (bf16 tcgen05, V read MN-major).
-//   K_hat and V blocks arrive by TMA on separate two-stage rings: a K_hat stage
-//   is refilled as soon as its QK has completed, a V stage after its PV.
-// Only the last block of a tile can contain keys beyond the diagonal.
+// Kernel 2: one CTA owns 64 consecutive tokens of one KV head, as two 128-row
+// tiles (32 tokens x the 4 query heads of the group each), Q0 and Q1, that share
+// every K_hat / V block of 128 keys; heaviest CTAs (longest key ranges) first.
+//   warp 0      TMA: both Q tiles, then K_hat / V blocks on two-stage rings.
+//   warp 1      MMA (one thread): QK0(0), QK1(0), then per block j
+//                 PV0(j), QK0(j+1), PV1(j), QK1(j+1)
+//               so the tensor core computes one tile's scores while the other
+//               tile's softmax runs.  S_t and P_t share TMEM columns (P packed bf16
+//               over S); the MMAs of one thread execute in issue order, so
+//               QK_t(j+1) overwrites S_t only after PV_t(j) has read P_t(j).
+//   warps 4-7   tile 0: normalise + rotate Q0; per block: scores from TMEM, the
+//               running max raised only when a block maximum exceeds it by 8
+//               (log2 units), O rescaled in place in TMEM when it moves (after
+//               PV0(j-1) has completed), P = exp2(...) in bf16 back to TMEM, row
+//               sums of the rounded P; finally O / l -> bf16 -> TMA store.
+//   warps 8-11  the same for tile 1.
+// TMEM: S0 [0,128), S1 [128,256), O0 [256,384), O1 [384,512).
+// Only the last key block of a CTA can contain keys beyond the diagonal.
 #include "zg_qk.cuh"
 
 namespace zg {
@@ -26,18 +34,19 @@ namespace {
 
 constexpr int D = 128;
 constexpr int G = 4;
-constexpr int T = 32;     // tokens per Q tile
-constexpr int BK = 128;   // keys per block
+constexpr int T = 32;                     // tokens per tile
+constexpr int BK = 128;                   // keys per block
 constexpr uint32_t TILE = 128 * 128 * 2;  // one 128 x 128 16-bit tile (two 64-column chunks)
-constexpr uint32_t CH = 128 * 128;        // bytes of one 64-column chunk of 128 rows
-constexpr uint32_t OFF_Q = 0;
-constexpr uint32_t OFF_K = OFF_Q + TILE;      // 2 stages
-constexpr uint32_t OFF_V = OFF_K + 2 * TILE;  // 2 stages
-constexpr uint32_t OFF_P = OFF_V + 2 * TILE;
-constexpr uint32_t OFF_BAR = OFF_P + TILE;
-constexpr uint32_t SMEM = OFF_BAR + 128;
-constexpr uint32_t TMEM_COLS = 512;  // S0 [0,128), S1 [128,256), O [256,384)
+constexpr uint32_t CH = 128 * 128;        // one 64-column chunk of 128 rows
+constexpr uint32_t OFF_Q = 0;             // Q0, Q1
+constexpr uint32_t OFF_K = 2 * TILE;      // 2 stages
+constexpr uint32_t OFF_V = 4 * TILE;      // 2 stages
+constexpr uint32_t OFF_BAR = 6 * TILE;
+constexpr int NBAR = 20;
+constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
+constexpr uint32_t SMEM = OFF_MISC + 32;
 constexpr float kTau = 8.0f;
+constexpr int kThreads = 384;
 
 // ---------------------------------------------------------------- kernel 1
 __global__ void __launch_bounds__(256) khat_kernel(const __grid_constant__ PrefillParams p) {
@@ -57,45 +66,52 @@ __global__ void __launch_bounds__(256) khat_kernel(const __grid_constant__ Prefi
 }
 
 // ---------------------------------------------------------------- kernel 2
-__global__ void __launch_bounds__(128, 1) global_attn_kernel(const __grid_constant__ PrefillParams p) {
+__global__ void __launch_bounds__(kThreads, 1) global_attn_kernel(const __grid_constant__ PrefillParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
-    uint64_t* bar_q = bars + 0;
-    uint64_t* bar_k = bars + 1;   // [2]
-    uint64_t* bar_v = bars + 3;   // [2]
-    uint64_t* bar_s = bars + 5;   // [2]
-    uint64_t* bar_pv = bars + 7;
-    uint64_t* bar_drain = bars + 8;
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 9);
-    int* sflag = reinterpret_cast<int*>(bars + 10);
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+    uint64_t* q_full = bar + 0;
+    uint64_t* q_ready = bar + 1;   // [2]
+    uint64_t* k_full = bar + 3;    // [2]
+    uint64_t* v_full = bar + 5;    // [2]
+    uint64_t* k_empty = bar + 7;   // [2]
+    uint64_t* v_empty = bar + 9;   // [2]
+    uint64_t* s_full = bar + 11;   // [2] per tile
+    uint64_t* p_ready = bar + 13;  // [2] per tile
+    uint64_t* pv_done = bar + 15;  // [2] per tile
+    uint64_t* out_bar = bar + 17;  // [2] per tile: the tile's output is in shared memory
+    uint64_t* drain = bar + 19;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
 
-    const int t = threadIdx.x, warp = t >> 5;
-    // heaviest tiles (longest key ranges) first
-    const int n_lt = p.n_ltiles;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nbg = p.B * p.Hkv;
-    const int lt = n_lt - 1 - static_cast<int>(blockIdx.x / nbg);
+    const int n_ct = (p.L + 2 * T - 1) / (2 * T);
+    const int ct = n_ct - 1 - static_cast<int>(blockIdx.x / nbg);  // heaviest (longest key range) first
     const int g = static_cast<int>(blockIdx.x % nbg) % p.Hkv;
     const int b = static_cast<int>(blockIdx.x % nbg) / p.Hkv;
-    const int i0 = lt * T;
-    const int nkb = (i0 + T + BK - 1) / BK;
+    const int i0 = ct * 2 * T;
+    const int nkb = (i0 + 2 * T + BK - 1) / BK;  // both tiles need the same key blocks
 
-    uint8_t* sQ = smem + OFF_Q;
-    uint8_t* sP = smem + OFF_P;
-    if (t == 0) {
-        *sflag = (smem_u32(smem) & 1023u) == 0 ? 1 : 0;
-        if (!*sflag) report(p.ctl, 20, kErrAlign);
-        mbar_init(bar_q, 1);
+    if (threadIdx.x == 0) {
+        *abort_flag = (smem_u32(smem) & 1023u) == 0 ? 0 : 1;
+        if (*abort_flag) report(p.ctl, 50, kErrAlign);
+        mbar_init(q_full, 1);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&bar_k[i], 1);
-            mbar_init(&bar_v[i], 1);
-            mbar_init(&bar_s[i], 1);
+            mbar_init(&q_ready[i], 128);
+            mbar_init(&k_full[i], 1);
+            mbar_init(&v_full[i], 1);
+            mbar_init(&k_empty[i], 1);
+            mbar_init(&v_empty[i], 1);
+            mbar_init(&s_full[i], 1);
+            mbar_init(&p_ready[i], 128);
+            mbar_init(&pv_done[i], 1);
+            mbar_init(&out_bar[i], 128);
         }
-        mbar_init(bar_pv, 1);
-        mbar_init(bar_drain, 1);
+        mbar_init(drain, 1);
         fence_barrier_init();
     }
-    if (warp == 0) {
-        tmem_alloc(tslot, TMEM_COLS);
+    if (warp == 1) {
+        tmem_alloc(tslot, 512);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -103,217 +119,224 @@ __global__ void __launch_bounds__(128, 1) global_attn_kernel(const __grid_consta
     tc_fence_after();
     const uint32_t tbase = *tslot;
     const uint32_t sbase = smem_u32(smem);
-    bool ok = *sflag != 0;
+    auto aborted = [&]() { return *abort_flag != 0; };
+    auto fail = [&]() { *abort_flag = 1; };
 
-    auto load_k = [&](int kb) {
-        uint64_t* bar = &bar_k[kb & 1];
-        uint8_t* dst = smem + OFF_K + (kb & 1) * TILE;
-        mbar_arrive_expect_tx(bar, TILE);
-        tma_load_4d(dst, &p.tm_kh, bar, 0, g, kb * BK, b);
-        tma_load_4d(dst + CH, &p.tm_kh, bar, 64, g, kb * BK, b);
-    };
-    auto load_v = [&](int kb) {
-        uint64_t* bar = &bar_v[kb & 1];
-        uint8_t* dst = smem + OFF_V + (kb & 1) * TILE;
-        mbar_arrive_expect_tx(bar, TILE);
-        tma_load_4d(dst, &p.tm_v, bar, 0, g, kb * BK, b);
-        tma_load_4d(dst + CH, &p.tm_v, bar, 64, g, kb * BK, b);
-    };
-    auto issue_qk = [&](int kb) {
-        constexpr uint32_t idesc = idesc_f16_f32(128, BK, false, false);
-        const uint32_t kofs = OFF_K + (kb & 1) * TILE;
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-            const uint32_t co = (ks >> 2) * CH + (ks & 3) * 32;
-            umma_bf16(tbase + (kb & 1) * 128, sdesc(sbase + OFF_Q + co, 16, 1024, kSw128),
-                      sdesc(sbase + kofs + co, 16, 1024, kSw128), idesc, ks > 0);
-        }
-        umma_commit(&bar_s[kb & 1]);
-    };
-
-    if (t == 0 && ok) {
-        tma_prefetch_desc(&p.tm_q);
-        tma_prefetch_desc(&p.tm_kh);
-        tma_prefetch_desc(&p.tm_v);
-        mbar_arrive_expect_tx(bar_q, TILE);
-        tma_load_4d(sQ, &p.tm_q, bar_q, 0, g * G, i0, b);
-        tma_load_4d(sQ + CH, &p.tm_q, bar_q, 64, g * G, i0, b);
-        load_k(0);
-        load_v(0);
-        if (nkb > 1) {
-            load_k(1);
-            load_v(1);
-        }
-    }
-    const int tt = t / G;
-    const int iq = i0 + tt;
-    const int pos_q = iq < p.L ? __ldg(p.pos + static_cast<long long>(b) * p.L + iq) : 0;
-    if (ok) ok = mbar_wait(bar_q, 0, p.ctl, 21);
-    if (ok) qk_norm_rope_row<D>(sQ, CH, t, p.wq, p.eps, pos_q, p.rope);
-    if (!ok) *sflag = 0;
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (t == 0 && *sflag) {
-        if (mbar_wait(&bar_k[0], 0, p.ctl, 22)) {
-            tc_fence_after();
-            issue_qk(0);
-        } else {
-            *sflag = 0;
-        }
-    }
-    __syncthreads();
-    ok = *sflag != 0;
-
-    const uint32_t lane_addr = tbase + (static_cast<uint32_t>(warp * 32) << 16);
-    const uint32_t o_col = 256;
-    float m_run = -INFINITY, l_run = 0.f;
-    for (int kb = 0; kb < nkb; ++kb) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&bar_s[kb & 1], (kb >> 1) & 1, p.ctl, 23));
-        tc_fence_after();
-        if (t == 0 && ok) {
-            if (kb + 2 < nkb) load_k(kb + 2);  // K stage kb&1 is free: QK(kb) has completed
-            if (kb + 1 < nkb) {
-                if (mbar_wait(&bar_k[(kb + 1) & 1], ((kb + 1) >> 1) & 1, p.ctl, 24))
-                    issue_qk(kb + 1);
-                else
-                    *sflag = 0;
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA
+        if (lane == 0 && !aborted()) {
+            tma_prefetch_desc(&p.tm_q);
+            tma_prefetch_desc(&p.tm_kh);
+            tma_prefetch_desc(&p.tm_v);
+            tma_prefetch_desc(&p.tm_out);
+            mbar_arrive_expect_tx(q_full, 2 * TILE);
+            for (int t = 0; t < 2; ++t)
+                for (int ch = 0; ch < 2; ++ch)
+                    tma_load_4d(smem + OFF_Q + t * TILE + ch * CH, &p.tm_q, q_full, ch * 64, g * G, i0 + t * T, b);
+            bool ok = true;
+            for (int j = 0; j < nkb && ok && !aborted(); ++j) {
+                const int st = j & 1;
+                ok = mbar_wait(&k_empty[st], ((j >> 1) & 1) ^ 1, p.ctl, 51);
+                if (!ok) break;
+                mbar_arrive_expect_tx(&k_full[st], TILE);
+                for (int ch = 0; ch < 2; ++ch)
+                    tma_load_4d(smem + OFF_K + st * TILE + ch * CH, &p.tm_kh, &k_full[st], ch * 64, g, j * BK, b);
+                ok = mbar_wait(&v_empty[st], ((j >> 1) & 1) ^ 1, p.ctl, 52);
+                if (!ok) break;
+                mbar_arrive_expect_tx(&v_full[st], TILE);
+                for (int ch = 0; ch < 2; ++ch)
+                    tma_load_4d(smem + OFF_V + st * TILE + ch * CH, &p.tm_v, &v_full[st], ch * 64, g, j * BK, b);
             }
+            if (!ok) fail();
         }
-        // ---- row max of block kb
-        const bool last = kb == nkb - 1;
-        if (!ok) *sflag = 0;
-        const int kmax = iq - kb * BK;  // last valid key column of this row in the block
-        const uint32_t s_addr = lane_addr + (kb & 1) * 128;
-        float mb = -INFINITY;
-#pragma unroll 1
-        for (int cb = 0; cb < BK && ok; cb += 32) {
-            uint32_t r[32];
-            tmem_ld32(s_addr + cb, r);
-            tmem_wait_ld();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA
+        if (lane == 0 && !aborted()) {
+            auto qk = [&](int t, int j) {
+                constexpr uint32_t idesc = idesc_f16_f32(128, BK, false, false);
+                const uint32_t kofs = OFF_K + (j & 1) * TILE;
 #pragma unroll
-            for (int k = 0; k < 32; ++k)
-                if (!last || cb + k <= kmax) mb = fmaxf(mb, __uint_as_float(r[k]));
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t co = (ks >> 2) * CH + (ks & 3) * 32;
+                    umma_bf16(tbase + t * 128, sdesc(sbase + OFF_Q + t * TILE + co, 16, 1024, kSw128),
+                              sdesc(sbase + kofs + co, 16, 1024, kSw128), idesc, ks > 0);
+                }
+                umma_commit(&s_full[t]);
+            };
+            auto pv = [&](int t, int j) {
+                constexpr uint32_t idesc = idesc_bf16_f32(128, D, false, true);
+                const uint32_t vofs = OFF_V + (j & 1) * TILE;
+#pragma unroll
+                for (int ks = 0; ks < BK / 16; ++ks)
+                    umma_tmem_a(tbase + 256 + t * 128, tbase + t * 128 + ks * 8,
+                                sdesc(sbase + vofs + ks * 16 * 128, CH, 1024, kSw128), idesc, (j > 0 || ks > 0) ? 1u : 0u);
+                umma_commit(&pv_done[t]);
+            };
+            bool ok = mbar_wait(&q_ready[0], 0, p.ctl, 53) && mbar_wait(&q_ready[1], 0, p.ctl, 53) &&
+                      mbar_wait(&k_full[0], 0, p.ctl, 54);
+            if (ok) {
+                tc_fence_after();
+                qk(0, 0);
+                qk(1, 0);
+                umma_commit(&k_empty[0]);
+            }
+            for (int j = 0; j < nkb && ok && !aborted(); ++j) {
+                const bool more = j + 1 < nkb;
+                ok = mbar_wait(&v_full[j & 1], (j >> 1) & 1, p.ctl, 55) && mbar_wait(&p_ready[0], j & 1, p.ctl, 56);
+                if (!ok) break;
+                tc_fence_after();
+                pv(0, j);
+                if (more) {
+                    ok = mbar_wait(&k_full[(j + 1) & 1], ((j + 1) >> 1) & 1, p.ctl, 57);
+                    if (!ok) break;
+                    tc_fence_after();
+                    qk(0, j + 1);
+                }
+                ok = mbar_wait(&p_ready[1], j & 1, p.ctl, 58);
+                if (!ok) break;
+                tc_fence_after();
+                pv(1, j);
+                umma_commit(&v_empty[j & 1]);
+                if (more) {
+                    qk(1, j + 1);
+                    umma_commit(&k_empty[(j + 1) & 1]);
+                }
+            }
+            if (!ok) fail();
+            umma_commit(drain);
+            (void)mbar_wait(drain, 0, p.ctl, 59);
         }
-        mb *= p.scale_log2;
-        float m_new = m_run;
-        if (mb > m_run + kTau || m_run == -INFINITY) m_new = mb;
-        const float corr = m_run == -INFINITY ? 0.f : ex2_approx(m_run - m_new);
-        // ---- previous PV must be done: P buffer free, O stable, V stage (kb-1)&1 free
-        if (kb > 0) {
-            ok = __all_sync(0xffffffffu, ok && mbar_wait(bar_pv, (kb - 1) & 1, p.ctl, 25));
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ softmax / epilogue
+        const int t = (warp - 4) >> 2;            // tile of this warpgroup
+        const int row = threadIdx.x - 128 - t * 128;  // tile row = TMEM lane
+        const uint32_t lane_addr = tbase + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+        const uint32_t s_addr = lane_addr + t * 128;
+        const uint32_t o_addr = lane_addr + 256 + t * 128;
+        uint8_t* qt = smem + OFF_Q + t * TILE;
+        const int tt = row / G;
+        const int iq = i0 + t * T + tt;
+        bool ok = __all_sync(0xffffffffu, mbar_wait(q_full, 0, p.ctl, 60));
+        if (ok) {
+            const int pos = iq < p.L ? __ldg(p.pos + static_cast<long long>(b) * p.L + iq) : 0;
+            qk_norm_rope_row<D>(qt, CH, row, p.wq, p.eps, pos, p.rope);
+            fence_async_smem();
+        }
+        mbar_arrive(&q_ready[t]);
+        if (!ok) fail();
+        float m_run = -INFINITY, l_run = 0.f;
+        const float sc = p.scale_log2;
+        for (int j = 0; j < nkb && ok; ++j) {
+            if (aborted() || !__all_sync(0xffffffffu, mbar_wait(&s_full[t], j & 1, p.ctl, 61))) {
+                fail();
+                break;
+            }
             tc_fence_after();
-            if (t == 0 && ok && kb + 1 < nkb) load_v(kb + 1);
-            // rescale O where the running max moved (warp-uniform TMEM access)
-            if (ok && __any_sync(0xffffffffu, m_new != m_run)) {
+            uint32_t r[128];
+            tmem_ld32(s_addr + 0, r);
+            tmem_ld32(s_addr + 32, r + 32);
+            tmem_ld32(s_addr + 64, r + 64);
+            tmem_ld32(s_addr + 96, r + 96);
+            tmem_wait_ld();
+            const bool diag = j == nkb - 1;
+            const int kmax = iq - j * BK;  // last valid key column of this row in the block
+            if (diag) {
+#pragma unroll
+                for (int k = 0; k < 128; ++k)
+                    if (k > kmax) r[k] = __float_as_uint(-INFINITY);
+            }
+            float mx = __uint_as_float(r[0]);
+#pragma unroll
+            for (int k = 1; k < 128; ++k) mx = fmaxf(mx, __uint_as_float(r[k]));
+            const float mb = mx * sc;
+            float m_new = m_run;
+            if (m_run == -INFINITY || mb > m_run + kTau) m_new = mb;
+            const float corr = m_run == -INFINITY ? 0.f : ex2_approx(m_run - m_new);
+            if (j > 0 && __any_sync(0xffffffffu, m_new != m_run)) {
+                // O(j-1) must be complete before it is scaled in place
+                if (!__all_sync(0xffffffffu, mbar_wait(&pv_done[t], (j - 1) & 1, p.ctl, 62))) {
+                    fail();
+                    break;
+                }
+                tc_fence_after();
 #pragma unroll 1
                 for (int cb = 0; cb < D; cb += 32) {
-                    uint32_t r[32];
-                    tmem_ld32(lane_addr + o_col + cb, r);
+                    uint32_t o[32];
+                    tmem_ld32(o_addr + cb, o);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * corr);
-                    tmem_st32(lane_addr + o_col + cb, r);
+                    for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * corr);
+                    tmem_st32(o_addr + cb, o);
                 }
                 tmem_wait_st();
             }
-        }
-        l_run *= corr;
-        m_run = m_new;
-        // ---- P = exp2(S * scale - m) in bf16 -> shared memory (K-major, 128-byte swizzle)
-#pragma unroll 1
-        for (int cb = 0; cb < BK && ok; cb += 32) {
-            uint32_t r[32];
-            tmem_ld32(s_addr + cb, r);
-            tmem_wait_ld();
-            uint32_t pk[16];
+            l_run *= corr;
+            m_run = m_new;
+            const float2 sc2 = make_float2(sc, sc), nm2 = make_float2(-m_run, -m_run);
+            float2 l2 = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int k = 0; k < 32; k += 2) {
-                const float p0 = (!last || cb + k <= kmax) ? ex2_approx(fmaf(__uint_as_float(r[k]), p.scale_log2, -m_run)) : 0.f;
-                const float p1 =
-                    (!last || cb + k + 1 <= kmax) ? ex2_approx(fmaf(__uint_as_float(r[k + 1]), p.scale_log2, -m_run)) : 0.f;
-                pk[k / 2] = pack_bf16x2(p0, p1);
-                l_run += bf16lo(pk[k / 2]) + bf16hi(pk[k / 2]);
-            }
+            for (int cb = 0; cb < 128; cb += 32) {
+                uint32_t pk[16];
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                const int c8 = cb / 8 + q4;
-                *reinterpret_cast<uint4*>(sP + (c8 >> 3) * CH + sw128_off(t, c8 & 7)) =
-                    make_uint4(pk[q4 * 4], pk[q4 * 4 + 1], pk[q4 * 4 + 2], pk[q4 * 4 + 3]);
-            }
-        }
-        if (!ok) *sflag = 0;
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-        ok = *sflag != 0;
-        if (!ok) break;  // uniform: every thread read the same flag after the barrier
-        if (t == 0 && ok) {
-            if (mbar_wait(&bar_v[kb & 1], (kb >> 1) & 1, p.ctl, 26)) {
-                tc_fence_after();
-                constexpr uint32_t idesc = idesc_bf16_f32(128, D, false, true);
-                const uint32_t vofs = OFF_V + (kb & 1) * TILE;
-#pragma unroll
-                for (int ks = 0; ks < BK / 16; ++ks) {
-                    const uint64_t a = sdesc(sbase + OFF_P + (ks >> 2) * CH + (ks & 3) * 32, 16, 1024, kSw128);
-                    const uint64_t bd = sdesc(sbase + vofs + ks * 16 * 128, CH, 1024, kSw128);
-                    umma_bf16(tbase + o_col, a, bd, idesc, (kb > 0 || ks > 0) ? 1u : 0u);
+                for (int k = 0; k < 32; k += 2) {
+                    const float2 x = fma2(make_float2(__uint_as_float(r[cb + k]), __uint_as_float(r[cb + k + 1])), sc2, nm2);
+                    pk[k / 2] = pack_bf16x2(ex2_approx(x.x), ex2_approx(x.y));
+                    l2 = add2(l2, bf2f2(pk[k / 2]));
                 }
-                umma_commit(bar_pv);
-            } else {
-                *sflag = 0;
+                tmem_st16(s_addr + cb / 2, pk);  // P over S (these columns are already in registers)
             }
+            l_run += l2.x + l2.y;
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&p_ready[t]);
         }
-    }
-    // ---- epilogue: O / l -> bf16 -> shared memory (Q buffer) -> TMA store
-    __syncthreads();
-    ok = *sflag != 0;
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_pv, (nkb - 1) & 1, p.ctl, 27));
-    tc_fence_after();
-    if (ok) {
-        const float inv_l = l_run > 0.f ? 1.0f / l_run : 0.f;
+        // ---- epilogue: O / l -> bf16 -> the tile's Q buffer -> TMA store
+        if (ok && !aborted()) ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[t], (nkb - 1) & 1, p.ctl, 63));
+        if (ok) {
+            tc_fence_after();
+            const float inv_l = l_run > 0.f ? 1.0f / l_run : 0.f;
 #pragma unroll 1
-        for (int cb = 0; cb < D; cb += 32) {
-            uint32_t r[32];
-            tmem_ld32(lane_addr + o_col + cb, r);
-            tmem_wait_ld();
+            for (int cb = 0; cb < D; cb += 32) {
+                uint32_t o[32];
+                tmem_ld32(o_addr + cb, o);
+                tmem_wait_ld();
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                uint32_t ou[4];
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    uint32_t ou[4];
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    ou[k] = pack_bf16x2(__uint_as_float(r[q4 * 8 + 2 * k]) * inv_l,
-                                        __uint_as_float(r[q4 * 8 + 2 * k + 1]) * inv_l);
-                const int e0 = cb + q4 * 8;
-                *reinterpret_cast<uint4*>(sQ + (e0 >> 6) * CH + sw128_off(t, (e0 & 63) >> 3)) =
-                    make_uint4(ou[0], ou[1], ou[2], ou[3]);
+                    for (int k = 0; k < 4; ++k)
+                        ou[k] = pack_bf16x2(__uint_as_float(o[q4 * 8 + 2 * k]) * inv_l,
+                                            __uint_as_float(o[q4 * 8 + 2 * k + 1]) * inv_l);
+                    const int e0 = cb + q4 * 8;
+                    *reinterpret_cast<uint4*>(qt + (e0 >> 6) * CH + sw128_off(row, (e0 & 63) >> 3)) =
+                        make_uint4(ou[0], ou[1], ou[2], ou[3]);
+                }
+            }
+            fence_async_smem();
+        }
+        tc_fence_before();
+        mbar_arrive(&out_bar[t]);
+        if (row == 0 && ok && i0 + t * T < p.L) {  // a tile that starts past the end has nothing to store
+            if (mbar_wait(&out_bar[t], 0, p.ctl, 64)) {
+                for (int ch = 0; ch < 2; ++ch) tma_store_4d(&p.tm_out, qt + ch * CH, ch * 64, g * G, i0 + t * T, b);
+                bulk_commit();
+                bulk_wait_all();
+            } else {
+                fail();
             }
         }
+        if (!ok) fail();
     }
-    if (!ok) *sflag = 0;
-    fence_async_smem();
-    tc_fence_before();
     __syncthreads();
-    if (t == 0 && *sflag) {
-        tma_store_4d(&p.tm_out, sQ, 0, g * G, i0, b);
-        tma_store_4d(&p.tm_out, sQ + CH, 64, g * G, i0, b);
-        bulk_commit();
-        bulk_wait_read_all();
-    }
-    if (t == 0 && !*sflag) {
-        // abandoned tile: wait (bounded) for every MMA this thread issued, then give
-        // copies still in flight a millisecond to land before the CTA releases its memory
-        umma_commit(bar_drain);
-        (void)mbar_wait(bar_drain, 0, p.ctl, 28);
-        const unsigned long long t0 = globaltimer_ns();
-        while (globaltimer_ns() - t0 < 1000000ull) {
+    if (aborted() && threadIdx.x == 0) {
+        // abandoned tile: give copies still in flight time to land before memory is released
+        const long long t0 = clock64();
+        while (clock64() - t0 < 4000000ll) {
         }
     }
     tc_fence_after();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tbase, TMEM_COLS);
+    if (warp == 1) tmem_dealloc(tbase, 512);
 }
 
 }  // namespace
@@ -328,8 +351,8 @@ cudaError_t launch_global_prefill(const PrefillParams& p, int d, cudaStream_t s)
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(global_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     if (e != cudaSuccess) return e;
-    const long long ctas = static_cast<long long>(p.B) * p.Hkv * p.n_ltiles;
-    global_attn_kernel<<<static_cast<unsigned>(ctas), 128, SMEM, s>>>(p);
+    const long long ctas = static_cast<long long>(p.B) * p.Hkv * ((p.L + 2 * T - 1) / (2 * T));
+    global_attn_kernel<<<static_cast<unsigned>(ctas), kThreads, SMEM, s>>>(p);
     return cudaGetLastError();
 }
 
