@@ -48,6 +48,15 @@ def test_medium_length_sampled(zg):
     _check(zg, inp, rows, 42, 1e6, "global L8192")
 
 
+def test_large_weights_take_running_maximum(zg):
+    # RMSNorm weights of magnitude ~1.5-4.5 put the score bound far above 50 log2 units, so every
+    # block takes the running row maximum with in-place rescaling of O instead of the bound
+    inp = _synthetic(2, 700, 32, 8, 128, seed=21)
+    inp["wq"] = inp["wq"] * 3.0
+    inp["wk"] = inp["wk"] * 3.0
+    _check(zg, inp, list(range(2 * 700)), 42, 1e6, "global large weights")
+
+
 def test_deterministic(zg):
     inp = {k: v.cuda() for k, v in _synthetic(1, 2000, 32, 8, 128, seed=12).items()}
     a = zg.global_prefill(inp["q"], inp["k"], inp["v"], inp["pos"], inp["wq"], inp["wk"], rotary_dim=42, theta=1e6)

@@ -75,6 +75,16 @@ def test_rotary_dim_zero_and_full(zg):
     _check(zg, inp, list(range(160)), 128, 64, 1e4, "r=d")
 
 
+@pytest.mark.parametrize("Hq,Hkv,d", [(32, 8, 128), (8, 1, 128), (4, 2, 64)])
+def test_large_weights_take_exact_maximum(zg, Hq, Hkv, d):
+    # RMSNorm weights of magnitude ~3-4.5 put the score bound sqrt(d) max|wq| * sqrt(d) max|wk|
+    # far above 50 log2 units, so the softmax takes the two-pass row maximum instead of the bound
+    inp = _synthetic(1, 300, Hq, Hkv, d, seed=77 + d + Hq)
+    inp["wq"] = inp["wq"] * 3.0
+    inp["wk"] = inp["wk"] * 3.0
+    _check(zg, inp, list(range(300)), 128, workloads.rotary_dim_for(d), 1e4, f"large weights {Hq}/{Hkv} d{d}")
+
+
 def test_swa_4k_config(zg):
     c = workloads.SWA_4K
     inp = workloads.prefill_inputs(c)
