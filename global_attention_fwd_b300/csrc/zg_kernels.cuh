@@ -75,7 +75,7 @@ struct DecodeParams {
 };
 
 constexpr int kMaxLayers = 96;
-constexpr int kDecodeSplitLen = 4096;  // keys of a global cache per split
+constexpr int kDecodeSplitLen = 8192;  // keys of a global cache per split
 
 cudaError_t launch_hybrid_decode(const DecodeParams& p, int d, cudaStream_t s);
 size_t decode_workspace_bytes(int NG, int B, int Hq, long long S);
