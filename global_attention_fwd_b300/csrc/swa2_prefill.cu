@@ -17,7 +17,7 @@
 // Warp roles (20 warps):
 //   warp 0      TMA loop (one thread): K slots into the key ring (refilled once the
 //               last QK reading a slot has completed), V slots (after the last PV),
-//               Q tiles into a 3-deep buffer ring, output stores.
+//               Q tiles into a 4-deep buffer ring, output stores.
 //   warp 1      MMA loop (one thread), QK and PV as soon as each is ready (below).
 //               Warp 1 owns TMEM (512 columns).
 //   warps 4-11  RMSNorm + RoPE of the Q tile rows, in place (bf16 -> fp16), two
@@ -26,9 +26,10 @@
 //               the window wraps around the key ring) into one of two TMEM S buffers.
 //   warps 2-3   the same for the K rows of every new slot.
 //   warps 12-15 softmax: exp2 against a bound on the scores, bf16 P written back
-//               over S in TMEM, after which the MMA loop issues O = P V (P read from
-//               TMEM, V MN-major from the ring) and l = P 1 (row sums); the softmax
-//               also fetches the gate tile into the freed Q buffer.
+//               over S in TMEM and the row sums l of that very bf16 P written to
+//               TMEM, after which the MMA loop issues O = P V (P read from TMEM, V
+//               MN-major from the ring); the softmax also fetches the gate tile into
+//               the freed Q buffer.
 //   warps 16-19 epilogue: O / l * sigmoid(gate), in place over the gate tile, which
 //               the TMA loop then stores.
 // Every hand-off is an mbarrier with a bounded wait; a wait that gives up sets
@@ -45,12 +46,12 @@ struct Swa2 {
     static constexpr int NS = WS + 1;         // slots per tile window
     static constexpr int NK = NS * T;         // keys per tile (N of the QK product)
     static constexpr int SLOT2 = T * 128 * (D / 64) * 2;  // bytes of one K slot + one V slot
-    static constexpr int BASE_SMEM = 3 * 128 * 128 * (D / 64) + 4096 + 2 * D * 4;
+    static constexpr int NQB = 4;             // Q / gate / out buffers (4 measured 5% faster than 3)
+    static constexpr int BASE_SMEM = NQB * 128 * 128 * (D / 64) + 2048 + 2 * D * 4;
     static constexpr int SPARE = (232448 - BASE_SMEM) / SLOT2 - (NS + 1);
     static constexpr int R = NS + 1 + (SPARE > 3 ? 3 : SPARE);  // ring slots
     static constexpr int RR = R * T;          // ring rows
     static constexpr int NCH = D / 64;        // 64-element chunks per head row
-    static constexpr int NQB = 3;             // Q / gate / out buffers
     static constexpr uint32_t QCH = 128 * 128;
     static constexpr uint32_t QBUF = QCH * NCH;
     static constexpr uint32_t KCH = RR * 128;
@@ -59,8 +60,7 @@ struct Swa2 {
     static constexpr uint32_t OFF_Q = 0;
     static constexpr uint32_t OFF_K = OFF_Q + NQB * QBUF;
     static constexpr uint32_t OFF_V = OFF_K + RING;
-    static constexpr uint32_t OFF_ONES = OFF_V + RING;  // 2 KB of bf16 1.0: B operand of the row-sum MMA
-    static constexpr uint32_t OFF_BAR = OFF_ONES + 2048;
+    static constexpr uint32_t OFF_BAR = OFF_V + RING;
     static constexpr int NBAR = 4 * NQB + 5 * R + 2 * 3 + 2 + 3;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr uint32_t OFF_W = (OFF_MISC + 16 + 15) / 16 * 16;  // wq [D], wk [D] fp32
@@ -68,8 +68,8 @@ struct Swa2 {
     static constexpr int SCOLS = (NK + 31) / 32 * 32;  // TMEM columns of one S buffer
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr int O_COL = 2 * SCOLS;
-    static constexpr int L_COL = O_COL + D;  // 16 columns: row sums of P (every column the same)
-    static_assert(L_COL + 16 <= 512, "TMEM budget");
+    static constexpr int L_COL = O_COL + D;  // 4 x 8 columns: row sums of P of tiles n mod 4
+    static_assert(L_COL + 32 <= 512, "TMEM budget");
     static_assert(SMEM <= 232448, "shared memory budget");
     static_assert(T % 16 == 0 && NK <= 256, "tile shape");
 };
@@ -188,8 +188,6 @@ __global__ void __launch_bounds__(kThreads, 1) swa2_kernel(const __grid_constant
         tmem_relinquish();
     }
     for (int e = threadIdx.x; e < 2 * D; e += kThreads) wq_s[e] = e < D ? __ldg(p.wq + e) : __ldg(p.wk + e - D);
-    for (int e = threadIdx.x; e < 512; e += kThreads)
-        reinterpret_cast<uint32_t*>(smem + C::OFF_ONES)[e] = 0x3F803F80u;  // bf16 pair (1.0, 1.0)
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -230,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa2_kernel(const __grid_constant
         for (int j = cn - C::WS; j <= (span_last ? cn : cn - C::WS); ++j) umma_commit(&k_empty[j % C::R]);
     };
     // PV(n): O = P V with P read from TMEM (packed bf16, over S buffer n&1) and V from the
-    // ring (MN-major); then l = P 1, the row sums of the very bf16 P the product used.
+    // ring (MN-major).
     auto issue_pv = [&](int n, int cn, bool span_last) {
         const int sb = n & 1;
         const int row0 = ((cn - C::WS) % C::R) * C::T;
@@ -241,11 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa2_kernel(const __grid_constant
             const uint64_t bd = sdesc(sbase + C::OFF_V + row * 128, C::KCH, 1024, kSw128);
             umma_tmem_a(tbase + C::O_COL, tbase + sb * C::SCOLS + ks * 8, bd, idesc_pv, ks > 0);
         }
-        constexpr uint32_t idesc_l = idesc_bf16_f32(128, 16, false, false);
-        const uint64_t ones = sdesc(sbase + C::OFF_ONES, 16, 1024, kSw128);
-#pragma unroll
-        for (int ks = 0; ks < C::NK / 16; ++ks)
-            umma_tmem_a(tbase + C::L_COL, tbase + sb * C::SCOLS + ks * 8, ones, idesc_l, ks > 0);
+
         umma_commit(o_full);
         umma_commit(&s_empty[sb]);
         for (int j = cn - C::WS; j <= (span_last ? cn : cn - C::WS); ++j) umma_commit(&v_empty[j % C::R]);
@@ -255,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa2_kernel(const __grid_constant
         // ------------------------------------------------------------ TMA loop (one thread)
         // Four independent streams, each advanced whenever its next step is possible, so
         // no stream ever waits behind another: K slots (refilled once the last QK reading
-        // them has completed), V slots (after the last PV), Q tiles into the 3-deep buffer
+        // them has completed), V slots (after the last PV), Q tiles into the 4-deep buffer
         // ring, output stores.  A Q buffer takes the next Q tile once the store of the
         // tile that last held it has been read.
         if (lane == 0 && !aborted()) {
@@ -532,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa2_kernel(const __grid_constant
                 mb = (m == -INFINITY ? 0.f : m) * p.scale_log2;
             }
             const float2 nm2 = make_float2(-mb, -mb);
-            // 16 key columns per step; the load of step c+1 is in flight while step c is computed
+            float2 lacc = make_float2(0.f, 0.f);
             auto soft16 = [&](const uint32_t* r, int cb) {
                 uint32_t pk[8];
                 if (cb >= kr_lo && cb + 15 <= kr_hi) {
@@ -551,6 +545,9 @@ __global__ void __launch_bounds__(kThreads, 1) swa2_kernel(const __grid_constant
                         pk[k / 2] = pack_bf16x2(e0, e1);
                     }
                 }
+                // row sums of the very bf16 P the PV product uses
+#pragma unroll
+                for (int k = 0; k < 8; ++k) lacc = add2(lacc, bf2f2(pk[k]));
                 // P (keys cb..cb+15) -> TMEM columns cb/2 .. cb/2+7 of this S buffer (already read)
                 tmem_st8(s_addr + cb / 2, pk);
             };
@@ -566,6 +563,16 @@ __global__ void __launch_bounds__(kThreads, 1) swa2_kernel(const __grid_constant
                 if (cb + 32 < C::NK) tmem_ld16(s_addr + cb + 32, ra);
                 soft16(rb, cb + 16);
                 tmem_wait_ld();
+            }
+            {
+                uint32_t lv[8];
+                const float lsum = lacc.x + lacc.y;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) lv[k] = __float_as_uint(lsum);
+                // l for the epilogue, four tiles deep: slot n & 3 is rewritten only by the
+                // softmax of tile n + 4, whose S needs PV(n + 2), which waits for the
+                // epilogue of tile n + 1 and so for that of tile n
+                tmem_st8(lane_addr + C::L_COL + (n & 3) * 8, lv);
             }
             tmem_wait_st();
             tc_fence_before();
@@ -588,7 +595,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa2_kernel(const __grid_constant
             }
             tc_fence_after();
             uint32_t lraw;
-            tmem_ld1(lane_addr + C::L_COL, lraw);
+            tmem_ld1(lane_addr + C::L_COL + (n & 3) * 8, lraw);
             uint32_t ra[16], rb[16];
             tmem_ld16(lane_addr + C::O_COL, ra);
             tmem_wait_ld();
