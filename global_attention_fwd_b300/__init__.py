@@ -26,6 +26,7 @@ STATUS = {
     -9: "ZG_ERR_UNIMPLEMENTED",
 }
 EXPORTS = ("zg_swa_prefill", "zg_global_prefill_workspace_bytes", "zg_global_prefill",
+           "zg_swa_prefill_with_cache", "zg_global_prefill_with_cache", "zg_kv_cache_write",
            "zg_hybrid_decode_workspace_bytes", "zg_hybrid_decode", "zg_hybrid_decode_noalloc",
            "zg_device_status", "zg_selftest_bounded_wait", "zg_status_string")
 
@@ -48,6 +49,12 @@ def _load() -> ctypes.CDLL:
     lib.zg_global_prefill_workspace_bytes.restype = SZ
     lib.zg_global_prefill.argtypes = [P] * 7 + [I] * 6 + [D, F, P, SZ, P]
     lib.zg_global_prefill.restype = I
+    lib.zg_swa_prefill_with_cache.argtypes = [P] * 8 + [I] * 7 + [D, F, P, P, I, P]
+    lib.zg_swa_prefill_with_cache.restype = I
+    lib.zg_global_prefill_with_cache.argtypes = [P] * 7 + [I] * 6 + [D, F, P, SZ, P, P, I64, P]
+    lib.zg_global_prefill_with_cache.restype = I
+    lib.zg_kv_cache_write.argtypes = [P] * 6 + [I] * 4 + [I64, I, I, D, F, P]
+    lib.zg_kv_cache_write.restype = I
     lib.zg_hybrid_decode_workspace_bytes.argtypes = [I, I, I, I, I64]
     lib.zg_hybrid_decode_workspace_bytes.restype = SZ
     lib.zg_hybrid_decode.argtypes = [P] * 13 + [I] * 5 + [I64, I, I, D, F, P, SZ, P]
@@ -137,6 +144,67 @@ def global_prefill(q, k, v, pos, wq, wk, *, rotary_dim, theta, eps=1e-6, out=Non
                                 ws_bytes, _stream(stream))
     _raise(st, "zg_global_prefill")
     return out
+
+
+def swa_prefill_with_cache(q, k, v, gate, pos, wq, wk, k_ring, v_ring, *, window=128, rotary_dim, theta, eps=1e-6,
+                           out=None, stream=None):
+    """swa_prefill, then this local layer's decode rings: k_ring, v_ring [B,Hkv,W,d] bf16 receive
+    k_hat and v of the last min(L, W) tokens at slot pos mod W (W = k_ring.shape[2])."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (gate, "gate"), (k_ring, "k_ring"), (v_ring, "v_ring")):
+        _check(t, n, torch.bfloat16, 4)
+    _check(pos, "pos", torch.int32, 2)
+    _check(wq, "wq", torch.float32)
+    _check(wk, "wk", torch.float32)
+    B, L, Hq, d = q.shape
+    Hkv = k.shape[2]
+    if out is None:
+        out = torch.empty_like(q)
+    _check(out, "out", torch.bfloat16, 4)
+    st = _lib.zg_swa_prefill_with_cache(_ptr(q), _ptr(k), _ptr(v), _ptr(gate), _ptr(pos), _ptr(wq), _ptr(wk),
+                                        _ptr(out), B, L, Hq, Hkv, d, int(window), int(rotary_dim), float(theta),
+                                        float(eps), _ptr(k_ring), _ptr(v_ring), int(k_ring.shape[2]), _stream(stream))
+    _raise(st, "zg_swa_prefill_with_cache")
+    return out
+
+
+def global_prefill_with_cache(q, k, v, pos, wq, wk, k_cache, v_cache, *, rotary_dim, theta, eps=1e-6, out=None,
+                              workspace=None, stream=None):
+    """global_prefill, then this global layer's decode caches: k_cache, v_cache [B,Hkv,S_max,d] bf16
+    receive k_hat and v of every token at slot pos (S_max = k_cache.shape[2])."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _check(t, n, torch.bfloat16, 4)
+    _check(pos, "pos", torch.int32, 2)
+    _check(wq, "wq", torch.float32)
+    _check(wk, "wk", torch.float32)
+    B, L, Hq, d = q.shape
+    Hkv = k.shape[2]
+    if out is None:
+        out = torch.empty_like(q)
+    _check(out, "out", torch.bfloat16, 4)
+    need = global_prefill_workspace_bytes(B, L, Hkv, d)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = _lib.zg_global_prefill_with_cache(_ptr(q), _ptr(k), _ptr(v), _ptr(pos), _ptr(wq), _ptr(wk), _ptr(out),
+                                           B, L, Hq, Hkv, d, int(rotary_dim), float(theta), float(eps),
+                                           _ptr(workspace), ws_bytes, _ptr(k_cache), _ptr(v_cache),
+                                           int(k_cache.shape[2]), _stream(stream))
+    _raise(st, "zg_global_prefill_with_cache")
+    return out
+
+
+def kv_cache_write(k, v, pos, wk, k_cache, v_cache, *, ring, rotary_dim, theta, eps=1e-6, stream=None):
+    """Decode caches from prefill keys / values: k_cache, v_cache [B,Hkv,S,d] bf16 receive k_hat and v
+    (ring=True: last min(L, S) tokens at slot pos mod S; ring=False: every token at slot pos)."""
+    for t, n in ((k, "k"), (v, "v"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _check(t, n, torch.bfloat16, 4)
+    _check(pos, "pos", torch.int32, 2)
+    _check(wk, "wk", torch.float32)
+    B, L, Hkv, d = k.shape
+    st = _lib.zg_kv_cache_write(_ptr(k), _ptr(v), _ptr(pos), _ptr(wk), _ptr(k_cache), _ptr(v_cache), B, L, Hkv, d,
+                                int(k_cache.shape[2]), 1 if ring else 0, int(rotary_dim), float(theta), float(eps),
+                                _stream(stream))
+    _raise(st, "zg_kv_cache_write")
 
 
 def hybrid_decode_workspace_bytes(NG, B, Hq, d, S_max) -> int:

@@ -95,6 +95,43 @@ zg_status check_prefill(const void* q, const void* k, const void* v, const void*
 }  // namespace
 }  // namespace zg
 
+namespace zg {
+namespace {
+// ---------------------------------------------------------------- prefill + decode caches
+// host checks of the cache arguments (done before anything is launched)
+zg_status check_cache(const zg_bf16* ck, const zg_bf16* cv, int d, long long S) {
+    if (!ck || !cv) return ZG_ERR_NULL;
+    if (!aligned16(ck) || !aligned16(cv)) return ZG_ERR_ALIGN;
+    if (S < 1) return ZG_ERR_SHAPE;
+    if (d != 128) return ZG_ERR_UNSUPPORTED;  // the decode step reads d = 128 caches
+    return ZG_OK;
+}
+zg_status write_cache(const zg_bf16* k, const zg_bf16* v, const int32_t* pos, const float* wk, zg_bf16* ck,
+                      zg_bf16* cv, int B, int L, int Hkv, int d, long long S, bool ring, int rotary_dim, double theta,
+                      float eps, zg_stream stream) {
+    if (B == 0 || L == 0) return ZG_OK;
+    CacheParams c;
+    std::memset(&c, 0, sizeof(c));
+    if (!dev_ctl(c.ctl)) return ZG_ERR_CUDA;
+    c.k = reinterpret_cast<const __nv_bfloat16*>(k);
+    c.v = reinterpret_cast<const __nv_bfloat16*>(v);
+    c.pos = pos;
+    c.wk = wk;
+    c.cache_k = reinterpret_cast<__nv_bfloat16*>(ck);
+    c.cache_v = reinterpret_cast<__nv_bfloat16*>(cv);
+    c.B = B;
+    c.L = L;
+    c.Hkv = Hkv;
+    c.S = S;
+    c.ring = ring ? 1 : 0;
+    c.i0 = ring && L > S ? static_cast<int>(L - S) : 0;
+    c.eps = eps;
+    if (!rope_consts(c.rope, rotary_dim, theta)) return ZG_ERR_SHAPE;
+    return launch_kv_cache(c, d, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? ZG_OK : ZG_ERR_CUDA;
+}
+}  // namespace
+}  // namespace zg
+
 using namespace zg;
 
 extern "C" {
@@ -180,6 +217,43 @@ zg_status zg_global_prefill(const zg_bf16* q, const zg_bf16* k, const zg_bf16* v
     return launch_global_prefill(p, d, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? ZG_OK : ZG_ERR_CUDA;
 }
 
+zg_status zg_kv_cache_write(const zg_bf16* k, const zg_bf16* v, const int32_t* pos, const float* wk,
+                            zg_bf16* k_cache, zg_bf16* v_cache, int B, int L, int Hkv, int d, int64_t S, int ring,
+                            int rotary_dim, double theta, float eps, zg_stream stream) {
+    if (!k || !v || !pos || !wk) return ZG_ERR_NULL;
+    if (!aligned16(k) || !aligned16(v) || !aligned16(pos) || !aligned16(wk)) return ZG_ERR_ALIGN;
+    zg_status st = check_cache(k_cache, v_cache, d, S);
+    if (st != ZG_OK) return st;
+    if (B < 0 || L < 0 || Hkv <= 0 || (ring != 0 && ring != 1)) return ZG_ERR_SHAPE;
+    if (rotary_dim < 0 || rotary_dim > d || (rotary_dim & 1) || !(theta > 0.0) || !(eps >= 0.0f)) return ZG_ERR_SHAPE;
+    if (static_cast<long long>(B) * L * Hkv / 8 >= (1ll << 31)) return ZG_ERR_UNSUPPORTED;
+    return write_cache(k, v, pos, wk, k_cache, v_cache, B, L, Hkv, d, S, ring != 0, rotary_dim, theta, eps, stream);
+}
+
+zg_status zg_swa_prefill_with_cache(const zg_bf16* q, const zg_bf16* k, const zg_bf16* v, const zg_bf16* gate,
+                                    const int32_t* pos, const float* wq, const float* wk, zg_bf16* out, int B, int L,
+                                    int Hq, int Hkv, int d, int window, int rotary_dim, double theta, float eps,
+                                    zg_bf16* k_ring, zg_bf16* v_ring, int ring_slots, zg_stream stream) {
+    zg_status st = check_cache(k_ring, v_ring, d, ring_slots);
+    if (st != ZG_OK) return st;
+    st = zg_swa_prefill(q, k, v, gate, pos, wq, wk, out, B, L, Hq, Hkv, d, window, rotary_dim, theta, eps, stream);
+    if (st != ZG_OK) return st;
+    return write_cache(k, v, pos, wk, k_ring, v_ring, B, L, Hkv, d, ring_slots, true, rotary_dim, theta, eps, stream);
+}
+
+zg_status zg_global_prefill_with_cache(const zg_bf16* q, const zg_bf16* k, const zg_bf16* v, const int32_t* pos,
+                                       const float* wq, const float* wk, zg_bf16* out, int B, int L, int Hq, int Hkv,
+                                       int d, int rotary_dim, double theta, float eps, void* workspace,
+                                       size_t workspace_bytes, zg_bf16* k_cache, zg_bf16* v_cache, int64_t S_max,
+                                       zg_stream stream) {
+    zg_status st = check_cache(k_cache, v_cache, d, S_max);
+    if (st != ZG_OK) return st;
+    st = zg_global_prefill(q, k, v, pos, wq, wk, out, B, L, Hq, Hkv, d, rotary_dim, theta, eps, workspace,
+                           workspace_bytes, stream);
+    if (st != ZG_OK) return st;
+    return write_cache(k, v, pos, wk, k_cache, v_cache, B, L, Hkv, d, S_max, false, rotary_dim, theta, eps, stream);
+}
+
 size_t zg_hybrid_decode_workspace_bytes(int NG, int B, int Hq, int d, int64_t S_max) {
     if (NG <= 0 || B <= 0 || Hq <= 0 || d <= 0 || S_max <= 0) return 0;
     (void)d;
@@ -258,7 +332,8 @@ zg_status zg_device_status(uint32_t* detail) {
     if (cudaMemcpyFromSymbol(&w, g_err_word, sizeof(w)) != cudaSuccess) return ZG_ERR_CUDA;
     if (w && cudaMemcpyToSymbol(g_err_word, &zero, sizeof(zero)) != cudaSuccess) return ZG_ERR_CUDA;
     if (detail) *detail = w;
-    return w ? ZG_ERR_DEVICE_TIMEOUT : ZG_OK;
+    if (!w) return ZG_OK;
+    return (w & 0xFFu) == kErrPosition ? ZG_ERR_POSITION : ZG_ERR_DEVICE_TIMEOUT;
 }
 
 zg_status zg_selftest_bounded_wait(uint64_t limit_ns, zg_stream stream) {

@@ -1,0 +1,63 @@
+// kv_cache.cu -- the decode caches a prefill leaves behind.
+//
+// "ZGCM-1-7B 完全解説" (gotosocial explainer), section "アーキテクチャ": a local
+// (sliding-window) layer keeps the keys and values of the most recent 128 tokens,
+// a global layer those of the whole sequence; the decode step reads exactly these
+// caches.  Keys are stored as the decode step uses them: normalised and rotated
+// (k_hat = RoPE(RMSNorm(k; wk, eps), pos)), rounded to bf16; values are stored raw.
+//
+// One warp per (sequence b, token i, KV head g) row of the tokens a layer keeps:
+//   global layer: every token, slot pos[b, i] of an S-slot cache (0 <= pos < S);
+//   local layer:  the last min(L, S) tokens, slot pos[b, i] mod S of an S-slot ring.
+// A row whose position has no slot (negative, or >= S in a global cache) is not
+// written and is reported in the device error word (code kErrPosition).
+#include "zg_qk.cuh"
+
+namespace zg {
+namespace {
+
+constexpr int D = 128;
+
+__global__ void __launch_bounds__(256) kv_cache_kernel(const __grid_constant__ CacheParams p) {
+    __shared__ float buf[8][D];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n_keep = p.L - p.i0;
+    const long long row = static_cast<long long>(blockIdx.x) * 8 + warp;  // (b, i - i0, g) flattened
+    if (row >= static_cast<long long>(p.B) * n_keep * p.Hkv) return;
+    const int g = static_cast<int>(row % p.Hkv);
+    const long long bt = row / p.Hkv;
+    const int b = static_cast<int>(bt / n_keep);
+    const int i = p.i0 + static_cast<int>(bt % n_keep);
+    const long long src = (static_cast<long long>(b) * p.L + i) * p.Hkv + g;  // row of k / v
+    const int pos = __ldg(p.pos + static_cast<long long>(b) * p.L + i);
+    long long slot;
+    if (p.ring) {
+        slot = pos >= 0 ? pos % p.S : -1;
+    } else {
+        slot = (pos >= 0 && pos < p.S) ? pos : -1;
+    }
+    if (slot < 0) {
+        if (lane == 0) report(p.ctl, 80, kErrPosition);
+        return;
+    }
+    const long long dst = ((static_cast<long long>(b) * p.Hkv + g) * p.S + slot) * D;
+    norm_rope_warp(p.k + src * D, p.wk, p.eps, pos, p.rope, 1.0f, buf[warp]);
+    const float4 kv = *reinterpret_cast<const float4*>(&buf[warp][lane * 4]);
+    uint2 ko;
+    ko.x = pack_bf16x2(kv.x, kv.y);
+    ko.y = pack_bf16x2(kv.z, kv.w);
+    *reinterpret_cast<uint2*>(p.cache_k + dst + lane * 4) = ko;
+    *reinterpret_cast<uint2*>(p.cache_v + dst + lane * 4) = *reinterpret_cast<const uint2*>(p.v + src * D + lane * 4);
+}
+
+}  // namespace
+
+cudaError_t launch_kv_cache(const CacheParams& p, int d, cudaStream_t s) {
+    if (d != D) return cudaErrorInvalidValue;
+    const long long rows = static_cast<long long>(p.B) * (p.L - p.i0) * p.Hkv;
+    if (rows <= 0) return cudaSuccess;
+    kv_cache_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace zg

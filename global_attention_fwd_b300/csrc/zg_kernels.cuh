@@ -80,6 +80,25 @@ constexpr int kDecodeSplitLen = 8192;  // keys of a global cache per split
 cudaError_t launch_hybrid_decode(const DecodeParams& p, int d, cudaStream_t s);
 size_t decode_workspace_bytes(int NG, int B, int Hq, long long S);
 
+// ---------------------------------------------------------------- decode caches from a prefill
+struct CacheParams {
+    const __nv_bfloat16* k;  // [B, L, Hkv, d]
+    const __nv_bfloat16* v;  // [B, L, Hkv, d]
+    const int32_t* pos;      // [B, L]
+    const float* wk;         // [d]
+    __nv_bfloat16* cache_k;  // [B, Hkv, S, d]: k_hat
+    __nv_bfloat16* cache_v;  // [B, Hkv, S, d]: v
+    int B, L, Hkv;
+    long long S;  // slots: S_max of a global cache, or the ring size
+    int ring;     // 1: ring (slot = pos mod S, last min(L, S) tokens); 0: slot = pos
+    int i0;       // first token written
+    float eps;
+    RopeConsts rope;
+    DevCtl ctl;
+};
+
+cudaError_t launch_kv_cache(const CacheParams& p, int d, cudaStream_t s);
+
 // bounded-wait self test: waits on a barrier nothing arrives on
 cudaError_t launch_wait_selftest(DevCtl ctl, cudaStream_t s);
 

@@ -14,7 +14,7 @@ namespace zg {
 // ----------------------------------------------------------- device errors
 // Error word: 0 = fine; otherwise (site << 8) | code.  Written once per launch
 // by the first failing thread (atomicCAS), read and cleared by the host.
-enum DeviceErr : uint32_t { kErrTimeout = 1, kErrAlign = 2, kErrTmem = 3 };
+enum DeviceErr : uint32_t { kErrTimeout = 1, kErrAlign = 2, kErrTmem = 3, kErrPosition = 4 };
 
 struct DevCtl {
     uint32_t* err_word;      // device pointer to the error word

@@ -39,7 +39,8 @@
  *   - Device-side waits are bounded (ZG_WAIT_LIMIT_NS in the environment,
  *     default 4 s).  A wait that runs out records itself in a device error
  *     word; zg_device_status() synchronises the device and returns
- *     ZG_ERR_DEVICE_TIMEOUT (or ZG_OK) and clears the word.
+ *     ZG_ERR_DEVICE_TIMEOUT (or ZG_ERR_POSITION for a cache position without a
+ *     slot, or ZG_OK) and clears the word.
  *   - The library allocates no device memory in these calls; scratch memory
  *     comes from a caller-provided workspace (global prefill, decode).
  */
@@ -100,6 +101,53 @@ zg_status zg_global_prefill(const zg_bf16 *q, const zg_bf16 *k, const zg_bf16 *v
                             int B, int L, int Hq, int Hkv, int d, int rotary_dim,
                             double theta, float eps, void *workspace, size_t workspace_bytes,
                             zg_stream stream);
+
+/*
+ * Prefill that also leaves the decode caches of its layer behind ("ZGCM-1-7B 完全解説",
+ * section "アーキテクチャ": local layers keep the most recent 128 tokens, global layers
+ * the whole sequence).  Each call runs the prefill above (same arguments, same output)
+ * and then writes, for its layer, the caches zg_hybrid_decode reads:
+ *   k cache slot = bf16(RoPE(RMSNorm(k[b,i,g]; wk, eps), pos[b,i]))   (k_hat)
+ *   v cache slot = v[b,i,g]
+ * zg_swa_prefill_with_cache: k_ring, v_ring are one local layer's rings
+ *   [B, Hkv, ring_slots, d] bf16; the last min(L, ring_slots) tokens of every
+ *   sequence go to slot pos[b,i] mod ring_slots (ring_slots = the decode window, 128
+ *   for ZGCM-1; the last ring_slots positions must differ mod ring_slots, as
+ *   consecutive positions do).  Other slots are left untouched.
+ * zg_global_prefill_with_cache: k_cache, v_cache are one global layer's caches
+ *   [B, Hkv, S_max, d] bf16; every token goes to slot pos[b,i], 0 <= pos < S_max.
+ * Only d = 128 (the decode step's head size) is supported: ZG_ERR_UNSUPPORTED
+ * otherwise.  The cache pointers must be 16-byte aligned and are written in place.
+ * A token whose position has no slot (negative, or >= S_max for a global cache) is
+ * skipped and recorded on the device: zg_device_status() then returns
+ * ZG_ERR_POSITION.  The pages define no interface; these calls follow the cache
+ * layout of zg_hybrid_decode.
+ */
+/*
+ * zg_kv_cache_write -- the cache writing of the two calls above on its own: for
+ * every sequence b and token i (ring = 1: the last min(L, S) tokens, slot
+ * pos[b,i] mod S; ring = 0: every token, slot pos[b,i], 0 <= pos < S) it stores
+ * k_hat (bf16) in k_cache and v in v_cache, [B, Hkv, S, d] bf16 each.
+ * k, v [B, L, Hkv, d] bf16; pos [B, L] int32; wk [d] float; d = 128.
+ * Errors as for the calls above; positions without a slot are skipped and
+ * reported through zg_device_status() as ZG_ERR_POSITION.
+ */
+zg_status zg_kv_cache_write(const zg_bf16 *k, const zg_bf16 *v, const int32_t *pos, const float *wk,
+                            zg_bf16 *k_cache, zg_bf16 *v_cache, int B, int L, int Hkv, int d,
+                            int64_t S, int ring, int rotary_dim, double theta, float eps,
+                            zg_stream stream);
+zg_status zg_swa_prefill_with_cache(const zg_bf16 *q, const zg_bf16 *k, const zg_bf16 *v,
+                                    const zg_bf16 *gate, const int32_t *pos, const float *wq,
+                                    const float *wk, zg_bf16 *out, int B, int L, int Hq, int Hkv,
+                                    int d, int window, int rotary_dim, double theta, float eps,
+                                    zg_bf16 *k_ring, zg_bf16 *v_ring, int ring_slots,
+                                    zg_stream stream);
+zg_status zg_global_prefill_with_cache(const zg_bf16 *q, const zg_bf16 *k, const zg_bf16 *v,
+                                       const int32_t *pos, const float *wq, const float *wk,
+                                       zg_bf16 *out, int B, int L, int Hq, int Hkv, int d,
+                                       int rotary_dim, double theta, float eps, void *workspace,
+                                       size_t workspace_bytes, zg_bf16 *k_cache, zg_bf16 *v_cache,
+                                       int64_t S_max, zg_stream stream);
 
 /*
  * Bytes of workspace zg_hybrid_decode needs for these sizes (0 when there is

@@ -92,3 +92,52 @@ def test_status_strings(zg):
     for s in range(-9, 1):
         assert zg.lib.zg_status_string(s)
     assert zg.lib.zg_status_string(-8) == b"device-side wait timed out"
+
+
+def _swa_cache(zg, **kw):
+    a = dict(q=A, k=A, v=A, gate=A, pos=A, wq=A, wk=A, out=A, B=1, L=16, Hq=32, Hkv=8, d=128, window=128,
+             rot=42, theta=1e6, eps=1e-6, kr=A, vr=A, slots=128)
+    a.update(kw)
+    return zg.lib.zg_swa_prefill_with_cache(a["q"], a["k"], a["v"], a["gate"], a["pos"], a["wq"], a["wk"], a["out"],
+                                            a["B"], a["L"], a["Hq"], a["Hkv"], a["d"], a["window"], a["rot"],
+                                            a["theta"], a["eps"], a["kr"], a["vr"], a["slots"], None)
+
+
+def _glob_cache(zg, **kw):
+    a = dict(q=A, k=A, v=A, pos=A, wq=A, wk=A, out=A, B=1, L=16, Hq=32, Hkv=8, d=128, rot=42, theta=1e6, eps=1e-6,
+             ws=A, ws_bytes=1 << 30, kc=A, vc=A, smax=4096)
+    a.update(kw)
+    return zg.lib.zg_global_prefill_with_cache(a["q"], a["k"], a["v"], a["pos"], a["wq"], a["wk"], a["out"], a["B"],
+                                               a["L"], a["Hq"], a["Hkv"], a["d"], a["rot"], a["theta"], a["eps"],
+                                               a["ws"], a["ws_bytes"], a["kc"], a["vc"], a["smax"], None)
+
+
+def test_prefill_with_cache_rejects_bad_cache_arguments_before_launch(zg):
+    # cache arguments are checked first; nothing (not even the prefill) is launched on failure
+    assert _swa_cache(zg, kr=None) == -1
+    assert _swa_cache(zg, vr=A + 4) == -2
+    assert _swa_cache(zg, slots=0) == -3
+    assert _swa_cache(zg, d=64, rot=20) == -4      # decode caches have d = 128
+    assert _swa_cache(zg, q=None) == -1            # then the prefill's own checks
+    assert _swa_cache(zg, window=0) == -3
+    assert _glob_cache(zg, vc=None) == -1
+    assert _glob_cache(zg, kc=A + 8) == -2
+    assert _glob_cache(zg, smax=0) == -3
+    assert _glob_cache(zg, ws=None) == -6
+    assert _glob_cache(zg, Hq=24) == -4
+
+
+def test_kv_cache_write_rejects_bad_arguments(zg):
+    def call(**kw):
+        a = dict(k=A, v=A, pos=A, wk=A, kc=A, vc=A, B=1, L=16, Hkv=8, d=128, S=128, ring=1, rot=42, theta=1e6,
+                 eps=1e-6)
+        a.update(kw)
+        return zg.lib.zg_kv_cache_write(a["k"], a["v"], a["pos"], a["wk"], a["kc"], a["vc"], a["B"], a["L"], a["Hkv"],
+                                        a["d"], a["S"], a["ring"], a["rot"], a["theta"], a["eps"], None)
+    assert call(k=None) == -1
+    assert call(kc=None) == -1
+    assert call(pos=A + 4) == -2
+    assert call(S=0) == -3
+    assert call(ring=2) == -3
+    assert call(rot=43) == -3
+    assert call(d=64, rot=20) == -4
