@@ -95,6 +95,10 @@ def decode_bytes(c):  # caches read once (global 0..p, rings all slots), new-tok
     return cache + tok
 
 
+def kv_cache_bytes(c):  # per (token, KV head) row: read k, v and the position, write k_hat, v
+    return c.B * c.L * c.Hkv * (4 * c.d * 2 + 4)
+
+
 class Clocks:
     """Samples SM clocks and throttle reasons with nvidia-smi while the timed region runs."""
 
@@ -351,6 +355,34 @@ def run_gpu(args):
                "sample": f"{args.cpu_rows} consecutive query rows x 32 heads of the gated-SWA 256K workload "
                          f"(rows 131072.., fp64 C oracle, {dt:.1f} s); tokens/s = rows/s"}
 
+    # ---- decode caches from a prefill (outside the step): the global 64K layer's k_hat / v
+    kc = torch.empty((GLB.B, GLB.Hkv, GLB.L, GLB.d), dtype=torch.bfloat16, device=dev)
+    vc = torch.empty_like(kc)
+
+    def kv_write():
+        zg.kv_cache_write(gx["k"], gx["v"], gx["pos"], gx["wk"], kc, vc, ring=False, rotary_dim=GLB.rotary_dim,
+                          theta=GLB.theta, eps=GLB.eps)
+
+    for _ in range(2):
+        kv_write()
+    kv_ev = []
+    for _ in range(5):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        kv_write()
+        b.record(stream)
+        kv_ev.append((a, b))
+    torch.cuda.synchronize()
+    st, detail = zg.device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} detail {detail:#x} after the cache writes")
+    kv_t = statistics.median(a.elapsed_time(b) for a, b in kv_ev) * 1e-3
+    kv_bytes = kv_cache_bytes(GLB)
+    kvc = {"workload": f"global layer caches of {GLB.name} ({GLB.B * GLB.L * GLB.Hkv} rows)", "us": kv_t * 1e6,
+           "roofline": {"bound": "hbm", "achieved": kv_bytes / kv_t / 1e9, "peak": hbm, "unit": "GB/s",
+                        "frac": kv_bytes / kv_t / 1e9 / hbm, "traffic": None, "algorithmic_bytes": kv_bytes}}
+
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
@@ -364,6 +396,7 @@ def run_gpu(args):
         "gpu_launches": args.steps * sum(n for _, _, n in parts),
         "clocks": clocks,
         "parts": {
+            "kv_cache_write": kvc,
             "swa_prefill": {"workload": SWA.name, "ms": sw_t * 1e3, "tokens_per_s": SWA.tokens / sw_t,
                             "roofline": rl_swa},
             "hybrid_decode": {"workload": DEC.name, "us_per_step": dc_t * 1e6, "roofline": rl_dec},
