@@ -381,7 +381,8 @@ def run_gpu(args):
     kv_bytes = kv_cache_bytes(GLB)
     kvc = {"workload": f"global layer caches of {GLB.name} ({GLB.B * GLB.L * GLB.Hkv} rows)", "us": kv_t * 1e6,
            "roofline": {"bound": "hbm", "achieved": kv_bytes / kv_t / 1e9, "peak": hbm, "unit": "GB/s",
-                        "frac": kv_bytes / kv_t / 1e9 / hbm, "traffic": None, "algorithmic_bytes": kv_bytes}}
+                        "frac": kv_bytes / kv_t / 1e9 / hbm, "traffic": _traffic("kv_cache_kernel"),
+                        "algorithmic_bytes": kv_bytes}}
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
@@ -435,6 +436,15 @@ def run_profile_case(args):
         def fn():
             zg.global_prefill(x["q"], x["k"], x["v"], x["pos"], x["wq"], x["wk"], rotary_dim=c.rotary_dim,
                               theta=c.theta, out=out, workspace=ws)
+    elif kind == "kvcache":
+        c = workloads.PrefillCase("kv_cache_B1_L65536_profile", 4, 1, 65536, 32, 8, 128, 0, 42, 1e6, False)
+        x = workloads.prefill_inputs_device(c, dev)
+        kc = torch.empty((c.B, c.Hkv, c.L, c.d), dtype=torch.bfloat16, device=dev)
+        vc = torch.empty_like(kc)
+
+        def fn():
+            zg.kv_cache_write(x["k"], x["v"], x["pos"], x["wk"], kc, vc, ring=False, rotary_dim=c.rotary_dim,
+                              theta=c.theta)
     else:
         c = workloads.DecodeCase("hybrid_decode_B1_p131071_profile", 5, 1, 32, (5, 11, 17, 23, 29), 32, 8, 128,
                                  131072, 128, 131071, 42, 1e6)
@@ -465,7 +475,7 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=4096)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--profile-case", choices=["swa", "global", "decode"], default=None,
+    ap.add_argument("--profile-case", choices=["swa", "global", "decode", "kvcache"], default=None,
                     help="run only a small case of one kernel (for ncu captures)")
     args = ap.parse_args()
     if args.profile_case:
