@@ -161,6 +161,21 @@ def _dist():
     return ws, rank, local
 
 
+def max_over_ranks(values, device):
+    """Element-wise maximum of `values` over every rank of the job (identity for one process)."""
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist = torch.distributed
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_tokens_per_s(ws: int, tokens: int, steps: int, ms: float) -> float:
+    """Whole-job throughput: each of the ws ranks processes `tokens` per step (weak scaling);
+    the time is the slowest rank's."""
+    return ws * tokens * steps / (ms * 1e-3)
+
+
 # ---------------------------------------------------------------- oracle arm
 def oracle_sample(rows: int, nthreads=None, seed_salt=0):
     """Time the fp64 oracle on `rows` consecutive gated-SWA rows (all heads) from the middle of
@@ -291,12 +306,8 @@ def run_gpu(args):
     total_ms = t_start.elapsed_time(t_end)
     part_ms = {name: [a.elapsed_time(b) for a, b in ev[name]] for name in ev}
     swa_ms = sum(part_ms["swa_prefill"])
-    # max over ranks
-    vals = torch.tensor([total_ms, swa_ms], dtype=torch.float64, device=dev)
-    if ws > 1:
-        torch.distributed.all_reduce(vals, op=torch.distributed.ReduceOp.MAX)
-    total_ms, swa_ms = vals.tolist()
-    value = ws * SWA.tokens * args.steps / (swa_ms * 1e-3)
+    total_ms, swa_ms = max_over_ranks([total_ms, swa_ms], dev)
+    value = job_tokens_per_s(ws, SWA.tokens, args.steps, swa_ms)
 
     # ---- rooflines per part (average launch durations on this stream)
     def avg(name):
