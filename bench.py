@@ -95,6 +95,10 @@ def decode_bytes(c):  # caches read once (global 0..p, rings all slots), new-tok
     return cache + tok
 
 
+def layer_gemm_flops(c, hidden):  # q/k/v/g projections and o_proj of one layer
+    return 2.0 * c.B * c.L * hidden * (3 * c.Hq + 2 * c.Hkv) * c.d
+
+
 def kv_cache_bytes(c):  # per (token, KV head) row: read k, v and the position, write k_hat, v
     return c.B * c.L * c.Hkv * (4 * c.d * 2 + 4)
 
@@ -395,6 +399,48 @@ def run_gpu(args):
                         "frac": kv_bytes / kv_t / 1e9 / hbm, "traffic": _traffic("kv_cache_kernel"),
                         "algorithmic_bytes": kv_bytes}}
 
+    # ---- a whole gated SWA layer from hidden states (outside the step): the 4K configuration's
+    # shapes with hidden = Hq * d, synthetic weights
+    C2 = workloads.SWA_4K
+    hid = C2.Hq * C2.d
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1000 * C2.cfg_id + 9)
+    mk = lambda *shape, scale=1.0: (torch.randn(*shape, generator=gen, device=dev) * scale).to(torch.bfloat16)
+    lh = mk(C2.B, C2.L, hid)
+    lw = [mk(hid, n, scale=hid ** -0.5) for n in (C2.Hq * C2.d, C2.Hkv * C2.d, C2.Hkv * C2.d, C2.Hq * C2.d)]
+    lwo = mk(C2.Hq * C2.d, hid, scale=(C2.Hq * C2.d) ** -0.5)
+    lpos = torch.arange(C2.L, dtype=torch.int32, device=dev).repeat(C2.B, 1).contiguous()
+    lnq = torch.ones(C2.d, dtype=torch.float32, device=dev)
+    ly = torch.empty_like(lh)
+    lws = torch.empty(zg.gated_swa_layer_workspace_bytes(C2.B, C2.L, C2.Hq, C2.Hkv, C2.d), dtype=torch.uint8,
+                      device=dev)
+
+    def layer():
+        zg.gated_swa_layer(lh, lw[0], lw[1], lw[2], lw[3], lwo, lpos, lnq, lnq, Hq=C2.Hq, Hkv=C2.Hkv, window=C2.window,
+                           rotary_dim=C2.rotary_dim, theta=C2.theta, out=ly, workspace=lws)
+
+    for _ in range(3):
+        layer()
+    l_ev = []
+    for _ in range(5):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        layer()
+        b.record(stream)
+        l_ev.append((a, b))
+    torch.cuda.synchronize()
+    st, detail = zg.device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} detail {detail:#x} after the layer")
+    l_t = statistics.median(a.elapsed_time(b) for a, b in l_ev) * 1e-3
+    l_fl = layer_gemm_flops(C2, hid)
+    lay = {"workload": f"{C2.name} hidden {hid}", "ms": l_t * 1e3, "tokens_per_s": C2.B * C2.L / l_t,
+           "roofline": {"bound": "tensor", "achieved": l_fl / l_t / 1e12, "peak": peaks["bf16_tflops"],
+                        "unit": "TFLOP/s", "frac": l_fl / l_t / 1e12 / peaks["bf16_tflops"], "traffic": None,
+                        "algorithmic_flops": l_fl,
+                        "note": "projection GEMM flops only; the attention inside is HBM-bound"}}
+
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
@@ -408,6 +454,7 @@ def run_gpu(args):
         "gpu_launches": args.steps * sum(n for _, _, n in parts),
         "clocks": clocks,
         "parts": {
+            "gated_swa_layer": lay,
             "kv_cache_write": kvc,
             "swa_prefill": {"workload": SWA.name, "ms": sw_t * 1e3, "tokens_per_s": SWA.tokens / sw_t,
                             "roofline": rl_swa},

@@ -27,6 +27,7 @@ STATUS = {
 }
 EXPORTS = ("zg_swa_prefill", "zg_global_prefill_workspace_bytes", "zg_global_prefill",
            "zg_swa_prefill_with_cache", "zg_global_prefill_with_cache", "zg_kv_cache_write",
+           "zg_gated_swa_layer_workspace_bytes", "zg_gated_swa_layer",
            "zg_hybrid_decode_workspace_bytes", "zg_hybrid_decode", "zg_hybrid_decode_noalloc",
            "zg_device_status", "zg_selftest_bounded_wait", "zg_status_string")
 
@@ -55,6 +56,10 @@ def _load() -> ctypes.CDLL:
     lib.zg_global_prefill_with_cache.restype = I
     lib.zg_kv_cache_write.argtypes = [P] * 6 + [I] * 4 + [I64, I, I, D, F, P]
     lib.zg_kv_cache_write.restype = I
+    lib.zg_gated_swa_layer_workspace_bytes.argtypes = [I] * 5
+    lib.zg_gated_swa_layer_workspace_bytes.restype = SZ
+    lib.zg_gated_swa_layer.argtypes = [P] * 10 + [I] * 8 + [D, F, P, SZ, P]
+    lib.zg_gated_swa_layer.restype = I
     lib.zg_hybrid_decode_workspace_bytes.argtypes = [I, I, I, I, I64]
     lib.zg_hybrid_decode_workspace_bytes.restype = SZ
     lib.zg_hybrid_decode.argtypes = [P] * 13 + [I] * 5 + [I64, I, I, D, F, P, SZ, P]
@@ -205,6 +210,37 @@ def kv_cache_write(k, v, pos, wk, k_cache, v_cache, *, ring, rotary_dim, theta, 
                                 int(k_cache.shape[2]), 1 if ring else 0, int(rotary_dim), float(theta), float(eps),
                                 _stream(stream))
     _raise(st, "zg_kv_cache_write")
+
+
+def gated_swa_layer_workspace_bytes(B, L, Hq, Hkv, d) -> int:
+    return int(_lib.zg_gated_swa_layer_workspace_bytes(int(B), int(L), int(Hq), int(Hkv), int(d)))
+
+
+def gated_swa_layer(h, w_q, w_k, w_v, w_g, w_o, pos, wq, wk, *, Hq, Hkv, window=128, rotary_dim, theta, eps=1e-6,
+                    out=None, workspace=None, stream=None):
+    """A whole gated SWA layer: y = o_proj(A_SWA(q, k, v) * sigmoid(g_proj(h))).
+    h [B,L,hidden] bf16; w_q, w_g [hidden, Hq*d], w_k, w_v [hidden, Hkv*d], w_o [Hq*d, hidden] bf16
+    (y = x W); pos [B,L] int32; wq, wk [d] float32.  Returns y [B,L,hidden] bf16."""
+    _check(h, "h", torch.bfloat16, 3)
+    for t, n in ((w_q, "w_q"), (w_k, "w_k"), (w_v, "w_v"), (w_g, "w_g"), (w_o, "w_o")):
+        _check(t, n, torch.bfloat16, 2)
+    _check(pos, "pos", torch.int32, 2)
+    _check(wq, "wq", torch.float32)
+    _check(wk, "wk", torch.float32)
+    B, L, hidden = h.shape
+    d = w_q.shape[1] // Hq
+    if out is None:
+        out = torch.empty_like(h)
+    _check(out, "out", torch.bfloat16, 3)
+    need = gated_swa_layer_workspace_bytes(B, L, Hq, Hkv, d)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=h.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = _lib.zg_gated_swa_layer(_ptr(h), _ptr(w_q), _ptr(w_k), _ptr(w_v), _ptr(w_g), _ptr(w_o), _ptr(pos), _ptr(wq),
+                                 _ptr(wk), _ptr(out), B, L, hidden, int(Hq), int(Hkv), d, int(window), int(rotary_dim),
+                                 float(theta), float(eps), _ptr(workspace), ws_bytes, _stream(stream))
+    _raise(st, "zg_gated_swa_layer")
+    return out
 
 
 def hybrid_decode_workspace_bytes(NG, B, Hq, d, S_max) -> int:

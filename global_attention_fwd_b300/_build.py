@@ -7,13 +7,14 @@ import subprocess
 HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libzgattn.so")
-SOURCES = ["api.cu", "swa_prefill.cu", "swa2_prefill.cu", "global_prefill.cu", "hybrid_decode.cu", "selftest.cu", "noalloc.cu", "kv_cache.cu"]
+SOURCES = ["api.cu", "swa_prefill.cu", "swa2_prefill.cu", "global_prefill.cu", "hybrid_decode.cu", "selftest.cu", "noalloc.cu", "kv_cache.cu", "layer.cu"]
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",
     "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "-shared",
     "-cudart", "shared", "-Xlinker", "-rpath,/usr/local/cuda/lib64",
     "--expt-relaxed-constexpr",
+    "-lcublasLt",
 ]
 
 

@@ -254,6 +254,71 @@ zg_status zg_global_prefill_with_cache(const zg_bf16* q, const zg_bf16* k, const
     return write_cache(k, v, pos, wk, k_cache, v_cache, B, L, Hkv, d, S_max, false, rotary_dim, theta, eps, stream);
 }
 
+// ---------------------------------------------------------------- whole gated SWA layer
+namespace {
+struct LayerWs {
+    size_t q, k, v, g, a, lt, total;
+};
+LayerWs layer_ws(long long B, long long L, long long Hq, long long Hkv, long long d) {
+    auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+    LayerWs w;
+    const size_t tq = static_cast<size_t>(B * L * Hq * d) * 2, tk = static_cast<size_t>(B * L * Hkv * d) * 2;
+    w.q = 0;
+    w.k = w.q + up(tq);
+    w.v = w.k + up(tk);
+    w.g = w.v + up(tk);
+    w.a = w.g + up(tq);
+    w.lt = w.a + up(tq);
+    w.total = w.lt + layer_gemm_workspace_bytes();
+    return w;
+}
+}  // namespace
+
+size_t zg_gated_swa_layer_workspace_bytes(int B, int L, int Hq, int Hkv, int d) {
+    if (B <= 0 || L <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0) return 0;
+    return layer_ws(B, L, Hq, Hkv, d).total;
+}
+
+zg_status zg_gated_swa_layer(const zg_bf16* h, const zg_bf16* w_q, const zg_bf16* w_k, const zg_bf16* w_v,
+                             const zg_bf16* w_g, const zg_bf16* w_o, const int32_t* pos, const float* wq,
+                             const float* wk, zg_bf16* y, int B, int L, int hidden, int Hq, int Hkv, int d,
+                             int window, int rotary_dim, double theta, float eps, void* workspace,
+                             size_t workspace_bytes, zg_stream stream) {
+    if (!h || !w_q || !w_k || !w_v || !w_g || !w_o || !y) return ZG_ERR_NULL;
+    if (!aligned16(h) || !aligned16(w_q) || !aligned16(w_k) || !aligned16(w_v) || !aligned16(w_g) ||
+        !aligned16(w_o) || !aligned16(y))
+        return ZG_ERR_ALIGN;
+    if (hidden <= 0 || hidden % 8) return ZG_ERR_SHAPE;  // rows of 16-byte multiples for the GEMMs
+    // the attention's own checks, on stand-in pointers (the real q/k/v/gate live in the workspace)
+    const zg_bf16* stand_in = h;
+    zg_status st = check_prefill(stand_in, stand_in, stand_in, stand_in, true, pos, wq, wk, y, B, L, Hq, Hkv, d,
+                                 rotary_dim, theta, eps);
+    if (st != ZG_OK) return st;
+    if (window < 1) return ZG_ERR_SHAPE;
+    const int G = Hq / Hkv;
+    if ((d != 64 && d != 128) || (G != 1 && G != 2 && G != 4 && G != 8) || window > 128 || Hkv > 65535)
+        return ZG_ERR_UNSUPPORTED;
+    if (B == 0 || L == 0) return ZG_OK;
+    const LayerWs w = layer_ws(B, L, Hq, Hkv, d);
+    if (!workspace || workspace_bytes < w.total || !aligned16(workspace)) return ZG_ERR_WORKSPACE;
+    uint8_t* base = static_cast<uint8_t*>(workspace);
+    zg_bf16 *q = reinterpret_cast<zg_bf16*>(base + w.q), *k = reinterpret_cast<zg_bf16*>(base + w.k),
+            *v = reinterpret_cast<zg_bf16*>(base + w.v), *g = reinterpret_cast<zg_bf16*>(base + w.g),
+            *a = reinterpret_cast<zg_bf16*>(base + w.a);
+    void* lt = base + w.lt;
+    const size_t lt_bytes = layer_gemm_workspace_bytes();
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const long long M = static_cast<long long>(B) * L;
+    if (!layer_gemm(h, w_q, q, M, static_cast<long long>(Hq) * d, hidden, lt, lt_bytes, s) ||
+        !layer_gemm(h, w_k, k, M, static_cast<long long>(Hkv) * d, hidden, lt, lt_bytes, s) ||
+        !layer_gemm(h, w_v, v, M, static_cast<long long>(Hkv) * d, hidden, lt, lt_bytes, s) ||
+        !layer_gemm(h, w_g, g, M, static_cast<long long>(Hq) * d, hidden, lt, lt_bytes, s))
+        return ZG_ERR_CUDA;
+    st = zg_swa_prefill(q, k, v, g, pos, wq, wk, a, B, L, Hq, Hkv, d, window, rotary_dim, theta, eps, stream);
+    if (st != ZG_OK) return st;
+    return layer_gemm(a, w_o, y, M, hidden, static_cast<long long>(Hq) * d, lt, lt_bytes, s) ? ZG_OK : ZG_ERR_CUDA;
+}
+
 size_t zg_hybrid_decode_workspace_bytes(int NG, int B, int Hq, int d, int64_t S_max) {
     if (NG <= 0 || B <= 0 || Hq <= 0 || d <= 0 || S_max <= 0) return 0;
     (void)d;

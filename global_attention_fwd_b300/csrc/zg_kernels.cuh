@@ -99,6 +99,12 @@ struct CacheParams {
 
 cudaError_t launch_kv_cache(const CacheParams& p, int d, cudaStream_t s);
 
+// ---------------------------------------------------------------- whole layer (plain GEMMs on cuBLASLt)
+size_t layer_gemm_workspace_bytes();
+// Y[M x N] = X[M x K] W[K x N], bf16 row-major, fp32 accumulate; false on any cuBLASLt failure
+bool layer_gemm(const void* X, const void* W, void* Y, long long M, long long N, long long K, void* ws,
+                size_t ws_bytes, cudaStream_t s);
+
 // bounded-wait self test: waits on a barrier nothing arrives on
 cudaError_t launch_wait_selftest(DevCtl ctl, cudaStream_t s);
 

@@ -218,6 +218,30 @@ zg_status zg_hybrid_decode_noalloc(const zg_bf16 *q, const zg_bf16 *k_new, const
                                    int NL, int B, int Hq, int Hkv, int d, int64_t S_max, int window, int rotary_dim,
                                    double theta, float eps, zg_stream stream);
 
+/*
+ * A whole gated sliding-window attention layer from the hidden states ("ZGCM-1-7B
+ * 完全解説", section "アーキテクチャ"; hyper.ai summary of arXiv 2609.13356, section
+ * "方法"): y = o_proj(A_SWA(q, k, v) ⊙ σ(g_proj(h))), with q, k, v and the gate
+ * logits projected in parallel from the normalised hidden state h:
+ *   q = h W_q, k = h W_k, v = h W_v, g = h W_g;  a = A_SWA(q, k, v) ⊙ σ(g)
+ *   (zg_swa_prefill, QK RMSNorm with wq / wk and partial RoPE);  y = a W_o.
+ * h [B, L, hidden] bf16; W_q, W_g [hidden, Hq*d], W_k, W_v [hidden, Hkv*d],
+ * W_o [Hq*d, hidden], all bf16 row-major with the input dimension first (y = x W);
+ * y [B, L, hidden] bf16.  Projections accumulate in fp32 and round q, k, v, g and a
+ * to bf16 (the attention's own input and output precision).  The five GEMMs run on
+ * cuBLASLt; hidden must be a multiple of 8.  Other shape limits as zg_swa_prefill.
+ *   workspace: device scratch of at least zg_gated_swa_layer_workspace_bytes()
+ *        bytes, 16-byte aligned (q, k, v, g, a and the GEMMs' workspace);
+ *        ZG_ERR_WORKSPACE if missing or too small.  ZG_ERR_CUDA if a GEMM fails.
+ */
+size_t zg_gated_swa_layer_workspace_bytes(int B, int L, int Hq, int Hkv, int d);
+zg_status zg_gated_swa_layer(const zg_bf16 *h, const zg_bf16 *w_q, const zg_bf16 *w_k,
+                             const zg_bf16 *w_v, const zg_bf16 *w_g, const zg_bf16 *w_o,
+                             const int32_t *pos, const float *wq, const float *wk, zg_bf16 *y,
+                             int B, int L, int hidden, int Hq, int Hkv, int d, int window,
+                             int rotary_dim, double theta, float eps, void *workspace,
+                             size_t workspace_bytes, zg_stream stream);
+
 /* Synchronise the current device, return ZG_ERR_DEVICE_TIMEOUT if a device wait
  * gave up since the last call (and clear that record), ZG_ERR_CUDA if the
  * device reports an error, else ZG_OK.  *detail (may be NULL) receives the raw

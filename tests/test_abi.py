@@ -141,3 +141,23 @@ def test_kv_cache_write_rejects_bad_arguments(zg):
     assert call(ring=2) == -3
     assert call(rot=43) == -3
     assert call(d=64, rot=20) == -4
+
+
+def test_gated_swa_layer_rejects_bad_arguments(zg):
+    def call(**kw):
+        a = dict(h=A, wq_=A, wk_=A, wv_=A, wg_=A, wo_=A, pos=A, wq=A, wk=A, y=A, B=1, L=16, hidden=4096, Hq=32, Hkv=8,
+                 d=128, window=128, rot=42, theta=1e6, eps=1e-6, ws=A, ws_bytes=1 << 40)
+        a.update(kw)
+        return zg.lib.zg_gated_swa_layer(a["h"], a["wq_"], a["wk_"], a["wv_"], a["wg_"], a["wo_"], a["pos"], a["wq"],
+                                         a["wk"], a["y"], a["B"], a["L"], a["hidden"], a["Hq"], a["Hkv"], a["d"],
+                                         a["window"], a["rot"], a["theta"], a["eps"], a["ws"], a["ws_bytes"], None)
+    assert call(wo_=None) == -1
+    assert call(pos=None) == -1
+    assert call(wg_=A + 2) == -2
+    assert call(hidden=4100) == -3
+    assert call(Hq=30) == -3
+    assert call(window=0) == -3
+    assert call(d=96, rot=20) == -4
+    assert call(ws=None) == -6
+    assert call(ws_bytes=1024) == -6
+    assert zg.gated_swa_layer_workspace_bytes(1, 16, 32, 8, 128) > 32 << 20
