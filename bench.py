@@ -95,6 +95,30 @@ def decode_bytes(c):  # caches read once (global 0..p, rings all slots), new-tok
     return cache + tok
 
 
+FP32_PEAK_TFLOPS = 148 * 128 * 2 * 2.032e9 / 1e12  # fp32 FMA lanes x 2 flop x maximum SM clock
+
+
+def window_pairs(c) -> int:
+    """(query, key) pairs one head of one sequence attends: sum over i of min(i + 1, W)."""
+    W = c.window if 0 < c.window < c.L else c.L
+    return W * (W + 1) // 2 + (c.L - W) * W
+
+
+def backward_flops(c) -> float:
+    """Algorithmic backward FLOPs: per (query head, key) pair the score, dA . v, and the dq, dk, dv
+    updates, each a d-long multiply-add: 10 d."""
+    return 10.0 * c.d * window_pairs(c) * c.B * c.Hq
+
+
+def backward_bytes(c) -> int:
+    """HBM bytes a fused backward must move: q, gate, dout in (bf16) and dq, dgate out (fp32) per query
+    row; k, v in (bf16) and dk, dv out (fp32) per key row; positions."""
+    per_tok = c.Hq * c.d * (3 * 2 + (2 if c.gated else 1) * 4) + c.Hkv * c.d * (2 * 2 + 2 * 4) + 4
+    if not c.gated:
+        per_tok -= c.Hq * c.d * 2
+    return c.B * c.L * per_tok
+
+
 def layer_gemm_flops(c, hidden):  # q/k/v/g projections and o_proj of one layer
     return 2.0 * c.B * c.L * hidden * (3 * c.Hq + 2 * c.Hkv) * c.d
 
@@ -441,6 +465,40 @@ def run_gpu(args):
                         "algorithmic_flops": l_fl,
                         "note": "projection GEMM flops only; the attention inside is HBM-bound"}}
 
+    # ---- backward of the gated SWA prefill (outside the step): the 4K training shape
+    bx = workloads.prefill_inputs_device(C2, dev)
+    bdout = torch.randn(C2.B, C2.L, C2.Hq, C2.d, generator=gen, device=dev).to(torch.bfloat16)
+    bws = torch.empty(zg.attention_backward_workspace_bytes(C2.B, C2.L, C2.Hq, C2.Hkv, C2.d), dtype=torch.uint8,
+                      device=dev)
+
+    def backward():
+        return zg.attention_backward(bx["q"], bx["k"], bx["v"], bx["gate"], bx["pos"], bx["wq"], bx["wk"], bdout,
+                                     window=C2.window, rotary_dim=C2.rotary_dim, theta=C2.theta, eps=C2.eps,
+                                     workspace=bws)
+
+    for _ in range(3):
+        backward()
+    b_ev = []
+    for _ in range(5):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        backward()
+        b.record(stream)
+        b_ev.append((a, b))
+    torch.cuda.synchronize()
+    st, detail = zg.device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} detail {detail:#x} after the backward pass")
+    b_t = statistics.median(a.elapsed_time(b) for a, b in b_ev) * 1e-3
+    b_fl = backward_flops(C2)
+    fp32_peak = FP32_PEAK_TFLOPS
+    bwd = {"workload": f"{C2.name} backward (dq, dk, dv, dgate)", "ms": b_t * 1e3, "tokens_per_s": C2.tokens / b_t,
+           "roofline": {"bound": "alu", "achieved": b_fl / b_t / 1e12, "peak": fp32_peak, "unit": "TFLOP/s",
+                        "frac": b_fl / b_t / 1e12 / fp32_peak, "traffic": None, "algorithmic_flops": b_fl,
+                        "peak_note": "fp32 FMA: 148 SMs x 128 lanes x 2 flop x 2032 MHz (nominal units and clock)"},
+           "hbm_bytes": backward_bytes(C2)}
+
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
@@ -456,6 +514,7 @@ def run_gpu(args):
         "parts": {
             "gated_swa_layer": lay,
             "kv_cache_write": kvc,
+            "attention_backward": bwd,
             "swa_prefill": {"workload": SWA.name, "ms": sw_t * 1e3, "tokens_per_s": SWA.tokens / sw_t,
                             "roofline": rl_swa},
             "hybrid_decode": {"workload": DEC.name, "us_per_step": dc_t * 1e6, "roofline": rl_dec},
@@ -503,6 +562,16 @@ def run_profile_case(args):
         def fn():
             zg.kv_cache_write(x["k"], x["v"], x["pos"], x["wk"], kc, vc, ring=False, rotary_dim=c.rotary_dim,
                               theta=c.theta)
+    elif kind == "backward":
+        c = workloads.PrefillCase("swa_backward_B1_L4096_profile", 2, 1, 4096, 32, 8, 128, 128, 42, 1e4, True)
+        x = workloads.prefill_inputs_device(c, dev)
+        dout = torch.randn(c.B, c.L, c.Hq, c.d, device=dev).to(torch.bfloat16)
+        ws = torch.empty(zg.attention_backward_workspace_bytes(c.B, c.L, c.Hq, c.Hkv, c.d), dtype=torch.uint8,
+                         device=dev)
+
+        def fn():
+            zg.attention_backward(x["q"], x["k"], x["v"], x["gate"], x["pos"], x["wq"], x["wk"], dout, window=128,
+                                  rotary_dim=c.rotary_dim, theta=c.theta, workspace=ws)
     else:
         c = workloads.DecodeCase("hybrid_decode_B1_p131071_profile", 5, 1, 32, (5, 11, 17, 23, 29), 32, 8, 128,
                                  131072, 128, 131071, 42, 1e6)
@@ -533,7 +602,7 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=4096)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--profile-case", choices=["swa", "global", "decode", "kvcache"], default=None,
+    ap.add_argument("--profile-case", choices=["swa", "global", "decode", "kvcache", "backward"], default=None,
                     help="run only a small case of one kernel (for ncu captures)")
     args = ap.parse_args()
     if args.profile_case:

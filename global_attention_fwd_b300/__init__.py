@@ -28,6 +28,7 @@ STATUS = {
 EXPORTS = ("zg_swa_prefill", "zg_global_prefill_workspace_bytes", "zg_global_prefill",
            "zg_swa_prefill_with_cache", "zg_global_prefill_with_cache", "zg_kv_cache_write",
            "zg_gated_swa_layer_workspace_bytes", "zg_gated_swa_layer",
+           "zg_attention_backward_workspace_bytes", "zg_attention_backward",
            "zg_hybrid_decode_workspace_bytes", "zg_hybrid_decode", "zg_hybrid_decode_noalloc",
            "zg_device_status", "zg_selftest_bounded_wait", "zg_status_string")
 
@@ -60,6 +61,10 @@ def _load() -> ctypes.CDLL:
     lib.zg_gated_swa_layer_workspace_bytes.restype = SZ
     lib.zg_gated_swa_layer.argtypes = [P] * 10 + [I] * 8 + [D, F, P, SZ, P]
     lib.zg_gated_swa_layer.restype = I
+    lib.zg_attention_backward_workspace_bytes.argtypes = [I] * 5
+    lib.zg_attention_backward_workspace_bytes.restype = SZ
+    lib.zg_attention_backward.argtypes = [P] * 12 + [I] * 7 + [D, F, P, SZ, P]
+    lib.zg_attention_backward.restype = I
     lib.zg_hybrid_decode_workspace_bytes.argtypes = [I, I, I, I, I64]
     lib.zg_hybrid_decode_workspace_bytes.restype = SZ
     lib.zg_hybrid_decode.argtypes = [P] * 13 + [I] * 5 + [I64, I, I, D, F, P, SZ, P]
@@ -241,6 +246,40 @@ def gated_swa_layer(h, w_q, w_k, w_v, w_g, w_o, pos, wq, wk, *, Hq, Hkv, window=
                                  float(theta), float(eps), _ptr(workspace), ws_bytes, _stream(stream))
     _raise(st, "zg_gated_swa_layer")
     return out
+
+
+def attention_backward_workspace_bytes(B, L, Hq, Hkv, d) -> int:
+    return int(_lib.zg_attention_backward_workspace_bytes(int(B), int(L), int(Hq), int(Hkv), int(d)))
+
+
+def attention_backward(q, k, v, gate, pos, wq, wk, dout, *, window, rotary_dim, theta, eps=1e-6, workspace=None,
+                       stream=None):
+    """Gradients of sum(out * dout) for the prefill out = swa_prefill(...) (gate given, window >= 1) or
+    global_prefill(...) (gate None, window <= 0).  Inputs as the forward takes them, dout [B,L,Hq,d] bf16.
+    Returns (dq, dk, dv, dgate) as float32 tensors, dgate None without a gate."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (dout, "dout")):
+        _check(t, n, torch.bfloat16, 4)
+    if gate is not None:
+        _check(gate, "gate", torch.bfloat16, 4)
+    _check(pos, "pos", torch.int32, 2)
+    _check(wq, "wq", torch.float32)
+    _check(wk, "wk", torch.float32)
+    B, L, Hq, d = q.shape
+    Hkv = k.shape[2]
+    dq = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+    dk = torch.empty(k.shape, dtype=torch.float32, device=q.device)
+    dv = torch.empty(v.shape, dtype=torch.float32, device=q.device)
+    dgate = torch.empty(q.shape, dtype=torch.float32, device=q.device) if gate is not None else None
+    need = attention_backward_workspace_bytes(B, L, Hq, Hkv, d)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = _lib.zg_attention_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(gate), _ptr(pos), _ptr(wq), _ptr(wk), _ptr(dout),
+                                    _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dgate), B, L, Hq, Hkv, d, int(window),
+                                    int(rotary_dim), float(theta), float(eps), _ptr(workspace), ws_bytes,
+                                    _stream(stream))
+    _raise(st, "zg_attention_backward")
+    return dq, dk, dv, dgate
 
 
 def hybrid_decode_workspace_bytes(NG, B, Hq, d, S_max) -> int:

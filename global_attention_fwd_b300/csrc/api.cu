@@ -319,6 +319,64 @@ zg_status zg_gated_swa_layer(const zg_bf16* h, const zg_bf16* w_q, const zg_bf16
     return layer_gemm(a, w_o, y, M, hidden, static_cast<long long>(Hq) * d, lt, lt_bytes, s) ? ZG_OK : ZG_ERR_CUDA;
 }
 
+// ---------------------------------------------------------------- attention backward
+size_t zg_attention_backward_workspace_bytes(int B, int L, int Hq, int Hkv, int d) {
+    if (B <= 0 || L <= 0 || Hq <= 0 || Hkv <= 0 || d != 128) return 0;
+    return backward_workspace_bytes(B, L, Hq, Hkv);
+}
+
+zg_status zg_attention_backward(const zg_bf16* q, const zg_bf16* k, const zg_bf16* v, const zg_bf16* gate,
+                                const int32_t* pos, const float* wq, const float* wk, const zg_bf16* dout, float* dq,
+                                float* dk, float* dv, float* dgate, int B, int L, int Hq, int Hkv, int d, int window,
+                                int rotary_dim, double theta, float eps, void* workspace, size_t workspace_bytes,
+                                zg_stream stream) {
+    const bool gated = gate != nullptr;
+    if (!q || !k || !v || !pos || !wq || !wk || !dout || !dq || !dk || !dv || (gated && !dgate)) return ZG_ERR_NULL;
+    if (!gated && dgate) return ZG_ERR_SHAPE;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || (gated && !aligned16(gate)) || !aligned16(pos) ||
+        !aligned16(wq) || !aligned16(wk) || !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
+        (gated && !aligned16(dgate)))
+        return ZG_ERR_ALIGN;
+    if (B < 0 || L < 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || Hq % Hkv) return ZG_ERR_SHAPE;
+    if (rotary_dim < 0 || rotary_dim > d || (rotary_dim & 1) || !(theta > 0.0) || !(eps >= 0.0f)) return ZG_ERR_SHAPE;
+    if (d != 128) return ZG_ERR_UNSUPPORTED;
+    if (B == 0 || L == 0) return ZG_OK;
+    if (static_cast<long long>(B) * L * (Hq + Hkv) / 8 >= (1ll << 31)) return ZG_ERR_UNSUPPORTED;
+    const size_t need = backward_workspace_bytes(B, L, Hq, Hkv);
+    if (!workspace || workspace_bytes < need || !aligned16(workspace)) return ZG_ERR_WORKSPACE;
+    BackwardParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.q = reinterpret_cast<const __nv_bfloat16*>(q);
+    p.k = reinterpret_cast<const __nv_bfloat16*>(k);
+    p.v = reinterpret_cast<const __nv_bfloat16*>(v);
+    p.gate = reinterpret_cast<const __nv_bfloat16*>(gate);
+    p.dout = reinterpret_cast<const __nv_bfloat16*>(dout);
+    p.pos = pos;
+    p.wq = wq;
+    p.wk = wk;
+    p.dq = dq;
+    p.dk = dk;
+    p.dv = dv;
+    p.dgate = dgate;
+    const size_t rq = static_cast<size_t>(B) * L * Hq * d, rk = static_cast<size_t>(B) * L * Hkv * d;
+    float* f = static_cast<float*>(workspace);
+    p.qh = f;
+    p.da = f + rq;
+    p.dqh = f + 2 * rq;
+    p.kh = f + 3 * rq;
+    p.dkh = f + 3 * rq + rk;
+    p.stat = f + 3 * rq + 2 * rk;
+    p.B = B;
+    p.L = L;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.window = window > 0 ? window : 0;
+    p.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
+    p.eps = eps;
+    if (!rope_consts(p.rope, rotary_dim, theta)) return ZG_ERR_SHAPE;
+    return launch_backward(p, d, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? ZG_OK : ZG_ERR_CUDA;
+}
+
 size_t zg_hybrid_decode_workspace_bytes(int NG, int B, int Hq, int d, int64_t S_max) {
     if (NG <= 0 || B <= 0 || Hq <= 0 || d <= 0 || S_max <= 0) return 0;
     (void)d;

@@ -99,6 +99,37 @@ struct CacheParams {
 
 cudaError_t launch_kv_cache(const CacheParams& p, int d, cudaStream_t s);
 
+// ---------------------------------------------------------------- attention backward (gated SWA or global)
+struct BackwardParams {
+    const __nv_bfloat16* q;     // [B, L, Hq, d]
+    const __nv_bfloat16* k;     // [B, L, Hkv, d]
+    const __nv_bfloat16* v;     // [B, L, Hkv, d]
+    const __nv_bfloat16* gate;  // [B, L, Hq, d] or null (no gate)
+    const __nv_bfloat16* dout;  // [B, L, Hq, d]
+    const int32_t* pos;         // [B, L]
+    const float* wq;            // [d]
+    const float* wk;            // [d]
+    float* dq;                  // [B, L, Hq, d]
+    float* dk;                  // [B, L, Hkv, d]
+    float* dv;                  // [B, L, Hkv, d]
+    float* dgate;               // [B, L, Hq, d] (only with a gate)
+    // workspace regions (fp32)
+    float* qh;    // [B, L, Hq, d]   q_hat
+    float* kh;    // [B, L, Hkv, d]  k_hat
+    float* da;    // [B, L, Hq, d]   dA
+    float* dqh;   // [B, L, Hq, d]   dq_hat
+    float* dkh;   // [B, L, Hkv, d]  dk_hat
+    float* stat;  // [B, L, Hq, 3]   row max, 1 / row sum, D = dA . A
+    int B, L, Hq, Hkv;
+    int window;   // <= 0: every earlier key (global layer)
+    float scale;  // 1 / sqrt(d)
+    float eps;
+    RopeConsts rope;
+};
+
+size_t backward_workspace_bytes(int B, int L, int Hq, int Hkv);
+cudaError_t launch_backward(const BackwardParams& p, int d, cudaStream_t s);
+
 // ---------------------------------------------------------------- whole layer (plain GEMMs on cuBLASLt)
 size_t layer_gemm_workspace_bytes();
 // Y[M x N] = X[M x K] W[K x N], bf16 row-major, fp32 accumulate; false on any cuBLASLt failure

@@ -242,6 +242,36 @@ zg_status zg_gated_swa_layer(const zg_bf16 *h, const zg_bf16 *w_q, const zg_bf16
                              int rotary_dim, double theta, float eps, void *workspace,
                              size_t workspace_bytes, zg_stream stream);
 
+/* Gradients of the attention prefill: the backward pass of zg_swa_prefill (gate
+ * given, window >= 1) or of zg_global_prefill (gate NULL, window <= 0), the
+ * training workload the pages run at 4K ("ZGCM-1-7B 完全解説", gotosocial
+ * explainer, section "アーキテクチャ", for the forward it differentiates).
+ * With q_hat = RoPE(RMSNorm(q; wq, eps), pos), k_hat likewise, p_ij the softmax
+ * over the window of q_hat_i . k_hat_j / sqrt(d), A_i = sum_j p_ij v_j and
+ * out_i = A_i * sigmoid(gate_i) (out_i = A_i without a gate), it returns the
+ * gradients of sum(out * dout) with respect to q, k, v and gate.  The gradients
+ * of the RMSNorm weights wq, wk are not computed.
+ *   q, gate, dout: [B, L, Hq, d] bf16;  k, v: [B, L, Hkv, d] bf16;  pos [B, L]
+ *        int32;  wq, wk [d] fp32 — the forward's own inputs, layouts as there.
+ *   window: keys i - window < j <= i; <= 0 means every j <= i.  Any window
+ *        and either gate setting may be combined.
+ *   dq, dgate: [B, L, Hq, d] fp32;  dk, dv: [B, L, Hkv, d] fp32, written in full
+ *        (not accumulated).  dgate must be NULL exactly when gate is.
+ *   d must be 128 (ZG_ERR_UNSUPPORTED otherwise); Hq a multiple of Hkv.
+ *   Scores are recomputed from q_hat, k_hat in fp32; nothing of the forward is
+ *   reused.  All pointers device memory, 16-byte aligned, owned by the caller.
+ *   workspace: at least zg_attention_backward_workspace_bytes() bytes, 16-byte
+ *        aligned (fp32 q_hat, k_hat, dA, dq_hat, dk_hat and three floats per
+ *        query row); ZG_ERR_WORKSPACE if missing or too small.
+ */
+size_t zg_attention_backward_workspace_bytes(int B, int L, int Hq, int Hkv, int d);
+zg_status zg_attention_backward(const zg_bf16 *q, const zg_bf16 *k, const zg_bf16 *v,
+                                const zg_bf16 *gate, const int32_t *pos, const float *wq,
+                                const float *wk, const zg_bf16 *dout, float *dq, float *dk,
+                                float *dv, float *dgate, int B, int L, int Hq, int Hkv, int d,
+                                int window, int rotary_dim, double theta, float eps,
+                                void *workspace, size_t workspace_bytes, zg_stream stream);
+
 /* Synchronise the current device, return ZG_ERR_DEVICE_TIMEOUT if a device wait
  * gave up since the last call (and clear that record), ZG_ERR_CUDA if the
  * device reports an error, else ZG_OK.  *detail (may be NULL) receives the raw

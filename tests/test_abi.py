@@ -161,3 +161,30 @@ def test_gated_swa_layer_rejects_bad_arguments(zg):
     assert call(ws=None) == -6
     assert call(ws_bytes=1024) == -6
     assert zg.gated_swa_layer_workspace_bytes(1, 16, 32, 8, 128) > 32 << 20
+
+
+def test_attention_backward_rejects_bad_arguments(zg):
+    def call(**kw):
+        a = dict(q=A, k=A, v=A, gate=A, pos=A, wq=A, wk=A, dout=A, dq=A, dk=A, dv=A, dg=A, B=1, L=16, Hq=32, Hkv=8,
+                 d=128, window=128, rot=42, theta=1e4, eps=1e-6, ws=A, ws_bytes=1 << 40)
+        a.update(kw)
+        return zg.lib.zg_attention_backward(a["q"], a["k"], a["v"], a["gate"], a["pos"], a["wq"], a["wk"], a["dout"],
+                                            a["dq"], a["dk"], a["dv"], a["dg"], a["B"], a["L"], a["Hq"], a["Hkv"],
+                                            a["d"], a["window"], a["rot"], a["theta"], a["eps"], a["ws"],
+                                            a["ws_bytes"], None)
+    assert call(dout=None) == -1
+    assert call(dv=None) == -1
+    assert call(dg=None) == -1            # a gate needs its gradient
+    assert call(gate=None) == -3          # and no gate, no gate gradient
+    assert call(dq=A + 4) == -2
+    assert call(gate=A + 8) == -2
+    assert call(Hq=30) == -3
+    assert call(rot=41) == -3
+    assert call(eps=-1.0) == -3
+    assert call(d=64, rot=20) == -4
+    assert call(ws=None) == -6
+    assert call(ws_bytes=1024) == -6
+    assert call(B=0) == 0 and call(L=0) == 0  # nothing to do, nothing launched
+    # fp32 q_hat, dA, dq_hat per query row, k_hat, dk_hat per key row, three floats per query row
+    assert zg.attention_backward_workspace_bytes(2, 16, 32, 8, 128) == 4 * (2 * 16 * (32 * 128 * 3 + 32 * 3 + 8 * 128 * 2))
+    assert zg.attention_backward_workspace_bytes(2, 16, 32, 8, 64) == 0

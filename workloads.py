@@ -6,7 +6,8 @@ the CUDA side (tests, bench), so both see bit-identical bf16 inputs.
 
 Recipe (the same for every consumer):
   * a CPU ``torch.Generator`` seeded with ``1000 * config + stream`` where the
-    stream is q:1, k:2, v:3, gate:4, w_q:5, w_k:6, outlier mask:7, row sample:8;
+    stream is q:1, k:2, v:3, gate:4, w_q:5, w_k:6, outlier mask:7, row sample:8,
+    output gradient (backward pass):9;
   * values are drawn in float32 and cast to bf16 with round-to-nearest-even;
     the bf16 tensor is the ground truth handed to both sides;
   * activations ~ N(0, 1); QK-norm weights ~ U[0.5, 1.5] in float32;
@@ -23,7 +24,7 @@ from dataclasses import dataclass, field
 
 import torch
 
-STREAM = {"q": 1, "k": 2, "v": 3, "gate": 4, "wq": 5, "wk": 6, "outlier": 7, "rows": 8}
+STREAM = {"q": 1, "k": 2, "v": 3, "gate": 4, "wq": 5, "wk": 6, "outlier": 7, "rows": 8, "dout": 9}
 _CHUNK = 1 << 24  # elements drawn per generator call (fixed, so chunking never changes values)
 
 
@@ -130,6 +131,11 @@ def prefill_inputs(c: PrefillCase, salt: int = 0) -> dict:
     pos = torch.arange(c.L, dtype=torch.int32).repeat(c.B, 1).contiguous()
     return dict(q=q, k=k, v=v, gate=gate, pos=pos,
                 wq=norm_weights(c.d, c.cfg_id, "wq", salt=salt), wk=norm_weights(c.d, c.cfg_id, "wk", salt=salt))
+
+
+def backward_dout(c: PrefillCase, salt: int = 0) -> torch.Tensor:
+    """The output gradient a backward pass of case c receives: [B, L, Hq, d] bf16 ~ N(0, 1)."""
+    return _randn_bf16((c.B, c.L, c.Hq, c.d), _gen(c.cfg_id, "dout", salt))
 
 
 def edge_rows(L: int) -> list:
