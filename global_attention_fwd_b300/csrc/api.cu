@@ -344,6 +344,47 @@ zg_status zg_attention_backward(const zg_bf16* q, const zg_bf16* k, const zg_bf1
     if (static_cast<long long>(B) * L * (Hq + Hkv) / 8 >= (1ll << 31)) return ZG_ERR_UNSUPPORTED;
     const size_t need = backward_workspace_bytes(B, L, Hq, Hkv);
     if (!workspace || workspace_bytes < need || !aligned16(workspace)) return ZG_ERR_WORKSPACE;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const bool tc = backward_tc_supports(d, Hq, Hkv, window) && Hkv <= 65535 &&
+                    static_cast<long long>(B) * Hkv * ((L + 31) / 32) < (1ll << 31);
+    if (tc) {
+        // tensor-core path (the ZGCM-1 local-layer shape)
+        BackwardTcParams t;
+        std::memset(&t, 0, sizeof(t));
+        if (!dev_ctl(t.ctl)) return ZG_ERR_CUDA;
+        const size_t rq = static_cast<size_t>(B) * L * Hq * d, rk = static_cast<size_t>(B) * L * Hkv * d;
+        uint8_t* w8 = static_cast<uint8_t*>(workspace);
+        t.qh = reinterpret_cast<__nv_bfloat16*>(w8);
+        t.da = reinterpret_cast<__nv_bfloat16*>(w8 + rq * 2);
+        t.kh = reinterpret_cast<__nv_bfloat16*>(w8 + rq * 4);
+        t.stat = reinterpret_cast<float4*>(w8 + rq * 4 + rk * 2);
+        const void* da_src = gated ? static_cast<const void*>(t.da) : static_cast<const void*>(dout);
+        if (!make_map(&t.tm_qh, t.qh, d, Hq, L, B, 4, 32) || !make_map(&t.tm_da, da_src, d, Hq, L, B, 4, 32) ||
+            !make_map(&t.tm_kq, t.kh, d, Hkv, L, B, 1, 160) || !make_map(&t.tm_vq, v, d, Hkv, L, B, 1, 160) ||
+            !make_map(&t.tm_kk, t.kh, d, Hkv, L, B, 1, 128) || !make_map(&t.tm_vk, v, d, Hkv, L, B, 1, 128))
+            return ZG_ERR_CUDA;
+        t.q = reinterpret_cast<const __nv_bfloat16*>(q);
+        t.k = reinterpret_cast<const __nv_bfloat16*>(k);
+        t.gate = reinterpret_cast<const __nv_bfloat16*>(gate);
+        t.dout = reinterpret_cast<const __nv_bfloat16*>(dout);
+        t.pos = pos;
+        t.wq = wq;
+        t.wk = wk;
+        t.dq = dq;
+        t.dk = dk;
+        t.dv = dv;
+        t.dgate = dgate;
+        t.B = B;
+        t.L = L;
+        t.Hq = Hq;
+        t.Hkv = Hkv;
+        t.window = window;
+        t.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
+        t.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
+        t.eps = eps;
+        if (!rope_consts(t.rope, rotary_dim, theta)) return ZG_ERR_SHAPE;
+        return launch_backward_tc(t, s) == cudaSuccess ? ZG_OK : ZG_ERR_CUDA;
+    }
     BackwardParams p;
     std::memset(&p, 0, sizeof(p));
     p.q = reinterpret_cast<const __nv_bfloat16*>(q);
@@ -374,7 +415,7 @@ zg_status zg_attention_backward(const zg_bf16* q, const zg_bf16* k, const zg_bf1
     p.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
     p.eps = eps;
     if (!rope_consts(p.rope, rotary_dim, theta)) return ZG_ERR_SHAPE;
-    return launch_backward(p, d, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? ZG_OK : ZG_ERR_CUDA;
+    return launch_backward(p, d, s) == cudaSuccess ? ZG_OK : ZG_ERR_CUDA;
 }
 
 size_t zg_hybrid_decode_workspace_bytes(int NG, int B, int Hq, int d, int64_t S_max) {

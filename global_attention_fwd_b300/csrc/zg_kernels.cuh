@@ -128,6 +128,35 @@ struct BackwardParams {
 };
 
 size_t backward_workspace_bytes(int B, int L, int Hq, int Hkv);
+// tensor-core path of the same gradients: d = 128, Hq = 4 Hkv, 1 <= window <= 128
+struct BackwardTcParams {
+    CUtensorMap tm_qh, tm_da;  // q_hat, dA workspace (bf16 [B, L, Hq, d]): box {64, 4 heads, 32 tokens}
+    CUtensorMap tm_kq, tm_vq;  // k_hat workspace, v: box {64, 1, 160 tokens}
+    CUtensorMap tm_kk, tm_vk;  // k_hat workspace, v: box {64, 1, 128 tokens}
+    const __nv_bfloat16* q;     // raw inputs (RMSNorm backward, dA)
+    const __nv_bfloat16* k;
+    const __nv_bfloat16* gate;  // or null
+    const __nv_bfloat16* dout;
+    const int32_t* pos;
+    const float* wq;
+    const float* wk;
+    float* dq;
+    float* dk;
+    float* dv;
+    float* dgate;
+    __nv_bfloat16* qh;   // workspace: q_hat [B, L, Hq, d]
+    __nv_bfloat16* kh;   // workspace: k_hat [B, L, Hkv, d]
+    __nv_bfloat16* da;   // workspace: dA [B, L, Hq, d] (gated layers; dout itself otherwise)
+    float4* stat;        // workspace: per query row (max of the log2-scaled scores, 1 / row sum, D, 0)
+    int B, L, Hq, Hkv, window;
+    float scale, scale_log2, eps;
+    RopeConsts rope;
+    DevCtl ctl;
+};
+bool backward_tc_supports(int d, int Hq, int Hkv, int window);
+size_t backward_tc_workspace_bytes(int B, int L, int Hq, int Hkv);
+cudaError_t launch_backward_tc(const BackwardTcParams& p, cudaStream_t s);
+
 cudaError_t launch_backward(const BackwardParams& p, int d, cudaStream_t s);
 
 // ---------------------------------------------------------------- whole layer (plain GEMMs on cuBLASLt)

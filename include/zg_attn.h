@@ -258,8 +258,11 @@ zg_status zg_gated_swa_layer(const zg_bf16 *h, const zg_bf16 *w_q, const zg_bf16
  *   dq, dgate: [B, L, Hq, d] fp32;  dk, dv: [B, L, Hkv, d] fp32, written in full
  *        (not accumulated).  dgate must be NULL exactly when gate is.
  *   d must be 128 (ZG_ERR_UNSUPPORTED otherwise); Hq a multiple of Hkv.
- *   Scores are recomputed from q_hat, k_hat in fp32; nothing of the forward is
- *   reused.  All pointers device memory, 16-byte aligned, owned by the caller.
+ *   Nothing of the forward is reused: scores are recomputed.  The ZGCM-1 local
+ *   layer shape (d = 128, Hq = 4 Hkv, 1 <= window <= 128) runs on the tensor cores
+ *   with bf16 operands (q_hat, k_hat, dA, P, dS) and fp32 accumulation; every other
+ *   shape (the global layer included) runs in fp32 on the CUDA cores.
+ *   All pointers device memory, 16-byte aligned, owned by the caller.
  *   workspace: at least zg_attention_backward_workspace_bytes() bytes, 16-byte
  *        aligned (fp32 q_hat, k_hat, dA, dq_hat, dk_hat and three floats per
  *        query row); ZG_ERR_WORKSPACE if missing or too small.

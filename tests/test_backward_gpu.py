@@ -1,7 +1,18 @@
 """Attention backward (gated SWA and global): CUDA path through the C ABI against the
 fp64 autograd oracle, every element of dq, dk, dv and dgate.
 
-Tolerance.  Both sides see the same bf16 inputs; the kernels compute in fp32 and
+Two paths.  The ZGCM-1 local-layer shape (d = 128, four query heads per KV head,
+window 1..128) runs on the tensor cores with bf16 MMA operands; every other shape
+runs in fp32 on the CUDA cores.
+
+Tolerance of the tensor-core path: the prefill's own bar, rel-L2 <= 1e-2 and max-abs
+<= 2e-2 relative to the gradient's largest element.  Its operands q_hat, k_hat, dA,
+P and dS are rounded to bf16 (2^-9 relative), which perturbs each score by about
+2^-9 |q_hat| |k_hat| / sqrt(128) and each product term by 2^-9; summed over a window
+these give relative errors of a few 1e-3.  The exact-zero gradients of window 1 stay
+at fp32 rounding because D is formed from the same bf16 dA as dP.
+
+Tolerance of the fp32 path: both sides see the same bf16 inputs; the kernels compute in fp32 and
 return fp32 gradients.  The scores |q_hat . k_hat| / sqrt(d) stay below
 sqrt(d) * max(wq) * max(wk) (about 25 for weights in [0.5, 1.5]), so an fp32 score
 carries an absolute error near 25 * 2^-20 and a softmax weight a relative one of the
@@ -21,8 +32,10 @@ from oracle import backward as bw
 
 pytestmark = pytest.mark.gpu
 
-REL_L2 = 1e-3
+REL_L2 = 1e-3           # fp32 path
 MAX_ABS_REL = 1e-3
+TC_REL_L2 = 1e-2        # tensor-core path
+TC_MAX_ABS_REL = 2e-2
 ABS_FLOOR = 1e-5  # where the exact gradient is zero (window 1: ds = p (dA . v - dA . A) with A = v)
 
 
@@ -32,7 +45,12 @@ def zg():
     return zg
 
 
-def _close(got, ref, what):
+def _tc(c):
+    """the shapes the tensor-core path takes"""
+    return c.d == 128 and c.Hq == 4 * c.Hkv and 1 <= c.window <= 128
+
+
+def _close(got, ref, what, tc=False):
     got = got.double().cpu().numpy() if isinstance(got, torch.Tensor) else np.asarray(got)
     ref = ref.detach().double().cpu().numpy() if isinstance(ref, torch.Tensor) else np.asarray(ref)
     assert np.all(np.isfinite(got)), f"{what}: non-finite"
@@ -41,7 +59,8 @@ def _close(got, ref, what):
     ref_norm = float(np.linalg.norm(ref))
     rel = float(np.linalg.norm(diff) / ref_norm) if ref_norm > 0 else 0.0
     mx = float(np.abs(diff).max()) if diff.size else 0.0
-    assert mx <= MAX_ABS_REL * scale + ABS_FLOOR and rel <= REL_L2, \
+    rel_bar, abs_bar = (TC_REL_L2, TC_MAX_ABS_REL) if tc else (REL_L2, MAX_ABS_REL)
+    assert mx <= abs_bar * scale + ABS_FLOOR and rel <= rel_bar, \
         f"{what}: max_abs={mx:.3e} (scale {scale:.3e}) rel_l2={rel:.3e}"
 
 
@@ -76,6 +95,8 @@ def _oracle(c, inp, sl=None):
     (2, 150, 8, 1, 200, True),    # window longer than the sequence, GQA 8:1
     (1, 70, 4, 1, 1, True),       # window 1: every query sees only itself (p = 1, dq = dk = 0)
     (1, 130, 8, 2, 128, False),   # window without gate
+    (1, 100, 4, 1, 37, True),     # odd window
+    (3, 33, 4, 1, 128, True),     # sequences shorter than the window
 ])
 def test_gradients_match_the_oracle(zg, B, L, Hq, Hkv, window, gated):
     c, inp = _case(B, L, Hq, Hkv, window, gated)
@@ -85,7 +106,7 @@ def test_gradients_match_the_oracle(zg, B, L, Hq, Hkv, window, gated):
         if r is None:
             assert g is None
             continue
-        _close(g, r, f"{c.name} {n}")
+        _close(g, r, f"{c.name} {n}", tc=_tc(c))
 
 
 def test_full_size_4k_training_shape_on_window_slices(zg):
@@ -105,7 +126,7 @@ def test_full_size_4k_training_shape_on_window_slices(zg):
         rq, rk, rv, rg = _oracle(c, one, slice(t0, t1))
         lo = (t0 + W - 1 if t0 > 0 else t0) - t0
         khi = (t1 - W + 1 if t1 < c.L else t1) - t0
-        _close(dq[b, t0 + lo:t1], rq[0, lo:], f"dq b{b} [{t0},{t1})")
-        _close(dg[b, t0 + lo:t1], rg[0, lo:], f"dgate b{b} [{t0},{t1})")
-        _close(dk[b, t0 + lo:t0 + khi], rk[0, lo:khi], f"dk b{b} [{t0},{t1})")
-        _close(dv[b, t0 + lo:t0 + khi], rv[0, lo:khi], f"dv b{b} [{t0},{t1})")
+        _close(dq[b, t0 + lo:t1], rq[0, lo:], f"dq b{b} [{t0},{t1})", tc=True)
+        _close(dg[b, t0 + lo:t1], rg[0, lo:], f"dgate b{b} [{t0},{t1})", tc=True)
+        _close(dk[b, t0 + lo:t0 + khi], rk[0, lo:khi], f"dk b{b} [{t0},{t1})", tc=True)
+        _close(dv[b, t0 + lo:t0 + khi], rv[0, lo:khi], f"dv b{b} [{t0},{t1})", tc=True)
