@@ -66,6 +66,20 @@ bool make_map(CUtensorMap* m, const void* base, int d, int heads, int L, int B, 
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 4-D fp32 tensor map over [outer][L][heads][d] with a {32, box_heads, box_rows, 1} box (128 bytes
+// inner), 128-byte swizzle
+bool make_map_f32(CUtensorMap* m, const void* base, int d, int heads, int L, int B, int box_heads, int box_rows) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)L, (cuuint64_t)B};
+    cuuint64_t strides[3] = {(cuuint64_t)d * 4, (cuuint64_t)heads * d * 4, (cuuint64_t)L * heads * d * 4};
+    cuuint32_t box[4] = {32, (cuuint32_t)box_heads, (cuuint32_t)box_rows, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void*>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // theta^(-2j/r) in double, split into float head + float tail
 bool rope_consts(RopeConsts& rc, int rotary_dim, double theta) {
     if (rotary_dim < 0 || (rotary_dim & 1) || rotary_dim / 2 > kMaxRotHalf) return false;
@@ -361,7 +375,13 @@ zg_status zg_attention_backward(const zg_bf16* q, const zg_bf16* k, const zg_bf1
         const void* da_src = gated ? static_cast<const void*>(t.da) : static_cast<const void*>(dout);
         if (!make_map(&t.tm_qh, t.qh, d, Hq, L, B, 4, 32) || !make_map(&t.tm_da, da_src, d, Hq, L, B, 4, 32) ||
             !make_map(&t.tm_kq, t.kh, d, Hkv, L, B, 1, 160) || !make_map(&t.tm_vq, v, d, Hkv, L, B, 1, 160) ||
-            !make_map(&t.tm_kk, t.kh, d, Hkv, L, B, 1, 128) || !make_map(&t.tm_vk, v, d, Hkv, L, B, 1, 128))
+            !make_map(&t.tm_kk, t.kh, d, Hkv, L, B, 1, 128) || !make_map(&t.tm_vk, v, d, Hkv, L, B, 1, 128) ||
+            !make_map(&t.tm_q, q, d, Hq, L, B, 4, 32) || !make_map(&t.tm_kraw, k, d, Hkv, L, B, 1, 128) ||
+            !make_map_f32(&t.tm_dqf, dq, d, Hq, L, B, 4, 32) || !make_map_f32(&t.tm_dkf, dk, d, Hkv, L, B, 1, 128) ||
+            !make_map_f32(&t.tm_dvf, dv, d, Hkv, L, B, 1, 128))
+            return ZG_ERR_CUDA;
+        if (gated && (!make_map(&t.tm_gate, gate, d, Hq, L, B, 4, 32) || !make_map(&t.tm_dout, dout, d, Hq, L, B, 4, 32) ||
+                      !make_map_f32(&t.tm_dg, dgate, d, Hq, L, B, 4, 32)))
             return ZG_ERR_CUDA;
         t.q = reinterpret_cast<const __nv_bfloat16*>(q);
         t.k = reinterpret_cast<const __nv_bfloat16*>(k);

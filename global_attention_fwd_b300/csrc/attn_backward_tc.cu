@@ -10,7 +10,7 @@
 //   dQ_hat = c dS K_hat,  dK_hat = c dS^T Q_hat,  dV = P^T dA.
 // All MMA operands are bf16 (q_hat, k_hat, dA, P, dS), accumulation fp32.
 //
-// Kernel 1 (prep, one warp per row): q_hat, k_hat and dA = dout * sigmoid(gate) in bf16.
+// Kernel 1 (prep, four rows per warp): q_hat, k_hat and dA = dout * sigmoid(gate) in bf16.
 //
 // Kernel 2 (query pass): one CTA per tile of 32 tokens x the 4 query heads of one KV
 // head (128 rows); the tile sees the 160 keys [t0 - 128, t0 + 32).
@@ -22,7 +22,9 @@
 //   warps 0-3 (thread = row = TMEM lane): exact row max and sum over the window, P
 //   (unnormalised, bf16) over S; A = O / l, D, dgate = dA * A * (1 - sigmoid(gate)) and
 //   the row statistics (max, 1 / l, D) for kernel 3; dS over dP; finally dQ_hat back
-//   through RoPE and RMSNorm into dq (fp32).
+//   through RoPE and RMSNorm into dq (fp32).  Gate and dout tiles are staged by TMA into
+//   Q_hat / dA once the first two products are done; dgate and dq leave through swizzled
+//   fp32 staging tiles and bulk tensor stores.
 //
 // Kernel 3 (key pass): one CTA per 128 keys of one KV head; the queries that see them
 // are the tokens [j0, j0 + 128 + W - 1), visited as query tiles of 32 tokens x 4 heads
@@ -31,8 +33,11 @@
 //     dV += P^T dA -> [256, 384), dK_hat += dS^T Q_hat -> [384, 512)
 //     (P^T, dS^T from TMEM, packed over S^T and dP^T; one thread's MMAs run in issue
 //     order, so the next tile's S^T overwrites P^T only after dV has read it).
-//   warps 0-3 (thread = key row): P^T and dS^T from the row statistics of kernel 2;
-//   at the end dV (fp32) and dK_hat back through RoPE and RMSNorm into dk.
+//   warps 0-3 (thread = key row, query columns 0-63) and warps 4-7 (columns 64-127): P^T
+//   and dS^T from the row statistics of kernel 2; the products of each column half are
+//   issued separately, so one half's accumulation runs while the other half's rows are
+//   computed.  At the end dV (fp32) and dK_hat back through RoPE and RMSNorm into dk, both
+//   through swizzled fp32 staging tiles and bulk tensor stores.
 #include "zg_qk.cuh"
 
 namespace zg {
@@ -47,111 +52,188 @@ constexpr uint32_t CH128 = 128 * 128;       // one 64-column chunk of 128 rows (
 constexpr uint32_t CH160 = NKQ * 128;       // one 64-column chunk of 160 rows
 constexpr uint32_t TILE128 = 2 * CH128;
 constexpr uint32_t TILE160 = 2 * CH160;
-constexpr int SROW = D + 1;                 // staging row stride in floats (conflict-free per-row access)
-constexpr uint32_t STAGE = 128 * SROW * 4;  // one staged 128-row fp32 tile
 constexpr int kThreads = 160;               // warps 0-3 rows, warp 4 TMA + MMA
 
-// query pass shared memory
+// query pass shared memory: Q_hat, dA (later the gate and dout tiles), V, K_hat, raw q,
+// the tile's RoPE cos / sin, wq
 constexpr uint32_t QP_Q = 0;
 constexpr uint32_t QP_DA = QP_Q + TILE128;
-constexpr uint32_t QP_K = QP_DA + TILE128;
-constexpr uint32_t QP_V = QP_K + TILE160;
-constexpr uint32_t QP_W = QP_V + TILE160;
+constexpr uint32_t QP_V = QP_DA + TILE128;
+constexpr uint32_t QP_K = QP_V + TILE160;
+constexpr uint32_t QP_X = QP_K + TILE160;
+constexpr uint32_t QP_ROPE = QP_X + TILE128;  // [T tokens][kMaxRotHalf] float2
+constexpr uint32_t QP_W = QP_ROPE + T * kMaxRotHalf * 8;
 constexpr uint32_t QP_BAR = QP_W + D * 4;
-constexpr uint32_t QP_MISC = QP_BAR + 8 * 8;
+constexpr uint32_t QP_MISC = QP_BAR + 16 * 8;
+constexpr uint32_t QP_DG = QP_V;   // dgate staging (two 32-column fp32 boxes) in the free V tile
+constexpr uint32_t QP_DQ = QP_Q;   // dq staging (four boxes) over the free Q_hat and dA tiles
+static_assert(QP_DG + 2 * 128 * 128 <= QP_K && QP_DQ + 4 * 128 * 128 <= QP_DG, "staging tiles");
 constexpr uint32_t QP_SMEM = QP_MISC + 32;
-static_assert(STAGE <= QP_W, "the dq staging tile reuses the operand tiles");
-static_assert(QP_K % 1024 == 0 && QP_V % 1024 == 0, "128-byte swizzle atoms");
+static_assert(QP_K % 1024 == 0 && QP_V % 1024 == 0 && QP_X % 1024 == 0, "128-byte swizzle atoms");
+static_assert(QP_SMEM <= 227 * 1024, "shared memory");
 
 // key pass shared memory
 constexpr uint32_t KP_K = 0;
 constexpr uint32_t KP_V = KP_K + TILE128;
 constexpr uint32_t KP_QD = KP_V + TILE128;      // 2 stages x (Q_hat, dA)
-constexpr uint32_t KP_STAT = KP_QD + 4 * TILE128;  // 4 warps x 128 float4
-constexpr uint32_t KP_W = KP_STAT + 4 * 128 * 16;
+constexpr uint32_t KP_STAT = KP_QD + 4 * TILE128;  // 8 warps x 64 float4
+constexpr uint32_t KP_W = KP_STAT + 8 * 64 * 16;
 constexpr uint32_t KP_BAR = KP_W + D * 4;
-constexpr uint32_t KP_MISC = KP_BAR + 12 * 8;
+constexpr uint32_t KP_MISC = KP_BAR + 16 * 8;
 constexpr uint32_t KP_SMEM = KP_MISC + 32;
-static_assert(STAGE <= 4 * TILE128, "the dk / dv staging tile reuses the query ring");
+constexpr uint32_t KP_X = KP_QD + 3 * TILE128;  // raw k tile, loaded into the free ring at the end
+constexpr uint32_t KP_DV = KP_K;    // dv staging (four 32-column fp32 boxes) over K_hat and V
+constexpr uint32_t KP_DK = KP_QD;   // dk staging over the first half of the query ring
+static_assert(KP_DV + 4 * 128 * 128 <= KP_QD && KP_DK + 4 * 128 * 128 <= KP_X, "staging tiles");
 static_assert(KP_SMEM <= 227 * 1024, "shared memory");
 
-// One row held by one thread in a staging row: dy (the gradient of x_hat) in, the gradient
-// of the raw row x out.  RoPE rotated (a, b) by +angle, so its transpose rotates by -angle;
-// RMSNorm x_hat = x * inv * w with inv = (mean x^2 + eps)^-1/2 gives
+// 16-byte group c8 (elements 8 c8 .. 8 c8 + 7) of row r of a 128-row tile of two 64-column
+// chunks with the 128-byte swizzle (the layout the TMA boxes land in)
+__device__ __forceinline__ uint4 ld_row8(const uint8_t* tile, int r, int c8) {
+    return *reinterpret_cast<const uint4*>(tile + (c8 >> 3) * CH128 + sw128_off(r, c8 & 7));
+}
+
+// A 128-row fp32 staging tile laid out as four boxes of 32 columns (128 rows x 128 bytes each)
+// with the 128-byte swizzle: the layout a bulk tensor store of box {32, ...} reads.
+constexpr uint32_t F32BOX = 128 * 128;
+constexpr uint32_t F32TILE = 4 * F32BOX;
+__device__ __forceinline__ float* f32_elem(uint8_t* t, int r, int e) {
+    return reinterpret_cast<float*>(t + (e >> 5) * F32BOX + r * 128 + ((((e & 31) >> 2) ^ (r & 7)) << 4) + (e & 3) * 4);
+}
+__device__ __forceinline__ float4* f32_chunk(uint8_t* t, int r, int c4) {  // floats 4 c4 .. 4 c4 + 3 of row r
+    return reinterpret_cast<float4*>(t + (c4 >> 3) * F32BOX + r * 128 + (((c4 & 7) ^ (r & 7)) << 4));
+}
+
+// One row, held by one thread in a staging tile: dy (the gradient of x_hat) in, the gradient of
+// the raw row x out, in place.  RoPE rotated (a, b) by +angle, so its transpose rotates by
+// -angle; RMSNorm x_hat = x * inv * w with inv = (mean x^2 + eps)^-1/2 gives
 // dx = inv * w * dy - inv^3 / d * x * sum(x * w * dy).
-__device__ __forceinline__ void row_norm_rope_bwd(float* st, const __nv_bfloat16* __restrict__ x, const float* w_s,
-                                                  float eps, int pos, const RopeConsts& rc) {
-    for (int j = 0; j < rc.half; ++j) {
-        float cs, sn;
-        rope_cos_sin(pos, rc.f_hi[j], rc.f_lo[j], cs, sn);
-        const float a = st[j], bb = st[j + rc.half];
-        st[j] = a * cs + bb * sn;
-        st[j + rc.half] = bb * cs - a * sn;
+// x: row r of a bf16 swizzled tile in shared memory; cos_sin(j) gives (cos, sin) of pair j.
+template <class CosSin>
+__device__ __forceinline__ void row_norm_rope_bwd(uint8_t* t, int r, const uint8_t* xtile, const float* w_s, float eps,
+                                                  int half, CosSin cos_sin) {
+    for (int j = 0; j < half; ++j) {
+        const float2 c = cos_sin(j);
+        float* pa = f32_elem(t, r, j);
+        float* pb = f32_elem(t, r, j + half);
+        const float a = *pa, bb = *pb;
+        *pa = a * c.x + bb * c.y;
+        *pb = bb * c.x - a * c.y;
     }
     float ss = 0.f, tw = 0.f;
 #pragma unroll 4
-    for (int c = 0; c < D; c += 8) {
-        const uint4 u = *reinterpret_cast<const uint4*>(x + c);
-        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+    for (int c8 = 0; c8 < D / 8; ++c8) {
+        const uint4 u = ld_row8(xtile, r, c8);
+        const float4 y0 = *f32_chunk(t, r, 2 * c8), y1 = *f32_chunk(t, r, 2 * c8 + 1);
+        const float x[8] = {bf16lo(u.x), bf16hi(u.x), bf16lo(u.y), bf16hi(u.y),
+                            bf16lo(u.z), bf16hi(u.z), bf16lo(u.w), bf16hi(u.w)};
+        const float y[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float x0 = bf16lo(w4[e]), x1 = bf16hi(w4[e]);
-            ss = fmaf(x0, x0, fmaf(x1, x1, ss));
-            tw = fmaf(x0 * w_s[c + 2 * e], st[c + 2 * e], fmaf(x1 * w_s[c + 2 * e + 1], st[c + 2 * e + 1], tw));
+        for (int e = 0; e < 8; ++e) {
+            ss = fmaf(x[e], x[e], ss);
+            tw = fmaf(x[e] * w_s[8 * c8 + e], y[e], tw);
         }
     }
     const float inv = ss > 0.f || eps > 0.f ? rsqrtf(ss * (1.0f / D) + eps) : 0.f;
     const float coef = inv * inv * inv * tw * (1.0f / D);
 #pragma unroll 4
-    for (int c = 0; c < D; c += 8) {
-        const uint4 u = *reinterpret_cast<const uint4*>(x + c);
-        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+    for (int c8 = 0; c8 < D / 8; ++c8) {
+        const uint4 u = ld_row8(xtile, r, c8);
+        float4* p0 = f32_chunk(t, r, 2 * c8);
+        float4* p1 = f32_chunk(t, r, 2 * c8 + 1);
+        const float4 y0 = *p0, y1 = *p1;
+        const float* w = w_s + 8 * c8;
+        *p0 = make_float4(inv * w[0] * y0.x - coef * bf16lo(u.x), inv * w[1] * y0.y - coef * bf16hi(u.x),
+                          inv * w[2] * y0.z - coef * bf16lo(u.y), inv * w[3] * y0.w - coef * bf16hi(u.y));
+        *p1 = make_float4(inv * w[4] * y1.x - coef * bf16lo(u.z), inv * w[5] * y1.y - coef * bf16hi(u.z),
+                          inv * w[6] * y1.z - coef * bf16lo(u.w), inv * w[7] * y1.w - coef * bf16hi(u.w));
+    }
+}
+
+// TMEM columns [col, col + 128) of this thread's lane, times `scale`, into row r of a staging tile
+__device__ __forceinline__ void tmem_row_to_tile(uint32_t taddr, uint8_t* t, int r, float scale) {
+#pragma unroll 1
+    for (int k = 0; k < D / 32; ++k) {
+        uint32_t v[32];
+        tmem_ld32(taddr + 32 * k, v);
+        tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            st[c + 2 * e] = inv * w_s[c + 2 * e] * st[c + 2 * e] - coef * bf16lo(w4[e]);
-            st[c + 2 * e + 1] = inv * w_s[c + 2 * e + 1] * st[c + 2 * e + 1] - coef * bf16hi(w4[e]);
-        }
+        for (int c = 0; c < 8; ++c)
+            *f32_chunk(t, r, 8 * k + c) =
+                make_float4(__uint_as_float(v[4 * c]) * scale, __uint_as_float(v[4 * c + 1]) * scale,
+                            __uint_as_float(v[4 * c + 2]) * scale, __uint_as_float(v[4 * c + 3]) * scale);
     }
 }
 
 // ---------------------------------------------------------------- kernel 1
+// Four rows per warp (the q rows first, then the k rows), every global load issued before
+// any arithmetic so that a warp keeps several rows in flight.
+constexpr int kPrepRows = 4;
+
 __global__ void __launch_bounds__(256) bwd_tc_prep_kernel(const __grid_constant__ BackwardTcParams p) {
-    __shared__ float buf[8][D];
+    __shared__ float buf[8][kPrepRows][D];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long long nq = static_cast<long long>(p.B) * p.L * p.Hq, nk = static_cast<long long>(p.B) * p.L * p.Hkv;
-    const long long row = static_cast<long long>(blockIdx.x) * 8 + warp;
-    if (row >= nq + nk) return;
-    const bool is_q = row < nq;
-    const long long r = is_q ? row : row - nq;
-    const long long tok = r / (is_q ? p.Hq : p.Hkv);
-    const int pos = __ldg(p.pos + tok);
-    norm_rope_warp(is_q ? p.q + r * D : p.k + r * D, is_q ? p.wq : p.wk, p.eps, pos, p.rope, 1.0f, buf[warp]);
-    const float4 v = *reinterpret_cast<const float4*>(&buf[warp][lane * 4]);
-    *reinterpret_cast<uint2*>((is_q ? p.qh : p.kh) + r * D + lane * 4) =
-        make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
-    if (is_q && p.gate) {
-        const uint2 go = *reinterpret_cast<const uint2*>(p.gate + r * D + lane * 4);
-        const uint2 dd = *reinterpret_cast<const uint2*>(p.dout + r * D + lane * 4);
-        auto sg = [](float x) { return 1.0f / (1.0f + __expf(-x)); };
-        *reinterpret_cast<uint2*>(p.da + r * D + lane * 4) =
-            make_uint2(pack_bf16x2(bf16lo(dd.x) * sg(bf16lo(go.x)), bf16hi(dd.x) * sg(bf16hi(go.x))),
-                       pack_bf16x2(bf16lo(dd.y) * sg(bf16lo(go.y)), bf16hi(dd.y) * sg(bf16hi(go.y))));
+    const long long row0 = (static_cast<long long>(blockIdx.x) * 8 + warp) * kPrepRows;
+    const bool gated = p.gate != nullptr;
+    uint2 xr[kPrepRows], gr[kPrepRows], dr[kPrepRows];
+    int pos[kPrepRows];
+#pragma unroll
+    for (int i = 0; i < kPrepRows; ++i) {
+        const long long row = row0 + i;
+        const bool is_q = row < nq;
+        const long long r = is_q ? row : row - nq;
+        const bool valid = row < nq + nk;
+        xr[i] = valid ? *reinterpret_cast<const uint2*>((is_q ? p.q : p.k) + r * D + lane * 4) : make_uint2(0u, 0u);
+        pos[i] = valid ? __ldg(p.pos + r / (is_q ? p.Hq : p.Hkv)) : 0;
+        if (valid && is_q && gated) {
+            gr[i] = *reinterpret_cast<const uint2*>(p.gate + r * D + lane * 4);
+            dr[i] = *reinterpret_cast<const uint2*>(p.dout + r * D + lane * 4);
+        }
     }
-}
-
-// warp-cooperative store of the 32 staged rows of this warp: row r goes to dst(r) when valid(r)
-template <class Dst>
-__device__ __forceinline__ void store_rows(const float* stage, int warp, int lane, Dst dst) {
+#pragma unroll
+    for (int i = 0; i < kPrepRows; ++i) {
+        const long long row = row0 + i;
+        const bool is_q = row < nq;
+        const float4 w = __ldg(reinterpret_cast<const float4*>((is_q ? p.wq : p.wk) + lane * 4));
+        const float v0 = bf16lo(xr[i].x), v1 = bf16hi(xr[i].x), v2 = bf16lo(xr[i].y), v3 = bf16hi(xr[i].y);
+        float ss = v0 * v0 + v1 * v1 + v2 * v2 + v3 * v3;
+#pragma unroll
+        for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        const float inv = ss > 0.f || p.eps > 0.f ? rsqrtf(ss * (1.0f / D) + p.eps) : 0.f;
+        *reinterpret_cast<float4*>(&buf[warp][i][lane * 4]) =
+            make_float4(v0 * inv * w.x, v1 * inv * w.y, v2 * inv * w.z, v3 * inv * w.w);
+    }
     __syncwarp();
-    for (int rr = 0; rr < 32; ++rr) {
-        const int r = warp * 32 + rr;
-        float* d = dst(r);
-        if (d) {
-            const float* s = stage + r * SROW + lane * 4;
-            *reinterpret_cast<float4*>(d + lane * 4) = make_float4(s[0], s[1], s[2], s[3]);
+    // rotate the pairs (j, j + half) of every row
+    for (int j = lane; j < p.rope.half; j += 32) {
+#pragma unroll
+        for (int i = 0; i < kPrepRows; ++i) {
+            float cs, sn;
+            rope_cos_sin(pos[i], p.rope.f_hi[j], p.rope.f_lo[j], cs, sn);
+            const float a = buf[warp][i][j], bb = buf[warp][i][j + p.rope.half];
+            buf[warp][i][j] = a * cs - bb * sn;
+            buf[warp][i][j + p.rope.half] = bb * cs + a * sn;
         }
     }
     __syncwarp();
+#pragma unroll
+    for (int i = 0; i < kPrepRows; ++i) {
+        const long long row = row0 + i;
+        if (row >= nq + nk) break;
+        const bool is_q = row < nq;
+        const long long r = is_q ? row : row - nq;
+        const float4 v = *reinterpret_cast<const float4*>(&buf[warp][i][lane * 4]);
+        *reinterpret_cast<uint2*>((is_q ? p.qh : p.kh) + r * D + lane * 4) =
+            make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+        if (is_q && gated) {
+            // the same sigmoid as the query pass, which rebuilds these bf16 values for D
+            const uint2 go = gr[i], dd = dr[i];
+            *reinterpret_cast<uint2*>(p.da + r * D + lane * 4) = make_uint2(
+                pack_bf16x2(bf16lo(dd.x) * sigmoid_fast(bf16lo(go.x)), bf16hi(dd.x) * sigmoid_fast(bf16hi(go.x))),
+                pack_bf16x2(bf16lo(dd.y) * sigmoid_fast(bf16lo(go.y)), bf16hi(dd.y) * sigmoid_fast(bf16hi(go.y))));
+        }
+    }
 }
 
 // ---------------------------------------------------------------- kernel 2: query pass
@@ -164,6 +246,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_qpass_kernel(const __grid_con
     uint64_t* o_full = bar + 3;
     uint64_t* ds_ready = bar + 4;
     uint64_t* dq_full = bar + 5;
+    uint64_t* gd_full = bar + 6;  // gate and dout tiles (gated layers)
+    uint64_t* stg_full = bar + 7;  // [2] dgate staging halves written (128 arrivals)
+    uint64_t* stg_free = bar + 9;  // the first half's bulk store has read its staging
+    uint64_t* dq_stg = bar + 10;   // dq staging written (128 arrivals)
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + QP_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + QP_MISC + 4);
     float* w_s = reinterpret_cast<float*>(smem + QP_W);
@@ -184,10 +270,16 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_qpass_kernel(const __grid_con
         mbar_init(o_full, 1);
         mbar_init(ds_ready, 128);
         mbar_init(dq_full, 1);
+        mbar_init(gd_full, 1);
+        mbar_init(&stg_full[0], 128);
+        mbar_init(&stg_full[1], 128);
+        mbar_init(stg_free, 1);
+        mbar_init(dq_stg, 128);
         fence_barrier_init();
     }
     if (threadIdx.x < 32)
         *reinterpret_cast<float4*>(w_s + lane * 4) = __ldg(reinterpret_cast<const float4*>(p.wq + lane * 4));
+    const bool gated = p.gate != nullptr;
     if (warp == 4) {
         tmem_alloc(tslot, 512);
         tmem_relinquish();
@@ -206,12 +298,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_qpass_kernel(const __grid_con
             tma_prefetch_desc(&p.tm_da);
             tma_prefetch_desc(&p.tm_kq);
             tma_prefetch_desc(&p.tm_vq);
-            mbar_arrive_expect_tx(ld_full, 2 * TILE128 + 2 * TILE160);
+            tma_prefetch_desc(&p.tm_q);
+            mbar_arrive_expect_tx(ld_full, 3 * TILE128 + 2 * TILE160);
             for (int ch = 0; ch < 2; ++ch) {
                 tma_load_4d(smem + QP_Q + ch * CH128, &p.tm_qh, ld_full, ch * 64, g * G, t0, b);
                 tma_load_4d(smem + QP_DA + ch * CH128, &p.tm_da, ld_full, ch * 64, g * G, t0, b);
                 tma_load_4d(smem + QP_K + ch * CH160, &p.tm_kq, ld_full, ch * 64, g, t0 - 128, b);
                 tma_load_4d(smem + QP_V + ch * CH160, &p.tm_vq, ld_full, ch * 64, g, t0 - 128, b);
+                tma_load_4d(smem + QP_X + ch * CH128, &p.tm_q, ld_full, ch * 64, g * G, t0, b);
             }
             constexpr uint32_t id_s = idesc_bf16_f32(128, NKQ, false, false);
             constexpr uint32_t id_o = idesc_bf16_f32(128, D, false, true);
@@ -233,7 +327,17 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_qpass_kernel(const __grid_con
                               sdesc(sbase + QP_V + ck, 16, 1024, kSw128), id_s, ks > 0);
                 }
                 umma_commit(s_full);
-                ok = mbar_wait(p_ready, 0, p.ctl, 102);
+                if (gated) {  // Q_hat and dA are read once the two products are done: reuse them
+                    ok = mbar_wait(s_full, 0, p.ctl, 107);
+                    if (ok) {
+                        mbar_arrive_expect_tx(gd_full, 2 * TILE128);
+                        for (int ch = 0; ch < 2; ++ch) {
+                            tma_load_4d(smem + QP_Q + ch * CH128, &p.tm_gate, gd_full, ch * 64, g * G, t0, b);
+                            tma_load_4d(smem + QP_DA + ch * CH128, &p.tm_dout, gd_full, ch * 64, g * G, t0, b);
+                        }
+                    }
+                }
+                if (ok) ok = mbar_wait(p_ready, 0, p.ctl, 102);
             }
             if (ok) {
                 tc_fence_after();
@@ -265,6 +369,17 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_qpass_kernel(const __grid_con
         const int lo = max(128 - t0, tt + 128 - p.window + 1);  // key columns [lo, hi] are in the window
         const int hi = tt + 128;
         const float sl = p.scale_log2;
+        // cos / sin of this row's token: the four rows (lanes) of a token share the work
+        float2* rope_tab = reinterpret_cast<float2*>(smem + QP_ROPE) + tt * kMaxRotHalf;
+        {
+            const int pos = valid_row ? __ldg(p.pos + static_cast<long long>(b) * p.L + t) : 0;
+            for (int j = row % G; j < p.rope.half; j += G) {
+                float cs, sn;
+                rope_cos_sin(pos, p.rope.f_hi[j], p.rope.f_lo[j], cs, sn);
+                rope_tab[j] = make_float2(cs, sn);
+            }
+            __syncwarp();  // a token's four rows sit in one warp
+        }
         bool ok = __all_sync(0xffffffffu, mbar_wait(s_full, 0, p.ctl, 104));
         float m = 0.f, l = 0.f;
         if (ok) {
@@ -307,38 +422,49 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_qpass_kernel(const __grid_con
         const float il = l > 0.f ? 1.0f / l : 0.f;
         // ---- A = O / l, D = dA . A, dgate
         if (ok && !aborted()) ok = __all_sync(0xffffffffu, mbar_wait(o_full, 0, p.ctl, 105));
+        if (ok && gated && !aborted()) ok = __all_sync(0xffffffffu, mbar_wait(gd_full, 0, p.ctl, 108));
         float Dd = 0.f;
         if (ok) {
             tc_fence_after();
+            const uint8_t* dout_t = smem + QP_DA;  // dout (gated: reloaded; ungated: dA is dout)
+            const uint8_t* gate_t = smem + QP_Q;
+            uint8_t* dg_t = smem + QP_DG;
+            // two halves of 64 columns; with a gate, each half's dgate goes through a swizzled
+            // staging tile (two boxes of 32 fp32 columns) and leaves by bulk tensor stores
 #pragma unroll 1
-            for (int k = 0; k < D / 32; ++k) {
-                uint32_t r[32];
-                tmem_ld32(lane_addr + C_O + 32 * k, r);
-                tmem_wait_ld();
-                if (valid_row) {
-                    const __nv_bfloat16* dop = p.dout + qrow * D + 32 * k;
+            for (int hh = 0; hh < 2 && ok; ++hh) {
+                if (hh == 1 && gated) ok = __all_sync(0xffffffffu, mbar_wait(stg_free, 0, p.ctl, 109));
+                if (!ok) break;
+#pragma unroll 1
+                for (int k = 2 * hh; k < 2 * hh + 2; ++k) {
+                    uint32_t r[32];
+                    tmem_ld32(lane_addr + C_O + 32 * k, r);
+                    tmem_wait_ld();
 #pragma unroll
                     for (int v8 = 0; v8 < 4; ++v8) {
-                        const uint4 du = *reinterpret_cast<const uint4*>(dop + 8 * v8);
+                        const uint4 du = ld_row8(dout_t, row, 4 * k + v8);
                         const uint32_t dw[4] = {du.x, du.y, du.z, du.w};
-                        float dg[8];
-                        if (p.gate) {
-                            const uint4 gu = *reinterpret_cast<const uint4*>(p.gate + qrow * D + 32 * k + 8 * v8);
+                        if (gated) {
+                            const uint4 gu = ld_row8(gate_t, row, 4 * k + v8);
                             const uint32_t gw[4] = {gu.x, gu.y, gu.z, gu.w};
+                            float dg[8];
 #pragma unroll
                             for (int e = 0; e < 8; ++e) {
                                 const float gv = (e & 1) ? bf16hi(gw[e / 2]) : bf16lo(gw[e / 2]);
-                                const float sg = 1.0f / (1.0f + __expf(-gv));
+                                const float sg = sigmoid_fast(gv);
                                 const float a = __uint_as_float(r[8 * v8 + e]) * il;
                                 const float dav = ((e & 1) ? bf16hi(dw[e / 2]) : bf16lo(dw[e / 2])) * sg;
-                                // D from the bf16 dA the dP product used (the same rounding as the
-                                // prep kernel), so that sum_j dS_ij = 0 holds to fp32 rounding
+                                // D from the bf16 dA the dP product used (the prep kernel's rounding
+                                // of the same value), so that sum_j dS_ij = 0 holds to fp32 rounding
                                 Dd = fmaf(__bfloat162float(__float2bfloat16_rn(dav)), a, Dd);
                                 dg[e] = dav * a * (1.0f - sg);
                             }
-                            float* dgp = p.dgate + qrow * D + 32 * k + 8 * v8;
-                            *reinterpret_cast<float4*>(dgp) = make_float4(dg[0], dg[1], dg[2], dg[3]);
-                            *reinterpret_cast<float4*>(dgp + 4) = make_float4(dg[4], dg[5], dg[6], dg[7]);
+                            // box k & 1 of this half: row `row`, 16-byte chunks 2 v8 and 2 v8 + 1
+                            uint8_t* bx = dg_t + (k & 1) * (128 * 128) + row * 128;
+                            *reinterpret_cast<float4*>(bx + (((2 * v8) ^ (row & 7)) << 4)) =
+                                make_float4(dg[0], dg[1], dg[2], dg[3]);
+                            *reinterpret_cast<float4*>(bx + (((2 * v8 + 1) ^ (row & 7)) << 4)) =
+                                make_float4(dg[4], dg[5], dg[6], dg[7]);
                         } else {
 #pragma unroll
                             for (int e = 0; e < 8; ++e) {
@@ -347,6 +473,23 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_qpass_kernel(const __grid_con
                             }
                         }
                     }
+                }
+                if (gated) {
+                    fence_async_smem();
+                    mbar_arrive(&stg_full[hh]);
+                    if (row == 0) {
+                        // rows past the sequence end fall outside the tensor and are not stored
+                        if (mbar_wait(&stg_full[hh], 0, p.ctl, 99)) {
+                            tma_store_4d(&p.tm_dg, dg_t, 64 * hh, g * G, t0, b);
+                            tma_store_4d(&p.tm_dg, dg_t + 128 * 128, 64 * hh + 32, g * G, t0, b);
+                            bulk_commit();
+                            bulk_wait_read_all();
+                            if (hh == 0) mbar_arrive(stg_free);
+                        } else {
+                            ok = false;
+                        }
+                    }
+                    ok = __all_sync(0xffffffffu, ok);  // keep the warp's tensor-memory accesses together
                 }
             }
             if (valid_row) p.stat[qrow] = make_float4(m, il, Dd, 0.f);
@@ -370,27 +513,27 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_qpass_kernel(const __grid_con
         tc_fence_before();
         mbar_arrive(ds_ready);
         if (!ok) fail();
-        // ---- dq: dQ_hat * c back through RoPE and RMSNorm
+        // ---- dq: dQ_hat * c back through RoPE and RMSNorm, out by bulk tensor stores
         if (ok && !aborted()) ok = __all_sync(0xffffffffu, mbar_wait(dq_full, 0, p.ctl, 106));
+        uint8_t* dq_t = smem + QP_DQ;  // every product is done: Q_hat and dA are free
         if (ok) {
             tc_fence_after();
-            float* st = reinterpret_cast<float*>(smem) + row * SROW;  // operand tiles are free now
-#pragma unroll 1
-            for (int k = 0; k < D / 32; ++k) {
-                uint32_t r[32];
-                tmem_ld32(lane_addr + C_O + 32 * k, r);
-                tmem_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) st[32 * k + i] = __uint_as_float(r[i]) * p.scale;
-            }
+            tmem_row_to_tile(lane_addr + C_O, dq_t, row, p.scale);
             if (valid_row)
-                row_norm_rope_bwd(st, p.q + qrow * D, w_s, p.eps, __ldg(p.pos + static_cast<long long>(b) * p.L + t),
-                                  p.rope);
-            store_rows(reinterpret_cast<const float*>(smem), warp, lane, [&](int r) -> float* {
-                const int tr = t0 + r / G;
-                return tr < p.L ? p.dq + ((static_cast<long long>(b) * p.L + tr) * p.Hq + g * G + r % G) * D : nullptr;
-            });
+                row_norm_rope_bwd(dq_t, row, smem + QP_X, w_s, p.eps, p.rope.half, [&](int j) { return rope_tab[j]; });
+            fence_async_smem();
         }
+        mbar_arrive(dq_stg);
+        if (row == 0 && ok) {
+            // rows past the sequence end fall outside the tensor and are not stored
+            if (mbar_wait(dq_stg, 0, p.ctl, 98)) {
+                for (int k = 0; k < 4; ++k) tma_store_4d(&p.tm_dqf, dq_t + k * F32BOX, 32 * k, g * G, t0, b);
+                bulk_commit();
+            } else {
+                ok = false;
+            }
+        }
+        if (row == 0) bulk_wait_all();  // the dgate and dq stores have landed
         if (!ok) fail();
     }
     __syncthreads();
@@ -406,19 +549,27 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_qpass_kernel(const __grid_con
 }
 
 // ---------------------------------------------------------------- kernel 3: key pass
-__global__ void __launch_bounds__(kThreads, 1) bwd_kpass_kernel(const __grid_constant__ BackwardTcParams p) {
+constexpr int kKThreads = 288;  // warps 0-7 rows (two column halves), warp 8 TMA + MMA
+
+__global__ void __launch_bounds__(kKThreads, 1) bwd_kpass_kernel(const __grid_constant__ BackwardTcParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem + KP_BAR);
     uint64_t* kv_full = bar + 0;
-    uint64_t* qd_full = bar + 1;   // [2]
-    uint64_t* qd_empty = bar + 3;  // [2]
-    uint64_t* s_full = bar + 5;
-    uint64_t* p_ready = bar + 6;
-    uint64_t* done = bar + 7;
+    uint64_t* qd_full = bar + 1;   // [2] ring stage
+    uint64_t* qd_empty = bar + 3;  // [2] ring stage
+    uint64_t* s_full = bar + 5;    // [2] column half
+    uint64_t* p_ready = bar + 7;   // [2] column half
+    uint64_t* done = bar + 9;
+    uint64_t* x_full = bar + 10;   // raw k tile
+    uint64_t* dv_stg = bar + 11;   // dv staging written (128 arrivals)
+    uint64_t* dk_stg = bar + 12;   // dk staging written (128 arrivals)
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + KP_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + KP_MISC + 4);
     float* w_s = reinterpret_cast<float*>(smem + KP_W);
-    float4* stat_s = reinterpret_cast<float4*>(smem + KP_STAT);  // [4 warps][128]
+    float4* stat_s = reinterpret_cast<float4*>(smem + KP_STAT);  // [8 warps][64]
+    // TMEM: S^T [0, 128) and dP^T [128, 256), each as two 64-column halves (one per half of
+    // the query tile; P^T / dS^T of a half are packed into the first 32 columns of that half),
+    // dV [256, 384), dK_hat [384, 512)
     constexpr uint32_t C_S = 0, C_DP = 128, C_DV = 256, C_DK = 384;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -436,15 +587,18 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kpass_kernel(const __grid_con
         for (int i = 0; i < 2; ++i) {
             mbar_init(&qd_full[i], 1);
             mbar_init(&qd_empty[i], 1);
+            mbar_init(&s_full[i], 1);
+            mbar_init(&p_ready[i], 128);
         }
-        mbar_init(s_full, 1);
-        mbar_init(p_ready, 128);
         mbar_init(done, 1);
+        mbar_init(x_full, 1);
+        mbar_init(dv_stg, 128);
+        mbar_init(dk_stg, 128);
         fence_barrier_init();
     }
     if (threadIdx.x < 32)
         *reinterpret_cast<float4*>(w_s + lane * 4) = __ldg(reinterpret_cast<const float4*>(p.wk + lane * 4));
-    if (warp == 4) {
+    if (warp == 8) {
         tmem_alloc(tslot, 512);
         tmem_relinquish();
     }
@@ -456,12 +610,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kpass_kernel(const __grid_con
     auto aborted = [&]() { return *abort_flag != 0; };
     auto fail = [&]() { *abort_flag = 1; };
 
-    if (warp == 4) {
+    if (warp == 8) {
         if (lane == 0 && !aborted()) {
             tma_prefetch_desc(&p.tm_qh);
             tma_prefetch_desc(&p.tm_da);
             tma_prefetch_desc(&p.tm_kk);
             tma_prefetch_desc(&p.tm_vk);
+            tma_prefetch_desc(&p.tm_kraw);
             mbar_arrive_expect_tx(kv_full, 2 * TILE128);
             for (int ch = 0; ch < 2; ++ch) {
                 tma_load_4d(smem + KP_K + ch * CH128, &p.tm_kk, kv_full, ch * 64, g, j0, b);
@@ -476,54 +631,63 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kpass_kernel(const __grid_con
                     tma_load_4d(dst + TILE128 + ch * CH128, &p.tm_da, &qd_full[st], ch * 64, g * G, j0 + n * T, b);
                 }
             };
-            constexpr uint32_t id_s = idesc_bf16_f32(128, 128, false, false);
+            constexpr uint32_t id_s = idesc_bf16_f32(128, 64, false, false);
             constexpr uint32_t id_o = idesc_bf16_f32(128, D, false, true);
-            auto issue_s = [&](int n) {  // S^T and dP^T of query tile n
-                const uint32_t qd = KP_QD + (n & 1) * 2 * TILE128;
+            auto issue_s = [&](int n, int h) {  // S^T and dP^T of the query rows [64 h, 64 h + 64) of tile n
+                const uint32_t qd = KP_QD + (n & 1) * 2 * TILE128 + h * 64 * 128;
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
                     const uint32_t co = (ks >> 2) * CH128 + (ks & 3) * 32;
-                    umma_bf16(tbase + C_S, sdesc(sbase + KP_K + co, 16, 1024, kSw128),
+                    umma_bf16(tbase + C_S + 64 * h, sdesc(sbase + KP_K + co, 16, 1024, kSw128),
                               sdesc(sbase + qd + co, 16, 1024, kSw128), id_s, ks > 0);
                 }
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
                     const uint32_t co = (ks >> 2) * CH128 + (ks & 3) * 32;
-                    umma_bf16(tbase + C_DP, sdesc(sbase + KP_V + co, 16, 1024, kSw128),
+                    umma_bf16(tbase + C_DP + 64 * h, sdesc(sbase + KP_V + co, 16, 1024, kSw128),
                               sdesc(sbase + qd + TILE128 + co, 16, 1024, kSw128), id_s, ks > 0);
                 }
-                umma_commit(s_full);
+                umma_commit(&s_full[h]);
             };
-            auto issue_acc = [&](int n) {  // dV += P^T dA, dK_hat += dS^T Q_hat
-                const uint32_t qd = KP_QD + (n & 1) * 2 * TILE128;
+            auto issue_acc = [&](int n, int h) {  // dV += P^T dA, dK_hat += dS^T Q_hat over those rows
+                const uint32_t qd = KP_QD + (n & 1) * 2 * TILE128 + h * 64 * 128;
 #pragma unroll
-                for (int ks = 0; ks < 128 / 16; ++ks) {
-                    umma_tmem_a(tbase + C_DV, tbase + C_S + ks * 8,
-                                sdesc(sbase + qd + TILE128 + ks * 16 * 128, CH128, 1024, kSw128), id_o,
-                                (n > 0 || ks > 0) ? 1u : 0u);
-                    umma_tmem_a(tbase + C_DK, tbase + C_DP + ks * 8, sdesc(sbase + qd + ks * 16 * 128, CH128, 1024, kSw128),
-                                id_o, (n > 0 || ks > 0) ? 1u : 0u);
+                for (int ks = 0; ks < 64 / 16; ++ks) {
+                    const uint32_t acc = (n > 0 || h > 0 || ks > 0) ? 1u : 0u;
+                    umma_tmem_a(tbase + C_DV, tbase + C_S + 64 * h + ks * 8,
+                                sdesc(sbase + qd + TILE128 + ks * 16 * 128, CH128, 1024, kSw128), id_o, acc);
+                    umma_tmem_a(tbase + C_DK, tbase + C_DP + 64 * h + ks * 8,
+                                sdesc(sbase + qd + ks * 16 * 128, CH128, 1024, kSw128), id_o, acc);
                 }
-                umma_commit(&qd_empty[n & 1]);
             };
             load_qd(0);
             if (n_tiles > 1) load_qd(1);
             bool ok = mbar_wait(kv_full, 0, p.ctl, 111) && mbar_wait(&qd_full[0], 0, p.ctl, 112);
             if (ok) {
                 tc_fence_after();
-                issue_s(0);
+                issue_s(0, 0);
+                issue_s(0, 1);
             }
+            // per tile: half 0's accumulation, then (once the next tile is in) the next
+            // tile's half-0 scores, so the warps of half 0 move on while half 1 finishes
             for (int n = 0; n < n_tiles && ok && !aborted(); ++n) {
-                ok = mbar_wait(p_ready, n & 1, p.ctl, 113);
+                const bool more = n + 1 < n_tiles;
+                ok = mbar_wait(&p_ready[0], n & 1, p.ctl, 113);
                 if (!ok) break;
                 tc_fence_after();
-                issue_acc(n);
-                if (n + 1 < n_tiles) {
+                issue_acc(n, 0);
+                if (more) {
                     ok = mbar_wait(&qd_full[(n + 1) & 1], ((n + 1) >> 1) & 1, p.ctl, 114);
                     if (!ok) break;
                     tc_fence_after();
-                    issue_s(n + 1);
+                    issue_s(n + 1, 0);
                 }
+                ok = mbar_wait(&p_ready[1], n & 1, p.ctl, 120);
+                if (!ok) break;
+                tc_fence_after();
+                issue_acc(n, 1);
+                umma_commit(&qd_empty[n & 1]);
+                if (more) issue_s(n + 1, 1);
                 if (n + 2 < n_tiles) {
                     ok = mbar_wait(&qd_empty[n & 1], (n >> 1) & 1, p.ctl, 115);
                     if (!ok) break;
@@ -531,12 +695,21 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kpass_kernel(const __grid_con
                 }
             }
             umma_commit(done);
+            // the raw keys for the RMSNorm backward, into the ring once every product is done
+            if (ok) ok = mbar_wait(done, 0, p.ctl, 118);
+            if (ok) {
+                mbar_arrive_expect_tx(x_full, TILE128);
+                for (int ch = 0; ch < 2; ++ch)
+                    tma_load_4d(smem + KP_X + ch * CH128, &p.tm_kraw, x_full, ch * 64, g, j0, b);
+            }
             if (!ok) fail();
         }
     } else {
-        // ------------------------------------------------------------ rows (thread = key row = TMEM lane)
-        const int row = threadIdx.x;
-        const uint32_t lane_addr = tbase + (static_cast<uint32_t>(warp * 32) << 16);
+        // ------------------------------------------------------------ rows (thread = key row = TMEM lane;
+        // warps 0-3 the query columns [0, 64) of every tile, warps 4-7 the columns [64, 128))
+        const int h = warp >> 2;
+        const int row = (warp & 3) * 32 + lane;
+        const uint32_t lane_addr = tbase + (static_cast<uint32_t>((warp & 3) * 32) << 16);
         const int kj = j0 + row;
         const bool valid_key = kj < p.L;
         const float sl = p.scale_log2;
@@ -544,37 +717,37 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kpass_kernel(const __grid_con
         bool ok = true;
         for (int n = 0; n < n_tiles && ok; ++n) {
             const int u0 = j0 + n * T;
-            // this tile's query-row statistics, one copy per warp (no barrier across warps:
-            // a warp that gives up on a wait must not leave the others blocked)
-            float4* sts = stat_s + warp * 128;
+            // the statistics of this half's 64 query rows, one copy per warp (no barrier across
+            // warps: a warp that gives up on a wait must not leave the others blocked)
+            float4* sts = stat_s + warp * 64;
             __syncwarp();
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int c = lane + 32 * i;
+            for (int i = 0; i < 2; ++i) {
+                const int c = 64 * h + lane + 32 * i;
                 const int u = u0 + c / G;
-                sts[c] = u < p.L ? p.stat[(static_cast<long long>(b) * p.L + u) * p.Hq + g * G + c % G]
-                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+                sts[lane + 32 * i] = u < p.L ? p.stat[(static_cast<long long>(b) * p.L + u) * p.Hq + g * G + c % G]
+                                             : make_float4(0.f, 0.f, 0.f, 0.f);
             }
             __syncwarp();
-            if (aborted() || !__all_sync(0xffffffffu, mbar_wait(s_full, n & 1, p.ctl, 116))) {
+            if (aborted() || !__all_sync(0xffffffffu, mbar_wait(&s_full[h], n & 1, p.ctl, 116))) {
                 ok = false;
                 break;
             }
             tc_fence_after();
 #pragma unroll 1
-            for (int k = 0; k < 128 / 32; ++k) {
+            for (int k = 0; k < 2; ++k) {
                 uint32_t r[32], dp[32], pp[16], dd[16];
-                tmem_ld32(lane_addr + C_S + 32 * k, r);
-                tmem_ld32(lane_addr + C_DP + 32 * k, dp);
+                tmem_ld32(lane_addr + C_S + 64 * h + 32 * k, r);
+                tmem_ld32(lane_addr + C_DP + 64 * h + 32 * k, dp);
                 tmem_wait_ld();
 #pragma unroll
                 for (int i = 0; i < 32; i += 2) {
                     float pv[2], dv2[2];
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
-                        const int c = 32 * k + i + e;
-                        const int u = u0 + c / G;
-                        const float4 s4 = sts[c];
+                        const int cl = 32 * k + i + e;  // column within the half
+                        const int u = u0 + (64 * h + cl) / G;
+                        const float4 s4 = sts[cl];
                         const bool v = valid_key && u >= kj && u - kj < W && u < p.L;
                         const float pr = v ? ex2_approx(fmaf(__uint_as_float(r[i + e]), sl, -s4.x)) * s4.y : 0.f;
                         pv[e] = pr;
@@ -583,47 +756,62 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kpass_kernel(const __grid_con
                     pp[i / 2] = pack_bf16x2(pv[0], pv[1]);
                     dd[i / 2] = pack_bf16x2(dv2[0], dv2[1]);
                 }
-                tmem_st16(lane_addr + C_S + 16 * k, pp);   // P^T over S^T
-                tmem_st16(lane_addr + C_DP + 16 * k, dd);  // dS^T over dP^T
+                tmem_st16(lane_addr + C_S + 64 * h + 16 * k, pp);   // P^T over S^T (columns already read)
+                tmem_st16(lane_addr + C_DP + 64 * h + 16 * k, dd);  // dS^T over dP^T
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(p_ready);
+            mbar_arrive(&p_ready[h]);
         }
         if (!ok) fail();
-        if (ok && !aborted()) ok = __all_sync(0xffffffffu, mbar_wait(done, 0, p.ctl, 117));
-        if (ok) {
-            tc_fence_after();
-            float* stage = reinterpret_cast<float*>(smem + KP_QD);  // the query ring is free now
-            float* st = stage + row * SROW;
-            const int L = p.L, Hkv = p.Hkv;
-            const long long row0 = (static_cast<long long>(b) * L + j0) * Hkv + g;  // (b, j0, g)
-            auto dst = [=](float* base) {
-                return [=](int r) -> float* { return j0 + r < L ? base + (row0 + static_cast<long long>(r) * Hkv) * D : nullptr; };
-            };
-#pragma unroll 1
-            for (int k = 0; k < D / 32; ++k) {
-                uint32_t r[32];
-                tmem_ld32(lane_addr + C_DV + 32 * k, r);
-                tmem_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) st[32 * k + i] = __uint_as_float(r[i]);
+        if (warp < 4) {
+            // ---- epilogue (warps 0-3): dV, then dK_hat back through RoPE and RMSNorm; both leave
+            // by bulk tensor stores (rows past the sequence end fall outside the tensor)
+            if (ok && !aborted()) ok = __all_sync(0xffffffffu, mbar_wait(done, 0, p.ctl, 117));
+            uint8_t* dv_t = smem + KP_DV;
+            uint8_t* dk_t = smem + KP_DK;
+            if (ok) {
+                tc_fence_after();
+                tmem_row_to_tile(lane_addr + C_DV, dv_t, row, 1.0f);
+                fence_async_smem();
             }
-            store_rows(stage, warp, lane, dst(p.dv));
-#pragma unroll 1
-            for (int k = 0; k < D / 32; ++k) {
-                uint32_t r[32];
-                tmem_ld32(lane_addr + C_DK + 32 * k, r);
-                tmem_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) st[32 * k + i] = __uint_as_float(r[i]) * p.scale;
+            mbar_arrive(dv_stg);
+            if (row == 0 && ok) {
+                if (mbar_wait(dv_stg, 0, p.ctl, 97)) {
+                    for (int k = 0; k < 4; ++k) tma_store_4d(&p.tm_dvf, dv_t + k * F32BOX, 32 * k, g, j0, b);
+                    bulk_commit();
+                } else {
+                    ok = false;
+                }
             }
-            if (valid_key)
-                row_norm_rope_bwd(st, p.k + ((static_cast<long long>(b) * p.L + kj) * p.Hkv + g) * D, w_s, p.eps,
-                                  __ldg(p.pos + static_cast<long long>(b) * p.L + kj), p.rope);
-            store_rows(stage, warp, lane, dst(p.dk));
+            ok = __all_sync(0xffffffffu, ok);
+            if (ok) {
+                tmem_row_to_tile(lane_addr + C_DK, dk_t, row, p.scale);
+                if (!aborted()) ok = __all_sync(0xffffffffu, mbar_wait(x_full, 0, p.ctl, 119));
+            }
+            if (ok) {
+                if (valid_key) {
+                    const int pos = __ldg(p.pos + static_cast<long long>(b) * p.L + kj);
+                    row_norm_rope_bwd(dk_t, row, smem + KP_X, w_s, p.eps, p.rope.half, [&](int j) {
+                        float cs, sn;
+                        rope_cos_sin(pos, p.rope.f_hi[j], p.rope.f_lo[j], cs, sn);
+                        return make_float2(cs, sn);
+                    });
+                }
+                fence_async_smem();
+            }
+            mbar_arrive(dk_stg);
+            if (row == 0 && ok) {
+                if (mbar_wait(dk_stg, 0, p.ctl, 96)) {
+                    for (int k = 0; k < 4; ++k) tma_store_4d(&p.tm_dkf, dk_t + k * F32BOX, 32 * k, g, j0, b);
+                    bulk_commit();
+                } else {
+                    ok = false;
+                }
+            }
+            if (row == 0) bulk_wait_all();
+            if (!ok) fail();
         }
-        if (!ok) fail();
     }
     __syncthreads();
     if (aborted() && threadIdx.x == 0) {
@@ -633,7 +821,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kpass_kernel(const __grid_con
     }
     tc_fence_after();
     __syncthreads();
-    if (warp == 4) tmem_dealloc(tbase, 512);
+    if (warp == 8) tmem_dealloc(tbase, 512);
 }
 
 }  // namespace
@@ -650,7 +838,7 @@ size_t backward_tc_workspace_bytes(int B, int L, int Hq, int Hkv) {
 cudaError_t launch_backward_tc(const BackwardTcParams& p, cudaStream_t s) {
     const long long nq = static_cast<long long>(p.B) * p.L * p.Hq, nk = static_cast<long long>(p.B) * p.L * p.Hkv;
     if (nq == 0) return cudaSuccess;
-    bwd_tc_prep_kernel<<<static_cast<unsigned>((nq + nk + 7) / 8), 256, 0, s>>>(p);
+    bwd_tc_prep_kernel<<<static_cast<unsigned>((nq + nk + 8 * kPrepRows - 1) / (8 * kPrepRows)), 256, 0, s>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(bwd_qpass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, QP_SMEM);
@@ -661,7 +849,7 @@ cudaError_t launch_backward_tc(const BackwardTcParams& p, cudaStream_t s) {
     bwd_qpass_kernel<<<static_cast<unsigned>(nbg * ((p.L + T - 1) / T)), kThreads, QP_SMEM, s>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    bwd_kpass_kernel<<<static_cast<unsigned>(nbg * ((p.L + BK - 1) / BK)), kThreads, KP_SMEM, s>>>(p);
+    bwd_kpass_kernel<<<static_cast<unsigned>(nbg * ((p.L + BK - 1) / BK)), kKThreads, KP_SMEM, s>>>(p);
     return cudaGetLastError();
 }
 

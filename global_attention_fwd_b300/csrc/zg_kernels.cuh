@@ -133,6 +133,10 @@ struct BackwardTcParams {
     CUtensorMap tm_qh, tm_da;  // q_hat, dA workspace (bf16 [B, L, Hq, d]): box {64, 4 heads, 32 tokens}
     CUtensorMap tm_kq, tm_vq;  // k_hat workspace, v: box {64, 1, 160 tokens}
     CUtensorMap tm_kk, tm_vk;  // k_hat workspace, v: box {64, 1, 128 tokens}
+    CUtensorMap tm_q, tm_gate, tm_dout;  // raw q, gate, dout: box {64, 4 heads, 32 tokens}
+    CUtensorMap tm_kraw;                 // raw k: box {64, 1, 128 tokens}
+    CUtensorMap tm_dg, tm_dqf;           // dgate, dq (fp32): box {32, 4 heads, 32 tokens}, stores
+    CUtensorMap tm_dkf, tm_dvf;          // dk, dv (fp32): box {32, 1, 128 tokens}, stores
     const __nv_bfloat16* q;     // raw inputs (RMSNorm backward, dA)
     const __nv_bfloat16* k;
     const __nv_bfloat16* gate;  // or null
