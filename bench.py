@@ -87,15 +87,13 @@ def global_flops(c):  # 2 matmuls x 2 flop x d per unmasked (row, key, head)
     return 4.0 * c.d * c.Hq * c.B * (c.L * (c.L + 1) / 2)
 
 
-def decode_bytes(c):  # caches read once (global 0..p, rings all slots), new-token rows, outputs
+def decode_bytes(c, cache_elem_bytes=2):  # caches read once (global 0..p, rings all slots), new-token rows, outputs
     ng = len(c.global_layers)
     ns = c.NL - ng
-    cache = 2 * ng * c.B * c.Hkv * (c.pos + 1) * c.d * 2 + 2 * ns * c.B * c.Hkv * c.W * c.d * 2
+    eb = cache_elem_bytes
+    cache = 2 * ng * c.B * c.Hkv * (c.pos + 1) * c.d * eb + 2 * ns * c.B * c.Hkv * c.W * c.d * eb
     tok = c.NL * c.B * (3 * c.Hq + 2 * c.Hkv) * c.d * 2
     return cache + tok
-
-
-FP32_PEAK_TFLOPS = 148 * 128 * 2 * 2.032e9 / 1e12  # fp32 FMA lanes x 2 flop x maximum SM clock
 
 
 def window_pairs(c) -> int:
@@ -465,6 +463,36 @@ def run_gpu(args):
                         "algorithmic_flops": l_fl,
                         "note": "projection GEMM flops only; the attention inside is HBM-bound"}}
 
+    # ---- the decode step over E4M3 caches (outside the step): the same workload, caches stored
+    # as e4m3(k_hat * 1) and e4m3(v * 8)
+    f8 = {k: workloads.to_e4m3(v, 1.0 if k.startswith("k") else 8.0) for k, v in caches.items()}
+
+    def dec8():
+        zg.hybrid_decode_fp8(tok["q"], tok["k_new"], tok["v_new"], tok["gate"], tok["pos"], tok["wq"], tok["wk"],
+                             flags, f8["k_glob"], f8["v_glob"], f8["k_ring"], f8["v_ring"], k_scale=1.0, v_scale=8.0,
+                             rotary_dim=DEC.rotary_dim, theta=DEC.theta, eps=DEC.eps, out=d_out, workspace=d_ws)
+
+    for _ in range(3):
+        dec8()
+    f8_ev = []
+    for _ in range(10):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        dec8()
+        b.record(stream)
+        f8_ev.append((a, b))
+    torch.cuda.synchronize()
+    st, detail = zg.device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} detail {detail:#x} after the fp8 decode")
+    f8_t = statistics.median(a.elapsed_time(b) for a, b in f8_ev) * 1e-3
+    f8_by = decode_bytes(DEC, cache_elem_bytes=1)
+    dec_fp8 = {"workload": f"{DEC.name} with E4M3 caches", "us_per_step": f8_t * 1e6,
+               "roofline": {"bound": "hbm", "achieved": f8_by / f8_t / 1e9, "peak": hbm, "unit": "GB/s",
+                            "frac": f8_by / f8_t / 1e9 / hbm, "traffic": None, "algorithmic_bytes": f8_by}}
+    del f8
+
     # ---- backward of the gated SWA prefill (outside the step): the 4K training shape
     bx = workloads.prefill_inputs_device(C2, dev)
     bdout = torch.randn(C2.B, C2.L, C2.Hq, C2.d, generator=gen, device=dev).to(torch.bfloat16)
@@ -492,12 +520,16 @@ def run_gpu(args):
         raise RuntimeError(f"device status {st} detail {detail:#x} after the backward pass")
     b_t = statistics.median(a.elapsed_time(b) for a, b in b_ev) * 1e-3
     b_fl = backward_flops(C2)
-    fp32_peak = FP32_PEAK_TFLOPS
-    bwd = {"workload": f"{C2.name} backward (dq, dk, dv, dgate)", "ms": b_t * 1e3, "tokens_per_s": C2.tokens / b_t,
-           "roofline": {"bound": "alu", "achieved": b_fl / b_t / 1e12, "peak": fp32_peak, "unit": "TFLOP/s",
-                        "frac": b_fl / b_t / 1e12 / fp32_peak, "traffic": None, "algorithmic_flops": b_fl,
-                        "peak_note": "fp32 FMA: 148 SMs x 128 lanes x 2 flop x 2032 MHz (nominal units and clock)"},
-           "hbm_bytes": backward_bytes(C2)}
+    b_by = backward_bytes(C2)
+    b_tr = [_traffic(k) for k in ("bwd_tc_prep_kernel", "bwd_qpass_kernel", "bwd_kpass_kernel")]
+    bwd = {"workload": f"{C2.name} backward (dq, dk, dv, dgate), three kernels per call", "ms": b_t * 1e3,
+           "tokens_per_s": C2.tokens / b_t,
+           "roofline": {"bound": "hbm", "achieved": b_by / b_t / 1e9, "peak": hbm, "unit": "GB/s",
+                        "frac": b_by / b_t / 1e9 / hbm,
+                        "traffic": sum(b_tr) if all(x is not None for x in b_tr) else None,
+                        "algorithmic_bytes": b_by},
+           "tensor": {"achieved_tflops": b_fl / b_t / 1e12, "peak": peaks["bf16_tflops"],
+                      "frac": b_fl / b_t / 1e12 / peaks["bf16_tflops"], "algorithmic_flops": b_fl}}
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
@@ -515,6 +547,7 @@ def run_gpu(args):
             "gated_swa_layer": lay,
             "kv_cache_write": kvc,
             "attention_backward": bwd,
+            "hybrid_decode_fp8": dec_fp8,
             "swa_prefill": {"workload": SWA.name, "ms": sw_t * 1e3, "tokens_per_s": SWA.tokens / sw_t,
                             "roofline": rl_swa},
             "hybrid_decode": {"workload": DEC.name, "us_per_step": dc_t * 1e6, "roofline": rl_dec},

@@ -30,6 +30,7 @@ EXPORTS = ("zg_swa_prefill", "zg_global_prefill_workspace_bytes", "zg_global_pre
            "zg_gated_swa_layer_workspace_bytes", "zg_gated_swa_layer",
            "zg_attention_backward_workspace_bytes", "zg_attention_backward",
            "zg_hybrid_decode_workspace_bytes", "zg_hybrid_decode", "zg_hybrid_decode_noalloc",
+           "zg_hybrid_decode_fp8", "zg_kv_cache_write_fp8",
            "zg_device_status", "zg_selftest_bounded_wait", "zg_status_string")
 
 
@@ -69,6 +70,10 @@ def _load() -> ctypes.CDLL:
     lib.zg_hybrid_decode_workspace_bytes.restype = SZ
     lib.zg_hybrid_decode.argtypes = [P] * 13 + [I] * 5 + [I64, I, I, D, F, P, SZ, P]
     lib.zg_hybrid_decode.restype = I
+    lib.zg_hybrid_decode_fp8.argtypes = [P] * 13 + [I] * 5 + [I64, I, I, D, F, F, F, P, SZ, P]
+    lib.zg_hybrid_decode_fp8.restype = I
+    lib.zg_kv_cache_write_fp8.argtypes = [P] * 6 + [I] * 4 + [I64, I, I, D, F, F, F, P]
+    lib.zg_kv_cache_write_fp8.restype = I
     lib.zg_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
     lib.zg_device_status.restype = I
     lib.zg_selftest_bounded_wait.argtypes = [U64, P]
@@ -217,6 +222,22 @@ def kv_cache_write(k, v, pos, wk, k_cache, v_cache, *, ring, rotary_dim, theta, 
     _raise(st, "zg_kv_cache_write")
 
 
+def kv_cache_write_fp8(k, v, pos, wk, k_cache, v_cache, *, ring, k_scale=1.0, v_scale=1.0, rotary_dim, theta,
+                       eps=1e-6, stream=None):
+    """kv_cache_write into E4M3 caches (float8_e4m3fn or uint8 [B,Hkv,S,d]): e4m3(k_hat * k_scale), e4m3(v * v_scale)."""
+    for t, n in ((k, "k"), (v, "v")):
+        _check(t, n, torch.bfloat16, 4)
+    _check_cache(k_cache, "k_cache", True, 4)
+    _check_cache(v_cache, "v_cache", True, 4)
+    _check(pos, "pos", torch.int32, 2)
+    _check(wk, "wk", torch.float32)
+    B, L, Hkv, d = k.shape
+    st = _lib.zg_kv_cache_write_fp8(_ptr(k), _ptr(v), _ptr(pos), _ptr(wk), _ptr(k_cache), _ptr(v_cache), B, L, Hkv,
+                                    d, int(k_cache.shape[2]), 1 if ring else 0, int(rotary_dim), float(theta),
+                                    float(eps), float(k_scale), float(v_scale), _stream(stream))
+    _raise(st, "zg_kv_cache_write_fp8")
+
+
 def gated_swa_layer_workspace_bytes(B, L, Hq, Hkv, d) -> int:
     return int(_lib.zg_gated_swa_layer_workspace_bytes(int(B), int(L), int(Hq), int(Hkv), int(d)))
 
@@ -291,6 +312,31 @@ def hybrid_decode(q, k_new, v_new, gate, pos, wq, wk, is_global, k_glob, v_glob,
     """One decode step through the hybrid layer stack (caches updated in place).
     q, gate [NL,B,Hq,d]; k_new, v_new [NL,B,Hkv,d]; pos [B] int32 (device); wq, wk [NL,d];
     is_global: sequence of NL flags (host); k_glob, v_glob [NG,B,Hkv,S,d]; k_ring, v_ring [NS,B,Hkv,W,d]."""
+    return _decode(q, k_new, v_new, gate, pos, wq, wk, is_global, k_glob, v_glob, k_ring, v_ring, rotary_dim, theta,
+                   eps, out, workspace, stream, fp8=False, k_scale=1.0, v_scale=1.0)
+
+
+def hybrid_decode_fp8(q, k_new, v_new, gate, pos, wq, wk, is_global, k_glob, v_glob, k_ring, v_ring, *,
+                      k_scale=1.0, v_scale=1.0, rotary_dim, theta, eps=1e-6, out=None, workspace=None, stream=None):
+    """hybrid_decode over E4M3 caches (torch.float8_e4m3fn or uint8 tensors of the same shapes) holding
+    e4m3(k_hat * k_scale) and e4m3(v * v_scale)."""
+    return _decode(q, k_new, v_new, gate, pos, wq, wk, is_global, k_glob, v_glob, k_ring, v_ring, rotary_dim, theta,
+                   eps, out, workspace, stream, fp8=True, k_scale=k_scale, v_scale=v_scale)
+
+
+def _check_cache(t, name, fp8, ndim):
+    if fp8:
+        if t is None:
+            raise ValueError(f"{name} is required")
+        if t.dtype not in (torch.uint8, getattr(torch, "float8_e4m3fn", torch.uint8)):
+            raise ValueError(f"{name} must be float8_e4m3fn or uint8, got {t.dtype}")
+        _check(t, name, t.dtype, ndim)
+    else:
+        _check(t, name, torch.bfloat16, ndim)
+
+
+def _decode(q, k_new, v_new, gate, pos, wq, wk, is_global, k_glob, v_glob, k_ring, v_ring, rotary_dim, theta, eps,
+            out, workspace, stream, *, fp8, k_scale, v_scale):
     for t, n in ((q, "q"), (k_new, "k_new"), (v_new, "v_new"), (gate, "gate")):
         _check(t, n, torch.bfloat16)
     _check(pos, "pos", torch.int32, 1)
@@ -303,12 +349,12 @@ def hybrid_decode(q, k_new, v_new, gate, pos, wq, wk, is_global, k_glob, v_glob,
     S = 0
     W = 0
     if NG:
-        _check(k_glob, "k_glob", torch.bfloat16, 5)
-        _check(v_glob, "v_glob", torch.bfloat16, 5)
+        _check_cache(k_glob, "k_glob", fp8, 5)
+        _check_cache(v_glob, "v_glob", fp8, 5)
         S = k_glob.shape[3]
     if NL - NG:
-        _check(k_ring, "k_ring", torch.bfloat16, 5)
-        _check(v_ring, "v_ring", torch.bfloat16, 5)
+        _check_cache(k_ring, "k_ring", fp8, 5)
+        _check_cache(v_ring, "v_ring", fp8, 5)
         W = k_ring.shape[3]
     else:
         W = 128
@@ -319,11 +365,16 @@ def hybrid_decode(q, k_new, v_new, gate, pos, wq, wk, is_global, k_glob, v_glob,
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     flag_buf = ctypes.create_string_buffer(flags, len(flags))
-    st = _lib.zg_hybrid_decode(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(gate), _ptr(pos), _ptr(wq), _ptr(wk),
-                               ctypes.cast(flag_buf, ctypes.c_void_p), _ptr(k_glob), _ptr(v_glob), _ptr(k_ring),
-                               _ptr(v_ring), _ptr(out), NL, B, Hq, Hkv, d, int(S), int(W), int(rotary_dim),
-                               float(theta), float(eps), _ptr(workspace), ws_bytes, _stream(stream))
-    _raise(st, "zg_hybrid_decode")
+    head = (_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(gate), _ptr(pos), _ptr(wq), _ptr(wk),
+            ctypes.cast(flag_buf, ctypes.c_void_p), _ptr(k_glob), _ptr(v_glob), _ptr(k_ring), _ptr(v_ring), _ptr(out),
+            NL, B, Hq, Hkv, d, int(S), int(W), int(rotary_dim), float(theta), float(eps))
+    if fp8:
+        st = _lib.zg_hybrid_decode_fp8(*head, float(k_scale), float(v_scale), _ptr(workspace), ws_bytes,
+                                       _stream(stream))
+        _raise(st, "zg_hybrid_decode_fp8")
+    else:
+        st = _lib.zg_hybrid_decode(*head, _ptr(workspace), ws_bytes, _stream(stream))
+        _raise(st, "zg_hybrid_decode")
     return out
 
 

@@ -113,16 +113,16 @@ namespace zg {
 namespace {
 // ---------------------------------------------------------------- prefill + decode caches
 // host checks of the cache arguments (done before anything is launched)
-zg_status check_cache(const zg_bf16* ck, const zg_bf16* cv, int d, long long S) {
+zg_status check_cache(const void* ck, const void* cv, int d, long long S) {
     if (!ck || !cv) return ZG_ERR_NULL;
     if (!aligned16(ck) || !aligned16(cv)) return ZG_ERR_ALIGN;
     if (S < 1) return ZG_ERR_SHAPE;
     if (d != 128) return ZG_ERR_UNSUPPORTED;  // the decode step reads d = 128 caches
     return ZG_OK;
 }
-zg_status write_cache(const zg_bf16* k, const zg_bf16* v, const int32_t* pos, const float* wk, zg_bf16* ck,
-                      zg_bf16* cv, int B, int L, int Hkv, int d, long long S, bool ring, int rotary_dim, double theta,
-                      float eps, zg_stream stream) {
+zg_status write_cache(const zg_bf16* k, const zg_bf16* v, const int32_t* pos, const float* wk, void* ck,
+                      void* cv, int B, int L, int Hkv, int d, long long S, bool ring, int rotary_dim, double theta,
+                      float eps, zg_stream stream, int fp8 = 0, float k_scale = 1.0f, float v_scale = 1.0f) {
     if (B == 0 || L == 0) return ZG_OK;
     CacheParams c;
     std::memset(&c, 0, sizeof(c));
@@ -131,8 +131,11 @@ zg_status write_cache(const zg_bf16* k, const zg_bf16* v, const int32_t* pos, co
     c.v = reinterpret_cast<const __nv_bfloat16*>(v);
     c.pos = pos;
     c.wk = wk;
-    c.cache_k = reinterpret_cast<__nv_bfloat16*>(ck);
-    c.cache_v = reinterpret_cast<__nv_bfloat16*>(cv);
+    c.cache_k = static_cast<__nv_bfloat16*>(ck);  // E4M3 bytes when fp8
+    c.cache_v = static_cast<__nv_bfloat16*>(cv);
+    c.fp8 = fp8;
+    c.k_scale = k_scale;
+    c.v_scale = v_scale;
     c.B = B;
     c.L = L;
     c.Hkv = Hkv;
@@ -242,6 +245,22 @@ zg_status zg_kv_cache_write(const zg_bf16* k, const zg_bf16* v, const int32_t* p
     if (rotary_dim < 0 || rotary_dim > d || (rotary_dim & 1) || !(theta > 0.0) || !(eps >= 0.0f)) return ZG_ERR_SHAPE;
     if (static_cast<long long>(B) * L * Hkv / 8 >= (1ll << 31)) return ZG_ERR_UNSUPPORTED;
     return write_cache(k, v, pos, wk, k_cache, v_cache, B, L, Hkv, d, S, ring != 0, rotary_dim, theta, eps, stream);
+}
+
+zg_status zg_kv_cache_write_fp8(const zg_bf16* k, const zg_bf16* v, const int32_t* pos, const float* wk,
+                                uint8_t* k_cache, uint8_t* v_cache, int B, int L, int Hkv, int d, int64_t S, int ring,
+                                int rotary_dim, double theta, float eps, float k_scale, float v_scale,
+                                zg_stream stream) {
+    if (!k || !v || !pos || !wk) return ZG_ERR_NULL;
+    if (!aligned16(k) || !aligned16(v) || !aligned16(pos) || !aligned16(wk)) return ZG_ERR_ALIGN;
+    zg_status st = check_cache(k_cache, v_cache, d, S);
+    if (st != ZG_OK) return st;
+    if (B < 0 || L < 0 || Hkv <= 0 || (ring != 0 && ring != 1)) return ZG_ERR_SHAPE;
+    if (rotary_dim < 0 || rotary_dim > d || (rotary_dim & 1) || !(theta > 0.0) || !(eps >= 0.0f)) return ZG_ERR_SHAPE;
+    if (!(std::isfinite(k_scale) && k_scale > 0.f && std::isfinite(v_scale) && v_scale > 0.f)) return ZG_ERR_SHAPE;
+    if (static_cast<long long>(B) * L * Hkv / 8 >= (1ll << 31)) return ZG_ERR_UNSUPPORTED;
+    return write_cache(k, v, pos, wk, k_cache, v_cache, B, L, Hkv, d, S, ring != 0, rotary_dim, theta, eps, stream, 1,
+                       k_scale, v_scale);
 }
 
 zg_status zg_swa_prefill_with_cache(const zg_bf16* q, const zg_bf16* k, const zg_bf16* v, const zg_bf16* gate,
@@ -444,12 +463,16 @@ size_t zg_hybrid_decode_workspace_bytes(int NG, int B, int Hq, int d, int64_t S_
     return decode_workspace_bytes(NG, B, Hq, S_max);
 }
 
-zg_status zg_hybrid_decode(const zg_bf16* q, const zg_bf16* k_new, const zg_bf16* v_new, const zg_bf16* gate,
-                           const int32_t* pos, const float* wq, const float* wk, const uint8_t* is_global,
-                           zg_bf16* k_glob, zg_bf16* v_glob, zg_bf16* k_ring, zg_bf16* v_ring, zg_bf16* out, int NL,
-                           int B, int Hq, int Hkv, int d, int64_t S_max, int window, int rotary_dim, double theta,
-                           float eps, void* workspace, size_t workspace_bytes, zg_stream stream) {
+// one decode step over bf16 (fp8 = 0) or E4M3 (fp8 = 1) caches
+static zg_status hybrid_decode_impl(const zg_bf16* q, const zg_bf16* k_new, const zg_bf16* v_new, const zg_bf16* gate,
+                                    const int32_t* pos, const float* wq, const float* wk, const uint8_t* is_global,
+                                    void* k_glob, void* v_glob, void* k_ring, void* v_ring, zg_bf16* out, int NL,
+                                    int B, int Hq, int Hkv, int d, int64_t S_max, int window, int rotary_dim,
+                                    double theta, float eps, void* workspace, size_t workspace_bytes, int fp8,
+                                    float k_scale, float v_scale, zg_stream stream) {
     if (!q || !k_new || !v_new || !gate || !pos || !wq || !wk || !is_global || !out) return ZG_ERR_NULL;
+    if (fp8 && !(std::isfinite(k_scale) && k_scale > 0.f && std::isfinite(v_scale) && v_scale > 0.f))
+        return ZG_ERR_SHAPE;
     if (NL < 0 || B < 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || Hq % Hkv || window <= 0) return ZG_ERR_SHAPE;
     if (rotary_dim < 0 || rotary_dim > d || (rotary_dim & 1) || !(theta > 0.0) || !(eps >= 0.0f)) return ZG_ERR_SHAPE;
     if (NL > kMaxLayers) return ZG_ERR_UNSUPPORTED;
@@ -484,10 +507,10 @@ zg_status zg_hybrid_decode(const zg_bf16* q, const zg_bf16* k_new, const zg_bf16
     p.pos = pos;
     p.wq = wq;
     p.wk = wk;
-    p.k_glob = reinterpret_cast<__nv_bfloat16*>(k_glob);
-    p.v_glob = reinterpret_cast<__nv_bfloat16*>(v_glob);
-    p.k_ring = reinterpret_cast<__nv_bfloat16*>(k_ring);
-    p.v_ring = reinterpret_cast<__nv_bfloat16*>(v_ring);
+    p.k_glob = static_cast<__nv_bfloat16*>(k_glob);  // E4M3 bytes when fp8
+    p.v_glob = static_cast<__nv_bfloat16*>(v_glob);
+    p.k_ring = static_cast<__nv_bfloat16*>(k_ring);
+    p.v_ring = static_cast<__nv_bfloat16*>(v_ring);
     p.out = reinterpret_cast<__nv_bfloat16*>(out);
     const size_t rows = static_cast<size_t>(NG) * B * Hq * static_cast<size_t>(nsplit);
     p.ws_o = static_cast<float*>(workspace);
@@ -504,10 +527,34 @@ zg_status zg_hybrid_decode(const zg_bf16* q, const zg_bf16* k_new, const zg_bf16
     p.nsplit = static_cast<int>(nsplit);
     for (int i = 0; i < NG; ++i) p.layer_of_global[i] = glob_layers[i];
     for (int i = 0; i < NS; ++i) p.layer_of_local[i] = loc_layers[i];
+    p.fp8 = fp8;
+    p.k_scale = k_scale;
+    p.v_scale = v_scale;
     p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
     p.eps = eps;
     if (!rope_consts(p.rope, rotary_dim, theta)) return ZG_ERR_SHAPE;
     return launch_hybrid_decode(p, d, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? ZG_OK : ZG_ERR_CUDA;
+}
+
+zg_status zg_hybrid_decode(const zg_bf16* q, const zg_bf16* k_new, const zg_bf16* v_new, const zg_bf16* gate,
+                           const int32_t* pos, const float* wq, const float* wk, const uint8_t* is_global,
+                           zg_bf16* k_glob, zg_bf16* v_glob, zg_bf16* k_ring, zg_bf16* v_ring, zg_bf16* out, int NL,
+                           int B, int Hq, int Hkv, int d, int64_t S_max, int window, int rotary_dim, double theta,
+                           float eps, void* workspace, size_t workspace_bytes, zg_stream stream) {
+    return hybrid_decode_impl(q, k_new, v_new, gate, pos, wq, wk, is_global, k_glob, v_glob, k_ring, v_ring, out, NL,
+                              B, Hq, Hkv, d, S_max, window, rotary_dim, theta, eps, workspace, workspace_bytes, 0,
+                              1.0f, 1.0f, stream);
+}
+
+zg_status zg_hybrid_decode_fp8(const zg_bf16* q, const zg_bf16* k_new, const zg_bf16* v_new, const zg_bf16* gate,
+                               const int32_t* pos, const float* wq, const float* wk, const uint8_t* is_global,
+                               uint8_t* k_glob, uint8_t* v_glob, uint8_t* k_ring, uint8_t* v_ring, zg_bf16* out,
+                               int NL, int B, int Hq, int Hkv, int d, int64_t S_max, int window, int rotary_dim,
+                               double theta, float eps, float k_scale, float v_scale, void* workspace,
+                               size_t workspace_bytes, zg_stream stream) {
+    return hybrid_decode_impl(q, k_new, v_new, gate, pos, wq, wk, is_global, k_glob, v_glob, k_ring, v_ring, out, NL,
+                              B, Hq, Hkv, d, S_max, window, rotary_dim, theta, eps, workspace, workspace_bytes, 1,
+                              k_scale, v_scale, stream);
 }
 
 zg_status zg_device_status(uint32_t* detail) {

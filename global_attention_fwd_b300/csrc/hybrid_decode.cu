@@ -25,6 +25,14 @@
 // local layers finish in place (1/l, sigmoid gate, bf16 store).  The CTA that
 // owns position p also writes the new cache slot and adds the new key itself.
 // Kernel 2 merges the splits of every global (layer, b, head) in a fixed order.
+//
+// FP8 caches (E4M3, the pages' forward FP8 format: "ZGCM-1-7B 完全解説", section on the
+// training recipe) hold e4m3(k_hat * k_scale) and e4m3(v * v_scale): the same stage bytes
+// carry 64 keys instead of 32, lanes widen e4m3 pairs to fp16 pairs, 1 / k_scale is folded
+// into q_hat and 1 / v_scale into the output.  RMSNorm bounds |k_hat| by sqrt(d) max|wk|,
+// far inside the E4M3 range, so keys need no scale beyond that bound.
+#include <cuda_fp8.h>
+
 #include "zg_qk.cuh"
 
 namespace zg {
@@ -32,7 +40,7 @@ namespace {
 
 constexpr int D = 128;
 constexpr int G = 4;               // query heads per KV head
-constexpr int KPS = 32;            // keys per stage
+constexpr int KPS = 32;            // keys per stage (bf16 caches; 64 for fp8 caches)
 constexpr int NST = 6;             // stages (6 x 32 keys measured faster than 3 x 64 on B300)
 constexpr int NCW = 8;             // compute warps
 constexpr int NTHR = (NCW + 1) * 32;
@@ -63,8 +71,29 @@ __device__ __forceinline__ void ffma2(float2& acc, float2 a, float2 b) {
     acc = *reinterpret_cast<float2*>(&r);
 }
 __device__ __forceinline__ float2 bf2_to_f2(uint32_t u) { return make_float2(bf16lo(u), bf16hi(u)); }
+__device__ __forceinline__ float2 e4m3x2_to_f2(uint16_t u) {  // two E4M3 values, low byte first
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(u), __NV_E4M3);
+    return __half22float2(*reinterpret_cast<const __half2*>(&h));
+}
 
+template <bool FP8>
 __global__ void __launch_bounds__(NTHR, 2) decode_attn_kernel(const __grid_constant__ DecodeParams p) {
+    // 8 elements of a cache row (bf16: four words; E4M3: the first two words) -> 4 float pairs
+    auto widen4 = [](const uint4& w, float2* f) {
+        if (FP8) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                f[k] = e4m3x2_to_f2(static_cast<uint16_t>((k < 2 ? w.x : w.y) >> (16 * (k & 1))));
+        } else {
+            f[0] = bf2_to_f2(w.x);
+            f[1] = bf2_to_f2(w.y);
+            f[2] = bf2_to_f2(w.z);
+            f[3] = bf2_to_f2(w.w);
+        }
+    };
+    constexpr int EB = FP8 ? 1 : 2;        // bytes per cache element
+    constexpr int KPT = FP8 ? 2 * KPS : KPS;  // keys per stage
+    static_assert(KPT * D * EB == STAGE_K, "a stage holds the same bytes for either cache type");
     extern __shared__ __align__(1024) uint8_t smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
     uint64_t* empty = full + NST;
@@ -98,8 +127,8 @@ __global__ void __launch_bounds__(NTHR, 2) decode_attn_kernel(const __grid_const
     const int pos = __ldg(p.pos + b);
     const bool pos_ok = pos >= 0 && static_cast<long long>(pos) < p.S;
     // keys streamed from the cache (positions before p) and whether this CTA owns p
-    const __nv_bfloat16 *kc, *vc;
-    __nv_bfloat16 *kslot = nullptr, *vslot = nullptr;
+    const uint8_t *kc, *vc;                       // cache rows of D elements, EB bytes each
+    uint8_t *kslot = nullptr, *vslot = nullptr;
     int nk = 0;
     bool owner = false;
     if (is_glob) {
@@ -108,21 +137,21 @@ __global__ void __launch_bounds__(NTHR, 2) decode_attn_kernel(const __grid_const
         long long k1 = k0 + p.split_len;
         if (pos_ok && k1 > pos) k1 = pos;
         nk = pos_ok && k1 > k0 ? static_cast<int>(k1 - k0) : 0;
-        kc = p.k_glob + (base + k0) * D;
-        vc = p.v_glob + (base + k0) * D;
+        kc = reinterpret_cast<const uint8_t*>(p.k_glob) + (base + k0) * D * EB;
+        vc = reinterpret_cast<const uint8_t*>(p.v_glob) + (base + k0) * D * EB;
         owner = pos_ok && pos / p.split_len == split;
-        kslot = p.k_glob + (base + pos) * D;
-        vslot = p.v_glob + (base + pos) * D;
+        kslot = reinterpret_cast<uint8_t*>(p.k_glob) + (base + pos) * D * EB;
+        vslot = reinterpret_cast<uint8_t*>(p.v_glob) + (base + pos) * D * EB;
     } else {
         const size_t base = ((static_cast<size_t>(lidx) * p.B + b) * p.Hkv + g) * static_cast<size_t>(p.W);
         nk = pos_ok ? p.W : 0;  // every slot is streamed; invalid ones are masked below
-        kc = p.k_ring + base * D;
-        vc = p.v_ring + base * D;
+        kc = reinterpret_cast<const uint8_t*>(p.k_ring) + base * D * EB;
+        vc = reinterpret_cast<const uint8_t*>(p.v_ring) + base * D * EB;
         owner = pos_ok;
-        kslot = p.k_ring + (base + (pos_ok ? pos % p.W : 0)) * D;
-        vslot = p.v_ring + (base + (pos_ok ? pos % p.W : 0)) * D;
+        kslot = reinterpret_cast<uint8_t*>(p.k_ring) + (base + (pos_ok ? pos % p.W : 0)) * D * EB;
+        vslot = reinterpret_cast<uint8_t*>(p.v_ring) + (base + (pos_ok ? pos % p.W : 0)) * D * EB;
     }
-    const int nstage = (nk + KPS - 1) / KPS;
+    const int nstage = (nk + KPT - 1) / KPT;
 
     if (threadIdx.x == 0) {
         *sflag = 1;
@@ -143,10 +172,12 @@ __global__ void __launch_bounds__(NTHR, 2) decode_attn_kernel(const __grid_const
                 const int buf = st % NST;
                 ok = mbar_wait(&empty[buf], ((st / NST) & 1) ^ 1, p.ctl, 40);
                 if (!ok) break;
-                const int rows = min(KPS, nk - st * KPS);
-                mbar_arrive_expect_tx(&full[buf], 2u * rows * D * 2);
-                bulk_load(smem + OFF_K + buf * STAGE_K, kc + static_cast<size_t>(st) * KPS * D, rows * D * 2, &full[buf]);
-                bulk_load(smem + OFF_V + buf * STAGE_K, vc + static_cast<size_t>(st) * KPS * D, rows * D * 2, &full[buf]);
+                const int rows = min(KPT, nk - st * KPT);
+                mbar_arrive_expect_tx(&full[buf], 2u * rows * D * EB);
+                bulk_load(smem + OFF_K + buf * STAGE_K, kc + static_cast<size_t>(st) * KPT * D * EB, rows * D * EB,
+                          &full[buf]);
+                bulk_load(smem + OFF_V + buf * STAGE_K, vc + static_cast<size_t>(st) * KPT * D * EB, rows * D * EB,
+                          &full[buf]);
                 ++issued;
             }
             if (!ok) {
@@ -170,9 +201,18 @@ __global__ void __launch_bounds__(NTHR, 2) decode_attn_kernel(const __grid_const
                 for (int e = lane; e < D; e += 32) vn[e] = __bfloat162float(vx[e]);
                 __syncwarp();
                 // the new cache slot: normalised + rotated key, raw value
-                for (int e = lane; e < D; e += 32) {
-                    kslot[e] = __float2bfloat16_rn(kh[e]);
-                    vslot[e] = vx[e];
+                if (FP8) {
+                    for (int e = 2 * lane; e < D; e += 64) {
+                        *reinterpret_cast<__nv_fp8x2_storage_t*>(kslot + e) = __nv_cvt_float2_to_fp8x2(
+                            make_float2(kh[e] * p.k_scale, kh[e + 1] * p.k_scale), __NV_SATFINITE, __NV_E4M3);
+                        *reinterpret_cast<__nv_fp8x2_storage_t*>(vslot + e) = __nv_cvt_float2_to_fp8x2(
+                            make_float2(vn[e] * p.v_scale, vn[e + 1] * p.v_scale), __NV_SATFINITE, __NV_E4M3);
+                    }
+                } else {
+                    for (int e = lane; e < D; e += 32) {
+                        reinterpret_cast<__nv_bfloat16*>(kslot)[e] = __float2bfloat16_rn(kh[e]);
+                        reinterpret_cast<__nv_bfloat16*>(vslot)[e] = vx[e];
+                    }
                 }
             }
         }
@@ -186,12 +226,14 @@ __global__ void __launch_bounds__(NTHR, 2) decode_attn_kernel(const __grid_const
     float2 qv[G][4];
     float m[G], l[G];
     float2 o[G][4];
+    const float qs = FP8 ? 1.0f / p.k_scale : 1.0f;  // scores of stored keys come out unscaled
+    const float vs = FP8 ? p.v_scale : 1.0f;         // stored values are v * vs
     if (warp < NCW) {
 #pragma unroll
         for (int h = 0; h < G; ++h) {
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                qv[h][k] = make_float2(qh[h * D + dl + 2 * k], qh[h * D + dl + 2 * k + 1]);
+                qv[h][k] = make_float2(qh[h * D + dl + 2 * k] * qs, qh[h * D + dl + 2 * k + 1] * qs);
                 o[h][k] = make_float2(0.f, 0.f);
             }
             m[h] = -INFINITY;
@@ -207,14 +249,24 @@ __global__ void __launch_bounds__(NTHR, 2) decode_attn_kernel(const __grid_const
             const uint8_t* sk = smem + OFF_K + buf * STAGE_K;
             const uint8_t* sv = smem + OFF_V + buf * STAGE_K;
 #pragma unroll 2
-            for (int it = 0; it < KPS / (NCW * 2); ++it) {
-                const int kr = warp * (KPS / NCW) + it * 2 + hw;  // key row within the stage
-                const int key = st * KPS + kr;
+            for (int it = 0; it < KPT / (NCW * 2); ++it) {
+                const int kr = warp * (KPT / NCW) + it * 2 + hw;  // key row within the stage
+                const int key = st * KPT + kr;
                 bool valid = key < nk;
                 if (ring) valid = valid && key != wslot && (pos >= p.W - 1 || key < pos);
-                const uint4 kraw = *reinterpret_cast<const uint4*>(sk + kr * (D * 2) + dl * 2);
-                const uint4 vraw = *reinterpret_cast<const uint4*>(sv + kr * (D * 2) + dl * 2);
-                const float2 k2[4] = {bf2_to_f2(kraw.x), bf2_to_f2(kraw.y), bf2_to_f2(kraw.z), bf2_to_f2(kraw.w)};
+                // raw words now, widened where they are used (keeps the live registers down)
+                uint4 kraw, vraw;
+                if (FP8) {
+                    const uint2 kq = *reinterpret_cast<const uint2*>(sk + kr * D + dl);
+                    const uint2 vq = *reinterpret_cast<const uint2*>(sv + kr * D + dl);
+                    kraw = make_uint4(kq.x, kq.y, 0u, 0u);
+                    vraw = make_uint4(vq.x, vq.y, 0u, 0u);
+                } else {
+                    kraw = *reinterpret_cast<const uint4*>(sk + kr * (D * 2) + dl * 2);
+                    vraw = *reinterpret_cast<const uint4*>(sv + kr * (D * 2) + dl * 2);
+                }
+                float2 k2[4];
+                widen4(kraw, k2);
                 float part[G];
 #pragma unroll
                 for (int h = 0; h < G; ++h) {
@@ -242,7 +294,8 @@ __global__ void __launch_bounds__(NTHR, 2) decode_attn_kernel(const __grid_const
                     part[2] = __shfl_sync(0xffffffffu, keep, src + 8);
                     part[3] = __shfl_sync(0xffffffffu, keep, src + 12);
                 }
-                const float2 v2[4] = {bf2_to_f2(vraw.x), bf2_to_f2(vraw.y), bf2_to_f2(vraw.z), bf2_to_f2(vraw.w)};
+                float2 v2[4];
+                widen4(vraw, v2);
                 if (valid) {
 #pragma unroll
                     for (int h = 0; h < G; ++h) {
@@ -297,9 +350,9 @@ __global__ void __launch_bounds__(NTHR, 2) decode_attn_kernel(const __grid_const
                 const float pr = ex2_approx(s - m[h]);
                 l[h] += pr;
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    o[h][k].x = fmaf(pr, vn[dl + 2 * k], o[h][k].x);
-                    o[h][k].y = fmaf(pr, vn[dl + 2 * k + 1], o[h][k].y);
+                for (int k = 0; k < 4; ++k) {  // in the units of the stored values
+                    o[h][k].x = fmaf(pr, vn[dl + 2 * k] * vs, o[h][k].x);
+                    o[h][k].y = fmaf(pr, vn[dl + 2 * k + 1] * vs, o[h][k].y);
                 }
             }
         }
@@ -356,6 +409,7 @@ __global__ void __launch_bounds__(NTHR, 2) decode_attn_kernel(const __grid_const
             lt += red_ml[(w * G + h) * 2 + 1] * c;
             ot += red_o[(w * G + h) * D + e] * c;
         }
+        ot *= 1.0f / vs;
         const int hq = g * G + h;
         if (is_glob) {
             const size_t row = ((static_cast<size_t>(lidx) * p.B + b) * p.Hq + hq) * p.nsplit + split;
@@ -410,11 +464,12 @@ size_t decode_workspace_bytes(int NG, int B, int Hq, long long S) {
 
 cudaError_t launch_hybrid_decode(const DecodeParams& p, int d, cudaStream_t s) {
     if (d != D || p.Hq != p.Hkv * G) return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(decode_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+    auto kern = p.fp8 ? decode_attn_kernel<true> : decode_attn_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     if (e != cudaSuccess) return e;
     const long long ctas = static_cast<long long>(p.NG) * p.B * p.Hkv * p.nsplit +
                            static_cast<long long>(p.NS) * p.B * p.Hkv;
-    if (ctas > 0) decode_attn_kernel<<<static_cast<unsigned>(ctas), NTHR, SMEM, s>>>(p);
+    if (ctas > 0) kern<<<static_cast<unsigned>(ctas), NTHR, SMEM, s>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (p.NG > 0) decode_combine_kernel<<<p.NG * p.B * p.Hq, 128, 0, s>>>(p);

@@ -11,6 +11,10 @@
 //   local layer:  the last min(L, S) tokens, slot pos[b, i] mod S of an S-slot ring.
 // A row whose position has no slot (negative, or >= S in a global cache) is not
 // written and is reported in the device error word (code kErrPosition).
+// E4M3 caches store e4m3(k_hat * k_scale) and e4m3(v * v_scale), rounded to nearest
+// and saturated at the largest finite value.
+#include <cuda_fp8.h>
+
 #include "zg_qk.cuh"
 
 namespace zg {
@@ -43,6 +47,18 @@ __global__ void __launch_bounds__(256) kv_cache_kernel(const __grid_constant__ C
     const long long dst = ((static_cast<long long>(b) * p.Hkv + g) * p.S + slot) * D;
     norm_rope_warp(p.k + src * D, p.wk, p.eps, pos, p.rope, 1.0f, buf[warp]);
     const float4 kv = *reinterpret_cast<const float4*>(&buf[warp][lane * 4]);
+    if (p.fp8) {
+        auto e4m3x2 = [](float a, float b) {
+            return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
+        };
+        const uint2 vr = *reinterpret_cast<const uint2*>(p.v + src * D + lane * 4);
+        const float ks = p.k_scale, vs = p.v_scale;
+        const uint32_t k8 = e4m3x2(kv.x * ks, kv.y * ks) | e4m3x2(kv.z * ks, kv.w * ks) << 16;
+        const uint32_t v8 = e4m3x2(bf16lo(vr.x) * vs, bf16hi(vr.x) * vs) | e4m3x2(bf16lo(vr.y) * vs, bf16hi(vr.y) * vs) << 16;
+        *reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(p.cache_k) + dst + lane * 4) = k8;
+        *reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(p.cache_v) + dst + lane * 4) = v8;
+        return;
+    }
     uint2 ko;
     ko.x = pack_bf16x2(kv.x, kv.y);
     ko.y = pack_bf16x2(kv.z, kv.w);

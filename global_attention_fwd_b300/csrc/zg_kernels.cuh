@@ -68,6 +68,8 @@ struct DecodeParams {
     int nsplit;     // splits per (global layer, b, kv head)
     int layer_of_global[96];  // global-layer index -> layer
     int layer_of_local[96];   // local-layer index -> layer
+    int fp8;                  // caches hold E4M3 bytes: e4m3(k_hat * k_scale), e4m3(v * v_scale)
+    float k_scale, v_scale;
     float scale_log2;
     float eps;
     RopeConsts rope;
@@ -92,6 +94,8 @@ struct CacheParams {
     long long S;  // slots: S_max of a global cache, or the ring size
     int ring;     // 1: ring (slot = pos mod S, last min(L, S) tokens); 0: slot = pos
     int i0;       // first token written
+    int fp8;      // E4M3 caches: e4m3(k_hat * k_scale), e4m3(v * v_scale)
+    float k_scale, v_scale;
     float eps;
     RopeConsts rope;
     DevCtl ctl;

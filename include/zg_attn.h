@@ -188,6 +188,38 @@ zg_status zg_hybrid_decode(const zg_bf16 *q, const zg_bf16 *k_new, const zg_bf16
                            double theta, float eps, void *workspace, size_t workspace_bytes, zg_stream stream);
 
 /*
+ * zg_hybrid_decode_fp8 -- zg_hybrid_decode over E4M3 (FP8) caches.  The pages train
+ * with E4M3 in the forward pass ("ZGCM-1-7B 完全解説", gotosocial explainer, training
+ * recipe section); here the format holds the decode caches, which are what a decode
+ * step reads from HBM, so the bytes per step halve.
+ *   k_glob, v_glob [NG, B, Hkv, S_max, d] and k_ring, v_ring [NS, B, Hkv, window, d]:
+ *        one byte per element, E4M3 (4 exponent bits, 3 mantissa bits, bias 7, no
+ *        infinities), holding e4m3(k_hat * k_scale) and e4m3(v * v_scale).
+ *   k_scale, v_scale: finite and > 0 (ZG_ERR_SHAPE otherwise).  QK RMSNorm bounds
+ *        |k_hat| by sqrt(d) * max|wk|, so k_scale = 1 keeps keys in range for any
+ *        weights below 26; v_scale should map the value range into +-448.
+ *   The step writes the new token's slot the same way: round to nearest, saturated
+ *   at +-448.  It attends with the new key and value at full precision, and with the
+ *   stored ones dequantised (divided by the scales).  Everything else is as
+ *   zg_hybrid_decode, including the workspace.
+ */
+zg_status zg_hybrid_decode_fp8(const zg_bf16 *q, const zg_bf16 *k_new, const zg_bf16 *v_new, const zg_bf16 *gate,
+                               const int32_t *pos, const float *wq, const float *wk, const uint8_t *is_global,
+                               uint8_t *k_glob, uint8_t *v_glob, uint8_t *k_ring, uint8_t *v_ring, zg_bf16 *out,
+                               int NL, int B, int Hq, int Hkv, int d, int64_t S_max, int window, int rotary_dim,
+                               double theta, float eps, float k_scale, float v_scale, void *workspace,
+                               size_t workspace_bytes, zg_stream stream);
+
+/* zg_kv_cache_write_fp8 -- zg_kv_cache_write into E4M3 caches (one byte per element):
+ * e4m3(k_hat * k_scale) and e4m3(v * v_scale), rounded to nearest, saturated at
+ * +-448.  Scales finite and > 0 (ZG_ERR_SHAPE otherwise); all else as
+ * zg_kv_cache_write. */
+zg_status zg_kv_cache_write_fp8(const zg_bf16 *k, const zg_bf16 *v, const int32_t *pos, const float *wk,
+                                uint8_t *k_cache, uint8_t *v_cache, int B, int L, int Hkv, int d, int64_t S,
+                                int ring, int rotary_dim, double theta, float eps, float k_scale, float v_scale,
+                                zg_stream stream);
+
+/*
  * zg_hybrid_decode_noalloc -- the same decode step as zg_hybrid_decode, for
  * callers that cannot allocate device memory (no counterpart in the paper: it
  * exists for how the library is called, not for what it computes).

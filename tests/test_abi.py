@@ -188,3 +188,32 @@ def test_attention_backward_rejects_bad_arguments(zg):
     # fp32 q_hat, dA, dq_hat per query row, k_hat, dk_hat per key row, three floats per query row
     assert zg.attention_backward_workspace_bytes(2, 16, 32, 8, 128) == 4 * (2 * 16 * (32 * 128 * 3 + 32 * 3 + 8 * 128 * 2))
     assert zg.attention_backward_workspace_bytes(2, 16, 32, 8, 64) == 0
+
+
+def test_fp8_entry_points_reject_bad_arguments(zg):
+    def dec(**kw):
+        a = dict(q=A, kn=A, vn=A, g=A, pos=A, wq=A, wk=A, flags=None, kg=A, vg=A, kr=A, vr=A, out=A, NL=2, B=1, Hq=4,
+                 Hkv=1, d=128, S=256, W=128, rot=42, theta=1e6, eps=1e-6, ks=1.0, vs=8.0, ws=A, wsb=1 << 40)
+        a.update(kw)
+        flags = ctypes.create_string_buffer(b"\x00\x01", 2)
+        return zg.lib.zg_hybrid_decode_fp8(a["q"], a["kn"], a["vn"], a["g"], a["pos"], a["wq"], a["wk"],
+                                           ctypes.cast(flags, ctypes.c_void_p), a["kg"], a["vg"], a["kr"], a["vr"],
+                                           a["out"], a["NL"], a["B"], a["Hq"], a["Hkv"], a["d"], a["S"], a["W"],
+                                           a["rot"], a["theta"], a["eps"], a["ks"], a["vs"], a["ws"], a["wsb"], None)
+    assert dec(ks=0.0) == -3
+    assert dec(vs=float("inf")) == -3
+    assert dec(kg=None) == -1
+    assert dec(vr=A + 8) == -2
+    assert dec(d=64, rot=20) == -4
+
+    def wr(**kw):
+        a = dict(k=A, v=A, pos=A, wk=A, kc=A, vc=A, B=1, L=16, Hkv=8, d=128, S=128, ring=1, rot=42, theta=1e6,
+                 eps=1e-6, ks=1.0, vs=8.0)
+        a.update(kw)
+        return zg.lib.zg_kv_cache_write_fp8(a["k"], a["v"], a["pos"], a["wk"], a["kc"], a["vc"], a["B"], a["L"],
+                                            a["Hkv"], a["d"], a["S"], a["ring"], a["rot"], a["theta"], a["eps"],
+                                            a["ks"], a["vs"], None)
+    assert wr(kc=None) == -1
+    assert wr(ks=-1.0) == -3
+    assert wr(vs=float("nan")) == -3
+    assert wr(S=0) == -3

@@ -225,6 +225,17 @@ def decode_caches_device(c: DecodeCase, device, salt: int = 0) -> dict:
     return out
 
 
+def to_e4m3(t: torch.Tensor, scale: float) -> torch.Tensor:
+    """Storage form of an E4M3 cache drawn from a bf16 one: t * scale rounded to float8_e4m3fn
+    (torch's round-to-nearest conversion), chunk by chunk on t's device."""
+    out = torch.empty(t.shape, dtype=torch.float8_e4m3fn, device=t.device)
+    src, dst = t.reshape(-1), out.view(-1)
+    for s in range(0, src.numel(), 1 << 28):
+        e = min(src.numel(), s + (1 << 28))
+        dst[s:e] = (src[s:e].float() * scale).to(torch.float8_e4m3fn)
+    return out
+
+
 def prefill_inputs_device(c: PrefillCase, device, salt: int = 0) -> dict:
     """Same recipe as prefill_inputs, drawn on the device with a seeded CUDA generator (used
     where the values are only timed, e.g. the benchmark; values differ from the CPU draw)."""
