@@ -189,8 +189,8 @@ zg_status zg_hybrid_decode(const zg_bf16 *q, const zg_bf16 *k_new, const zg_bf16
 
 /*
  * zg_hybrid_decode_fp8 -- zg_hybrid_decode over E4M3 (FP8) caches.  The pages train
- * with E4M3 in the forward pass ("ZGCM-1-7B 完全解説", gotosocial explainer, training
- * recipe section); here the format holds the decode caches, which are what a decode
+ * with E4M3 in the forward pass ("ZGCM-1-7B 完全解説", gotosocial explainer,
+ * section "学習の高速化 — FP8・Muon・TWEOが生む約4.2倍の効率"); here the format holds the decode caches, which are what a decode
  * step reads from HBM, so the bytes per step halve.
  *   k_glob, v_glob [NG, B, Hkv, S_max, d] and k_ring, v_ring [NS, B, Hkv, window, d]:
  *        one byte per element, E4M3 (4 exponent bits, 3 mantissa bits, bias 7, no
