@@ -14,12 +14,13 @@
 //
 // Kernel 2 (query pass): one CTA per tile of 32 tokens x the 4 query heads of one KV
 // head (128 rows); the tile sees the 160 keys [t0 - 128, t0 + 32).
-//   warp 4 (one thread): TMA of Q_hat, dA, K_hat, V; the MMAs
+//   warp 8 (one thread): TMA of Q_hat, dA, K_hat, V; the MMAs
 //     S = Q_hat K_hat^T  (N = 160)  -> TMEM [0, 160)
 //     dP = dA V^T        (N = 160)  -> TMEM [160, 320)
 //     O = P V   (P from TMEM, packed over S)          -> TMEM [320, 448)
 //     dQ_hat = dS K_hat  (dS from TMEM, packed over dP) -> TMEM [320, 448) (after O is read)
-//   warps 0-3 (thread = row = TMEM lane): exact row max and sum over the window, P
+//   warps 0-7 (thread = row = TMEM lane, two warps per row, one per column half): exact
+//   row max and sum over the window, P
 //   (unnormalised, bf16) over S; A = O / l, D, dgate = dA * A * (1 - sigmoid(gate)) and
 //   the row statistics (max, 1 / l, D) for kernel 3; dS over dP; finally dQ_hat back
 //   through RoPE and RMSNorm into dq (fp32).  Gate and dout tiles are staged by TMA into
@@ -52,24 +53,27 @@ constexpr uint32_t CH128 = 128 * 128;       // one 64-column chunk of 128 rows (
 constexpr uint32_t CH160 = NKQ * 128;       // one 64-column chunk of 160 rows
 constexpr uint32_t TILE128 = 2 * CH128;
 constexpr uint32_t TILE160 = 2 * CH160;
-constexpr int kThreads = 160;               // warps 0-3 rows, warp 4 TMA + MMA
 
 // query pass shared memory: Q_hat, dA (later the gate and dout tiles), V, K_hat, raw q,
-// the tile's RoPE cos / sin, wq
+// the second half's dgate staging, the pair-exchange slots, wq
 constexpr uint32_t QP_Q = 0;
 constexpr uint32_t QP_DA = QP_Q + TILE128;
 constexpr uint32_t QP_V = QP_DA + TILE128;
 constexpr uint32_t QP_K = QP_V + TILE160;
 constexpr uint32_t QP_X = QP_K + TILE160;
-constexpr uint32_t QP_ROPE = QP_X + TILE128;  // [T tokens][kMaxRotHalf] float2
-constexpr uint32_t QP_W = QP_ROPE + T * kMaxRotHalf * 8;
+constexpr uint32_t QP_DG1 = QP_X + TILE128;          // dgate staging of column half 1 (two boxes)
+constexpr uint32_t QP_XCH = QP_DG1 + 2 * 128 * 128;  // [2 parities][2 halves][128 rows] float2
+constexpr uint32_t QP_W = QP_XCH + 2 * 2 * 128 * 8;
 constexpr uint32_t QP_BAR = QP_W + D * 4;
-constexpr uint32_t QP_MISC = QP_BAR + 16 * 8;
-constexpr uint32_t QP_DG = QP_V;   // dgate staging (two 32-column fp32 boxes) in the free V tile
-constexpr uint32_t QP_DQ = QP_Q;   // dq staging (four boxes) over the free Q_hat and dA tiles
-static_assert(QP_DG + 2 * 128 * 128 <= QP_K && QP_DQ + 4 * 128 * 128 <= QP_DG, "staging tiles");
+constexpr int QP_NBAR = 64;
+constexpr uint32_t QP_MISC = QP_BAR + QP_NBAR * 8;
 constexpr uint32_t QP_SMEM = QP_MISC + 32;
-static_assert(QP_K % 1024 == 0 && QP_V % 1024 == 0 && QP_X % 1024 == 0, "128-byte swizzle atoms");
+constexpr uint32_t QP_DG0 = QP_V;   // dgate staging of column half 0 (two boxes) in the free V tile
+constexpr uint32_t QP_DQ = QP_Q;    // dq staging (four boxes) over the free Q_hat and dA tiles
+constexpr uint32_t QP_ROPE = QP_K;  // [T tokens][kMaxRotHalf] float2 in the free K_hat tile, at the end
+static_assert(QP_DG0 + 2 * 128 * 128 <= QP_K && QP_DQ + 4 * 128 * 128 <= QP_DG0, "staging tiles");
+static_assert(QP_ROPE + T * kMaxRotHalf * 8 <= QP_X, "RoPE table inside the K_hat tile");
+static_assert(QP_K % 1024 == 0 && QP_V % 1024 == 0 && QP_X % 1024 == 0 && QP_DG1 % 1024 == 0, "swizzle atoms");
 static_assert(QP_SMEM <= 227 * 1024, "shared memory");
 
 // key pass shared memory
@@ -237,7 +241,15 @@ __global__ void __launch_bounds__(256) bwd_tc_prep_kernel(const __grid_constant_
 }
 
 // ---------------------------------------------------------------- kernel 2: query pass
-__global__ void __launch_bounds__(kThreads, 1) bwd_qpass_kernel(const __grid_constant__ BackwardTcParams p) {
+// Warps 0-7 own the rows two warps per TMEM lane quarter: warp w has the rows of quarter
+// w & 3 and the column half w >> 2 (keys [80 h, 80 h + 80) of the score tiles, columns
+// [64 h, 64 h + 64) of O and dQ_hat).  The two warps of a quarter exchange row partials
+// (max, sum, D, RMSNorm sums) through shared memory and a 64-arrival barrier per exchange.
+// Warp 8: TMA and MMA.
+constexpr int kQThreads = 288;
+constexpr int kNX = 6;  // pair exchanges per tile
+
+__global__ void __launch_bounds__(kQThreads, 1) bwd_qpass_kernel(const __grid_constant__ BackwardTcParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem + QP_BAR);
     uint64_t* ld_full = bar + 0;
@@ -246,14 +258,16 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_qpass_kernel(const __grid_con
     uint64_t* o_full = bar + 3;
     uint64_t* ds_ready = bar + 4;
     uint64_t* dq_full = bar + 5;
-    uint64_t* gd_full = bar + 6;  // gate and dout tiles (gated layers)
-    uint64_t* stg_full = bar + 7;  // [2] dgate staging halves written (128 arrivals)
-    uint64_t* stg_free = bar + 9;  // the first half's bulk store has read its staging
-    uint64_t* dq_stg = bar + 10;   // dq staging written (128 arrivals)
+    uint64_t* gd_full = bar + 6;   // gate and dout tiles (gated layers)
+    uint64_t* stg_full = bar + 7;  // [2] dgate staging of a column half written (128 arrivals)
+    uint64_t* dq_stg = bar + 9;    // dq staging written (256 arrivals)
+    uint64_t* xbar = bar + 16;     // [kNX][4 quarters] pair exchanges (64 arrivals)
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + QP_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + QP_MISC + 4);
     float* w_s = reinterpret_cast<float*>(smem + QP_W);
+    float2* xch = reinterpret_cast<float2*>(smem + QP_XCH);
     constexpr uint32_t C_S = 0, C_DP = NKQ, C_O = 2 * NKQ;
+    static_assert(16 + kNX * 4 <= QP_NBAR, "barrier slots");
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nbg = p.B * p.Hkv;
@@ -266,21 +280,21 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_qpass_kernel(const __grid_con
         if (*abort_flag) report(p.ctl, 100, kErrAlign);
         mbar_init(ld_full, 1);
         mbar_init(s_full, 1);
-        mbar_init(p_ready, 128);
+        mbar_init(p_ready, 256);
         mbar_init(o_full, 1);
-        mbar_init(ds_ready, 128);
+        mbar_init(ds_ready, 256);
         mbar_init(dq_full, 1);
         mbar_init(gd_full, 1);
         mbar_init(&stg_full[0], 128);
         mbar_init(&stg_full[1], 128);
-        mbar_init(stg_free, 1);
-        mbar_init(dq_stg, 128);
+        mbar_init(dq_stg, 256);
+        for (int i = 0; i < kNX * 4; ++i) mbar_init(&xbar[i], 64);
         fence_barrier_init();
     }
     if (threadIdx.x < 32)
         *reinterpret_cast<float4*>(w_s + lane * 4) = __ldg(reinterpret_cast<const float4*>(p.wq + lane * 4));
     const bool gated = p.gate != nullptr;
-    if (warp == 4) {
+    if (warp == 8) {
         tmem_alloc(tslot, 512);
         tmem_relinquish();
     }
@@ -291,8 +305,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_qpass_kernel(const __grid_con
     const uint32_t sbase = smem_u32(smem);
     auto aborted = [&]() { return *abort_flag != 0; };
     auto fail = [&]() { *abort_flag = 1; };
+    // TMEM column of the packed 16-bit operand for keys [16 ks, 16 ks + 16): each column half
+    // packs its 80 keys into the first 40 columns of its own 80-column region
+    auto packed_col = [](uint32_t base, int ks) { return base + 80 * (ks / 5) + 8 * (ks % 5); };
 
-    if (warp == 4) {
+    if (warp == 8) {
         if (lane == 0 && !aborted()) {
             tma_prefetch_desc(&p.tm_qh);
             tma_prefetch_desc(&p.tm_da);
@@ -343,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_qpass_kernel(const __grid_con
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < NKQ / 16; ++ks)
-                    umma_tmem_a(tbase + C_O, tbase + C_S + ks * 8,
+                    umma_tmem_a(tbase + C_O, packed_col(tbase + C_S, ks),
                                 sdesc(sbase + QP_V + ks * 16 * 128, CH160, 1024, kSw128), id_o, ks > 0);
                 umma_commit(o_full);
                 ok = mbar_wait(ds_ready, 0, p.ctl, 103);
@@ -352,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_qpass_kernel(const __grid_con
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < NKQ / 16; ++ks)
-                    umma_tmem_a(tbase + C_O, tbase + C_DP + ks * 8,
+                    umma_tmem_a(tbase + C_O, packed_col(tbase + C_DP, ks),
                                 sdesc(sbase + QP_K + ks * 16 * 128, CH160, 1024, kSw128), id_o, ks > 0);
                 umma_commit(dq_full);
             }
@@ -360,8 +377,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_qpass_kernel(const __grid_con
         }
     } else {
         // ------------------------------------------------------------ rows (thread = row = TMEM lane)
-        const int row = threadIdx.x;
-        const uint32_t lane_addr = tbase + (static_cast<uint32_t>(warp * 32) << 16);
+        const int q4 = warp & 3, hf = warp >> 2;
+        const int row = q4 * 32 + lane;
+        const uint32_t lane_addr = tbase + (static_cast<uint32_t>(q4 * 32) << 16);
         const int tt = row / G;
         const int t = t0 + tt;
         const bool valid_row = t < p.L;
@@ -369,144 +387,144 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_qpass_kernel(const __grid_con
         const int lo = max(128 - t0, tt + 128 - p.window + 1);  // key columns [lo, hi] are in the window
         const int hi = tt + 128;
         const float sl = p.scale_log2;
-        // cos / sin of this row's token: the four rows (lanes) of a token share the work
-        float2* rope_tab = reinterpret_cast<float2*>(smem + QP_ROPE) + tt * kMaxRotHalf;
-        {
-            const int pos = valid_row ? __ldg(p.pos + static_cast<long long>(b) * p.L + t) : 0;
-            for (int j = row % G; j < p.rope.half; j += G) {
-                float cs, sn;
-                rope_cos_sin(pos, p.rope.f_hi[j], p.rope.f_lo[j], cs, sn);
-                rope_tab[j] = make_float2(cs, sn);
-            }
-            __syncwarp();  // a token's four rows sit in one warp
-        }
-        bool ok = __all_sync(0xffffffffu, mbar_wait(s_full, 0, p.ctl, 104));
+        const int c0 = 80 * hf;  // this warp's key columns [c0, c0 + 80)
+        // pair exchange k: publish a float pair, wait for the partner, return its pair.  Every
+        // thread arrives at every exchange, so a partner that gave up never leaves this one
+        // blocked longer than the bounded wait.
+        bool ok = true;
+        auto exchange = [&](int k, float2 v) -> float2 {
+            float2* slot = xch + (k & 1) * 256;
+            slot[hf * 128 + row] = v;
+            mbar_arrive(&xbar[k * 4 + q4]);
+            if (ok && !aborted()) ok = __all_sync(0xffffffffu, mbar_wait(&xbar[k * 4 + q4], 0, p.ctl, 90 + k));
+            return slot[(1 - hf) * 128 + row];
+        };
         float m = 0.f, l = 0.f;
+        ok = __all_sync(0xffffffffu, mbar_wait(s_full, 0, p.ctl, 104));
+        float mx = -INFINITY;
         if (ok) {
             tc_fence_after();
-            float mx = -INFINITY;
 #pragma unroll 1
-            for (int k = 0; k < NKQ / 32; ++k) {
-                uint32_t r[32];
-                tmem_ld32(lane_addr + C_S + 32 * k, r);
+            for (int k = 0; k < 5; ++k) {
+                uint32_t r[16];
+                tmem_ld16(lane_addr + C_S + c0 + 16 * k, r);
                 tmem_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int c = 32 * k + i;
+                for (int i = 0; i < 16; ++i) {
+                    const int c = c0 + 16 * k + i;
                     if (c >= lo && c <= hi) mx = fmaxf(mx, __uint_as_float(r[i]));
                 }
             }
-            m = (valid_row && mx > -INFINITY) ? mx * sl : 0.f;
+        }
+        mx = fmaxf(mx, exchange(0, make_float2(mx, 0.f)).x);
+        m = (valid_row && mx > -INFINITY) ? mx * sl : 0.f;
+        float lp = 0.f;
+        if (ok) {
 #pragma unroll 1
-            for (int k = 0; k < NKQ / 32; ++k) {
-                uint32_t r[32], pk[16];
-                tmem_ld32(lane_addr + C_S + 32 * k, r);
+            for (int k = 0; k < 5; ++k) {
+                uint32_t r[16], pk[8];
+                tmem_ld16(lane_addr + C_S + c0 + 16 * k, r);
                 tmem_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 32; i += 2) {
-                    const int c = 32 * k + i;
+                for (int i = 0; i < 16; i += 2) {
+                    const int c = c0 + 16 * k + i;
                     const bool v0 = valid_row && c >= lo && c <= hi, v1 = valid_row && c + 1 >= lo && c + 1 <= hi;
                     const float e0 = v0 ? ex2_approx(fmaf(__uint_as_float(r[i]), sl, -m)) : 0.f;
                     const float e1 = v1 ? ex2_approx(fmaf(__uint_as_float(r[i + 1]), sl, -m)) : 0.f;
                     pk[i / 2] = pack_bf16x2(e0, e1);
                     const float2 f = bf2f2(pk[i / 2]);  // the sum of the rounded values the MMA uses
-                    l += f.x + f.y;
+                    lp += f.x + f.y;
                 }
-                tmem_st16(lane_addr + C_S + 16 * k, pk);  // P over S: these columns are already read
+                tmem_st8(lane_addr + C_S + c0 + 8 * k, pk);  // P over S: these columns are already read
             }
             tmem_wait_st();
         }
         tc_fence_before();
         mbar_arrive(p_ready);
+        l = lp + exchange(1, make_float2(lp, 0.f)).x;
         if (!ok) fail();
         const float il = l > 0.f ? 1.0f / l : 0.f;
-        // ---- A = O / l, D = dA . A, dgate
+        // ---- A = O / l on this warp's 64 columns, D = dA . A (pair sum), dgate
         if (ok && !aborted()) ok = __all_sync(0xffffffffu, mbar_wait(o_full, 0, p.ctl, 105));
         if (ok && gated && !aborted()) ok = __all_sync(0xffffffffu, mbar_wait(gd_full, 0, p.ctl, 108));
-        float Dd = 0.f;
+        float Dp = 0.f;
+        uint8_t* dg_t = smem + (hf ? QP_DG1 : QP_DG0);
         if (ok) {
             tc_fence_after();
             const uint8_t* dout_t = smem + QP_DA;  // dout (gated: reloaded; ungated: dA is dout)
             const uint8_t* gate_t = smem + QP_Q;
-            uint8_t* dg_t = smem + QP_DG;
-            // two halves of 64 columns; with a gate, each half's dgate goes through a swizzled
-            // staging tile (two boxes of 32 fp32 columns) and leaves by bulk tensor stores
 #pragma unroll 1
-            for (int hh = 0; hh < 2 && ok; ++hh) {
-                if (hh == 1 && gated) ok = __all_sync(0xffffffffu, mbar_wait(stg_free, 0, p.ctl, 109));
-                if (!ok) break;
-#pragma unroll 1
-                for (int k = 2 * hh; k < 2 * hh + 2; ++k) {
-                    uint32_t r[32];
-                    tmem_ld32(lane_addr + C_O + 32 * k, r);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int v8 = 0; v8 < 4; ++v8) {
-                        const uint4 du = ld_row8(dout_t, row, 4 * k + v8);
-                        const uint32_t dw[4] = {du.x, du.y, du.z, du.w};
-                        if (gated) {
-                            const uint4 gu = ld_row8(gate_t, row, 4 * k + v8);
-                            const uint32_t gw[4] = {gu.x, gu.y, gu.z, gu.w};
-                            float dg[8];
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) {
-                                const float gv = (e & 1) ? bf16hi(gw[e / 2]) : bf16lo(gw[e / 2]);
-                                const float sg = sigmoid_fast(gv);
-                                const float a = __uint_as_float(r[8 * v8 + e]) * il;
-                                const float dav = ((e & 1) ? bf16hi(dw[e / 2]) : bf16lo(dw[e / 2])) * sg;
-                                // D from the bf16 dA the dP product used (the prep kernel's rounding
-                                // of the same value), so that sum_j dS_ij = 0 holds to fp32 rounding
-                                Dd = fmaf(__bfloat162float(__float2bfloat16_rn(dav)), a, Dd);
-                                dg[e] = dav * a * (1.0f - sg);
-                            }
-                            // box k & 1 of this half: row `row`, 16-byte chunks 2 v8 and 2 v8 + 1
-                            uint8_t* bx = dg_t + (k & 1) * (128 * 128) + row * 128;
-                            *reinterpret_cast<float4*>(bx + (((2 * v8) ^ (row & 7)) << 4)) =
-                                make_float4(dg[0], dg[1], dg[2], dg[3]);
-                            *reinterpret_cast<float4*>(bx + (((2 * v8 + 1) ^ (row & 7)) << 4)) =
-                                make_float4(dg[4], dg[5], dg[6], dg[7]);
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) {
-                                const float a = __uint_as_float(r[8 * v8 + e]) * il;
-                                Dd = fmaf((e & 1) ? bf16hi(dw[e / 2]) : bf16lo(dw[e / 2]), a, Dd);
-                            }
-                        }
-                    }
-                }
-                if (gated) {
-                    fence_async_smem();
-                    mbar_arrive(&stg_full[hh]);
-                    if (row == 0) {
-                        // rows past the sequence end fall outside the tensor and are not stored
-                        if (mbar_wait(&stg_full[hh], 0, p.ctl, 99)) {
-                            tma_store_4d(&p.tm_dg, dg_t, 64 * hh, g * G, t0, b);
-                            tma_store_4d(&p.tm_dg, dg_t + 128 * 128, 64 * hh + 32, g * G, t0, b);
-                            bulk_commit();
-                            bulk_wait_read_all();
-                            if (hh == 0) mbar_arrive(stg_free);
-                        } else {
-                            ok = false;
-                        }
-                    }
-                    ok = __all_sync(0xffffffffu, ok);  // keep the warp's tensor-memory accesses together
-                }
-            }
-            if (valid_row) p.stat[qrow] = make_float4(m, il, Dd, 0.f);
-            // ---- dS = P (dP - D), packed bf16 over dP
-#pragma unroll 1
-            for (int k = 0; k < NKQ / 32; ++k) {
-                uint32_t pr[16], r[32], dk16[16];
-                tmem_ld16(lane_addr + C_S + 16 * k, pr);
-                tmem_ld32(lane_addr + C_DP + 32 * k, r);
+            for (int k = 2 * hf; k < 2 * hf + 2; ++k) {
+                uint32_t r[32];
+                tmem_ld32(lane_addr + C_O + 32 * k, r);
                 tmem_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float2 pp = bf2f2(pr[i]);
-                    dk16[i] = pack_bf16x2(pp.x * il * (__uint_as_float(r[2 * i]) - Dd),
-                                          pp.y * il * (__uint_as_float(r[2 * i + 1]) - Dd));
+                for (int v8 = 0; v8 < 4; ++v8) {
+                    const uint4 du = ld_row8(dout_t, row, 4 * k + v8);
+                    const uint32_t dw[4] = {du.x, du.y, du.z, du.w};
+                    if (gated) {
+                        const uint4 gu = ld_row8(gate_t, row, 4 * k + v8);
+                        const uint32_t gw[4] = {gu.x, gu.y, gu.z, gu.w};
+                        float dg[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const float gv = (e & 1) ? bf16hi(gw[e / 2]) : bf16lo(gw[e / 2]);
+                            const float sg = sigmoid_fast(gv);
+                            const float a = __uint_as_float(r[8 * v8 + e]) * il;
+                            const float dav = ((e & 1) ? bf16hi(dw[e / 2]) : bf16lo(dw[e / 2])) * sg;
+                            // D from the bf16 dA the dP product used (the prep kernel's rounding of
+                            // the same value), so that sum_j dS_ij = 0 holds to fp32 rounding
+                            Dp = fmaf(__bfloat162float(__float2bfloat16_rn(dav)), a, Dp);
+                            dg[e] = dav * a * (1.0f - sg);
+                        }
+                        // box k & 1 of this half's staging: row `row`, 16-byte chunks 2 v8, 2 v8 + 1
+                        uint8_t* bx = dg_t + (k & 1) * (128 * 128) + row * 128;
+                        *reinterpret_cast<float4*>(bx + (((2 * v8) ^ (row & 7)) << 4)) =
+                            make_float4(dg[0], dg[1], dg[2], dg[3]);
+                        *reinterpret_cast<float4*>(bx + (((2 * v8 + 1) ^ (row & 7)) << 4)) =
+                            make_float4(dg[4], dg[5], dg[6], dg[7]);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const float a = __uint_as_float(r[8 * v8 + e]) * il;
+                            Dp = fmaf((e & 1) ? bf16hi(dw[e / 2]) : bf16lo(dw[e / 2]), a, Dp);
+                        }
+                    }
                 }
-                tmem_st16(lane_addr + C_DP + 16 * k, dk16);
+            }
+        }
+        if (gated) {
+            fence_async_smem();
+            mbar_arrive(&stg_full[hf]);
+            if (q4 == 0 && lane == 0 && ok) {
+                // rows past the sequence end fall outside the tensor and are not stored
+                if (mbar_wait(&stg_full[hf], 0, p.ctl, 99)) {
+                    tma_store_4d(&p.tm_dg, dg_t, 64 * hf, g * G, t0, b);
+                    tma_store_4d(&p.tm_dg, dg_t + 128 * 128, 64 * hf + 32, g * G, t0, b);
+                    bulk_commit();
+                } else {
+                    ok = false;
+                }
+            }
+            ok = __all_sync(0xffffffffu, ok);
+        }
+        const float Dd = Dp + exchange(2, make_float2(Dp, 0.f)).x;
+        if (ok && hf == 0 && valid_row) p.stat[qrow] = make_float4(m, il, Dd, 0.f);
+        // ---- dS = P (dP - D) / l on this warp's 80 keys, packed bf16 over dP
+        if (ok) {
+#pragma unroll 1
+            for (int k = 0; k < 5; ++k) {
+                uint32_t pr[8], r[16], d8[8];
+                tmem_ld8(lane_addr + C_S + c0 + 8 * k, pr);
+                tmem_ld16(lane_addr + C_DP + c0 + 16 * k, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float2 pp = bf2f2(pr[i]);
+                    d8[i] = pack_bf16x2(pp.x * il * (__uint_as_float(r[2 * i]) - Dd),
+                                        pp.y * il * (__uint_as_float(r[2 * i + 1]) - Dd));
+                }
+                tmem_st8(lane_addr + C_DP + c0 + 8 * k, d8);
             }
             tmem_wait_st();
         }
@@ -515,17 +533,83 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_qpass_kernel(const __grid_con
         if (!ok) fail();
         // ---- dq: dQ_hat * c back through RoPE and RMSNorm, out by bulk tensor stores
         if (ok && !aborted()) ok = __all_sync(0xffffffffu, mbar_wait(dq_full, 0, p.ctl, 106));
-        uint8_t* dq_t = smem + QP_DQ;  // every product is done: Q_hat and dA are free
+        uint8_t* dq_t = smem + QP_DQ;  // every product is done: Q_hat, dA and K_hat are free
+        float2* rope_tab = reinterpret_cast<float2*>(smem + QP_ROPE) + tt * kMaxRotHalf;
         if (ok) {
             tc_fence_after();
-            tmem_row_to_tile(lane_addr + C_O, dq_t, row, p.scale);
-            if (valid_row)
-                row_norm_rope_bwd(dq_t, row, smem + QP_X, w_s, p.eps, p.rope.half, [&](int j) { return rope_tab[j]; });
+#pragma unroll 1
+            for (int k = 2 * hf; k < 2 * hf + 2; ++k) {
+                uint32_t v[32];
+                tmem_ld32(lane_addr + C_O + 32 * k, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    *f32_chunk(dq_t, row, 8 * k + c) =
+                        make_float4(__uint_as_float(v[4 * c]) * p.scale, __uint_as_float(v[4 * c + 1]) * p.scale,
+                                    __uint_as_float(v[4 * c + 2]) * p.scale, __uint_as_float(v[4 * c + 3]) * p.scale);
+            }
+            // cos / sin of this row's token: its eight threads (4 rows x 2 halves) share the pairs
+            const int pos = valid_row ? __ldg(p.pos + static_cast<long long>(b) * p.L + t) : 0;
+            for (int j = (row % G) * 2 + hf; j < p.rope.half; j += 2 * G) {
+                float cs, sn;
+                rope_cos_sin(pos, p.rope.f_hi[j], p.rope.f_lo[j], cs, sn);
+                rope_tab[j] = make_float2(cs, sn);
+            }
+        }
+        (void)exchange(3, make_float2(0.f, 0.f));  // both halves staged, the table is complete
+        const int half = p.rope.half;
+        if (ok && valid_row) {
+            for (int j = hf; j < half; j += 2) {  // pairs split between the halves
+                const float2 c = rope_tab[j];
+                float* pa = f32_elem(dq_t, row, j);
+                float* pb = f32_elem(dq_t, row, j + half);
+                const float a = *pa, bb = *pb;
+                *pa = a * c.x + bb * c.y;
+                *pb = bb * c.x - a * c.y;
+            }
+        }
+        (void)exchange(4, make_float2(0.f, 0.f));  // rotated
+        float ss = 0.f, tw = 0.f;
+        const uint8_t* xt = smem + QP_X;
+        if (ok) {
+#pragma unroll 4
+            for (int c8 = 8 * hf; c8 < 8 * hf + 8; ++c8) {
+                const uint4 u = ld_row8(xt, row, c8);
+                const float4 y0 = *f32_chunk(dq_t, row, 2 * c8), y1 = *f32_chunk(dq_t, row, 2 * c8 + 1);
+                const float x[8] = {bf16lo(u.x), bf16hi(u.x), bf16lo(u.y), bf16hi(u.y),
+                                    bf16lo(u.z), bf16hi(u.z), bf16lo(u.w), bf16hi(u.w)};
+                const float y[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    ss = fmaf(x[e], x[e], ss);
+                    tw = fmaf(x[e] * w_s[8 * c8 + e], y[e], tw);
+                }
+            }
+        }
+        const float2 other = exchange(5, make_float2(ss, tw));
+        ss += other.x;
+        tw += other.y;
+        if (ok) {
+            if (valid_row) {
+                const float inv = ss > 0.f || p.eps > 0.f ? rsqrtf(ss * (1.0f / D) + p.eps) : 0.f;
+                const float coef = inv * inv * inv * tw * (1.0f / D);
+#pragma unroll 4
+                for (int c8 = 8 * hf; c8 < 8 * hf + 8; ++c8) {
+                    const uint4 u = ld_row8(xt, row, c8);
+                    float4* p0 = f32_chunk(dq_t, row, 2 * c8);
+                    float4* p1 = f32_chunk(dq_t, row, 2 * c8 + 1);
+                    const float4 y0 = *p0, y1 = *p1;
+                    const float* w = w_s + 8 * c8;
+                    *p0 = make_float4(inv * w[0] * y0.x - coef * bf16lo(u.x), inv * w[1] * y0.y - coef * bf16hi(u.x),
+                                      inv * w[2] * y0.z - coef * bf16lo(u.y), inv * w[3] * y0.w - coef * bf16hi(u.y));
+                    *p1 = make_float4(inv * w[4] * y1.x - coef * bf16lo(u.z), inv * w[5] * y1.y - coef * bf16hi(u.z),
+                                      inv * w[6] * y1.z - coef * bf16lo(u.w), inv * w[7] * y1.w - coef * bf16hi(u.w));
+                }
+            }
             fence_async_smem();
         }
         mbar_arrive(dq_stg);
-        if (row == 0 && ok) {
-            // rows past the sequence end fall outside the tensor and are not stored
+        if (threadIdx.x == 0 && ok) {
             if (mbar_wait(dq_stg, 0, p.ctl, 98)) {
                 for (int k = 0; k < 4; ++k) tma_store_4d(&p.tm_dqf, dq_t + k * F32BOX, 32 * k, g * G, t0, b);
                 bulk_commit();
@@ -533,7 +617,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_qpass_kernel(const __grid_con
                 ok = false;
             }
         }
-        if (row == 0) bulk_wait_all();  // the dgate and dq stores have landed
+        if (q4 == 0 && lane == 0) bulk_wait_all();  // this half's dgate stores (and dq) have landed
         if (!ok) fail();
     }
     __syncthreads();
@@ -545,7 +629,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_qpass_kernel(const __grid_con
     }
     tc_fence_after();
     __syncthreads();
-    if (warp == 4) tmem_dealloc(tbase, 512);
+    if (warp == 8) tmem_dealloc(tbase, 512);
 }
 
 // ---------------------------------------------------------------- kernel 3: key pass
@@ -846,7 +930,7 @@ cudaError_t launch_backward_tc(const BackwardTcParams& p, cudaStream_t s) {
     e = cudaFuncSetAttribute(bwd_kpass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, KP_SMEM);
     if (e != cudaSuccess) return e;
     const long long nbg = static_cast<long long>(p.B) * p.Hkv;
-    bwd_qpass_kernel<<<static_cast<unsigned>(nbg * ((p.L + T - 1) / T)), kThreads, QP_SMEM, s>>>(p);
+    bwd_qpass_kernel<<<static_cast<unsigned>(nbg * ((p.L + T - 1) / T)), kQThreads, QP_SMEM, s>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     bwd_kpass_kernel<<<static_cast<unsigned>(nbg * ((p.L + BK - 1) / BK)), kKThreads, KP_SMEM, s>>>(p);
