@@ -490,7 +490,8 @@ def run_gpu(args):
     f8_by = decode_bytes(DEC, cache_elem_bytes=1)
     dec_fp8 = {"workload": f"{DEC.name} with E4M3 caches", "us_per_step": f8_t * 1e6,
                "roofline": {"bound": "hbm", "achieved": f8_by / f8_t / 1e9, "peak": hbm, "unit": "GB/s",
-                            "frac": f8_by / f8_t / 1e9 / hbm, "traffic": None, "algorithmic_bytes": f8_by}}
+                            "frac": f8_by / f8_t / 1e9 / hbm, "traffic": _traffic("decode_attn_kernel_fp8"),
+                            "algorithmic_bytes": f8_by}}
     del f8
 
     # ---- backward of the gated SWA prefill (outside the step): the 4K training shape
@@ -605,6 +606,19 @@ def run_profile_case(args):
         def fn():
             zg.attention_backward(x["q"], x["k"], x["v"], x["gate"], x["pos"], x["wq"], x["wk"], dout, window=128,
                                   rotary_dim=c.rotary_dim, theta=c.theta, workspace=ws)
+    elif kind == "decode8":
+        c = workloads.DecodeCase("hybrid_decode_fp8_B1_p131071_profile", 5, 1, 32, (5, 11, 17, 23, 29), 32, 8, 128,
+                                 131072, 128, 131071, 42, 1e6)
+        tok = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in workloads.decode_token_inputs(c).items()}
+        caches = {k: workloads.to_e4m3(v, 1.0 if k[0] == "k" else 8.0)
+                  for k, v in workloads.decode_caches_device(c, dev).items()}
+        ws = torch.empty(zg.hybrid_decode_workspace_bytes(5, 1, 32, 128, c.S), dtype=torch.uint8, device=dev)
+        flags = c.layer_flags()
+
+        def fn():
+            zg.hybrid_decode_fp8(tok["q"], tok["k_new"], tok["v_new"], tok["gate"], tok["pos"], tok["wq"], tok["wk"],
+                                 flags, caches["k_glob"], caches["v_glob"], caches["k_ring"], caches["v_ring"],
+                                 k_scale=1.0, v_scale=8.0, rotary_dim=c.rotary_dim, theta=c.theta, workspace=ws)
     else:
         c = workloads.DecodeCase("hybrid_decode_B1_p131071_profile", 5, 1, 32, (5, 11, 17, 23, 29), 32, 8, 128,
                                  131072, 128, 131071, 42, 1e6)
@@ -635,7 +649,7 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=4096)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--profile-case", choices=["swa", "global", "decode", "kvcache", "backward"], default=None,
+    ap.add_argument("--profile-case", choices=["swa", "global", "decode", "kvcache", "backward", "decode8"], default=None,
                     help="run only a small case of one kernel (for ncu captures)")
     args = ap.parse_args()
     if args.profile_case:
