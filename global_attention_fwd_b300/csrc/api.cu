@@ -149,6 +149,40 @@ zg_status write_cache(const zg_bf16* k, const zg_bf16* v, const int32_t* pos, co
 }  // namespace
 }  // namespace zg
 
+namespace zg {
+// Every argument check of one decode step except the workspace's, in the order the entry points
+// report them; *ng receives the number of global layers.  Shared by zg_hybrid_decode(_fp8) and
+// the allocation-free entry point, so a bad call gets the same status from each.
+int hybrid_decode_check(const void* q, const void* k_new, const void* v_new, const void* gate, const void* pos,
+                        const void* wq, const void* wk, const uint8_t* is_global, const void* k_glob,
+                        const void* v_glob, const void* k_ring, const void* v_ring, const void* out, int NL, int B,
+                        int Hq, int Hkv, int d, int64_t S_max, int window, int rotary_dim, double theta, float eps,
+                        int fp8, float k_scale, float v_scale, int* ng) {
+    if (!q || !k_new || !v_new || !gate || !pos || !wq || !wk || !is_global || !out) return ZG_ERR_NULL;
+    if (fp8 && !(std::isfinite(k_scale) && k_scale > 0.f && std::isfinite(v_scale) && v_scale > 0.f))
+        return ZG_ERR_SHAPE;
+    if (NL < 0 || B < 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || Hq % Hkv || window <= 0) return ZG_ERR_SHAPE;
+    if (rotary_dim < 0 || rotary_dim > d || (rotary_dim & 1) || !(theta > 0.0) || !(eps >= 0.0f)) return ZG_ERR_SHAPE;
+    if (NL > kMaxLayers) return ZG_ERR_UNSUPPORTED;
+    int NG = 0;
+    for (int l = 0; l < NL; ++l) NG += is_global[l] ? 1 : 0;
+    const int NS = NL - NG;
+    if ((NG && (!k_glob || !v_glob)) || (NS && (!k_ring || !v_ring))) return ZG_ERR_NULL;
+    const void* ptrs[] = {q, k_new, v_new, gate, pos, wq, wk, out};
+    for (const void* x : ptrs)
+        if (!aligned16(x)) return ZG_ERR_ALIGN;
+    if ((NG && (!aligned16(k_glob) || !aligned16(v_glob))) || (NS && (!aligned16(k_ring) || !aligned16(v_ring))))
+        return ZG_ERR_ALIGN;
+    if (NG && S_max <= 0) return ZG_ERR_SHAPE;
+    if (d != 128 || Hq != 4 * Hkv || window > 4096 || S_max >= (1ll << 31)) return ZG_ERR_UNSUPPORTED;
+    const long long nsplit = NG ? (S_max + kDecodeSplitLen - 1) / kDecodeSplitLen : 1;
+    const long long ctas = static_cast<long long>(NG) * B * Hkv * nsplit + static_cast<long long>(NS) * B * Hkv;
+    if (ctas >= (1ll << 31) || static_cast<long long>(NG) * B * Hq >= (1ll << 31)) return ZG_ERR_UNSUPPORTED;
+    *ng = NG;
+    return ZG_OK;
+}
+}  // namespace zg
+
 using namespace zg;
 
 extern "C" {
@@ -463,6 +497,7 @@ size_t zg_hybrid_decode_workspace_bytes(int NG, int B, int Hq, int d, int64_t S_
     return decode_workspace_bytes(NG, B, Hq, S_max);
 }
 
+
 // one decode step over bf16 (fp8 = 0) or E4M3 (fp8 = 1) caches
 static zg_status hybrid_decode_impl(const zg_bf16* q, const zg_bf16* k_new, const zg_bf16* v_new, const zg_bf16* gate,
                                     const int32_t* pos, const float* wq, const float* wk, const uint8_t* is_global,
@@ -470,32 +505,22 @@ static zg_status hybrid_decode_impl(const zg_bf16* q, const zg_bf16* k_new, cons
                                     int B, int Hq, int Hkv, int d, int64_t S_max, int window, int rotary_dim,
                                     double theta, float eps, void* workspace, size_t workspace_bytes, int fp8,
                                     float k_scale, float v_scale, zg_stream stream) {
-    if (!q || !k_new || !v_new || !gate || !pos || !wq || !wk || !is_global || !out) return ZG_ERR_NULL;
-    if (fp8 && !(std::isfinite(k_scale) && k_scale > 0.f && std::isfinite(v_scale) && v_scale > 0.f))
-        return ZG_ERR_SHAPE;
-    if (NL < 0 || B < 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || Hq % Hkv || window <= 0) return ZG_ERR_SHAPE;
-    if (rotary_dim < 0 || rotary_dim > d || (rotary_dim & 1) || !(theta > 0.0) || !(eps >= 0.0f)) return ZG_ERR_SHAPE;
-    if (NL > kMaxLayers) return ZG_ERR_UNSUPPORTED;
-    int NG = 0, NS = 0;
+    int NG = 0;
+    const zg_status st = (zg_status)hybrid_decode_check(q, k_new, v_new, gate, pos, wq, wk, is_global, k_glob, v_glob, k_ring, v_ring,
+                                       out, NL, B, Hq, Hkv, d, S_max, window, rotary_dim, theta, eps, fp8, k_scale,
+                                       v_scale, &NG);
+    if (st != ZG_OK) return st;
+    if (NL == 0 || B == 0) return ZG_OK;
+    int NS = 0;
     int glob_layers[kMaxLayers], loc_layers[kMaxLayers];
+    NG = 0;
     for (int l = 0; l < NL; ++l) {
         if (is_global[l]) glob_layers[NG++] = l;
         else loc_layers[NS++] = l;
     }
-    if ((NG && (!k_glob || !v_glob)) || (NS && (!k_ring || !v_ring))) return ZG_ERR_NULL;
-    const void* ptrs[] = {q, k_new, v_new, gate, pos, wq, wk, out};
-    for (const void* x : ptrs)
-        if (!aligned16(x)) return ZG_ERR_ALIGN;
-    if ((NG && (!aligned16(k_glob) || !aligned16(v_glob))) || (NS && (!aligned16(k_ring) || !aligned16(v_ring))))
-        return ZG_ERR_ALIGN;
-    if (NG && S_max <= 0) return ZG_ERR_SHAPE;
-    if (d != 128 || Hq != 4 * Hkv || window > 4096 || S_max >= (1ll << 31)) return ZG_ERR_UNSUPPORTED;
-    if (NL == 0 || B == 0) return ZG_OK;
     const size_t need = NG ? decode_workspace_bytes(NG, B, Hq, S_max) : 0;
     if (need && (!workspace || workspace_bytes < need || !aligned16(workspace))) return ZG_ERR_WORKSPACE;
     const long long nsplit = NG ? (S_max + kDecodeSplitLen - 1) / kDecodeSplitLen : 1;
-    const long long ctas = static_cast<long long>(NG) * B * Hkv * nsplit + static_cast<long long>(NS) * B * Hkv;
-    if (ctas >= (1ll << 31) || static_cast<long long>(NG) * B * Hq >= (1ll << 31)) return ZG_ERR_UNSUPPORTED;
 
     DecodeParams p;
     std::memset(&p, 0, sizeof(p));

@@ -94,11 +94,14 @@ __global__ void __launch_bounds__(256) bwd_query_kernel(const __grid_constant__ 
     float4 da = dout;
     if (p.gate) {
         const float4 gv = ld_bf4(p.gate + row * D + lane * 4);
-        const float s0 = 1.f / (1.f + __expf(-gv.x)), s1 = 1.f / (1.f + __expf(-gv.y));
-        const float s2 = 1.f / (1.f + __expf(-gv.z)), s3 = 1.f / (1.f + __expf(-gv.w));
+        // sigma and 1 - sigma, both without cancellation
+        float s0, s1, s2, s3, c0, c1, c2, c3;
+        sigmoid_pair(gv.x, s0, c0);
+        sigmoid_pair(gv.y, s1, c1);
+        sigmoid_pair(gv.z, s2, c2);
+        sigmoid_pair(gv.w, s3, c3);
         da = make_float4(dout.x * s0, dout.y * s1, dout.z * s2, dout.w * s3);
-        st4(p.dgate + row * D + lane * 4,
-            make_float4(da.x * a.x * (1.f - s0), da.y * a.y * (1.f - s1), da.z * a.z * (1.f - s2), da.w * a.w * (1.f - s3)));
+        st4(p.dgate + row * D + lane * 4, make_float4(da.x * a.x * c0, da.y * a.y * c1, da.z * a.z * c2, da.w * a.w * c3));
     }
     const float Dd = warp_sum(dot4(da, a));
     // dq_hat

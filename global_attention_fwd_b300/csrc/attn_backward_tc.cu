@@ -234,8 +234,8 @@ __global__ void __launch_bounds__(256) bwd_tc_prep_kernel(const __grid_constant_
             // the same sigmoid as the query pass, which rebuilds these bf16 values for D
             const uint2 go = gr[i], dd = dr[i];
             *reinterpret_cast<uint2*>(p.da + r * D + lane * 4) = make_uint2(
-                pack_bf16x2(bf16lo(dd.x) * sigmoid_fast(bf16lo(go.x)), bf16hi(dd.x) * sigmoid_fast(bf16hi(go.x))),
-                pack_bf16x2(bf16lo(dd.y) * sigmoid_fast(bf16lo(go.y)), bf16hi(dd.y) * sigmoid_fast(bf16hi(go.y))));
+                pack_bf16x2(bf16lo(dd.x) * sigmoid_f32(bf16lo(go.x)), bf16hi(dd.x) * sigmoid_f32(bf16hi(go.x))),
+                pack_bf16x2(bf16lo(dd.y) * sigmoid_f32(bf16lo(go.y)), bf16hi(dd.y) * sigmoid_f32(bf16hi(go.y))));
         }
     }
 }
@@ -469,13 +469,14 @@ __global__ void __launch_bounds__(kQThreads, 1) bwd_qpass_kernel(const __grid_co
 #pragma unroll
                         for (int e = 0; e < 8; ++e) {
                             const float gv = (e & 1) ? bf16hi(gw[e / 2]) : bf16lo(gw[e / 2]);
-                            const float sg = sigmoid_fast(gv);
+                            float sg, sgc;  // sigma and 1 - sigma, neither by subtraction
+                            sigmoid_pair(gv, sg, sgc);
                             const float a = __uint_as_float(r[8 * v8 + e]) * il;
                             const float dav = ((e & 1) ? bf16hi(dw[e / 2]) : bf16lo(dw[e / 2])) * sg;
                             // D from the bf16 dA the dP product used (the prep kernel's rounding of
                             // the same value), so that sum_j dS_ij = 0 holds to fp32 rounding
                             Dp = fmaf(__bfloat162float(__float2bfloat16_rn(dav)), a, Dp);
-                            dg[e] = dav * a * (1.0f - sg);
+                            dg[e] = dav * a * sgc;
                         }
                         // box k & 1 of this half's staging: row `row`, 16-byte chunks 2 v8, 2 v8 + 1
                         uint8_t* bx = dg_t + (k & 1) * (128 * 128) + row * 128;

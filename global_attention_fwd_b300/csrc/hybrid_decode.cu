@@ -424,7 +424,7 @@ __global__ void __launch_bounds__(NTHR, 2) decode_attn_kernel(const __grid_const
             float r = 0.f;
             if (all_ok && lt > 0.f) {
                 const float gt = __bfloat162float(p.gate[orow * D + e]);
-                r = ot / lt * sigmoid_fast(gt);
+                r = ot / lt * sigmoid_f32(gt);
             }
             p.out[orow * D + e] = __float2bfloat16_rn(r);
         }

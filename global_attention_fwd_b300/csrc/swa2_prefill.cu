@@ -600,8 +600,8 @@ __global__ void __launch_bounds__(kThreads, 1) swa2_kernel(const __grid_constant
             tmem_ld16(lane_addr + C::O_COL, ra);
             tmem_wait_ld();
             const float lsum = __uint_as_float(lraw);
-            // out = O / l * sigmoid(g) = (O * 0.5/l) * (1 + tanh(g / 2))
-            const float c = lsum > 0.f ? 0.5f / lsum : 0.f;
+            // out = O / l * sigmoid(g), the sigmoid in fp32 (sigmoid2_f32: no cancellation for g < 0)
+            const float c = lsum > 0.f ? 1.0f / lsum : 0.f;
             const float2 c2 = make_float2(c, c);
             uint8_t* buf = qbuf0 + qb * C::QBUF;
             auto epi16 = [&](const uint32_t* r, int cb) {
@@ -614,10 +614,10 @@ __global__ void __launch_bounds__(kThreads, 1) swa2_kernel(const __grid_constant
                     uint32_t ou[4];
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
-                        const float2 t = bf2f2(tanh_bf16x2(mul_bf16x2(gu[k], 0x3F003F00u)));  // tanh(g/2)
+                        const float2 sg = sigmoid2_f32(bf2f2(gu[k]));
                         const float2 oc = mul2(
                             make_float2(__uint_as_float(r[q2 * 8 + 2 * k]), __uint_as_float(r[q2 * 8 + 2 * k + 1])), c2);
-                        const float2 o = fma2(oc, t, oc);
+                        const float2 o = mul2(oc, sg);
                         ou[k] = pack_bf16x2(o.x, o.y);
                     }
                     *reinterpret_cast<uint4*>(gp) = make_uint4(ou[0], ou[1], ou[2], ou[3]);

@@ -278,8 +278,8 @@ __global__ void __launch_bounds__(128, 2) swa_prefill_kernel(const __grid_consta
                 uint32_t ou[4];
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    const float o0 = __uint_as_float(r[q4 * 8 + 2 * k]) * inv_l * sigmoid_fast(bf16lo(gu[k]));
-                    const float o1 = __uint_as_float(r[q4 * 8 + 2 * k + 1]) * inv_l * sigmoid_fast(bf16hi(gu[k]));
+                    const float o0 = __uint_as_float(r[q4 * 8 + 2 * k]) * inv_l * sigmoid_f32(bf16lo(gu[k]));
+                    const float o1 = __uint_as_float(r[q4 * 8 + 2 * k + 1]) * inv_l * sigmoid_f32(bf16hi(gu[k]));
                     ou[k] = pack_bf16x2(o0, o1);
                 }
                 *reinterpret_cast<uint4*>(gp) = make_uint4(ou[0], ou[1], ou[2], ou[3]);

@@ -80,6 +80,12 @@ constexpr int kMaxLayers = 96;
 constexpr int kDecodeSplitLen = 8192;  // keys of a global cache per split
 
 cudaError_t launch_hybrid_decode(const DecodeParams& p, int d, cudaStream_t s);
+// the host argument checks of one decode step (all but the workspace's); *ng = global layers
+int hybrid_decode_check(const void* q, const void* k_new, const void* v_new, const void* gate, const void* pos,
+                        const void* wq, const void* wk, const uint8_t* is_global, const void* k_glob,
+                        const void* v_glob, const void* k_ring, const void* v_ring, const void* out, int NL, int B,
+                        int Hq, int Hkv, int d, int64_t S_max, int window, int rotary_dim, double theta, float eps,
+                        int fp8, float k_scale, float v_scale, int* ng);
 size_t decode_workspace_bytes(int NG, int B, int Hq, long long S);
 
 // ---------------------------------------------------------------- decode caches from a prefill

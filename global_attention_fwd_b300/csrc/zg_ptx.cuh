@@ -254,11 +254,6 @@ __device__ __forceinline__ float ex2_approx(float x) {  // hardware 2^x
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
-__device__ __forceinline__ float tanh_approx(float x) {  // hardware tanh
-    float y;
-    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
 // packed fp32 pairs (two lanes of work per instruction)
 __device__ __forceinline__ unsigned long long f2_bits(float2 a) { return *reinterpret_cast<unsigned long long*>(&a); }
 __device__ __forceinline__ float2 bits_f2(unsigned long long u) { return *reinterpret_cast<float2*>(&u); }
@@ -279,20 +274,31 @@ __device__ __forceinline__ float2 add2(float2 a, float2 b) {
 }
 __device__ __forceinline__ float2 bf2f2(uint32_t u) { return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u)); }
 
-__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
-    uint32_t y;
-    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(y) : "r"(a), "r"(b));
-    return y;
-}
-// hardware tanh on a packed bf16 pair
-__device__ __forceinline__ uint32_t tanh_bf16x2(uint32_t x) {
-    uint32_t y;
-    asm("tanh.approx.bf16x2 %0, %1;" : "=r"(y) : "r"(x));
+__device__ __forceinline__ float rcp_approx(float x) {  // hardware reciprocal
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
 
-// logistic function through tanh: sigma(x) = 0.5 + 0.5 * tanh(x / 2)
-__device__ __forceinline__ float sigmoid_fast(float x) { return fmaf(0.5f, tanh_approx(0.5f * x), 0.5f); }
+// Logistic function sigma(x) = 1 / (1 + e^-x), evaluated in fp32 as 1 / (1 + 2^(-x log2 e)) with the
+// hardware exp2 and reciprocal.  Nothing cancels for either sign of x: the relative error stays
+// within a few ulp for every x above about -87 (below it 2^(-x log2 e) overflows and sigma flushes
+// to 0; its true value there is under 2^-125).  The suppressing gates (x << 0) keep full precision.
+constexpr float kLog2e = 1.4426950408889634f;
+__device__ __forceinline__ float sigmoid_f32(float x) { return rcp_approx(1.0f + ex2_approx(-kLog2e * x)); }
+// sigma(x) and its complement 1 - sigma(x) = sigma(-x) = e / (1 + e), e = e^-x, neither by subtraction
+__device__ __forceinline__ void sigmoid_pair(float x, float& s, float& sc) {
+    const float e = ex2_approx(-kLog2e * x);
+    s = rcp_approx(1.0f + e);
+    sc = e * s;
+    if (e == INFINITY) sc = 1.0f;  // x below about -87: sigma = 0, complement 1
+}
+// the same on a pair of values (packed fp32 arithmetic around the two MUFU operations)
+__device__ __forceinline__ float2 sigmoid2_f32(float2 x) {
+    const float2 t = mul2(x, make_float2(-kLog2e, -kLog2e));
+    const float2 d = add2(make_float2(ex2_approx(t.x), ex2_approx(t.y)), make_float2(1.0f, 1.0f));
+    return make_float2(rcp_approx(d.x), rcp_approx(d.y));
+}
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);

@@ -25,8 +25,10 @@
  *   A = sum_j softmax_j(q_hat . k_hat_j / sqrt(d)) v[j,g]
  *   SWA:    j in [max(0, i - window + 1), i]   -> out = A * sigmoid(gate)
  *   global: j in [0, i]                        -> out = A
- * Scores, softmax and accumulation run in fp32; q_hat, k_hat and the softmax
- * weights are rounded to bf16 for the tensor cores; out is rounded to bf16.
+ * Scores, softmax and accumulation run in fp32; for the prefill tensor cores
+ * q_hat and k_hat are rounded to fp16 (RMSNorm bounds them far inside its range)
+ * and the softmax weights to bf16; out is rounded to bf16.  sigmoid(gate) is
+ * evaluated in fp32 without cancellation for negative logits.
  *
  * Conventions for every call:
  *   - All tensors are device memory, row-major and contiguous, owned by the
@@ -236,9 +238,13 @@ zg_status zg_kv_cache_write_fp8(const zg_bf16 *k, const zg_bf16 *v, const int32_
  *     ZG_NOALLOC_SCRATCH_BYTES are rejected with ZG_ERR_WORKSPACE before any
  *     launch.  64 MiB covers, e.g., 5 global layers x 8 sequences x 32 query
  *     heads with 256K-slot caches (42.6 MB).
- *   - The first call on a device looks up the array's device address on that
- *     device (the device must be current); make that first call before any
- *     stream capture begins.
+ *   - The first call in a CUDA context looks up the array's device address in
+ *     that context (the device must be current) and keeps it for the context;
+ *     a new context on the same device (after cudaDeviceReset, for instance)
+ *     gets its own lookup on its first call.  Make the first call of a context
+ *     before any stream capture begins.
+ *   - Argument errors are reported with the same status as zg_hybrid_decode
+ *     would give, before the scratch size is considered.
  *   - All calls share the one array, which keeps the last call's contents; no
  *     clearing is needed between calls, but calls whose kernels overlap on the
  *     GPU (unordered streams) race on it.

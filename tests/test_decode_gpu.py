@@ -110,5 +110,48 @@ def test_full_hybrid_decode_config(zg):
     inp.pop("is_global")
     flags = c.layer_flags()
     _run_and_check(zg, inp, flags, [c.pos] * c.B, c.rotary_dim, c.theta, c.eps, seqs=seqs, host_caches=host)
-    # a second step at the next position must see the key written by the first (global caches only
-    # hold S slots, so step back instead: position p-1 with the same inputs is a valid, different step)
+
+
+def test_two_chained_steps_see_the_written_slot(zg):
+    """Step at p, then at p + 1 on the same device caches: the second step must attend to the key and
+    value the first one wrote (and, at p + 1 = 128, a ring must have dropped position 0).  The oracle's
+    caches for the second step are the pre-step caches with slot p holding the oracle's own k_hat of
+    step 1 (in the bf16 cache format) and step 1's v_new."""
+    flags = [0, 1, 0, 0, 1]
+    NL, B, Hq, Hkv, S, W = len(flags), 2, 8, 2, 600, 128
+    first = _small_case(NL, flags, B, Hq, Hkv, S, W, seed=31)
+    g = torch.Generator().manual_seed(32)
+    second = {k: _draw(tuple(first[k].shape), g) for k in ("q", "k_new", "v_new", "gate")}
+    positions = [127, 598]
+    dev = {k: v.cuda() for k, v in first.items()}
+    pre = {k: first[k].clone() for k in ("k_glob", "v_glob", "k_ring", "v_ring")}
+    outs = []
+    for step, x in enumerate((first, second)):
+        pos = torch.tensor([p + step for p in positions], dtype=torch.int32, device="cuda")
+        xd = {k: x[k].cuda() for k in ("q", "k_new", "v_new", "gate")}
+        outs.append(zg.hybrid_decode(xd["q"], xd["k_new"], xd["v_new"], xd["gate"], pos, dev["wq"], dev["wk"], flags,
+                                     dev["k_glob"], dev["v_glob"], dev["k_ring"], dev["v_ring"], rotary_dim=42,
+                                     theta=1e6))
+    torch.cuda.synchronize()
+    assert zg.device_status()[0] == 0
+    for b, p in enumerate(positions):
+        args = dict(rotary_dim=42, theta=1e6, eps=1e-6)
+        caches = {k: pre[k][:, b].clone() for k in pre}
+        _, khat = oracle.decode_seq(first["q"][:, b], first["k_new"][:, b], first["v_new"][:, b],
+                                    first["gate"][:, b], first["wq"], first["wk"], flags, caches["k_glob"],
+                                    caches["v_glob"], caches["k_ring"], caches["v_ring"], p=p, **args)
+        gi = si = 0
+        for l, f in enumerate(flags):
+            kk = torch.from_numpy(khat[l]).to(torch.bfloat16)
+            if f:
+                caches["k_glob"][gi, :, p] = kk
+                caches["v_glob"][gi, :, p] = first["v_new"][l, b]
+                gi += 1
+            else:
+                caches["k_ring"][si, :, p % W] = kk
+                caches["v_ring"][si, :, p % W] = first["v_new"][l, b]
+                si += 1
+        ref2, _ = oracle.decode_seq(second["q"][:, b], second["k_new"][:, b], second["v_new"][:, b],
+                                    second["gate"][:, b], first["wq"], first["wk"], flags, caches["k_glob"],
+                                    caches["v_glob"], caches["k_ring"], caches["v_ring"], p=p + 1, **args)
+        assert_close(outs[1][:, b].double().cpu().numpy(), ref2, f"second step seq {b} p={p + 1}")

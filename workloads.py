@@ -133,6 +133,13 @@ def prefill_inputs(c: PrefillCase, salt: int = 0) -> dict:
                 wq=norm_weights(c.d, c.cfg_id, "wq", salt=salt), wk=norm_weights(c.d, c.cfg_id, "wk", salt=salt))
 
 
+def suppressing_gate(shape, cfg_id: int, salt: int = 0, mean: float = -3.0, std: float = 2.0) -> torch.Tensor:
+    """Gate logits that mostly suppress: N(mean, std^2) drawn in float32 (stream gate, salt + 50), cast to
+    bf16.  With the default N(-3, 2^2) about half of the entries have sigmoid(g) < 0.05."""
+    x = _randn_bf16(shape, _gen(cfg_id, "gate", salt + 50)).float()
+    return (x * std + mean).to(torch.bfloat16)
+
+
 def backward_dout(c: PrefillCase, salt: int = 0) -> torch.Tensor:
     """The output gradient a backward pass of case c receives: [B, L, Hq, d] bf16 ~ N(0, 1)."""
     return _randn_bf16((c.B, c.L, c.Hq, c.d), _gen(c.cfg_id, "dout", salt))
