@@ -80,6 +80,25 @@ bool make_map_f32(CUtensorMap* m, const void* base, int d, int heads, int L, int
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D tensor map over a decode cache [slices][rows][d] (bf16, or E4M3 bytes when fp8) with a
+// {min(d * elem, 128 B), box_rows, 1} box and the 128-byte (64-byte for 64-byte rows) swizzle
+bool make_cache_map(CUtensorMap* m, const void* base, int d, long long rows, long long slices, bool fp8,
+                    int box_rows) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const int eb = fp8 ? 1 : 2;
+    const int row_bytes = d * eb;
+    const int box_bytes = row_bytes < 128 ? row_bytes : 128;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)slices};
+    cuuint64_t strides[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows * row_bytes};
+    cuuint32_t box[3] = {(cuuint32_t)(box_bytes / eb), (cuuint32_t)box_rows, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base),
+               dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               box_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // theta^(-2j/r) in double, split into float head + float tail
 bool rope_consts(RopeConsts& rc, int rotary_dim, double theta) {
     if (rotary_dim < 0 || (rotary_dim & 1) || rotary_dim / 2 > kMaxRotHalf) return false;
@@ -117,7 +136,7 @@ zg_status check_cache(const void* ck, const void* cv, int d, long long S) {
     if (!ck || !cv) return ZG_ERR_NULL;
     if (!aligned16(ck) || !aligned16(cv)) return ZG_ERR_ALIGN;
     if (S < 1) return ZG_ERR_SHAPE;
-    if (d != 128) return ZG_ERR_UNSUPPORTED;  // the decode step reads d = 128 caches
+    if (d != 64 && d != 128) return ZG_ERR_UNSUPPORTED;  // the head sizes the decode step reads
     return ZG_OK;
 }
 zg_status write_cache(const zg_bf16* k, const zg_bf16* v, const int32_t* pos, const float* wk, void* ck,
@@ -174,10 +193,12 @@ int hybrid_decode_check(const void* q, const void* k_new, const void* v_new, con
     if ((NG && (!aligned16(k_glob) || !aligned16(v_glob))) || (NS && (!aligned16(k_ring) || !aligned16(v_ring))))
         return ZG_ERR_ALIGN;
     if (NG && S_max <= 0) return ZG_ERR_SHAPE;
-    if (d != 128 || Hq != 4 * Hkv || window > 4096 || S_max >= (1ll << 31)) return ZG_ERR_UNSUPPORTED;
+    if (!decode_supports(d, Hq / Hkv) || window > 4096 || S_max >= (1ll << 31)) return ZG_ERR_UNSUPPORTED;
     const long long nsplit = NG ? (S_max + kDecodeSplitLen - 1) / kDecodeSplitLen : 1;
     const long long ctas = static_cast<long long>(NG) * B * Hkv * nsplit + static_cast<long long>(NS) * B * Hkv;
-    if (ctas >= (1ll << 31) || static_cast<long long>(NG) * B * Hq >= (1ll << 31)) return ZG_ERR_UNSUPPORTED;
+    if (ctas >= (1ll << 31) || static_cast<long long>(NG) * B * Hq >= (1ll << 31) ||
+        static_cast<long long>(NL) * B * Hkv >= (1ll << 31))
+        return ZG_ERR_UNSUPPORTED;
     *ng = NG;
     return ZG_OK;
 }
@@ -194,7 +215,7 @@ zg_status zg_swa_prefill(const zg_bf16* q, const zg_bf16* k, const zg_bf16* v, c
     if (st != ZG_OK) return st;
     if (window < 1) return ZG_ERR_SHAPE;
     const int G = Hq / Hkv;
-    if ((d != 64 && d != 128) || (G != 1 && G != 2 && G != 4 && G != 8) || window > 128 || Hkv > 65535)
+    if ((d != 64 && d != 128) || (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) || window > 128 || Hkv > 65535)
         return ZG_ERR_UNSUPPORTED;
     if (B == 0 || L == 0) return ZG_OK;
     const int T = 128 / G;
@@ -235,11 +256,12 @@ zg_status zg_global_prefill(const zg_bf16* q, const zg_bf16* k, const zg_bf16* v
                             zg_stream stream) {
     zg_status st = check_prefill(q, k, v, nullptr, false, pos, wq, wk, out, B, L, Hq, Hkv, d, rotary_dim, theta, eps);
     if (st != ZG_OK) return st;
-    if (d != 128 || Hq / Hkv != 4 || Hkv > 65535) return ZG_ERR_UNSUPPORTED;
+    const int G = Hq / Hkv;
+    if (!global_supports(d, G) || Hkv > 65535) return ZG_ERR_UNSUPPORTED;
     if (B == 0 || L == 0) return ZG_OK;
     const size_t need = zg_global_prefill_workspace_bytes(B, L, Hkv, d);
     if (!workspace || workspace_bytes < need || !aligned16(workspace)) return ZG_ERR_WORKSPACE;
-    const int T = global_q_tile_tokens();
+    const int T = global_q_tile_tokens(G);
     const long long n_lt = (L + T - 1) / T;
     if (n_lt * Hkv * B >= (1ll << 31) || static_cast<long long>(B) * L * Hkv / 8 >= (1ll << 31))
         return ZG_ERR_UNSUPPORTED;
@@ -247,7 +269,7 @@ zg_status zg_global_prefill(const zg_bf16* q, const zg_bf16* k, const zg_bf16* v
     PrefillParams p;
     std::memset(&p, 0, sizeof(p));
     if (!dev_ctl(p.ctl)) return ZG_ERR_CUDA;
-    if (!make_map(&p.tm_q, q, d, Hq, L, B, 4, T) || !make_map(&p.tm_out, out, d, Hq, L, B, 4, T) ||
+    if (!make_map(&p.tm_q, q, d, Hq, L, B, G, T) || !make_map(&p.tm_out, out, d, Hq, L, B, G, T) ||
         !make_map(&p.tm_kh, workspace, d, Hkv, L, B, 1, 128, CU_TENSOR_MAP_DATA_TYPE_FLOAT16) ||
         !make_map(&p.tm_v, v, d, Hkv, L, B, 1, 128))
         return ZG_ERR_CUDA;
@@ -363,7 +385,7 @@ zg_status zg_gated_swa_layer(const zg_bf16* h, const zg_bf16* w_q, const zg_bf16
     if (st != ZG_OK) return st;
     if (window < 1) return ZG_ERR_SHAPE;
     const int G = Hq / Hkv;
-    if ((d != 64 && d != 128) || (G != 1 && G != 2 && G != 4 && G != 8) || window > 128 || Hkv > 65535)
+    if ((d != 64 && d != 128) || (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) || window > 128 || Hkv > 65535)
         return ZG_ERR_UNSUPPORTED;
     if (B == 0 || L == 0) return ZG_OK;
     const LayerWs w = layer_ws(B, L, Hq, Hkv, d);
@@ -493,8 +515,7 @@ zg_status zg_attention_backward(const zg_bf16* q, const zg_bf16* k, const zg_bf1
 
 size_t zg_hybrid_decode_workspace_bytes(int NG, int B, int Hq, int d, int64_t S_max) {
     if (NG <= 0 || B <= 0 || Hq <= 0 || d <= 0 || S_max <= 0) return 0;
-    (void)d;
-    return decode_workspace_bytes(NG, B, Hq, S_max);
+    return decode_workspace_bytes(NG, B, Hq, d, S_max);
 }
 
 
@@ -518,13 +539,20 @@ static zg_status hybrid_decode_impl(const zg_bf16* q, const zg_bf16* k_new, cons
         if (is_global[l]) glob_layers[NG++] = l;
         else loc_layers[NS++] = l;
     }
-    const size_t need = NG ? decode_workspace_bytes(NG, B, Hq, S_max) : 0;
+    const size_t need = NG ? decode_workspace_bytes(NG, B, Hq, d, S_max) : 0;
     if (need && (!workspace || workspace_bytes < need || !aligned16(workspace))) return ZG_ERR_WORKSPACE;
     const long long nsplit = NG ? (S_max + kDecodeSplitLen - 1) / kDecodeSplitLen : 1;
 
     DecodeParams p;
     std::memset(&p, 0, sizeof(p));
     if (!dev_ctl(p.ctl)) return ZG_ERR_CUDA;
+    const int box_rows = decode_cache_box_rows(d, fp8 != 0);
+    if (NG && (!make_cache_map(&p.tm_kg, k_glob, d, S_max, static_cast<long long>(NG) * B * Hkv, fp8, box_rows) ||
+               !make_cache_map(&p.tm_vg, v_glob, d, S_max, static_cast<long long>(NG) * B * Hkv, fp8, box_rows)))
+        return ZG_ERR_CUDA;
+    if (NS && (!make_cache_map(&p.tm_kr, k_ring, d, window, static_cast<long long>(NS) * B * Hkv, fp8, box_rows) ||
+               !make_cache_map(&p.tm_vr, v_ring, d, window, static_cast<long long>(NS) * B * Hkv, fp8, box_rows)))
+        return ZG_ERR_CUDA;
     p.q = reinterpret_cast<const __nv_bfloat16*>(q);
     p.k_new = reinterpret_cast<const __nv_bfloat16*>(k_new);
     p.v_new = reinterpret_cast<const __nv_bfloat16*>(v_new);

@@ -9,9 +9,10 @@
 // Kernel 1 normalises and rotates every key once (one warp per key row) into
 // an fp16 workspace, so the quadratic loop below never repeats that work.
 //
-// Kernel 2: one CTA owns 64 consecutive tokens of one KV head, as two 128-row
-// tiles (32 tokens x the 4 query heads of the group each), Q0 and Q1, that share
-// every K_hat / V block of 128 keys; heaviest CTAs (longest key ranges) first.
+// Kernel 2: one CTA owns 2T consecutive tokens of one KV head, as two 128-row
+// tiles (T = 128 / G tokens x the G query heads of the group each), Q0 and Q1,
+// that share every K_hat / V block of 128 keys; heaviest CTAs (longest key ranges)
+// first.  Head sizes 64 and 128; GQA ratios G = 1, 2, 4, 8, 16.
 //   warp 0      TMA: both Q tiles, then K_hat / V blocks on two-stage rings.
 //   warp 1      MMA (one thread): QK0(0), QK1(0), then per block j
 //                 PV0(j), QK0(j+1), PV1(j), QK1(j+1)
@@ -25,48 +26,51 @@
 //               PV0(j-1) has completed), P = exp2(...) in bf16 back to TMEM, row
 //               sums of the rounded P; finally O / l -> bf16 -> TMA store.
 //   warps 8-11  the same for tile 1.
-// TMEM: S0 [0,128), S1 [128,256), O0 [256,384), O1 [384,512).
-// Only the last key block of a CTA can contain keys beyond the diagonal.
+// TMEM: S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [384,384+D).
+// Only blocks that reach past the CTA's first query hold keys beyond a diagonal.
 #include "zg_qk.cuh"
 
 namespace zg {
 namespace {
 
-constexpr int D = 128;
-constexpr int G = 4;
-constexpr int T = 32;                     // tokens per tile
-constexpr int BK = 128;                   // keys per block
-constexpr uint32_t TILE = 128 * 128 * 2;  // one 128 x 128 16-bit tile (two 64-column chunks)
-constexpr uint32_t CH = 128 * 128;        // one 64-column chunk of 128 rows
-constexpr uint32_t OFF_Q = 0;             // Q0, Q1
-constexpr uint32_t OFF_K = 2 * TILE;      // 2 stages
-constexpr uint32_t OFF_V = 4 * TILE;      // 2 stages
-constexpr uint32_t OFF_BAR = 6 * TILE;
+constexpr int BK = 128;               // keys per block
+constexpr uint32_t CH = 128 * 128;    // one 64-column chunk of 128 rows (16-bit elements)
 constexpr int NBAR = 20;
-constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
-constexpr uint32_t SMEM = OFF_MISC + 32;
 constexpr float kTau = 8.0f;
 constexpr int kThreads = 384;
 
+template <int D>
+struct Glb {
+    static constexpr uint32_t TILE = 128 * D * 2;  // one 128-row x D tile of 16-bit values (D/64 chunks)
+    static constexpr uint32_t OFF_Q = 0;           // Q0, Q1
+    static constexpr uint32_t OFF_K = 2 * TILE;    // 2 stages
+    static constexpr uint32_t OFF_V = 4 * TILE;    // 2 stages
+    static constexpr uint32_t OFF_BAR = 6 * TILE;
+    static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
+    static constexpr uint32_t SMEM = OFF_MISC + 32;
+};
+
 // ---------------------------------------------------------------- kernel 1
+template <int D>
 __global__ void __launch_bounds__(256) khat_kernel(const __grid_constant__ PrefillParams p) {
-    __shared__ float buf[8][D];
+    __shared__ __align__(16) float buf[8][D];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long long row = static_cast<long long>(blockIdx.x) * 8 + warp;  // (b, j, g) flattened
     const long long nrows = static_cast<long long>(p.B) * p.L * p.Hkv;
     if (row >= nrows) return;
     const long long tok = row / p.Hkv;  // b * L + j
     const int pos = __ldg(p.pos + tok);
-    norm_rope_warp(p.k_raw + row * D, p.wk, p.eps, pos, p.rope, 1.0f, buf[warp]);
-    const float4 v = *reinterpret_cast<const float4*>(&buf[warp][lane * 4]);
-    uint2 o;
-    o.x = pack_half2(v.x, v.y);
-    o.y = pack_half2(v.z, v.w);
-    *reinterpret_cast<uint2*>(p.khat + row * D + lane * 4) = o;
+    norm_rope_warp_d<D>(p.k_raw + row * D, p.wk, p.eps, pos, p.rope, 1.0f, buf[warp]);
+    for (int e = 2 * lane; e < D; e += 64)
+        *reinterpret_cast<uint32_t*>(p.khat + row * D + e) = pack_half2(buf[warp][e], buf[warp][e + 1]);
 }
 
 // ---------------------------------------------------------------- kernel 2
+template <int D, int G>
 __global__ void __launch_bounds__(kThreads, 1) global_attn_kernel(const __grid_constant__ PrefillParams p) {
+    constexpr int T = 128 / G;  // tokens per tile
+    constexpr uint32_t TILE = Glb<D>::TILE, OFF_Q = Glb<D>::OFF_Q, OFF_K = Glb<D>::OFF_K, OFF_V = Glb<D>::OFF_V;
+    constexpr uint32_t OFF_BAR = Glb<D>::OFF_BAR, OFF_MISC = Glb<D>::OFF_MISC;
     extern __shared__ __align__(1024) uint8_t smem[];
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
     uint64_t* q_full = bar + 0;
@@ -131,7 +135,7 @@ __global__ void __launch_bounds__(kThreads, 1) global_attn_kernel(const __grid_c
             tma_prefetch_desc(&p.tm_out);
             mbar_arrive_expect_tx(q_full, 2 * TILE);
             for (int t = 0; t < 2; ++t)
-                for (int ch = 0; ch < 2; ++ch)
+                for (int ch = 0; ch < D / 64; ++ch)
                     tma_load_4d(smem + OFF_Q + t * TILE + ch * CH, &p.tm_q, q_full, ch * 64, g * G, i0 + t * T, b);
             bool ok = true;
             for (int j = 0; j < nkb && ok && !aborted(); ++j) {
@@ -139,12 +143,12 @@ __global__ void __launch_bounds__(kThreads, 1) global_attn_kernel(const __grid_c
                 ok = mbar_wait(&k_empty[st], ((j >> 1) & 1) ^ 1, p.ctl, 51);
                 if (!ok) break;
                 mbar_arrive_expect_tx(&k_full[st], TILE);
-                for (int ch = 0; ch < 2; ++ch)
+                for (int ch = 0; ch < D / 64; ++ch)
                     tma_load_4d(smem + OFF_K + st * TILE + ch * CH, &p.tm_kh, &k_full[st], ch * 64, g, j * BK, b);
                 ok = mbar_wait(&v_empty[st], ((j >> 1) & 1) ^ 1, p.ctl, 52);
                 if (!ok) break;
                 mbar_arrive_expect_tx(&v_full[st], TILE);
-                for (int ch = 0; ch < 2; ++ch)
+                for (int ch = 0; ch < D / 64; ++ch)
                     tma_load_4d(smem + OFF_V + st * TILE + ch * CH, &p.tm_v, &v_full[st], ch * 64, g, j * BK, b);
             }
             if (!ok) fail();
@@ -238,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1) global_attn_kernel(const __grid_c
             tmem_ld32(s_addr + 64, r + 64);
             tmem_ld32(s_addr + 96, r + 96);
             tmem_wait_ld();
-            const bool diag = j == nkb - 1;
+            const bool diag = (j + 1) * BK - 1 > i0;  // the block reaches past the CTA's first query
             const int kmax = iq - j * BK;  // last valid key column of this row in the block
             if (diag) {
 #pragma unroll
@@ -318,7 +322,8 @@ __global__ void __launch_bounds__(kThreads, 1) global_attn_kernel(const __grid_c
         mbar_arrive(&out_bar[t]);
         if (row == 0 && ok && i0 + t * T < p.L) {  // a tile that starts past the end has nothing to store
             if (mbar_wait(&out_bar[t], 0, p.ctl, 64)) {
-                for (int ch = 0; ch < 2; ++ch) tma_store_4d(&p.tm_out, qt + ch * CH, ch * 64, g * G, i0 + t * T, b);
+                for (int ch = 0; ch < D / 64; ++ch)
+                    tma_store_4d(&p.tm_out, qt + ch * CH, ch * 64, g * G, i0 + t * T, b);
                 bulk_commit();
                 bulk_wait_all();
             } else {
@@ -339,21 +344,41 @@ __global__ void __launch_bounds__(kThreads, 1) global_attn_kernel(const __grid_c
     if (warp == 1) tmem_dealloc(tbase, 512);
 }
 
-}  // namespace
-
-int global_q_tile_tokens() { return T; }
-
-cudaError_t launch_global_prefill(const PrefillParams& p, int d, cudaStream_t s) {
-    if (d != D || p.Hq != p.Hkv * G) return cudaErrorInvalidValue;
+template <int D, int G>
+cudaError_t launch_t(const PrefillParams& p, cudaStream_t s) {
+    constexpr int T = 128 / G;
     const long long rows = static_cast<long long>(p.B) * p.L * p.Hkv;
-    khat_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, s>>>(p);
+    khat_kernel<D><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, s>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(global_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+    auto k = global_attn_kernel<D, G>;
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Glb<D>::SMEM);
     if (e != cudaSuccess) return e;
     const long long ctas = static_cast<long long>(p.B) * p.Hkv * ((p.L + 2 * T - 1) / (2 * T));
-    global_attn_kernel<<<static_cast<unsigned>(ctas), kThreads, SMEM, s>>>(p);
+    k<<<static_cast<unsigned>(ctas), kThreads, Glb<D>::SMEM, s>>>(p);
     return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_d(const PrefillParams& p, cudaStream_t s) {
+    switch (p.Hq / p.Hkv) {
+        case 1: return launch_t<D, 1>(p, s);
+        case 2: return launch_t<D, 2>(p, s);
+        case 4: return launch_t<D, 4>(p, s);
+        case 8: return launch_t<D, 8>(p, s);
+        case 16: return launch_t<D, 16>(p, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+bool global_supports(int d, int G) { return (d == 64 || d == 128) && (G == 1 || G == 2 || G == 4 || G == 8 || G == 16); }
+int global_q_tile_tokens(int G) { return 128 / G; }
+
+cudaError_t launch_global_prefill(const PrefillParams& p, int d, cudaStream_t s) {
+    if (p.Hkv <= 0 || p.Hq % p.Hkv || !global_supports(d, p.Hq / p.Hkv)) return cudaErrorInvalidValue;
+    return d == 128 ? launch_d<128>(p, s) : launch_d<64>(p, s);
 }
 
 }  // namespace zg

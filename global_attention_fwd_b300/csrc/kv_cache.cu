@@ -20,10 +20,9 @@
 namespace zg {
 namespace {
 
-constexpr int D = 128;
-
+template <int D>
 __global__ void __launch_bounds__(256) kv_cache_kernel(const __grid_constant__ CacheParams p) {
-    __shared__ float buf[8][D];
+    __shared__ __align__(16) float buf[8][D];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_keep = p.L - p.i0;
     const long long row = static_cast<long long>(blockIdx.x) * 8 + warp;  // (b, i - i0, g) flattened
@@ -45,34 +44,35 @@ __global__ void __launch_bounds__(256) kv_cache_kernel(const __grid_constant__ C
         return;
     }
     const long long dst = ((static_cast<long long>(b) * p.Hkv + g) * p.S + slot) * D;
-    norm_rope_warp(p.k + src * D, p.wk, p.eps, pos, p.rope, 1.0f, buf[warp]);
-    const float4 kv = *reinterpret_cast<const float4*>(&buf[warp][lane * 4]);
-    if (p.fp8) {
-        auto e4m3x2 = [](float a, float b) {
-            return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
-        };
-        const uint2 vr = *reinterpret_cast<const uint2*>(p.v + src * D + lane * 4);
-        const float ks = p.k_scale, vs = p.v_scale;
-        const uint32_t k8 = e4m3x2(kv.x * ks, kv.y * ks) | e4m3x2(kv.z * ks, kv.w * ks) << 16;
-        const uint32_t v8 = e4m3x2(bf16lo(vr.x) * vs, bf16hi(vr.x) * vs) | e4m3x2(bf16lo(vr.y) * vs, bf16hi(vr.y) * vs) << 16;
-        *reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(p.cache_k) + dst + lane * 4) = k8;
-        *reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(p.cache_v) + dst + lane * 4) = v8;
-        return;
+    // the same per-warp arithmetic as the decode step's own cache write (bit-identical keys)
+    norm_rope_warp_d<D>(p.k + src * D, p.wk, p.eps, pos, p.rope, 1.0f, buf[warp]);
+    for (int e = 2 * lane; e < D; e += 64) {
+        const float k0 = buf[warp][e], k1 = buf[warp][e + 1];
+        const __nv_bfloat162 vv = *reinterpret_cast<const __nv_bfloat162*>(p.v + src * D + e);
+        if (p.fp8) {
+            const float ks = p.k_scale, vs = p.v_scale;
+            *reinterpret_cast<__nv_fp8x2_storage_t*>(reinterpret_cast<uint8_t*>(p.cache_k) + dst + e) =
+                __nv_cvt_float2_to_fp8x2(make_float2(k0 * ks, k1 * ks), __NV_SATFINITE, __NV_E4M3);
+            *reinterpret_cast<__nv_fp8x2_storage_t*>(reinterpret_cast<uint8_t*>(p.cache_v) + dst + e) =
+                __nv_cvt_float2_to_fp8x2(make_float2(__low2float(vv) * vs, __high2float(vv) * vs), __NV_SATFINITE,
+                                         __NV_E4M3);
+        } else {
+            *reinterpret_cast<uint32_t*>(p.cache_k + dst + e) = pack_bf16x2(k0, k1);
+            *reinterpret_cast<__nv_bfloat162*>(p.cache_v + dst + e) = vv;
+        }
     }
-    uint2 ko;
-    ko.x = pack_bf16x2(kv.x, kv.y);
-    ko.y = pack_bf16x2(kv.z, kv.w);
-    *reinterpret_cast<uint2*>(p.cache_k + dst + lane * 4) = ko;
-    *reinterpret_cast<uint2*>(p.cache_v + dst + lane * 4) = *reinterpret_cast<const uint2*>(p.v + src * D + lane * 4);
 }
 
 }  // namespace
 
 cudaError_t launch_kv_cache(const CacheParams& p, int d, cudaStream_t s) {
-    if (d != D) return cudaErrorInvalidValue;
+    if (d != 64 && d != 128) return cudaErrorInvalidValue;
     const long long rows = static_cast<long long>(p.B) * (p.L - p.i0) * p.Hkv;
     if (rows <= 0) return cudaSuccess;
-    kv_cache_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, s>>>(p);
+    if (d == 128)
+        kv_cache_kernel<128><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, s>>>(p);
+    else
+        kv_cache_kernel<64><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, s>>>(p);
     return cudaGetLastError();
 }
 

@@ -331,6 +331,8 @@ cudaError_t launch_swa_prefill(const PrefillParams& p, int d, cudaStream_t s) {
     if (d == 64 && G == 2) return launch_swa_t<64, 2>(p, s);
     if (d == 128 && G == 1) return launch_swa_t<128, 1>(p, s);
     if (d == 64 && G == 1) return launch_swa_t<64, 1>(p, s);
+    if (d == 128 && G == 16) return launch_swa_t<128, 16>(p, s);
+    if (d == 64 && G == 16) return launch_swa_t<64, 16>(p, s);
     return cudaErrorInvalidValue;
 }
 

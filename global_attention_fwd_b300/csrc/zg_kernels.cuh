@@ -44,10 +44,13 @@ int swa_kv_box_rows(int G);  // rows of the K/V TMA box the SWA kernel for GQA r
 bool swa2_supports(int d, int G);
 cudaError_t launch_swa2_prefill(const PrefillParams& p, int d, cudaStream_t s);
 cudaError_t launch_global_prefill(const PrefillParams& p, int d, cudaStream_t s);
-int global_q_tile_tokens();
+bool global_supports(int d, int G);  // head sizes and GQA ratios the global prefill implements
+int global_q_tile_tokens(int G);     // tokens of one 128-row query tile (128 / G)
 
 // ---------------------------------------------------------------- decode
 struct DecodeParams {
+    CUtensorMap tm_kg, tm_vg;    // 3-D maps {d, S, NG*B*Hkv} over the global caches (bf16 or E4M3 bytes)
+    CUtensorMap tm_kr, tm_vr;    // 3-D maps {d, W, NS*B*Hkv} over the rings
     const __nv_bfloat16* q;      // [NL, B, Hq, d]
     const __nv_bfloat16* k_new;  // [NL, B, Hkv, d]
     const __nv_bfloat16* v_new;  // [NL, B, Hkv, d]
@@ -86,7 +89,9 @@ int hybrid_decode_check(const void* q, const void* k_new, const void* v_new, con
                         const void* v_glob, const void* k_ring, const void* v_ring, const void* out, int NL, int B,
                         int Hq, int Hkv, int d, int64_t S_max, int window, int rotary_dim, double theta, float eps,
                         int fp8, float k_scale, float v_scale, int* ng);
-size_t decode_workspace_bytes(int NG, int B, int Hq, long long S);
+size_t decode_workspace_bytes(int NG, int B, int Hq, int d, long long S);
+bool decode_supports(int d, int G);          // head sizes and GQA ratios the decode kernels implement
+int decode_cache_box_rows(int d, bool fp8);  // cache rows per TMA box of one decode stage
 
 // ---------------------------------------------------------------- decode caches from a prefill
 struct CacheParams {

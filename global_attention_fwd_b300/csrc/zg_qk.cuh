@@ -318,6 +318,40 @@ __device__ __forceinline__ void qk_norm_rope_row_pair_ct(uint8_t* base, uint32_t
     }
 }
 
+// RMSNorm + partial RoPE of one D-element head vector with one warp (x: bf16, global memory);
+// the result times `scale` goes to dst[D] (fp32, shared memory).  The decode step and the cache
+// writer both use it, so a key cached by a prefill and one cached by a decode step agree bit for bit.
+template <int D>
+__device__ __forceinline__ void norm_rope_warp_d(const __nv_bfloat16* x, const float* w, float eps, int pos,
+                                                 const RopeConsts& rc, float scale, float* dst) {
+    constexpr int PER = D / 32;
+    const int lane = threadIdx.x & 31;
+    float v[PER];
+    float ss = 0.f;
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+        v[k] = __bfloat162float(x[lane * PER + k]);
+        ss = fmaf(v[k], v[k], ss);
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float inv = ss > 0.f || eps > 0.f ? rsqrtf(ss * (1.0f / D) + eps) : 0.f;
+#pragma unroll
+    for (int k = 0; k < PER; ++k) dst[lane * PER + k] = v[k] * inv * __ldg(w + lane * PER + k);
+    __syncwarp();
+    for (int j = lane; j < rc.half; j += 32) {
+        const float a = dst[j], b = dst[j + rc.half];
+        float cs, sn;
+        rope_cos_sin(pos, rc.f_hi[j], rc.f_lo[j], cs, sn);
+        dst[j] = a * cs - b * sn;
+        dst[j + rc.half] = b * cs + a * sn;
+    }
+    __syncwarp();
+    if (scale != 1.0f)
+        for (int e = lane; e < D; e += 32) dst[e] *= scale;
+    __syncwarp();
+}
+
 // RMSNorm + partial RoPE of one 128-element head vector with one warp; x is bf16 in global memory.
 // Result (fp32, times `scale`) goes to smem dst[128].
 __device__ __forceinline__ void norm_rope_warp(const __nv_bfloat16* x, const float* w, float eps, int pos, const RopeConsts& rc,

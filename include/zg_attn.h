@@ -79,7 +79,9 @@ typedef enum {
  *   wq, wk: [d] float32 QK-norm weights (shared by all heads)
  *   out: [B, L, Hq, d] bf16 (written; must not overlap the inputs)
  *   window: keys per query including itself, 1 <= window <= 128
- * Kernel shapes: d in {64, 128}; Hq / Hkv in {1, 2, 4, 8}; Hkv <= 65535.
+ * Kernel shapes: d in {64, 128}; Hq / Hkv in {1, 2, 4, 8, 16} (a 128-row
+ * tensor-core tile packs 128 / G tokens x the G heads of a KV head, so G must
+ * divide 128); Hkv <= 65535.
  * B == 0 or L == 0 is a no-op returning ZG_OK.
  */
 zg_status zg_swa_prefill(const zg_bf16 *q, const zg_bf16 *k, const zg_bf16 *v, const zg_bf16 *gate,
@@ -96,7 +98,7 @@ size_t zg_global_prefill_workspace_bytes(int B, int L, int Hkv, int d);
  *   workspace: device scratch of at least zg_global_prefill_workspace_bytes()
  *        bytes, 16-byte aligned; it receives the normalised, rotated keys (fp16)
  *        and needs no initialisation.  ZG_ERR_WORKSPACE if missing or too small.
- * Kernel shapes: d == 128; Hq / Hkv == 4.
+ * Kernel shapes: d in {64, 128}; Hq / Hkv in {1, 2, 4, 8, 16} (as zg_swa_prefill).
  */
 zg_status zg_global_prefill(const zg_bf16 *q, const zg_bf16 *k, const zg_bf16 *v,
                             const int32_t *pos, const float *wq, const float *wk, zg_bf16 *out,
@@ -118,8 +120,8 @@ zg_status zg_global_prefill(const zg_bf16 *q, const zg_bf16 *k, const zg_bf16 *v
  *   consecutive positions do).  Other slots are left untouched.
  * zg_global_prefill_with_cache: k_cache, v_cache are one global layer's caches
  *   [B, Hkv, S_max, d] bf16; every token goes to slot pos[b,i], 0 <= pos < S_max.
- * Only d = 128 (the decode step's head size) is supported: ZG_ERR_UNSUPPORTED
- * otherwise.  The cache pointers must be 16-byte aligned and are written in place.
+ * Head sizes d = 64 and 128 (those of the decode step) are supported:
+ * ZG_ERR_UNSUPPORTED otherwise.  The cache pointers must be 16-byte aligned and are written in place.
  * A token whose position has no slot (negative, or >= S_max for a global cache) is
  * skipped and recorded on the device: zg_device_status() then returns
  * ZG_ERR_POSITION.  The pages define no interface; these calls follow the cache
@@ -130,7 +132,7 @@ zg_status zg_global_prefill(const zg_bf16 *q, const zg_bf16 *k, const zg_bf16 *v
  * every sequence b and token i (ring = 1: the last min(L, S) tokens, slot
  * pos[b,i] mod S; ring = 0: every token, slot pos[b,i], 0 <= pos < S) it stores
  * k_hat (bf16) in k_cache and v in v_cache, [B, Hkv, S, d] bf16 each.
- * k, v [B, L, Hkv, d] bf16; pos [B, L] int32; wk [d] float; d = 128.
+ * k, v [B, L, Hkv, d] bf16; pos [B, L] int32; wk [d] float; d = 64 or 128.
  * Errors as for the calls above; positions without a slot are skipped and
  * reported through zg_device_status() as ZG_ERR_POSITION.
  */
@@ -181,7 +183,11 @@ size_t zg_hybrid_decode_workspace_bytes(int NG, int B, int Hq, int d, int64_t S_
  *   out: [NL, B, Hq, d] bf16
  *   workspace: device scratch of at least zg_hybrid_decode_workspace_bytes()
  *        bytes (may be NULL when NG == 0); its contents need no initialisation.
- * Kernel shapes: d == 128, Hq / Hkv == 4, W == 128, NL <= 96.
+ * Kernel shapes: d = 64 or 128; any GQA ratio 1 <= Hq / Hkv <= 16 (Hq a multiple
+ * of Hkv); 1 <= W <= 4096; NL <= 96.  The products run on the warp-level tensor
+ * core instruction with fp32 accumulation; q_hat enters them as a bf16 head plus
+ * a bf16 tail (about 16 mantissa bits), the softmax weights as bf16 (E4M3
+ * caches: q_hat and the weights in fp16).
  */
 zg_status zg_hybrid_decode(const zg_bf16 *q, const zg_bf16 *k_new, const zg_bf16 *v_new, const zg_bf16 *gate,
                            const int32_t *pos, const float *wq, const float *wk, const uint8_t *is_global,

@@ -61,7 +61,8 @@ def test_swa_rejects_bad_arguments_before_launch(zg):
     assert _swa(zg, eps=-1.0) == -3
     assert _swa(zg, window=129) == -4
     assert _swa(zg, d=96, rot=30) == -4
-    assert _swa(zg, Hq=12, Hkv=1) == -4
+    assert _swa(zg, Hq=12, Hkv=1) == -4   # G must divide 128
+    assert _swa(zg, Hq=32, Hkv=1) == -4   # G > 16
     # empty inputs are a no-op
     assert _swa(zg, L=0) == 0
     assert _swa(zg, B=0) == 0
@@ -79,8 +80,8 @@ def test_global_rejects_bad_arguments_before_launch(zg):
     assert _glob(zg, v=None) == -1
     assert _glob(zg, pos=A + 4) == -2
     assert _glob(zg, L=-5) == -3
-    assert _glob(zg, d=64, rot=20) == -4
-    assert _glob(zg, Hq=16) == -4
+    assert _glob(zg, d=96, rot=30) == -4
+    assert _glob(zg, Hq=24) == -4          # G = 3 does not divide 128
     assert _glob(zg, L=0) == 0
     assert _glob(zg, ws=None) == -6
     assert _glob(zg, ws_bytes=16 * 8 * 128 * 2 - 1) == -6
@@ -117,7 +118,7 @@ def test_prefill_with_cache_rejects_bad_cache_arguments_before_launch(zg):
     assert _swa_cache(zg, kr=None) == -1
     assert _swa_cache(zg, vr=A + 4) == -2
     assert _swa_cache(zg, slots=0) == -3
-    assert _swa_cache(zg, d=64, rot=20) == -4      # decode caches have d = 128
+    assert _swa_cache(zg, d=96, rot=30) == -4      # decode caches have d = 64 or 128
     assert _swa_cache(zg, q=None) == -1            # then the prefill's own checks
     assert _swa_cache(zg, window=0) == -3
     assert _glob_cache(zg, vc=None) == -1
@@ -125,6 +126,7 @@ def test_prefill_with_cache_rejects_bad_cache_arguments_before_launch(zg):
     assert _glob_cache(zg, smax=0) == -3
     assert _glob_cache(zg, ws=None) == -6
     assert _glob_cache(zg, Hq=24) == -4
+    assert _glob_cache(zg, d=96, rot=30) == -4
 
 
 def test_kv_cache_write_rejects_bad_arguments(zg):
@@ -140,7 +142,7 @@ def test_kv_cache_write_rejects_bad_arguments(zg):
     assert call(S=0) == -3
     assert call(ring=2) == -3
     assert call(rot=43) == -3
-    assert call(d=64, rot=20) == -4
+    assert call(d=96, rot=30) == -4
 
 
 def test_gated_swa_layer_rejects_bad_arguments(zg):
@@ -204,7 +206,9 @@ def test_fp8_entry_points_reject_bad_arguments(zg):
     assert dec(vs=float("inf")) == -3
     assert dec(kg=None) == -1
     assert dec(vr=A + 8) == -2
-    assert dec(d=64, rot=20) == -4
+    assert dec(d=96, rot=30) == -4
+    assert dec(Hq=17, Hkv=1) == -4   # more than 16 query heads per KV head
+    assert dec(W=0) == -3
 
     def wr(**kw):
         a = dict(k=A, v=A, pos=A, wk=A, kc=A, vc=A, B=1, L=16, Hkv=8, d=128, S=128, ring=1, rot=42, theta=1e6,

@@ -20,9 +20,8 @@ def _draw(shape, g):
     return torch.randn(*shape, generator=g).bfloat16()
 
 
-def _small_case(NL, flags, B, Hq, Hkv, S, W, seed):
+def _small_case(NL, flags, B, Hq, Hkv, S, W, seed, d=128):
     g = torch.Generator().manual_seed(seed)
-    d = 128
     NG = sum(flags)
     NS = NL - NG
     return dict(q=_draw((NL, B, Hq, d), g), k_new=_draw((NL, B, Hkv, d), g), v_new=_draw((NL, B, Hkv, d), g),
@@ -75,6 +74,24 @@ def test_small_hybrid_decode(zg, positions):
     flags = [0, 0, 1, 0, 0, 1]
     inp = _small_case(6, flags, 3, 8, 2, 5000, 128, seed=sum(positions))
     _run_and_check(zg, inp, flags, positions, 42, 1e6, 1e-6, seqs=[0, 1, 2])
+
+
+@pytest.mark.parametrize("d,Hq,Hkv,W", [
+    (64, 8, 8, 128),     # no head sharing, d = 64
+    (64, 8, 4, 128),     # GQA 2:1
+    (128, 16, 2, 128),   # GQA 8:1
+    (128, 32, 2, 128),   # GQA 16:1 (two groups of 8 fragment rows)
+    (64, 16, 1, 128),    # GQA 16:1, d = 64
+    (128, 12, 4, 128),   # GQA 3:1 (not a power of two)
+    (128, 8, 2, 200),    # a 200-slot ring (stages past the ring read as zeros)
+    (64, 8, 2, 40),      # a 40-slot ring
+])
+def test_decode_head_sizes_gqa_ratios_and_windows(zg, d, Hq, Hkv, W):
+    flags = [0, 1, 0, 1]
+    S = 9000  # two splits of 8192 keys
+    inp = _small_case(len(flags), flags, 3, Hq, Hkv, S, W, seed=d + Hq + W, d=d)
+    positions = [8999, 8192, min(W, 30)]
+    _run_and_check(zg, inp, flags, positions, workloads.rotary_dim_for(d), 1e6, 1e-6, seqs=[0, 1, 2])
 
 
 def test_decode_only_local_and_only_global(zg):

@@ -25,9 +25,8 @@ def zg():
     return zg
 
 
-def _case(NL, flags, B, Hq, Hkv, S, W, seed, k_scale, v_scale):
+def _case(NL, flags, B, Hq, Hkv, S, W, seed, k_scale, v_scale, d=128):
     g = torch.Generator().manual_seed(seed)
-    d = 128
     NG, NS = sum(flags), NL - sum(flags)
     bf = lambda *sh: torch.randn(*sh, generator=g).bfloat16()
     inp = dict(q=bf(NL, B, Hq, d), k_new=bf(NL, B, Hkv, d), v_new=bf(NL, B, Hkv, d), gate=bf(NL, B, Hq, d),
@@ -69,6 +68,13 @@ def _run(zg, inp, flags, positions, seqs, k_scale, v_scale, host=None, rotary_di
             assert np.all(np.abs(got_k - want_k) <= 2.0 ** -4 * np.abs(want_k) + 2.0 ** -10), f"key slot layer {l}"
             want_v = (inp["v_new"][l, b].float() * v_scale).to(F8)
             assert torch.equal(vc[:, slot].cpu().view(torch.uint8), want_v.view(torch.uint8)), f"value slot layer {l}"
+
+
+@pytest.mark.parametrize("d,Hq,Hkv", [(64, 8, 2), (128, 16, 1), (64, 12, 4), (128, 8, 8)])
+def test_fp8_decode_head_sizes_and_gqa_ratios(zg, d, Hq, Hkv):
+    flags = [1, 0, 0, 1]
+    inp = _case(4, flags, 2, Hq, Hkv, 9000, 128, d + Hq, 1.0, 8.0, d=d)
+    _run(zg, inp, flags, [8999, 77], [0, 1], 1.0, 8.0, rotary_dim=workloads.rotary_dim_for(d))
 
 
 @pytest.mark.parametrize("positions,k_scale,v_scale", [([4999, 130, 50], 1.0, 8.0), ([0, 127, 4096], 2.0, 3.0),

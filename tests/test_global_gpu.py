@@ -42,6 +42,19 @@ def test_small_lengths_all_rows(zg, B, L):
     _check(zg, inp, list(range(B * L)), 42, 1e6, f"global B{B} L{L}")
 
 
+@pytest.mark.parametrize("d,Hq,Hkv,L", [
+    (64, 8, 2, 700),      # d = 64, GQA 4:1
+    (128, 8, 8, 600),     # no head sharing: 128 tokens per query tile
+    (64, 4, 2, 530),      # GQA 2:1
+    (128, 16, 2, 450),    # GQA 8:1 (16 tokens per tile)
+    (128, 32, 2, 300),    # GQA 16:1 (8 tokens per tile)
+    (64, 16, 1, 257),     # GQA 16:1, d = 64
+])
+def test_head_sizes_and_gqa_ratios_all_rows(zg, d, Hq, Hkv, L):
+    inp = _synthetic(2, L, Hq, Hkv, d, seed=d + Hq + L)
+    _check(zg, inp, list(range(2 * L)), workloads.rotary_dim_for(d), 1e6, f"global d{d} {Hq}/{Hkv} L{L}")
+
+
 def test_medium_length_sampled(zg):
     inp = _synthetic(1, 8192, 8, 2, 128, seed=11)
     rows = sorted(set(range(0, 8192, 37)) | set(workloads.edge_rows(8192)))

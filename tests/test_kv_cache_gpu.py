@@ -20,12 +20,12 @@ def zg():
     return zg
 
 
-def _inputs(B, L, seed, pos0=(0,)):
+def _inputs(B, L, seed, pos0=(0,), d=D, Hq=HQ, Hkv=HKV):
     g = torch.Generator().manual_seed(seed)
     pos = torch.stack([torch.arange(L, dtype=torch.int32) + int(pos0[b % len(pos0)]) for b in range(B)]).contiguous()
-    return dict(q=torch.randn(B, L, HQ, D, generator=g).bfloat16(), k=torch.randn(B, L, HKV, D, generator=g).bfloat16(),
-                v=torch.randn(B, L, HKV, D, generator=g).bfloat16(), gate=torch.randn(B, L, HQ, D, generator=g).bfloat16(),
-                pos=pos, wq=0.5 + torch.rand(D, generator=g), wk=0.5 + torch.rand(D, generator=g))
+    return dict(q=torch.randn(B, L, Hq, d, generator=g).bfloat16(), k=torch.randn(B, L, Hkv, d, generator=g).bfloat16(),
+                v=torch.randn(B, L, Hkv, d, generator=g).bfloat16(), gate=torch.randn(B, L, Hq, d, generator=g).bfloat16(),
+                pos=pos, wq=0.5 + torch.rand(d, generator=g), wk=0.5 + torch.rand(d, generator=g))
 
 
 def _khat(inp, b, i, g):
@@ -118,11 +118,12 @@ def test_position_without_a_slot_is_reported(zg):
     _check_slot(kc, vc, inp, 0, 2, 31, 31, "in range")
 
 
-def test_prefill_then_decode_matches_the_longer_prefill(zg):
+@pytest.mark.parametrize("D,HQ,HKV,R", [(128, 32, 8, 42), (64, 16, 8, 20)])
+def test_prefill_then_decode_matches_the_longer_prefill(zg, D, HQ, HKV, R):
     # a two-layer stack (layer 0 local, layer 1 global): prefill L tokens with cache emission,
     # decode token L from those caches, and compare with the oracle's prefill of L + 1 tokens
     B, L, W, S = 2, 300, 128, 512
-    layers = [_inputs(B, L + 1, seed=20 + l) for l in range(2)]
+    layers = [_inputs(B, L + 1, seed=20 + l, d=D, Hq=HQ, Hkv=HKV) for l in range(2)]
     k_ring = torch.full((1, B, HKV, W, D), SENTINEL, dtype=torch.bfloat16, device="cuda")
     v_ring = k_ring.clone()
     k_glob = torch.full((1, B, HKV, S, D), SENTINEL, dtype=torch.bfloat16, device="cuda")

@@ -62,6 +62,8 @@ def test_tiny_config_all_rows(zg):
     (1, 150, 8, 1, 128, 128),   # GQA 8:1 (16 tokens per tile)
     (1, 150, 4, 2, 128, 128),   # GQA 2:1
     (1, 150, 2, 2, 64, 128),    # MHA (128 tokens per tile)
+    (2, 170, 32, 2, 128, 128),  # GQA 16:1 (8 tokens per tile)
+    (1, 140, 16, 1, 64, 100),   # GQA 16:1, d = 64
 ])
 def test_edge_shapes(zg, B, L, Hq, Hkv, d, window):
     inp = _synthetic(B, L, Hq, Hkv, d, seed=B * 1000 + L + d + window)
