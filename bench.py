@@ -13,7 +13,13 @@ steps.  `value` is the gated-SWA prefill throughput (tokens/s summed over all
 ranks, from CUDA events around that call); `parts` reports every call with its
 own roofline.  `e2e` repeats the SWA prefill through the same public API with
 the inputs in pinned host memory, the host->device copies and the device->host
-copy of the output inside the timed region.
+copy of the output inside the timed region.  Outside the step, `parts` also
+times the other workloads one by one: the tiny gated SWA prefill (latency, L2
+flushed), the B=4 L=4096 gated SWA prefill (L2 flushed), the global prefill at
+L=262144, the decode step over E4M3 caches, the cache writer, the whole gated
+layer and the backward pass.  `cpu_baseline` times the fp64 oracle on a slice of
+the 256K workload, on the whole tiny configuration and on one decode step of one
+sequence, with the host CPU model and thread count.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 Under torchrun (N > 1) every rank runs the same per-GPU work (replicas, no
@@ -224,6 +230,54 @@ def oracle_sample(rows: int, nthreads=None, seed_salt=0):
     return rows / dt, n, dt
 
 
+def cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def oracle_tiny(nthreads=None):
+    """The fp64 oracle on the whole tiny gated-SWA configuration (B=1, L=512, 4/1 heads, d=64)."""
+    import oracle
+
+    c = workloads.TINY_SWA
+    inp = workloads.prefill_inputs(c)
+    n = nthreads or oracle.default_threads()
+    t0 = time.perf_counter()
+    oracle.prefill_rows(inp["q"], inp["k"], inp["v"], inp["gate"], inp["pos"], inp["wq"], inp["wk"], window=c.window,
+                        rotary_dim=c.rotary_dim, theta=c.theta, eps=c.eps, rows=list(range(c.B * c.L)), nthreads=n)
+    dt = time.perf_counter() - t0
+    return c.tokens / dt, dt
+
+
+# bounded stand-in for the decode workload's per-sequence oracle time: the same 32-layer stack
+# at position 32767 (32768-slot global caches); the oracle's work grows linearly with the position
+DEC_SAMPLE = workloads.DecodeCase("hybrid_decode_B1_p32767_32L", 5, 1, 32, (5, 11, 17, 23, 29), 32, 8, 128,
+                                  32768, 128, 32767, 42, 1e6)
+
+
+def oracle_decode_seq(nthreads=None):
+    """Seconds for the fp64 oracle to run one decode step of one sequence of DEC_SAMPLE, and that time
+    extrapolated to position 262143 (global-layer work x 8)."""
+    import oracle
+
+    c = DEC_SAMPLE
+    tok = workloads.decode_token_inputs(c)
+    caches = workloads.decode_caches_cpu(c, batches=[0])
+    t0 = time.perf_counter()
+    oracle.decode_seq(tok["q"][:, 0], tok["k_new"][:, 0], tok["v_new"][:, 0], tok["gate"][:, 0], tok["wq"], tok["wk"],
+                      c.layer_flags(), caches["k_glob"][:, 0], caches["v_glob"][:, 0], caches["k_ring"][:, 0],
+                      caches["v_ring"][:, 0], p=c.pos, rotary_dim=c.rotary_dim, theta=c.theta, eps=c.eps,
+                      nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    return dt, dt * (DEC.pos + 1) / (c.pos + 1)
+
+
 def run_reference(args):
     ws, rank, _ = _dist()
     if rank != 0:
@@ -245,7 +299,8 @@ def run_reference(args):
         "warmup": args.warmup, "ms_per_step": 1e3 * statistics.median(dts), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": SWA.name, "global_batch": SWA.B, "seq_len": SWA.L, "parallelism": "none (host)"},
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": n, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": n, "cpu_model": cpu_model(), "kind": "oracle",
+                         "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -341,12 +396,27 @@ def run_gpu(args):
 
     sw_t, dc_t, gl_t = avg("swa_prefill"), avg("hybrid_decode"), avg("global_prefill")
     hbm = peaks["hbm_gbs"]
+    # a read-only stream (the decode step's access pattern) runs above the copy figure: measure what
+    # a library reduction reads per second from one 20 GiB cache tensor, to put beside the copy peak
+    rd_src = caches["k_glob"].view(-1)
+    rd = []
+    for i in range(4):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        torch.sum(rd_src, dtype=torch.float32)
+        b.record(stream)
+        torch.cuda.synchronize()
+        if i:
+            rd.append(a.elapsed_time(b) * 1e-3)
+    read_peak = rd_src.numel() * rd_src.element_size() / min(rd) / 1e9
     rl_swa = {"bound": "hbm", "achieved": swa_bytes(SWA) / sw_t / 1e9, "peak": hbm, "unit": "GB/s",
               "frac": swa_bytes(SWA) / sw_t / 1e9 / hbm, "traffic": _traffic("swa_prefill_kernel"),
               "algorithmic_bytes": swa_bytes(SWA)}
     rl_dec = {"bound": "hbm", "achieved": decode_bytes(DEC) / dc_t / 1e9, "peak": hbm, "unit": "GB/s",
               "frac": decode_bytes(DEC) / dc_t / 1e9 / hbm, "traffic": _traffic("decode_attn_kernel"),
-              "algorithmic_bytes": decode_bytes(DEC)}
+              "algorithmic_bytes": decode_bytes(DEC), "read_peak_live": read_peak,
+              "frac_of_read_peak": decode_bytes(DEC) / dc_t / 1e9 / read_peak}
     gf = global_flops(GLB)
     rl_glb = {"bound": "tensor", "achieved": gf / gl_t / 1e12, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
               "frac": gf / gl_t / 1e12 / peaks["bf16_tflops"],
@@ -388,9 +458,19 @@ def run_gpu(args):
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu:
         r, n, dt = oracle_sample(args.cpu_rows)
-        cpu = {"value": r, "unit": "tokens/s", "cores": n, "kind": "oracle",
+        tiny_r, tiny_dt = oracle_tiny(n)
+        dec_s, dec_s_full = oracle_decode_seq(n)
+        cpu = {"value": r, "unit": "tokens/s", "cores": n, "cpu_model": cpu_model(), "kind": "oracle",
                "sample": f"{args.cpu_rows} consecutive query rows x 32 heads of the gated-SWA 256K workload "
-                         f"(rows 131072.., fp64 C oracle, {dt:.1f} s); tokens/s = rows/s"}
+                         f"(rows 131072.., fp64 C oracle, {dt:.1f} s); tokens/s = rows/s",
+               "tiny_config": {"workload": workloads.TINY_SWA.name, "value": tiny_r, "unit": "tokens/s",
+                               "s": tiny_dt, "sample": "every row of the configuration"},
+               "decode_step_per_sequence": {"workload": DEC_SAMPLE.name, "s": dec_s,
+                                            "s_at_p262143_extrapolated": dec_s_full,
+                                            "s_for_B8_extrapolated": 8 * dec_s_full,
+                                            "sample": "one sequence, all 32 layers, at position 32767; the "
+                                                      "oracle's global-layer work grows linearly with the "
+                                                      "position, so x8 for p = 262143 (labelled extrapolated)"}}
 
     # ---- decode caches from a prefill (outside the step): the global 64K layer's k_hat / v
     kc = torch.empty((GLB.B, GLB.Hkv, GLB.L, GLB.d), dtype=torch.bfloat16, device=dev)
@@ -463,6 +543,73 @@ def run_gpu(args):
                         "algorithmic_flops": l_fl,
                         "note": "projection GEMM flops only; the attention inside is HBM-bound"}}
 
+    # ---- the other configurations of the workload set (outside the step), each on its own
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # twice the 126 MB L2
+
+    def time_part(fn, n, warm=3, flush_l2=False):
+        """median seconds of n launches on this stream (L2 overwritten before each when flush_l2)"""
+        for _ in range(warm):
+            fn()
+        evs = []
+        for _ in range(n):
+            if flush_l2:
+                flush.zero_()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            evs.append((a, b))
+        torch.cuda.synchronize()
+        st_, det_ = zg.device_status()
+        if st_ != 0:
+            raise RuntimeError(f"device status {st_} detail {det_:#x}")
+        return statistics.median(a.elapsed_time(b) for a, b in evs) * 1e-3
+
+    # config 1: the tiny gated SWA prefill (latency; L2 flushed before every launch)
+    T1 = workloads.TINY_SWA
+    tx = workloads.prefill_inputs_device(T1, dev)
+    t_out = torch.empty_like(tx["q"])
+    t1_t = time_part(lambda: zg.swa_prefill(tx["q"], tx["k"], tx["v"], tx["gate"], tx["pos"], tx["wq"], tx["wk"],
+                                            window=T1.window, rotary_dim=T1.rotary_dim, theta=T1.theta, eps=T1.eps,
+                                            out=t_out), 50, flush_l2=True)
+    tiny = {"workload": T1.name, "us": t1_t * 1e6, "tokens_per_s": T1.tokens / t1_t, "l2": "flushed before each launch",
+            "roofline": {"bound": "latency", "achieved": swa_bytes(T1) / t1_t / 1e9, "peak": hbm, "unit": "GB/s",
+                         "frac": swa_bytes(T1) / t1_t / 1e9 / hbm, "algorithmic_bytes": swa_bytes(T1),
+                         "note": "0.92 MB in one launch: launch and pipeline latency, not bandwidth"}}
+    del tx, t_out
+
+    # config 2: gated SWA prefill B=4, L=4096 (L2 flushed before every launch: 470 MB of traffic)
+    C2x = workloads.SWA_4K
+    x2 = workloads.prefill_inputs_device(C2x, dev)
+    o2 = torch.empty_like(x2["q"])
+    s4_t = time_part(lambda: zg.swa_prefill(x2["q"], x2["k"], x2["v"], x2["gate"], x2["pos"], x2["wq"], x2["wk"],
+                                            window=C2x.window, rotary_dim=C2x.rotary_dim, theta=C2x.theta,
+                                            eps=C2x.eps, out=o2), 20, flush_l2=True)
+    swa4k = {"workload": C2x.name, "us": s4_t * 1e6, "tokens_per_s": C2x.tokens / s4_t,
+             "l2": "flushed before each launch",
+             "roofline": {"bound": "hbm", "achieved": swa_bytes(C2x) / s4_t / 1e9, "peak": hbm, "unit": "GB/s",
+                          "frac": swa_bytes(C2x) / s4_t / 1e9 / hbm, "traffic": None,
+                          "algorithmic_bytes": swa_bytes(C2x)}}
+    del x2, o2
+
+    # config 4b: global prefill at L = 262144
+    G4b = workloads.GLOBAL_256K
+    gbx = workloads.prefill_inputs_device(G4b, dev)
+    gb_out = torch.empty_like(gbx["q"])
+    gb_ws = torch.empty(zg.global_prefill_workspace_bytes(G4b.B, G4b.L, G4b.Hkv, G4b.d), dtype=torch.uint8,
+                        device=dev)
+    g4_t = time_part(lambda: zg.global_prefill(gbx["q"], gbx["k"], gbx["v"], gbx["pos"], gbx["wq"], gbx["wk"],
+                                               rotary_dim=G4b.rotary_dim, theta=G4b.theta, eps=G4b.eps, out=gb_out,
+                                               workspace=gb_ws), 2, warm=1)
+    gf4 = global_flops(G4b)
+    glob256 = {"workload": G4b.name, "ms": g4_t * 1e3, "tokens_per_s": G4b.tokens / g4_t,
+               "roofline": {"bound": "tensor", "achieved": gf4 / g4_t / 1e12, "peak": peaks["bf16_tflops"],
+                            "unit": "TFLOP/s", "frac": gf4 / g4_t / 1e12 / peaks["bf16_tflops"],
+                            "frac_of_sustained": gf4 / g4_t / 1e12 / peaks["bf16_tflops_sustained"],
+                            "traffic": None, "algorithmic_flops": gf4}}
+    del gbx, gb_out, gb_ws, flush
+
     # ---- the decode step over E4M3 caches (outside the step): the same workload, caches stored
     # as e4m3(k_hat * 1) and e4m3(v * 8)
     f8 = {k: workloads.to_e4m3(v, 1.0 if k.startswith("k") else 8.0) for k, v in caches.items()}
@@ -491,7 +638,7 @@ def run_gpu(args):
     dec_fp8 = {"workload": f"{DEC.name} with E4M3 caches", "us_per_step": f8_t * 1e6,
                "roofline": {"bound": "hbm", "achieved": f8_by / f8_t / 1e9, "peak": hbm, "unit": "GB/s",
                             "frac": f8_by / f8_t / 1e9 / hbm, "traffic": _traffic("decode_attn_kernel_fp8"),
-                            "algorithmic_bytes": f8_by}}
+                            "algorithmic_bytes": f8_by, "frac_of_read_peak": f8_by / f8_t / 1e9 / read_peak}}
     del f8
 
     # ---- backward of the gated SWA prefill (outside the step): the 4K training shape
@@ -549,6 +696,9 @@ def run_gpu(args):
             "kv_cache_write": kvc,
             "attention_backward": bwd,
             "hybrid_decode_fp8": dec_fp8,
+            "tiny_swa_prefill": tiny,
+            "swa_prefill_4k": swa4k,
+            "global_prefill_256k": glob256,
             "swa_prefill": {"workload": SWA.name, "ms": sw_t * 1e3, "tokens_per_s": SWA.tokens / sw_t,
                             "roofline": rl_swa},
             "hybrid_decode": {"workload": DEC.name, "us_per_step": dc_t * 1e6, "roofline": rl_dec},
