@@ -472,6 +472,27 @@ def run_gpu(args):
                                                       "oracle's global-layer work grows linearly with the "
                                                       "position, so x8 for p = 262143 (labelled extrapolated)"}}
 
+    if args.step_only:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"{SWA.name} + {DEC.name} + {GLB.name}", "global_batch": SWA.B * ws,
+                       "seq_len": SWA.L, "parallelism": "replicas" if ws > 1 else "single GPU",
+                       "l2": "no flush: every input is larger than L2"},
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": args.steps * sum(n for _, _, n in parts), "clocks": clocks,
+            "parts": {"swa_prefill": {"workload": SWA.name, "ms": sw_t * 1e3, "roofline": rl_swa},
+                      "hybrid_decode": {"workload": DEC.name, "us_per_step": dc_t * 1e6, "roofline": rl_dec},
+                      "global_prefill": {"workload": GLB.name, "ms": gl_t * 1e3, "roofline": rl_glb}},
+            "note": "--step-only: parts outside the step not run",
+        }
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        if ws > 1:
+            torch.distributed.destroy_process_group()
+        return 0
+
     # ---- decode caches from a prefill (outside the step): the global 64K layer's k_hat / v
     kc = torch.empty((GLB.B, GLB.Hkv, GLB.L, GLB.d), dtype=torch.bfloat16, device=dev)
     vc = torch.empty_like(kc)
@@ -799,6 +820,8 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=4096)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--step-only", action="store_true",
+                    help="time the step alone: skip the parts measured outside it (for ncu launch lists)")
     ap.add_argument("--profile-case", choices=["swa", "global", "decode", "kvcache", "backward", "decode8"], default=None,
                     help="run only a small case of one kernel (for ncu captures)")
     args = ap.parse_args()
