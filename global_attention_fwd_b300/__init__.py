@@ -18,12 +18,13 @@ import os
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libzgattn.so")
+# ZG_LIBRARY=debug selects libzgattn_debug.so, the same kernels with device-side index checks
+LIB_PATH = os.path.join(_HERE, "libzgattn_debug.so" if os.environ.get("ZG_LIBRARY") == "debug" else "libzgattn.so")
 
 STATUS = {
     0: "ZG_OK", -1: "ZG_ERR_NULL", -2: "ZG_ERR_ALIGN", -3: "ZG_ERR_SHAPE", -4: "ZG_ERR_UNSUPPORTED",
     -5: "ZG_ERR_POSITION", -6: "ZG_ERR_WORKSPACE", -7: "ZG_ERR_CUDA", -8: "ZG_ERR_DEVICE_TIMEOUT",
-    -9: "ZG_ERR_UNIMPLEMENTED",
+    -9: "ZG_ERR_UNIMPLEMENTED", -10: "ZG_ERR_DEVICE_INDEX",
 }
 EXPORTS = ("zg_swa_prefill", "zg_global_prefill_workspace_bytes", "zg_global_prefill",
            "zg_swa_prefill_with_cache", "zg_global_prefill_with_cache", "zg_kv_cache_write",
@@ -31,7 +32,8 @@ EXPORTS = ("zg_swa_prefill", "zg_global_prefill_workspace_bytes", "zg_global_pre
            "zg_attention_backward_workspace_bytes", "zg_attention_backward",
            "zg_hybrid_decode_workspace_bytes", "zg_hybrid_decode", "zg_hybrid_decode_noalloc",
            "zg_hybrid_decode_fp8", "zg_kv_cache_write_fp8",
-           "zg_device_status", "zg_selftest_bounded_wait", "zg_status_string")
+           "zg_device_status", "zg_selftest_bounded_wait", "zg_selftest_index_check", "zg_debug_build",
+           "zg_status_string")
 
 
 class ZgError(RuntimeError):
@@ -78,6 +80,10 @@ def _load() -> ctypes.CDLL:
     lib.zg_device_status.restype = I
     lib.zg_selftest_bounded_wait.argtypes = [U64, P]
     lib.zg_selftest_bounded_wait.restype = I
+    lib.zg_selftest_index_check.argtypes = [P]
+    lib.zg_selftest_index_check.restype = I
+    lib.zg_debug_build.argtypes = []
+    lib.zg_debug_build.restype = I
     lib.zg_status_string.argtypes = [I]
     lib.zg_status_string.restype = ctypes.c_char_p
     return lib
@@ -387,3 +393,11 @@ def device_status():
 
 def selftest_bounded_wait(limit_ns: int, stream=None):
     _raise(_lib.zg_selftest_bounded_wait(int(limit_ns), _stream(stream)), "zg_selftest_bounded_wait")
+
+
+def selftest_index_check(stream=None):
+    _raise(_lib.zg_selftest_index_check(_stream(stream)), "zg_selftest_index_check")
+
+
+def debug_build() -> bool:
+    return bool(_lib.zg_debug_build())

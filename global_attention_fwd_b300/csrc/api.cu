@@ -617,7 +617,23 @@ zg_status zg_device_status(uint32_t* detail) {
     if (w && cudaMemcpyToSymbol(g_err_word, &zero, sizeof(zero)) != cudaSuccess) return ZG_ERR_CUDA;
     if (detail) *detail = w;
     if (!w) return ZG_OK;
-    return (w & 0xFFu) == kErrPosition ? ZG_ERR_POSITION : ZG_ERR_DEVICE_TIMEOUT;
+    if ((w & 0xFFu) == kErrPosition) return ZG_ERR_POSITION;
+    if ((w & 0xFFu) == kErrIndex) return ZG_ERR_DEVICE_INDEX;
+    return ZG_ERR_DEVICE_TIMEOUT;
+}
+
+zg_status zg_selftest_index_check(zg_stream stream) {
+    DevCtl ctl;
+    if (!dev_ctl(ctl)) return ZG_ERR_CUDA;
+    return launch_index_selftest(ctl, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? ZG_OK : ZG_ERR_CUDA;
+}
+
+int zg_debug_build(void) {
+#ifdef ZG_DEBUG
+    return 1;
+#else
+    return 0;
+#endif
 }
 
 zg_status zg_selftest_bounded_wait(uint64_t limit_ns, zg_stream stream) {
@@ -639,6 +655,7 @@ const char* zg_status_string(int s) {
         case ZG_ERR_CUDA: return "CUDA runtime error";
         case ZG_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
         case ZG_ERR_UNIMPLEMENTED: return "not implemented";
+        case ZG_ERR_DEVICE_INDEX: return "device-side index out of range (debug build)";
         default: return "unknown status";
     }
 }

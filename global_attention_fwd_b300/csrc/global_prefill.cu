@@ -59,6 +59,7 @@ __global__ void __launch_bounds__(256) khat_kernel(const __grid_constant__ Prefi
     const long long nrows = static_cast<long long>(p.B) * p.L * p.Hkv;
     if (row >= nrows) return;
     const long long tok = row / p.Hkv;  // b * L + j
+    if (!idx_ok(p.ctl, tok, static_cast<long long>(p.B) * p.L, 82)) return;
     const int pos = __ldg(p.pos + tok);
     norm_rope_warp_d<D>(p.k_raw + row * D, p.wk, p.eps, pos, p.rope, 1.0f, buf[warp]);
     for (int e = 2 * lane; e < D; e += 64)
@@ -222,7 +223,8 @@ __global__ void __launch_bounds__(kThreads, 1) global_attn_kernel(const __grid_c
         const int iq = i0 + t * T + tt;
         bool ok = __all_sync(0xffffffffu, mbar_wait(q_full, 0, p.ctl, 60));
         if (ok) {
-            const int pos = iq < p.L ? __ldg(p.pos + static_cast<long long>(b) * p.L + iq) : 0;
+            const long long pi = static_cast<long long>(b) * p.L + iq;
+            const int pos = iq < p.L && idx_ok(p.ctl, pi, static_cast<long long>(p.B) * p.L, 83) ? __ldg(p.pos + pi) : 0;
             qk_norm_rope_row<D>(qt, CH, row, p.wq, p.eps, pos, p.rope);
             fence_async_smem();
         }

@@ -169,8 +169,12 @@ __global__ void __launch_bounds__(NTHR, 2) decode_attn_kernel(const __grid_const
     g = static_cast<int>(slice % p.Hkv);
     b = static_cast<int>((slice / p.Hkv) % p.B);
     lidx = static_cast<int>(slice / (static_cast<long long>(p.Hkv) * p.B));
-    const int pos = __ldg(p.pos + b);
+    const int pos = idx_ok(p.ctl, b, p.B, 70) ? __ldg(p.pos + b) : -1;
     const bool pos_ok = pos >= 0 && static_cast<long long>(pos) < p.S;
+    // the new token's cache row (debug builds check it before the slot is written)
+    const long long slot_row = is_glob ? slice * p.S + pos : slice * p.W + (pos_ok ? pos % p.W : 0);
+    const long long slot_rows = is_glob ? static_cast<long long>(p.NG) * p.B * p.Hkv * p.S
+                                        : static_cast<long long>(p.NS) * p.B * p.Hkv * p.W;
     // keys streamed from the cache: [k0, k0 + nk) of the slice; whether this CTA owns p
     long long k0 = 0;
     int nk = 0;
@@ -230,7 +234,9 @@ __global__ void __launch_bounds__(NTHR, 2) decode_attn_kernel(const __grid_const
             tma_prefetch_desc(mv);
             for (int st = 0; st < first; ++st) issue_stage(st);  // the ring starts empty: no waits
         }
-        if (owner && *sflag) {
+        if (owner && *sflag && idx_ok(p.ctl, slot_row, slot_rows, 71) &&
+            idx_ok(p.ctl, (static_cast<long long>(layer) * p.B + b) * p.Hkv + g,
+                   static_cast<long long>(p.NL) * p.B * p.Hkv, 72)) {
             const size_t tok = static_cast<size_t>(layer) * p.B + b;
             norm_rope_warp_d<D>(p.k_new + (tok * p.Hkv + g) * D, p.wk + static_cast<size_t>(layer) * D, p.eps, pos,
                                 p.rope, 1.0f, kh);
@@ -294,7 +300,9 @@ __global__ void __launch_bounds__(NTHR, 2) decode_attn_kernel(const __grid_const
             const size_t tok = static_cast<size_t>(layer) * p.B + b;
             const float qscale = FP8 ? p.scale_log2 / p.k_scale : p.scale_log2;  // scores in log2 units
             for (int h = warp; h < G; h += NCW)
-                norm_rope_warp_d<D>(p.q + (tok * p.Hq + static_cast<size_t>(g) * G + h) * D,
+                if (idx_ok(p.ctl, static_cast<long long>(tok * p.Hq + static_cast<size_t>(g) * G + h),
+                           static_cast<long long>(p.NL) * p.B * p.Hq, 73))
+                    norm_rope_warp_d<D>(p.q + (tok * p.Hq + static_cast<size_t>(g) * G + h) * D,
                                     p.wq + static_cast<size_t>(layer) * D, p.eps, pos, p.rope, qscale, qh + h * D);
         }
         asm volatile("bar.sync 1, %0;" ::"r"(NCW * 32) : "memory");
@@ -547,6 +555,8 @@ __global__ void __launch_bounds__(NTHR, 2) decode_attn_kernel(const __grid_const
         const int hq = g * G + h;
         if (is_glob) {
             const size_t row = ((static_cast<size_t>(lidx) * p.B + b) * p.Hq + hq) * p.nsplit + split;
+            if (!idx_ok(p.ctl, static_cast<long long>(row), static_cast<long long>(p.NG) * p.B * p.Hq * p.nsplit, 74))
+                continue;
             p.ws_o[row * D + e] = (all_ok ? ot : 0.f);
             if (e == 0) {
                 p.ws_ml[row * 2 + 0] = all_ok ? mt : -INFINITY;
@@ -554,6 +564,7 @@ __global__ void __launch_bounds__(NTHR, 2) decode_attn_kernel(const __grid_const
             }
         } else {
             const size_t orow = (static_cast<size_t>(layer) * p.B + b) * p.Hq + hq;
+            if (!idx_ok(p.ctl, static_cast<long long>(orow), static_cast<long long>(p.NL) * p.B * p.Hq, 75)) continue;
             float r = 0.f;
             if (all_ok && lt > 0.f) r = ot / lt * sigmoid_f32(__bfloat162float(p.gate[orow * D + e]));
             p.out[orow * D + e] = __float2bfloat16_rn(r);
@@ -583,6 +594,7 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const __grid_consta
         ot += os[static_cast<size_t>(s) * D + e] * c;
     }
     const size_t orow = (static_cast<size_t>(layer) * p.B + b) * p.Hq + hq;
+    if (!idx_ok(p.ctl, static_cast<long long>(orow), static_cast<long long>(p.NL) * p.B * p.Hq, 76)) return;
     p.out[orow * D + e] = __float2bfloat16_rn(lt > 0.f ? ot / lt : 0.f);
 }
 

@@ -32,6 +32,7 @@ __global__ void __launch_bounds__(256) kv_cache_kernel(const __grid_constant__ C
     const int b = static_cast<int>(bt / n_keep);
     const int i = p.i0 + static_cast<int>(bt % n_keep);
     const long long src = (static_cast<long long>(b) * p.L + i) * p.Hkv + g;  // row of k / v
+    if (!idx_ok(p.ctl, src, static_cast<long long>(p.B) * p.L * p.Hkv, 80)) return;
     const int pos = __ldg(p.pos + static_cast<long long>(b) * p.L + i);
     long long slot;
     if (p.ring) {
@@ -44,6 +45,7 @@ __global__ void __launch_bounds__(256) kv_cache_kernel(const __grid_constant__ C
         return;
     }
     const long long dst = ((static_cast<long long>(b) * p.Hkv + g) * p.S + slot) * D;
+    if (!idx_ok(p.ctl, dst / D, static_cast<long long>(p.B) * p.Hkv * p.S, 81)) return;
     // the same per-warp arithmetic as the decode step's own cache write (bit-identical keys)
     norm_rope_warp_d<D>(p.k + src * D, p.wk, p.eps, pos, p.rope, 1.0f, buf[warp]);
     for (int e = 2 * lane; e < D; e += 64) {

@@ -396,7 +396,8 @@ __global__ void __launch_bounds__(kThreads, 1) swa2_kernel(const __grid_constant
         // position of this row's token, fetched one tile ahead
         auto qpos = [&](const TileIdx& t) {
             const int tok = t.lt * C::T + row / G;
-            return tok < p.L ? __ldg(p.pos + static_cast<long long>(t.b) * p.L + tok) : 0;
+            const long long pi = static_cast<long long>(t.b) * p.L + tok;
+            return tok < p.L && idx_ok(p.ctl, pi, static_cast<long long>(p.B) * p.L, 84) ? __ldg(p.pos + pi) : 0;
         };
         int pos_next = n_tiles > 0 ? qpos(ti) : 0;
         for (int it = 0; it < n_tiles; ++it, next_tile(ti, p.n_ltiles, p.Hkv)) {
@@ -433,7 +434,10 @@ __global__ void __launch_bounds__(kThreads, 1) swa2_kernel(const __grid_constant
             for (int q = 0; q < (C::T + 31) / 32; ++q) {
                 const int r = min(q * 32 + (kt >> 1), C::T - 1);
                 const int tok = tile_l * C::T + r;
-                posr[q] = (tok >= 0 && tok < p.L) ? __ldg(p.pos + static_cast<long long>(ti.b) * p.L + tok) : 0;
+                const long long pi = static_cast<long long>(ti.b) * p.L + tok;
+                posr[q] = (tok >= 0 && tok < p.L && idx_ok(p.ctl, pi, static_cast<long long>(p.B) * p.L, 85))
+                              ? __ldg(p.pos + pi)
+                              : 0;
             }
             if (!__all_sync(0xffffffffu, mbar_wait(&k_full[s], (cc / C::R) & 1, p.ctl, 42))) return false;
 #pragma unroll

@@ -121,13 +121,15 @@ __global__ void __launch_bounds__(128, 2) swa_prefill_kernel(const __grid_consta
     const int tt = t / G;  // token of tile row t
     const int iq = i0 + tt;
     const int64_t seq = static_cast<int64_t>(b) * p.L;
-    const int pos_q = iq < p.L ? __ldg(p.pos + seq + iq) : 0;
+    const int pos_q = iq < p.L && idx_ok(p.ctl, seq + iq, static_cast<long long>(p.B) * p.L, 86) ? __ldg(p.pos + seq + iq) : 0;
     int pos_k[2];
 #pragma unroll
     for (int s = 0; s < 2; ++s) {
         const int kr = t + s * 128;
         const int j = j0 + kr;
-        pos_k[s] = (kr < C::NK && j >= 0 && j < p.L) ? __ldg(p.pos + seq + j) : 0;
+        pos_k[s] = (kr < C::NK && j >= 0 && j < p.L && idx_ok(p.ctl, seq + j, static_cast<long long>(p.B) * p.L, 87))
+                       ? __ldg(p.pos + seq + j)
+                       : 0;
     }
 
     // ---- 2. QK-norm + RoPE in place

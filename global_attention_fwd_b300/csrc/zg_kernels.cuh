@@ -186,5 +186,7 @@ bool layer_gemm(const void* X, const void* W, void* Y, long long M, long long N,
 
 // bounded-wait self test: waits on a barrier nothing arrives on
 cudaError_t launch_wait_selftest(DevCtl ctl, cudaStream_t s);
+// index-check self test: records ZG_ERR_DEVICE_INDEX in the debug build, nothing in the normal one
+cudaError_t launch_index_selftest(DevCtl ctl, cudaStream_t s);
 
 }  // namespace zg

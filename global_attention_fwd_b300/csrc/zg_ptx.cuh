@@ -14,7 +14,7 @@ namespace zg {
 // ----------------------------------------------------------- device errors
 // Error word: 0 = fine; otherwise (site << 8) | code.  Written once per launch
 // by the first failing thread (atomicCAS), read and cleared by the host.
-enum DeviceErr : uint32_t { kErrTimeout = 1, kErrAlign = 2, kErrTmem = 3, kErrPosition = 4 };
+enum DeviceErr : uint32_t { kErrTimeout = 1, kErrAlign = 2, kErrTmem = 3, kErrPosition = 4, kErrIndex = 5 };
 
 struct DevCtl {
     uint32_t* err_word;      // device pointer to the error word
@@ -24,6 +24,21 @@ struct DevCtl {
 __device__ __forceinline__ void report(const DevCtl& ctl, uint32_t site, uint32_t code) {
     atomicCAS(ctl.err_word, 0u, (site << 8) | code);
 }
+
+// Index checks of the debug build (compiled with ZG_DEBUG): every plain global-memory access of
+// the kernels (the TMA copies are bounds-checked by the hardware) first asks idx_ok(); an index
+// outside [0, n) is recorded as (site << 8) | kErrIndex and the access is skipped, so the
+// context survives and the host reads the record through zg_device_status().  In the normal
+// build idx_ok() is the constant true and costs nothing.
+#ifdef ZG_DEBUG
+__device__ __forceinline__ bool idx_ok(const DevCtl& ctl, long long i, long long n, uint32_t site) {
+    if (i >= 0 && i < n) return true;
+    report(ctl, site, kErrIndex);
+    return false;
+}
+#else
+__device__ __forceinline__ constexpr bool idx_ok(const DevCtl&, long long, long long, uint32_t) { return true; }
+#endif
 
 __device__ __forceinline__ unsigned long long globaltimer_ns() {
     unsigned long long t;

@@ -43,6 +43,11 @@
  *     word; zg_device_status() synchronises the device and returns
  *     ZG_ERR_DEVICE_TIMEOUT (or ZG_ERR_POSITION for a cache position without a
  *     slot, or ZG_OK) and clears the word.
+ *   - Debug build (libzgattn_debug.so, the same sources compiled with ZG_DEBUG):
+ *     before every plain global-memory access (TMA copies are bounds-checked by
+ *     the hardware) the kernels check the index against the tensor's extent; an
+ *     index out of range is skipped and recorded, and zg_device_status() then
+ *     returns ZG_ERR_DEVICE_INDEX.  No trap, no fault: the context stays usable.
  *   - The library allocates no device memory in these calls; scratch memory
  *     comes from a caller-provided workspace (global prefill, decode).
  */
@@ -69,7 +74,8 @@ typedef enum {
     ZG_ERR_WORKSPACE = -6,      /* workspace missing or too small */
     ZG_ERR_CUDA = -7,           /* a CUDA runtime call failed */
     ZG_ERR_DEVICE_TIMEOUT = -8, /* a device-side wait gave up */
-    ZG_ERR_UNIMPLEMENTED = -9
+    ZG_ERR_UNIMPLEMENTED = -9,
+    ZG_ERR_DEVICE_INDEX = -10   /* debug build only: a kernel met a global-memory index out of range */
 } zg_status;
 
 /*
@@ -329,6 +335,15 @@ zg_status zg_device_status(uint32_t *detail);
  * completes, with the given limit in ns; used to test the timeout path.  The
  * caller then reads the outcome with zg_device_status(). */
 zg_status zg_selftest_bounded_wait(uint64_t limit_ns, zg_stream stream);
+
+/* Launch a kernel that asks the debug build's index check about an index one past
+ * the end of a range, while the access it guards stays in range.  Debug build:
+ * zg_device_status() afterwards returns ZG_ERR_DEVICE_INDEX (site 98); normal
+ * build: ZG_OK.  Used to test the debug build's error path without a fault. */
+zg_status zg_selftest_index_check(zg_stream stream);
+
+/* 1 for the debug build (libzgattn_debug.so, compiled with ZG_DEBUG), else 0. */
+int zg_debug_build(void);
 
 /* Static text for a status code. */
 const char *zg_status_string(int status);

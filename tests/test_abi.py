@@ -36,6 +36,17 @@ def test_library_exports_every_declared_symbol(zg):
     assert set(_declared()) == set(zg.EXPORTS)
 
 
+def test_debug_library_exports_the_same_symbols(zg):
+    path = os.path.join(os.path.dirname(zg.LIB_PATH), "libzgattn_debug.so")
+    if not os.path.exists(path):
+        pytest.skip("debug library not built")
+    dbg = ctypes.CDLL(path)
+    missing = [n for n in _declared() if not hasattr(dbg, n)]
+    assert not missing, missing
+    assert dbg.zg_debug_build() == 1
+    assert zg.lib.zg_debug_build() == 0
+
+
 A = 1 << 20  # a fake, 16-byte aligned, non-null address (never dereferenced: validation fails first)
 
 
@@ -90,7 +101,7 @@ def test_global_rejects_bad_arguments_before_launch(zg):
 
 
 def test_status_strings(zg):
-    for s in range(-9, 1):
+    for s in range(-10, 1):
         assert zg.lib.zg_status_string(s)
     assert zg.lib.zg_status_string(-8) == b"device-side wait timed out"
 
