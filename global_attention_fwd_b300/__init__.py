@@ -28,7 +28,7 @@ STATUS = {
 }
 EXPORTS = ("zg_swa_prefill", "zg_global_prefill_workspace_bytes", "zg_global_prefill",
            "zg_swa_prefill_with_cache", "zg_global_prefill_with_cache", "zg_kv_cache_write",
-           "zg_gated_swa_layer_workspace_bytes", "zg_gated_swa_layer",
+           "zg_gated_swa_layer_workspace_bytes", "zg_gated_swa_layer", "zg_linear",
            "zg_attention_backward_workspace_bytes", "zg_attention_backward",
            "zg_hybrid_decode_workspace_bytes", "zg_hybrid_decode", "zg_hybrid_decode_noalloc",
            "zg_hybrid_decode_fp8", "zg_kv_cache_write_fp8",
@@ -64,6 +64,8 @@ def _load() -> ctypes.CDLL:
     lib.zg_gated_swa_layer_workspace_bytes.restype = SZ
     lib.zg_gated_swa_layer.argtypes = [P] * 10 + [I] * 8 + [D, F, P, SZ, P]
     lib.zg_gated_swa_layer.restype = I
+    lib.zg_linear.argtypes = [P, P, P, I64, I, I, P]
+    lib.zg_linear.restype = I
     lib.zg_attention_backward_workspace_bytes.argtypes = [I] * 5
     lib.zg_attention_backward_workspace_bytes.restype = SZ
     lib.zg_attention_backward.argtypes = [P] * 12 + [I] * 7 + [D, F, P, SZ, P]
@@ -242,6 +244,21 @@ def kv_cache_write_fp8(k, v, pos, wk, k_cache, v_cache, *, ring, k_scale=1.0, v_
                                     d, int(k_cache.shape[2]), 1 if ring else 0, int(rotary_dim), float(theta),
                                     float(eps), float(k_scale), float(v_scale), _stream(stream))
     _raise(st, "zg_kv_cache_write_fp8")
+
+
+def linear(x, w, *, out=None, stream=None):
+    """y = x @ w on the library's tensor-core GEMM: x [..., K], w [K, N] bf16 -> y [..., N] bf16."""
+    _check(x, "x", torch.bfloat16)
+    _check(w, "w", torch.bfloat16, 2)
+    K, N = w.shape
+    if x.shape[-1] != K:
+        raise ValueError(f"x has {x.shape[-1]} columns, w has {K} rows")
+    M = x.numel() // K
+    if out is None:
+        out = torch.empty(*x.shape[:-1], N, dtype=torch.bfloat16, device=x.device)
+    _check(out, "out", torch.bfloat16)
+    _raise(_lib.zg_linear(_ptr(x), _ptr(w), _ptr(out), M, N, K, _stream(stream)), "zg_linear")
+    return out
 
 
 def gated_swa_layer_workspace_bytes(B, L, Hq, Hkv, d) -> int:

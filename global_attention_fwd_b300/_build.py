@@ -16,11 +16,11 @@ LIB = os.path.join(HERE, "libzgattn.so")
 LIB_DEBUG = os.path.join(HERE, "libzgattn_debug.so")
 OBJ_DIR = os.path.join(HERE, "..", "_build")
 SOURCES = ["api.cu", "swa_prefill.cu", "swa2_prefill.cu", "global_prefill.cu", "hybrid_decode.cu", "selftest.cu",
-           "noalloc.cu", "kv_cache.cu", "layer.cu", "attn_backward.cu", "attn_backward_tc.cu"]
+           "noalloc.cu", "kv_cache.cu", "attn_backward.cu", "attn_backward_tc.cu", "gemm.cu"]
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr"]
-LDFLAGS = ["-shared", "-cudart", "shared", "-Xlinker", "-rpath,/usr/local/cuda/lib64", "-lcublasLt"]
+LDFLAGS = ["-shared", "-cudart", "shared", "-Xlinker", "-rpath,/usr/local/cuda/lib64"]
 
 
 def _stale(lib: str) -> bool:

@@ -343,10 +343,58 @@ zg_status zg_global_prefill_with_cache(const zg_bf16* q, const zg_bf16* k, const
     return write_cache(k, v, pos, wk, k_cache, v_cache, B, L, Hkv, d, S_max, false, rotary_dim, theta, eps, stream);
 }
 
-// ---------------------------------------------------------------- whole gated SWA layer
+// ---------------------------------------------------------------- projections and the whole gated SWA layer
 namespace {
+// 2-D bf16 tensor map over a row-major [outer][inner] matrix, {64, box_outer} box, 128-byte swizzle
+bool make_map_2d(CUtensorMap* m, const void* base, long long inner, long long outer, int box_outer) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+    cuuint64_t strides[1] = {(cuuint64_t)inner * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)box_outer};
+    cuuint32_t es[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct Proj {
+    const void* w;  // W [K, n]
+    void* y;        // Y [M, n]
+    int n, mode;
+    const float* norm_w;
+};
+// Y_i = epilogue_i(X W_i) for up to four projections of X [M, K] in one launch
+zg_status run_projections(const void* x, long long M, int K, const Proj* pr, int nb, int head_dim,
+                          const int32_t* pos, const RopeConsts* rope, float eps, cudaStream_t s) {
+    GemmParams g;
+    std::memset(&g, 0, sizeof(g));
+    if (!dev_ctl(g.ctl)) return ZG_ERR_CUDA;
+    if (!make_map_2d(&g.tm_a, x, K, M, gemm_tile_m())) return ZG_ERR_CUDA;
+    g.nb = nb;
+    g.M = static_cast<int>(M);
+    g.K = K;
+    g.tiles_m = static_cast<int>((M + gemm_tile_m() - 1) / gemm_tile_m());
+    g.head_dim = head_dim;
+    g.pos = pos;
+    g.eps = eps;
+    if (rope) g.rope = *rope;
+    long long tn = 0;
+    for (int i = 0; i < nb; ++i) {
+        if (!make_map_2d(&g.tm_b[i], pr[i].w, pr[i].n, K, 64)) return ZG_ERR_CUDA;
+        g.y[i] = pr[i].y;
+        g.w[i] = pr[i].norm_w;
+        g.n[i] = pr[i].n;
+        g.mode[i] = pr[i].mode;
+        g.tiles_n[i] = (pr[i].n + gemm_tile_n() - 1) / gemm_tile_n();
+        tn += g.tiles_n[i];
+    }
+    g.tiles = tn * g.tiles_m;
+    return launch_gemm(g, s) == cudaSuccess ? ZG_OK : ZG_ERR_CUDA;
+}
+
 struct LayerWs {
-    size_t q, k, v, g, a, lt, total;
+    size_t q, k, v, g, a, total;
 };
 LayerWs layer_ws(long long B, long long L, long long Hq, long long Hkv, long long d) {
     auto up = [](size_t x) { return (x + 255) / 256 * 256; };
@@ -357,11 +405,20 @@ LayerWs layer_ws(long long B, long long L, long long Hq, long long Hkv, long lon
     w.v = w.k + up(tk);
     w.g = w.v + up(tk);
     w.a = w.g + up(tq);
-    w.lt = w.a + up(tq);
-    w.total = w.lt + layer_gemm_workspace_bytes();
+    w.total = w.a + up(tq);
     return w;
 }
 }  // namespace
+
+zg_status zg_linear(const zg_bf16* x, const zg_bf16* w, zg_bf16* y, int64_t M, int N, int K, zg_stream stream) {
+    if (!x || !w || !y) return ZG_ERR_NULL;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(y)) return ZG_ERR_ALIGN;
+    if (M < 0 || N <= 0 || K <= 0 || N % 8 || K % 8) return ZG_ERR_SHAPE;
+    if (M >= (1ll << 31)) return ZG_ERR_UNSUPPORTED;
+    if (M == 0) return ZG_OK;
+    const Proj pr{w, y, N, 0, nullptr};
+    return run_projections(x, M, K, &pr, 1, 0, nullptr, nullptr, 0.f, reinterpret_cast<cudaStream_t>(stream));
+}
 
 size_t zg_gated_swa_layer_workspace_bytes(int B, int L, int Hq, int Hkv, int d) {
     if (B <= 0 || L <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0) return 0;
@@ -385,27 +442,55 @@ zg_status zg_gated_swa_layer(const zg_bf16* h, const zg_bf16* w_q, const zg_bf16
     if (st != ZG_OK) return st;
     if (window < 1) return ZG_ERR_SHAPE;
     const int G = Hq / Hkv;
-    if ((d != 64 && d != 128) || (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) || window > 128 || Hkv > 65535)
+    if ((d != 64 && d != 128) || (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) || window > 128 ||
+        Hkv > 65535 || rotary_dim > 64)  // the fused epilogue rotates inside a head's first 64 columns
         return ZG_ERR_UNSUPPORTED;
     if (B == 0 || L == 0) return ZG_OK;
+    const long long M = static_cast<long long>(B) * L;
+    if (M >= (1ll << 31)) return ZG_ERR_UNSUPPORTED;
     const LayerWs w = layer_ws(B, L, Hq, Hkv, d);
     if (!workspace || workspace_bytes < w.total || !aligned16(workspace)) return ZG_ERR_WORKSPACE;
     uint8_t* base = static_cast<uint8_t*>(workspace);
-    zg_bf16 *q = reinterpret_cast<zg_bf16*>(base + w.q), *k = reinterpret_cast<zg_bf16*>(base + w.k),
-            *v = reinterpret_cast<zg_bf16*>(base + w.v), *g = reinterpret_cast<zg_bf16*>(base + w.g),
-            *a = reinterpret_cast<zg_bf16*>(base + w.a);
-    void* lt = base + w.lt;
-    const size_t lt_bytes = layer_gemm_workspace_bytes();
+    void *qh = base + w.q, *kh = base + w.k, *v = base + w.v, *sg = base + w.g, *a = base + w.a;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const long long M = static_cast<long long>(B) * L;
-    if (!layer_gemm(h, w_q, q, M, static_cast<long long>(Hq) * d, hidden, lt, lt_bytes, s) ||
-        !layer_gemm(h, w_k, k, M, static_cast<long long>(Hkv) * d, hidden, lt, lt_bytes, s) ||
-        !layer_gemm(h, w_v, v, M, static_cast<long long>(Hkv) * d, hidden, lt, lt_bytes, s) ||
-        !layer_gemm(h, w_g, g, M, static_cast<long long>(Hq) * d, hidden, lt, lt_bytes, s))
-        return ZG_ERR_CUDA;
-    st = zg_swa_prefill(q, k, v, g, pos, wq, wk, a, B, L, Hq, Hkv, d, window, rotary_dim, theta, eps, stream);
+    RopeConsts rc;
+    if (!rope_consts(rc, rotary_dim, theta)) return ZG_ERR_SHAPE;
+    // 1. the four input projections in one launch, h read once: q_hat, k_hat (fp16, RMSNorm and RoPE
+    //    from the fp32 accumulator), v (bf16), sigmoid(g) (bf16)
+    const Proj in[4] = {{w_q, qh, Hq * d, 1, wq}, {w_k, kh, Hkv * d, 1, wk}, {w_v, v, Hkv * d, 0, nullptr},
+                        {w_g, sg, Hq * d, 2, nullptr}};
+    st = run_projections(h, M, hidden, in, 4, d, pos, &rc, eps, s);
     if (st != ZG_OK) return st;
-    return layer_gemm(a, w_o, y, M, hidden, static_cast<long long>(Hq) * d, lt, lt_bytes, s) ? ZG_OK : ZG_ERR_CUDA;
+    // 2. the windowed attention on the pre-normalised inputs (no Q / K transform, no sigmoid)
+    const int T = 128 / G;
+    const long long n_lt = (L + T - 1) / T;
+    if (n_lt * Hkv * B >= (1ll << 31)) return ZG_ERR_UNSUPPORTED;
+    PrefillParams p;
+    std::memset(&p, 0, sizeof(p));
+    if (!dev_ctl(p.ctl)) return ZG_ERR_CUDA;
+    const int NK = swa_kv_box_rows(G);
+    if (!make_map(&p.tm_q, qh, d, Hq, L, B, G, T, CU_TENSOR_MAP_DATA_TYPE_FLOAT16) ||
+        !make_map(&p.tm_gate, sg, d, Hq, L, B, G, T) || !make_map(&p.tm_out, a, d, Hq, L, B, G, T) ||
+        !make_map(&p.tm_k, kh, d, Hkv, L, B, 1, NK, CU_TENSOR_MAP_DATA_TYPE_FLOAT16) ||
+        !make_map(&p.tm_v, v, d, Hkv, L, B, 1, NK))
+        return ZG_ERR_CUDA;
+    p.pos = pos;
+    p.wq = wq;
+    p.wk = wk;
+    p.B = B;
+    p.L = L;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.window = window;
+    p.n_ltiles = static_cast<int>(n_lt);
+    p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
+    p.eps = eps;
+    p.rope = rc;
+    p.pre = 1;
+    if (launch_swa_prefill(p, d, s) != cudaSuccess) return ZG_ERR_CUDA;
+    // 3. o_proj
+    const Proj out{w_o, y, hidden, 0, nullptr};
+    return run_projections(a, M, Hq * d, &out, 1, 0, nullptr, nullptr, 0.f, s);
 }
 
 // ---------------------------------------------------------------- attention backward

@@ -125,7 +125,10 @@ struct SlotCursor {
 };
 
 // ROT: rotary width compiled in (the dims then stay in registers), or 0 = any width.
-template <int D, int G, int ROT>
+// PRE: the inputs arrive pre-normalised (q_hat, k_hat in fp16, the gate as sigmoid(g) in bf16, as
+// the fused projections of the whole layer write them): the Q / K transforms and the sigmoid are
+// skipped and the tiles go to the tensor cores as loaded.
+template <int D, int G, int ROT, bool PRE>
 __global__ void __launch_bounds__(kThreads, 1) swa2_kernel(const __grid_constant__ PrefillParams p) {
     using C = Swa2<D, G>;
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -413,7 +416,9 @@ __global__ void __launch_bounds__(kThreads, 1) swa2_kernel(const __grid_constant
                 fail();
                 break;
             }
-            if constexpr (ROT > 0)
+            if constexpr (PRE)
+                (void)pos;
+            else if constexpr (ROT > 0)
                 qk_norm_rope_row_pair_ct<D, 2 * G, ROT / 2>(qbuf0 + qb * C::QBUF, C::QCH, row, wq_s, p.eps, pos, p.rope);
             else
                 qk_norm_rope_row_pair<D, 2 * G>(qbuf0 + qb * C::QBUF, C::QCH, row, wq_s, p.eps, pos, p.rope);
@@ -447,7 +452,9 @@ __global__ void __launch_bounds__(kThreads, 1) swa2_kernel(const __grid_constant
                 const bool active = r0 + (kt >> 1) < C::T;
                 const int r = min(r0 + (kt >> 1), C::T - 1);
                 const int pos = posr[r0 / 32];
-                if constexpr (ROT > 0)
+                if constexpr (PRE)
+                    (void)pos;
+                else if constexpr (ROT > 0)
                     qk_norm_rope_row_pair_ct<D, 2, ROT / 2>(kring, C::KCH, s * C::T + r, wk_s, p.eps, pos, p.rope,
                                                             active);
                 else
@@ -618,7 +625,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa2_kernel(const __grid_constant
                     uint32_t ou[4];
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
-                        const float2 sg = sigmoid2_f32(bf2f2(gu[k]));
+                        const float2 sg = PRE ? bf2f2(gu[k]) : sigmoid2_f32(bf2f2(gu[k]));
                         const float2 oc = mul2(
                             make_float2(__uint_as_float(r[q2 * 8 + 2 * k]), __uint_as_float(r[q2 * 8 + 2 * k + 1])), c2);
                         const float2 o = mul2(oc, sg);
@@ -655,10 +662,10 @@ __global__ void __launch_bounds__(kThreads, 1) swa2_kernel(const __grid_constant
     if (warp == 1) tmem_dealloc(tbase, C::TMEM_COLS);
 }
 
-template <int D, int G, int ROT>
+template <int D, int G, int ROT, bool PRE = false>
 cudaError_t launch_t(const PrefillParams& p, cudaStream_t s) {
     using C = Swa2<D, G>;
-    auto k = swa2_kernel<D, G, ROT>;
+    auto k = swa2_kernel<D, G, ROT, PRE>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     int dev = 0, sms = 0;
@@ -681,6 +688,7 @@ bool swa2_supports(int d, int G) { return (d == 64 || d == 128) && (G == 4 || G 
 template <int D, int G>
 cudaError_t launch_rot(const PrefillParams& p, cudaStream_t s) {
     constexpr int ROT_STD = D == 128 ? 42 : 20;
+    if (p.pre) return launch_t<D, G, 0, true>(p, s);
     if (2 * p.rope.half == ROT_STD) return launch_t<D, G, ROT_STD>(p, s);
     return launch_t<D, G, 0>(p, s);
 }

@@ -59,7 +59,8 @@ struct SwaCfg {
     static_assert(NK <= (int)TMEM_COLS && D <= (int)TMEM_COLS, "TMEM");
 };
 
-template <int D, int G>
+// PRE: inputs pre-normalised (q_hat, k_hat fp16; gate = sigmoid(g) bf16): transforms and sigmoid skipped
+template <int D, int G, bool PRE>
 __global__ void __launch_bounds__(128, 2) swa_prefill_kernel(const __grid_constant__ PrefillParams p) {
     using C = SwaCfg<D, G>;
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -134,7 +135,7 @@ __global__ void __launch_bounds__(128, 2) swa_prefill_kernel(const __grid_consta
 
     // ---- 2. QK-norm + RoPE in place
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_qk, 0, p.ctl, 11));
-    if (ok) {
+    if (ok && !PRE) {
         qk_norm_rope_row<D>(sQ, C::Q_CHUNK, t, p.wq, p.eps, pos_q, p.rope);
 #pragma unroll
         for (int s = 0; s < 2; ++s) {
@@ -280,8 +281,10 @@ __global__ void __launch_bounds__(128, 2) swa_prefill_kernel(const __grid_consta
                 uint32_t ou[4];
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    const float o0 = __uint_as_float(r[q4 * 8 + 2 * k]) * inv_l * sigmoid_f32(bf16lo(gu[k]));
-                    const float o1 = __uint_as_float(r[q4 * 8 + 2 * k + 1]) * inv_l * sigmoid_f32(bf16hi(gu[k]));
+                    const float s0 = PRE ? bf16lo(gu[k]) : sigmoid_f32(bf16lo(gu[k]));
+                    const float s1 = PRE ? bf16hi(gu[k]) : sigmoid_f32(bf16hi(gu[k]));
+                    const float o0 = __uint_as_float(r[q4 * 8 + 2 * k]) * inv_l * s0;
+                    const float o1 = __uint_as_float(r[q4 * 8 + 2 * k + 1]) * inv_l * s1;
                     ou[k] = pack_bf16x2(o0, o1);
                 }
                 *reinterpret_cast<uint4*>(gp) = make_uint4(ou[0], ou[1], ou[2], ou[3]);
@@ -306,7 +309,7 @@ __global__ void __launch_bounds__(128, 2) swa_prefill_kernel(const __grid_consta
 template <int D, int G>
 cudaError_t launch_swa_t(const PrefillParams& p, cudaStream_t s) {
     using C = SwaCfg<D, G>;
-    auto k = swa_prefill_kernel<D, G>;
+    auto k = p.pre ? swa_prefill_kernel<D, G, true> : swa_prefill_kernel<D, G, false>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     const long long tiles = static_cast<long long>(p.B) * p.Hkv * p.n_ltiles;

@@ -33,6 +33,7 @@ struct PrefillParams {
     const float* wk;                                 // [d]
     int B, L, Hq, Hkv, window;
     int n_ltiles;      // query tiles along L per (b, kv head)
+    int pre;           // SWA: q, k already q_hat, k_hat (fp16) and gate already sigmoid(g) (bf16)
     float scale_log2;  // log2(e) / sqrt(d)
     float eps;
     RopeConsts rope;
@@ -178,11 +179,27 @@ cudaError_t launch_backward_tc(const BackwardTcParams& p, cudaStream_t s);
 
 cudaError_t launch_backward(const BackwardParams& p, int d, cudaStream_t s);
 
-// ---------------------------------------------------------------- whole layer (plain GEMMs on cuBLASLt)
-size_t layer_gemm_workspace_bytes();
-// Y[M x N] = X[M x K] W[K x N], bf16 row-major, fp32 accumulate; false on any cuBLASLt failure
-bool layer_gemm(const void* X, const void* W, void* Y, long long M, long long N, long long K, void* ws,
-                size_t ws_bytes, cudaStream_t s);
+// ---------------------------------------------------------------- projections (tcgen05 GEMM, fused epilogues)
+// Y_i = epilogue_i(X W_i) for up to four W_i sharing X; row-major bf16 X [M, K], W_i [K, N_i].
+// mode 0: bf16(acc); mode 1: fp16(RoPE(RMSNorm(acc per head_dim columns; w_i), pos[row]));
+// mode 2: bf16(sigmoid(acc)).  Requires K % 8 == 0, N_i % 8 == 0 (mode 1: N_i % head_dim == 0,
+// head_dim in {64, 128}, rope.half <= 32).
+struct GemmParams {
+    CUtensorMap tm_a;     // X: box {64 (K), 128 rows}, 128-byte swizzle
+    CUtensorMap tm_b[4];  // W_i: box {64 (N), 64 (K)}, 128-byte swizzle
+    void* y[4];
+    const float* w[4];    // RMSNorm weights [head_dim] (mode 1)
+    int n[4], mode[4], tiles_n[4];
+    int nb, M, K, tiles_m, head_dim;
+    long long tiles;
+    const int32_t* pos;   // [M] RoPE positions (mode 1)
+    float eps;
+    RopeConsts rope;
+    DevCtl ctl;
+};
+cudaError_t launch_gemm(const GemmParams& p, cudaStream_t s);
+int gemm_tile_m();
+int gemm_tile_n();
 
 // bounded-wait self test: waits on a barrier nothing arrives on
 cudaError_t launch_wait_selftest(DevCtl ctl, cudaStream_t s);

@@ -274,15 +274,19 @@ zg_status zg_hybrid_decode_noalloc(const zg_bf16 *q, const zg_bf16 *k_new, const
  * "方法"): y = o_proj(A_SWA(q, k, v) ⊙ σ(g_proj(h))), with q, k, v and the gate
  * logits projected in parallel from the normalised hidden state h:
  *   q = h W_q, k = h W_k, v = h W_v, g = h W_g;  a = A_SWA(q, k, v) ⊙ σ(g)
- *   (zg_swa_prefill, QK RMSNorm with wq / wk and partial RoPE);  y = a W_o.
+ *   (QK RMSNorm with wq / wk and partial RoPE as zg_swa_prefill);  y = a W_o.
  * h [B, L, hidden] bf16; W_q, W_g [hidden, Hq*d], W_k, W_v [hidden, Hkv*d],
  * W_o [Hq*d, hidden], all bf16 row-major with the input dimension first (y = x W);
- * y [B, L, hidden] bf16.  Projections accumulate in fp32 and round q, k, v, g and a
- * to bf16 (the attention's own input and output precision).  The five GEMMs run on
- * cuBLASLt; hidden must be a multiple of 8.  Other shape limits as zg_swa_prefill.
+ * y [B, L, hidden] bf16.  All on the library's own tensor-core kernels, in three
+ * launches: the four input projections in one GEMM (h read once) whose epilogues
+ * apply RMSNorm + RoPE to q and k straight from the fp32 accumulator (q_hat, k_hat
+ * stored fp16), and sigmoid to g (stored bf16; v stored bf16); the windowed
+ * attention on those pre-normalised tensors; o_proj (a rounded to bf16).
+ * hidden must be a multiple of 8; rotary_dim <= 64; other shape limits as
+ * zg_swa_prefill.
  *   workspace: device scratch of at least zg_gated_swa_layer_workspace_bytes()
- *        bytes, 16-byte aligned (q, k, v, g, a and the GEMMs' workspace);
- *        ZG_ERR_WORKSPACE if missing or too small.  ZG_ERR_CUDA if a GEMM fails.
+ *        bytes, 16-byte aligned (q_hat, k_hat, v, sigmoid(g), a);
+ *        ZG_ERR_WORKSPACE if missing or too small.
  */
 size_t zg_gated_swa_layer_workspace_bytes(int B, int L, int Hq, int Hkv, int d);
 zg_status zg_gated_swa_layer(const zg_bf16 *h, const zg_bf16 *w_q, const zg_bf16 *w_k,
@@ -291,6 +295,14 @@ zg_status zg_gated_swa_layer(const zg_bf16 *h, const zg_bf16 *w_q, const zg_bf16
                              int B, int L, int hidden, int Hq, int Hkv, int d, int window,
                              int rotary_dim, double theta, float eps, void *workspace,
                              size_t workspace_bytes, zg_stream stream);
+
+/*
+ * y = x W on the library's tensor-core GEMM (the layer's projections): x [M, K],
+ * W [K, N], y [M, N], bf16 row-major, fp32 accumulation, y rounded to bf16.
+ * N and K multiples of 8 (16-byte rows); M < 2^31.  The pages' model uses it for
+ * o_proj (hyper.ai summary of arXiv 2609.13356, section "方法").
+ */
+zg_status zg_linear(const zg_bf16 *x, const zg_bf16 *w, zg_bf16 *y, int64_t M, int N, int K, zg_stream stream);
 
 /* Gradients of the attention prefill: the backward pass of zg_swa_prefill (gate
  * given, window >= 1) or of zg_global_prefill (gate NULL, window <= 0), the

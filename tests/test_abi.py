@@ -173,7 +173,23 @@ def test_gated_swa_layer_rejects_bad_arguments(zg):
     assert call(d=96, rot=20) == -4
     assert call(ws=None) == -6
     assert call(ws_bytes=1024) == -6
-    assert zg.gated_swa_layer_workspace_bytes(1, 16, 32, 8, 128) > 32 << 20
+    assert call(rot=130) == -3                # rotary_dim > d
+    assert call(rot=80) == -4                 # the fused epilogue takes rotary_dim <= 64
+    # q_hat, k_hat, v, sigmoid(g), a: (Hq + Hkv + Hkv + Hq + Hq) * d * 2 bytes per token, 256-byte aligned
+    assert zg.gated_swa_layer_workspace_bytes(1, 16, 32, 8, 128) == 16 * (32 * 3 + 8 * 2) * 128 * 2
+
+
+def test_linear_rejects_bad_arguments(zg):
+    def call(**kw):
+        a = dict(x=A, w=A, y=A, M=64, N=256, K=128)
+        a.update(kw)
+        return zg.lib.zg_linear(a["x"], a["w"], a["y"], a["M"], a["N"], a["K"], None)
+    assert call(w=None) == -1
+    assert call(y=A + 8) == -2
+    assert call(N=100) == -3    # rows of W must be 16-byte multiples
+    assert call(K=0) == -3
+    assert call(M=-1) == -3
+    assert call(M=0) == 0       # nothing to do, nothing launched
 
 
 def test_attention_backward_rejects_bad_arguments(zg):
