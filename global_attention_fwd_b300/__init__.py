@@ -31,7 +31,8 @@ EXPORTS = ("zg_swa_prefill", "zg_global_prefill_workspace_bytes", "zg_global_pre
            "zg_gated_swa_layer_workspace_bytes", "zg_gated_swa_layer", "zg_linear",
            "zg_attention_backward_workspace_bytes", "zg_attention_backward",
            "zg_hybrid_decode_workspace_bytes", "zg_hybrid_decode", "zg_hybrid_decode_noalloc",
-           "zg_hybrid_decode_fp8", "zg_kv_cache_write_fp8",
+           "zg_hybrid_decode_fp8", "zg_kv_cache_write_fp8", "zg_global_prefill_fp8_workspace_bytes",
+           "zg_global_prefill_fp8",
            "zg_device_status", "zg_selftest_bounded_wait", "zg_selftest_index_check", "zg_debug_build",
            "zg_status_string")
 
@@ -78,6 +79,10 @@ def _load() -> ctypes.CDLL:
     lib.zg_hybrid_decode_fp8.restype = I
     lib.zg_kv_cache_write_fp8.argtypes = [P] * 6 + [I] * 4 + [I64, I, I, D, F, F, F, P]
     lib.zg_kv_cache_write_fp8.restype = I
+    lib.zg_global_prefill_fp8_workspace_bytes.argtypes = [I, I, I, I]
+    lib.zg_global_prefill_fp8_workspace_bytes.restype = SZ
+    lib.zg_global_prefill_fp8.argtypes = [P] * 7 + [I] * 6 + [D, F, F, F, F, P, SZ, P]
+    lib.zg_global_prefill_fp8.restype = I
     lib.zg_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
     lib.zg_device_status.restype = I
     lib.zg_selftest_bounded_wait.argtypes = [U64, P]
@@ -166,6 +171,35 @@ def global_prefill(q, k, v, pos, wq, wk, *, rotary_dim, theta, eps=1e-6, out=Non
                                 B, L, Hq, Hkv, d, int(rotary_dim), float(theta), float(eps), _ptr(workspace),
                                 ws_bytes, _stream(stream))
     _raise(st, "zg_global_prefill")
+    return out
+
+
+def global_prefill_fp8_workspace_bytes(B, L, Hkv, d) -> int:
+    return int(_lib.zg_global_prefill_fp8_workspace_bytes(int(B), int(L), int(Hkv), int(d)))
+
+
+def global_prefill_fp8(q, k, v, pos, wq, wk, *, q_scale=1.0, k_scale=1.0, v_scale=1.0, rotary_dim, theta, eps=1e-6,
+                       out=None, workspace=None, stream=None):
+    """global_prefill on E4M3 inputs: q [B,L,Hq,d], k, v [B,L,Hkv,d] uint8 holding e4m3(x * scale);
+    products on the E4M3 tensor-core path.  Returns out [B,L,Hq,d] bf16."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, n, torch.uint8, 4)
+    _check(pos, "pos", torch.int32, 2)
+    _check(wq, "wq", torch.float32)
+    _check(wk, "wk", torch.float32)
+    B, L, Hq, d = q.shape
+    Hkv = k.shape[2]
+    if out is None:
+        out = torch.empty(B, L, Hq, d, dtype=torch.bfloat16, device=q.device)
+    _check(out, "out", torch.bfloat16, 4)
+    need = global_prefill_fp8_workspace_bytes(B, L, Hkv, d)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = _lib.zg_global_prefill_fp8(_ptr(q), _ptr(k), _ptr(v), _ptr(pos), _ptr(wq), _ptr(wk), _ptr(out),
+                                    B, L, Hq, Hkv, d, int(rotary_dim), float(theta), float(eps), float(q_scale),
+                                    float(k_scale), float(v_scale), _ptr(workspace), ws_bytes, _stream(stream))
+    _raise(st, "zg_global_prefill_fp8")
     return out
 
 

@@ -66,6 +66,20 @@ bool make_map(CUtensorMap* m, const void* base, int d, int heads, int L, int B, 
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 4-D tensor map of one-byte elements (E4M3) over a row-major [d3][d2][d1][d0] array, 128-byte swizzle
+bool make_map_u8(CUtensorMap* m, const void* base, long long d0, long long d1, long long d2, long long d3,
+                 uint32_t b0, uint32_t b1, uint32_t b2) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[4] = {(cuuint64_t)d0, (cuuint64_t)d1, (cuuint64_t)d2, (cuuint64_t)d3};
+    cuuint64_t strides[3] = {(cuuint64_t)d0, (cuuint64_t)(d0 * d1), (cuuint64_t)(d0 * d1 * d2)};
+    cuuint32_t box[4] = {b0, b1, b2, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 4-D fp32 tensor map over [outer][L][heads][d] with a {32, box_heads, box_rows, 1} box (128 bytes
 // inner), 128-byte swizzle
 bool make_map_f32(CUtensorMap* m, const void* base, int d, int heads, int L, int B, int box_heads, int box_rows) {
@@ -273,8 +287,65 @@ zg_status zg_global_prefill(const zg_bf16* q, const zg_bf16* k, const zg_bf16* v
         !make_map(&p.tm_kh, workspace, d, Hkv, L, B, 1, 128, CU_TENSOR_MAP_DATA_TYPE_FLOAT16) ||
         !make_map(&p.tm_v, v, d, Hkv, L, B, 1, 128))
         return ZG_ERR_CUDA;
-    p.k_raw = reinterpret_cast<const __nv_bfloat16*>(k);
-    p.khat = static_cast<__half*>(workspace);
+    p.k_raw = k;
+    p.khat = workspace;
+    p.pos = pos;
+    p.wq = wq;
+    p.wk = wk;
+    p.B = B;
+    p.L = L;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.window = L;
+    p.n_ltiles = static_cast<int>(n_lt);
+    p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
+    p.eps = eps;
+    if (!rope_consts(p.rope, rotary_dim, theta)) return ZG_ERR_SHAPE;
+    return launch_global_prefill(p, d, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? ZG_OK : ZG_ERR_CUDA;
+}
+
+size_t zg_global_prefill_fp8_workspace_bytes(int B, int L, int Hkv, int d) {
+    if (B <= 0 || L <= 0 || Hkv <= 0 || d <= 0) return 0;
+    const size_t lp = (static_cast<size_t>(L) + 15) / 16 * 16;
+    return static_cast<size_t>(B) * Hkv * d * (static_cast<size_t>(L) + lp);  // k_hat, then V^T
+}
+
+zg_status zg_global_prefill_fp8(const uint8_t* q, const uint8_t* k, const uint8_t* v, const int32_t* pos,
+                                const float* wq, const float* wk, zg_bf16* out, int B, int L, int Hq, int Hkv,
+                                int d, int rotary_dim, double theta, float eps, float q_scale, float k_scale,
+                                float v_scale, void* workspace, size_t workspace_bytes, zg_stream stream) {
+    zg_status st = check_prefill(q, k, v, nullptr, false, pos, wq, wk, out, B, L, Hq, Hkv, d, rotary_dim, theta, eps);
+    if (st != ZG_OK) return st;
+    if (!(std::isfinite(q_scale) && q_scale > 0.f && std::isfinite(k_scale) && k_scale > 0.f &&
+          std::isfinite(v_scale) && v_scale > 0.f))
+        return ZG_ERR_SHAPE;
+    const int G = Hq / Hkv;
+    if (d != 128 || !global_supports(d, G) || Hkv > 65535) return ZG_ERR_UNSUPPORTED;
+    if (B == 0 || L == 0) return ZG_OK;
+    const size_t need = zg_global_prefill_fp8_workspace_bytes(B, L, Hkv, d);
+    if (!workspace || workspace_bytes < need || !aligned16(workspace)) return ZG_ERR_WORKSPACE;
+    const int T = global_q_tile_tokens(G);
+    const long long n_lt = (L + T - 1) / T;
+    if (n_lt * Hkv * B >= (1ll << 31) || static_cast<long long>(B) * L * Hkv / 8 >= (1ll << 31))
+        return ZG_ERR_UNSUPPORTED;
+    const int lp = (L + 15) / 16 * 16;
+    uint8_t* kh = static_cast<uint8_t*>(workspace);
+    uint8_t* vt = kh + static_cast<size_t>(B) * L * Hkv * d;
+    PrefillParams p;
+    std::memset(&p, 0, sizeof(p));
+    if (!dev_ctl(p.ctl)) return ZG_ERR_CUDA;
+    if (!make_map_u8(&p.tm_q, q, d, Hq, L, B, 128, G, T) || !make_map(&p.tm_out, out, d, Hq, L, B, G, T) ||
+        !make_map_u8(&p.tm_kh, kh, d, Hkv, L, B, 128, 1, 128) || !make_map_u8(&p.tm_vt, vt, lp, d, Hkv, B, 128, 128, 1))
+        return ZG_ERR_CUDA;
+    p.fp8 = 1;
+    p.k_raw = k;
+    p.v_raw = v;
+    p.khat = kh;
+    p.vt_ws = vt;
+    p.vt_lp = lp;
+    p.in_dequant_q = 1.0f / q_scale;
+    p.in_dequant_k = 1.0f / k_scale;
+    p.in_dequant_v = 1.0f / v_scale;
     p.pos = pos;
     p.wq = wq;
     p.wk = wk;

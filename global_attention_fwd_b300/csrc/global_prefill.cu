@@ -28,6 +28,8 @@
 //   warps 8-11  the same for tile 1.
 // TMEM: S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [384,384+D).
 // Only blocks that reach past the CTA's first query hold keys beyond a diagonal.
+#include <cuda_fp8.h>
+
 #include "zg_qk.cuh"
 
 namespace zg {
@@ -39,9 +41,9 @@ constexpr int NBAR = 20;
 constexpr float kTau = 8.0f;
 constexpr int kThreads = 384;
 
-template <int D>
+template <int D, bool F8 = false>
 struct Glb {
-    static constexpr uint32_t TILE = 128 * D * 2;  // one 128-row x D tile of 16-bit values (D/64 chunks)
+    static constexpr uint32_t TILE = 128 * D * (F8 ? 1 : 2);  // one 128-row x D tile (16-bit: D/64 chunks)
     static constexpr uint32_t OFF_Q = 0;           // Q0, Q1
     static constexpr uint32_t OFF_K = 2 * TILE;    // 2 stages
     static constexpr uint32_t OFF_V = 4 * TILE;    // 2 stages
@@ -61,17 +63,139 @@ __global__ void __launch_bounds__(256) khat_kernel(const __grid_constant__ Prefi
     const long long tok = row / p.Hkv;  // b * L + j
     if (!idx_ok(p.ctl, tok, static_cast<long long>(p.B) * p.L, 82)) return;
     const int pos = __ldg(p.pos + tok);
-    norm_rope_warp_d<D>(p.k_raw + row * D, p.wk, p.eps, pos, p.rope, 1.0f, buf[warp]);
+    norm_rope_warp_d<D>(static_cast<const __nv_bfloat16*>(p.k_raw) + row * D, p.wk, p.eps, pos, p.rope, 1.0f,
+                        buf[warp]);
+    __half* kh = static_cast<__half*>(p.khat);
     for (int e = 2 * lane; e < D; e += 64)
-        *reinterpret_cast<uint32_t*>(p.khat + row * D + e) = pack_half2(buf[warp][e], buf[warp][e + 1]);
+        *reinterpret_cast<uint32_t*>(kh + row * D + e) = pack_half2(buf[warp][e], buf[warp][e + 1]);
+}
+
+// ---------------------------------------------------------------- E4M3 variant: pre-passes
+// E4M3 (FP8) inputs: q, k, v hold e4m3(x * scale) with per-tensor scales.  The products run on
+// tcgen05.mma.kind::f8f6f4: q_hat and k_hat are re-quantised to E4M3 after RMSNorm and RoPE with a
+// power-of-two scale that maps their bound sqrt(d) max|w| inside the E4M3 range, P is quantised
+// to E4M3, V is used as stored.  Both fp8 operands of every product are K-major: the pre-pass
+// writes V transposed, [B, Hkv, d, Lp] (Lp = L rounded up to 16, zero padded).
+__device__ __forceinline__ float e4m3_to_f(uint8_t u) {
+    const __half_raw h = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(u), __NV_E4M3);
+    return __half2float(__half(h));
+}
+__device__ __forceinline__ uint8_t f_to_e4m3(float x) {
+    return static_cast<uint8_t>(__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3));
+}
+// power-of-two scale s with s * sqrt(D) * max|w| <= 448 (the largest finite E4M3); warp-collective
+template <int D>
+__device__ __forceinline__ float e4m3_hat_scale(const float* w) {
+    float m = 0.f;
+    for (int e = threadIdx.x & 31; e < D; e += 32) m = fmaxf(m, fabsf(__ldg(w + e)));
+#pragma unroll
+    for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const float bound = sqrtf(static_cast<float>(D)) * fmaxf(m, 1e-30f) * 1.001f;
+    return exp2f(floorf(log2f(448.f / bound)));
+}
+
+// In-place RMSNorm + partial RoPE of one E4M3 row (D = 128 bytes, 128-byte swizzle) of a tile:
+// x = stored * dq; out = e4m3(RoPE(RMSNorm(x) * w) * s_out).  One thread per row.
+template <int D>
+__device__ __forceinline__ void qk_norm_rope_row_e4m3(uint8_t* tile, int row, const float* w, float eps, int pos,
+                                                      const RopeConsts& rc, float dq, float s_out) {
+    static_assert(D == 128, "one 128-byte swizzle row per head row");
+    auto at = [&](int e) { return tile + sw128_off(row, e >> 4) + (e & 15); };
+    float ss = 0.f;
+#pragma unroll
+    for (int c = 0; c < D / 16; ++c) {
+        const uint4 v = *reinterpret_cast<const uint4*>(tile + sw128_off(row, c));
+        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float a = e4m3_to_f(u[k] & 0xFF), b = e4m3_to_f((u[k] >> 8) & 0xFF);
+            const float c2 = e4m3_to_f((u[k] >> 16) & 0xFF), d2 = e4m3_to_f(u[k] >> 24);
+            ss = fmaf(a, a, fmaf(b, b, fmaf(c2, c2, fmaf(d2, d2, ss))));
+        }
+    }
+    ss *= dq * dq;
+    const float f = (ss > 0.f || eps > 0.f ? rsqrtf(ss * (1.0f / D) + eps) : 0.f) * dq;
+#pragma unroll 1
+    for (int j = 0; j < rc.half; ++j) {
+        const float a = e4m3_to_f(*at(j)) * f * __ldg(w + j);
+        const float c = e4m3_to_f(*at(j + rc.half)) * f * __ldg(w + j + rc.half);
+        float cs, sn;
+        rope_cos_sin(pos, rc.f_hi[j], rc.f_lo[j], cs, sn);
+        *at(j) = f_to_e4m3((a * cs - c * sn) * s_out);
+        *at(j + rc.half) = f_to_e4m3((c * cs + a * sn) * s_out);
+    }
+#pragma unroll 4
+    for (int e = 2 * rc.half; e < D; ++e) *at(e) = f_to_e4m3(e4m3_to_f(*at(e)) * f * __ldg(w + e) * s_out);
+}
+
+// k_hat in E4M3 (one warp per key row), from E4M3 keys
+template <int D>
+__global__ void __launch_bounds__(256) khat_e4m3_kernel(const __grid_constant__ PrefillParams p) {
+    __shared__ __align__(16) float buf[8][D];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long long row = static_cast<long long>(blockIdx.x) * 8 + warp;  // (b, j, g)
+    const long long nrows = static_cast<long long>(p.B) * p.L * p.Hkv;
+    if (row >= nrows) return;
+    const float s_kh = e4m3_hat_scale<D>(p.wk);
+    const long long tok = row / p.Hkv;
+    if (!idx_ok(p.ctl, tok, static_cast<long long>(p.B) * p.L, 94)) return;
+    const int pos = __ldg(p.pos + tok);
+    const uint8_t* kr = reinterpret_cast<const uint8_t*>(p.k_raw) + row * D;
+    for (int e = lane; e < D; e += 32) buf[warp][e] = e4m3_to_f(kr[e]) * p.in_dequant_k;
+    __syncwarp();
+    float ss = 0.f;
+    for (int e = lane; e < D; e += 32) ss = fmaf(buf[warp][e], buf[warp][e], ss);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float inv = ss > 0.f || p.eps > 0.f ? rsqrtf(ss * (1.0f / D) + p.eps) : 0.f;
+    for (int e = lane; e < D; e += 32) buf[warp][e] *= inv * __ldg(p.wk + e);
+    __syncwarp();
+    for (int j = lane; j < p.rope.half; j += 32) {
+        const float a = buf[warp][j], c = buf[warp][j + p.rope.half];
+        float cs, sn;
+        rope_cos_sin(pos, p.rope.f_hi[j], p.rope.f_lo[j], cs, sn);
+        buf[warp][j] = a * cs - c * sn;
+        buf[warp][j + p.rope.half] = c * cs + a * sn;
+    }
+    __syncwarp();
+    uint8_t* kh = reinterpret_cast<uint8_t*>(p.khat) + row * D;
+    for (int e = lane; e < D; e += 32) kh[e] = f_to_e4m3(buf[warp][e] * s_kh);
+}
+
+// V^T in E4M3: [B, Hkv, D, Lp] from [B, L, Hkv, D]; one CTA per 128 keys of one (b, KV head)
+template <int D>
+__global__ void __launch_bounds__(256) vt_e4m3_kernel(const __grid_constant__ PrefillParams p, uint8_t* vt, int Lp) {
+    __shared__ uint8_t tile[128][D + 4];
+    const int j0 = blockIdx.x * 128, g = blockIdx.y, b = blockIdx.z;
+    const uint8_t* v = reinterpret_cast<const uint8_t*>(p.v_raw);
+    for (int idx = threadIdx.x; idx < 128 * (D / 4); idx += 256) {
+        const int kr = idx / (D / 4), c4 = idx % (D / 4);
+        const int j = j0 + kr;
+        uint32_t w = 0u;
+        if (j < p.L) w = *reinterpret_cast<const uint32_t*>(v + ((static_cast<long long>(b) * p.L + j) * p.Hkv + g) * D + 4 * c4);
+        *reinterpret_cast<uint32_t*>(&tile[kr][4 * c4]) = w;
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < D * 32; idx += 256) {
+        const int dim = idx / 32, k4 = idx % 32;  // keys 4 k4 .. 4 k4 + 3 of row `dim`
+        const int j = j0 + 4 * k4;
+        if (j >= Lp) continue;
+        const uint32_t w = uint32_t(tile[4 * k4][dim]) | uint32_t(tile[4 * k4 + 1][dim]) << 8 |
+                           uint32_t(tile[4 * k4 + 2][dim]) << 16 | uint32_t(tile[4 * k4 + 3][dim]) << 24;
+        *reinterpret_cast<uint32_t*>(vt + ((static_cast<long long>(b) * p.Hkv + g) * D + dim) * Lp + j) = w;
+    }
 }
 
 // ---------------------------------------------------------------- kernel 2
-template <int D, int G>
+// F8: E4M3 inputs and products (see the pre-passes above); D = 128 only.
+template <int D, int G, bool F8>
 __global__ void __launch_bounds__(kThreads, 1) global_attn_kernel(const __grid_constant__ PrefillParams p) {
     constexpr int T = 128 / G;  // tokens per tile
-    constexpr uint32_t TILE = Glb<D>::TILE, OFF_Q = Glb<D>::OFF_Q, OFF_K = Glb<D>::OFF_K, OFF_V = Glb<D>::OFF_V;
-    constexpr uint32_t OFF_BAR = Glb<D>::OFF_BAR, OFF_MISC = Glb<D>::OFF_MISC;
+    using C = Glb<D, F8>;
+    constexpr uint32_t TILE = C::TILE, OFF_Q = C::OFF_Q, OFF_K = C::OFF_K, OFF_V = C::OFF_V;
+    constexpr uint32_t OFF_BAR = C::OFF_BAR, OFF_MISC = C::OFF_MISC;
+    constexpr int NCH = F8 ? 1 : D / 64;  // TMA boxes per 128-row tile (128-byte box rows)
+    static_assert(!F8 || D == 128, "E4M3 rows of 128 bytes");
     extern __shared__ __align__(1024) uint8_t smem[];
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
     uint64_t* q_full = bar + 0;
@@ -132,11 +256,11 @@ __global__ void __launch_bounds__(kThreads, 1) global_attn_kernel(const __grid_c
         if (lane == 0 && !aborted()) {
             tma_prefetch_desc(&p.tm_q);
             tma_prefetch_desc(&p.tm_kh);
-            tma_prefetch_desc(&p.tm_v);
+            tma_prefetch_desc(F8 ? &p.tm_vt : &p.tm_v);
             tma_prefetch_desc(&p.tm_out);
             mbar_arrive_expect_tx(q_full, 2 * TILE);
             for (int t = 0; t < 2; ++t)
-                for (int ch = 0; ch < D / 64; ++ch)
+                for (int ch = 0; ch < NCH; ++ch)
                     tma_load_4d(smem + OFF_Q + t * TILE + ch * CH, &p.tm_q, q_full, ch * 64, g * G, i0 + t * T, b);
             bool ok = true;
             for (int j = 0; j < nkb && ok && !aborted(); ++j) {
@@ -144,13 +268,16 @@ __global__ void __launch_bounds__(kThreads, 1) global_attn_kernel(const __grid_c
                 ok = mbar_wait(&k_empty[st], ((j >> 1) & 1) ^ 1, p.ctl, 51);
                 if (!ok) break;
                 mbar_arrive_expect_tx(&k_full[st], TILE);
-                for (int ch = 0; ch < D / 64; ++ch)
+                for (int ch = 0; ch < NCH; ++ch)
                     tma_load_4d(smem + OFF_K + st * TILE + ch * CH, &p.tm_kh, &k_full[st], ch * 64, g, j * BK, b);
                 ok = mbar_wait(&v_empty[st], ((j >> 1) & 1) ^ 1, p.ctl, 52);
                 if (!ok) break;
                 mbar_arrive_expect_tx(&v_full[st], TILE);
-                for (int ch = 0; ch < D / 64; ++ch)
-                    tma_load_4d(smem + OFF_V + st * TILE + ch * CH, &p.tm_v, &v_full[st], ch * 64, g, j * BK, b);
+                if constexpr (F8)  // V^T block: 128 key bytes per row, D rows
+                    tma_load_4d(smem + OFF_V + st * TILE, &p.tm_vt, &v_full[st], j * BK, 0, g, b);
+                else
+                    for (int ch = 0; ch < NCH; ++ch)
+                        tma_load_4d(smem + OFF_V + st * TILE + ch * CH, &p.tm_v, &v_full[st], ch * 64, g, j * BK, b);
             }
             if (!ok) fail();
         }
@@ -158,23 +285,41 @@ __global__ void __launch_bounds__(kThreads, 1) global_attn_kernel(const __grid_c
         // ------------------------------------------------------------ MMA
         if (lane == 0 && !aborted()) {
             auto qk = [&](int t, int j) {
-                constexpr uint32_t idesc = idesc_f16_f32(128, BK, false, false);
+                constexpr uint32_t idesc = idesc_f16_f32(128, BK, false, false);  // fp16, or E4M3 (code 0)
                 const uint32_t kofs = OFF_K + (j & 1) * TILE;
+                if constexpr (F8) {
 #pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t co = (ks >> 2) * CH + (ks & 3) * 32;
-                    umma_bf16(tbase + t * 128, sdesc(sbase + OFF_Q + t * TILE + co, 16, 1024, kSw128),
-                              sdesc(sbase + kofs + co, 16, 1024, kSw128), idesc, ks > 0);
+                    for (int ks = 0; ks < D / 32; ++ks)  // 32 E4M3 values = 32 bytes per k-step
+                        umma_f8(tbase + t * 128, sdesc(sbase + OFF_Q + t * TILE + ks * 32, 16, 1024, kSw128),
+                                sdesc(sbase + kofs + ks * 32, 16, 1024, kSw128), idesc, ks > 0);
+                } else {
+#pragma unroll
+                    for (int ks = 0; ks < D / 16; ++ks) {
+                        const uint32_t co = (ks >> 2) * CH + (ks & 3) * 32;
+                        umma_bf16(tbase + t * 128, sdesc(sbase + OFF_Q + t * TILE + co, 16, 1024, kSw128),
+                                  sdesc(sbase + kofs + co, 16, 1024, kSw128), idesc, ks > 0);
+                    }
                 }
                 umma_commit(&s_full[t]);
             };
             auto pv = [&](int t, int j) {
-                constexpr uint32_t idesc = idesc_bf16_f32(128, D, false, true);
                 const uint32_t vofs = OFF_V + (j & 1) * TILE;
+                if constexpr (F8) {
+                    // P (E4M3, four per TMEM column) times V^T (K-major: rows = dims, 128 key bytes each)
+                    constexpr uint32_t idesc = idesc_f16_f32(128, D, false, false);
 #pragma unroll
-                for (int ks = 0; ks < BK / 16; ++ks)
-                    umma_tmem_a(tbase + 256 + t * 128, tbase + t * 128 + ks * 8,
-                                sdesc(sbase + vofs + ks * 16 * 128, CH, 1024, kSw128), idesc, (j > 0 || ks > 0) ? 1u : 0u);
+                    for (int ks = 0; ks < BK / 32; ++ks)
+                        umma_f8_tmem_a(tbase + 256 + t * 128, tbase + t * 128 + ks * 8,
+                                       sdesc(sbase + vofs + ks * 32, 16, 1024, kSw128), idesc,
+                                       (j > 0 || ks > 0) ? 1u : 0u);
+                } else {
+                    constexpr uint32_t idesc = idesc_bf16_f32(128, D, false, true);
+#pragma unroll
+                    for (int ks = 0; ks < BK / 16; ++ks)
+                        umma_tmem_a(tbase + 256 + t * 128, tbase + t * 128 + ks * 8,
+                                    sdesc(sbase + vofs + ks * 16 * 128, CH, 1024, kSw128), idesc,
+                                    (j > 0 || ks > 0) ? 1u : 0u);
+                }
                 umma_commit(&pv_done[t]);
             };
             bool ok = mbar_wait(&q_ready[0], 0, p.ctl, 53) && mbar_wait(&q_ready[1], 0, p.ctl, 53) &&
@@ -221,17 +366,23 @@ __global__ void __launch_bounds__(kThreads, 1) global_attn_kernel(const __grid_c
         uint8_t* qt = smem + OFF_Q + t * TILE;
         const int tt = row / G;
         const int iq = i0 + t * T + tt;
+        // E4M3: q_hat and k_hat are stored times power-of-two scales (undone in the score scale)
+        const float s_qh = F8 ? e4m3_hat_scale<D>(p.wq) : 1.f;
+        const float s_kh = F8 ? e4m3_hat_scale<D>(p.wk) : 1.f;
         bool ok = __all_sync(0xffffffffu, mbar_wait(q_full, 0, p.ctl, 60));
         if (ok) {
             const long long pi = static_cast<long long>(b) * p.L + iq;
             const int pos = iq < p.L && idx_ok(p.ctl, pi, static_cast<long long>(p.B) * p.L, 83) ? __ldg(p.pos + pi) : 0;
-            qk_norm_rope_row<D>(qt, CH, row, p.wq, p.eps, pos, p.rope);
+            if constexpr (F8)
+                qk_norm_rope_row_e4m3<D>(qt, row, p.wq, p.eps, pos, p.rope, p.in_dequant_q, s_qh);
+            else
+                qk_norm_rope_row<D>(qt, CH, row, p.wq, p.eps, pos, p.rope);
             fence_async_smem();
         }
         mbar_arrive(&q_ready[t]);
         if (!ok) fail();
         float m_run = -INFINITY, l_run = 0.f;
-        const float sc = p.scale_log2;
+        const float sc = F8 ? p.scale_log2 / (s_qh * s_kh) : p.scale_log2;
         for (int j = 0; j < nkb && ok; ++j) {
             if (aborted() || !__all_sync(0xffffffffu, mbar_wait(&s_full[t], j & 1, p.ctl, 61))) {
                 fail();
@@ -282,25 +433,49 @@ __global__ void __launch_bounds__(kThreads, 1) global_attn_kernel(const __grid_c
             float2 l2 = make_float2(0.f, 0.f);
 #pragma unroll
             for (int cb = 0; cb < 128; cb += 32) {
-                uint32_t pk[16];
+                if constexpr (F8) {
+                    // P in E4M3 (at most 2^8 with the lazy maximum: inside the range), four per column;
+                    // the row sums are those of the rounded values the product uses
+                    uint32_t pk[8];
 #pragma unroll
-                for (int k = 0; k < 32; k += 2) {
-                    const float2 x = fma2(make_float2(__uint_as_float(r[cb + k]), __uint_as_float(r[cb + k + 1])), sc2, nm2);
-                    pk[k / 2] = pack_bf16x2(ex2_approx(x.x), ex2_approx(x.y));
-                    l2 = add2(l2, bf2f2(pk[k / 2]));
+                    for (int k = 0; k < 32; k += 4) {
+                        const float2 x0 = fma2(make_float2(__uint_as_float(r[cb + k]), __uint_as_float(r[cb + k + 1])), sc2, nm2);
+                        const float2 x1 = fma2(make_float2(__uint_as_float(r[cb + k + 2]), __uint_as_float(r[cb + k + 3])), sc2, nm2);
+                        const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
+                            make_float2(ex2_approx(x0.x), ex2_approx(x0.y)), __NV_SATFINITE, __NV_E4M3);
+                        const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
+                            make_float2(ex2_approx(x1.x), ex2_approx(x1.y)), __NV_SATFINITE, __NV_E4M3);
+                        pk[k / 4] = uint32_t(lo) | (uint32_t(hi) << 16);
+                        const __half2_raw hl = __nv_cvt_fp8x2_to_halfraw2(lo, __NV_E4M3);
+                        const __half2_raw hh = __nv_cvt_fp8x2_to_halfraw2(hi, __NV_E4M3);
+                        l2 = add2(l2, __half22float2(__half2(hl)));
+                        l2 = add2(l2, __half22float2(__half2(hh)));
+                    }
+                    tmem_st8(s_addr + cb / 4, pk);  // P over S (these columns are already in registers)
+                } else {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int k = 0; k < 32; k += 2) {
+                        const float2 x = fma2(make_float2(__uint_as_float(r[cb + k]), __uint_as_float(r[cb + k + 1])), sc2, nm2);
+                        pk[k / 2] = pack_bf16x2(ex2_approx(x.x), ex2_approx(x.y));
+                        l2 = add2(l2, bf2f2(pk[k / 2]));
+                    }
+                    tmem_st16(s_addr + cb / 2, pk);  // P over S (these columns are already in registers)
                 }
-                tmem_st16(s_addr + cb / 2, pk);  // P over S (these columns are already in registers)
             }
             l_run += l2.x + l2.y;
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(&p_ready[t]);
         }
-        // ---- epilogue: O / l -> bf16 -> the tile's Q buffer -> TMA store
+        // ---- epilogue: O / l -> bf16 -> staging tile -> TMA store.  The staging tile is the tile's
+        // Q buffer, or (E4M3, whose Q buffer is half the size of the bf16 output) the K stages for
+        // tile 0 and the V stages for tile 1, free once the tile's last product has completed.
+        uint8_t* stg = F8 ? smem + (t == 0 ? OFF_K : OFF_V) : qt;
         if (ok && !aborted()) ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[t], (nkb - 1) & 1, p.ctl, 63));
         if (ok) {
             tc_fence_after();
-            const float inv_l = l_run > 0.f ? 1.0f / l_run : 0.f;
+            const float inv_l = l_run > 0.f ? (F8 ? p.in_dequant_v : 1.0f) / l_run : 0.f;
 #pragma unroll 1
             for (int cb = 0; cb < D; cb += 32) {
                 uint32_t o[32];
@@ -314,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1) global_attn_kernel(const __grid_c
                         ou[k] = pack_bf16x2(__uint_as_float(o[q4 * 8 + 2 * k]) * inv_l,
                                             __uint_as_float(o[q4 * 8 + 2 * k + 1]) * inv_l);
                     const int e0 = cb + q4 * 8;
-                    *reinterpret_cast<uint4*>(qt + (e0 >> 6) * CH + sw128_off(row, (e0 & 63) >> 3)) =
+                    *reinterpret_cast<uint4*>(stg + (e0 >> 6) * CH + sw128_off(row, (e0 & 63) >> 3)) =
                         make_uint4(ou[0], ou[1], ou[2], ou[3]);
                 }
             }
@@ -325,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1) global_attn_kernel(const __grid_c
         if (row == 0 && ok && i0 + t * T < p.L) {  // a tile that starts past the end has nothing to store
             if (mbar_wait(&out_bar[t], 0, p.ctl, 64)) {
                 for (int ch = 0; ch < D / 64; ++ch)
-                    tma_store_4d(&p.tm_out, qt + ch * CH, ch * 64, g * G, i0 + t * T, b);
+                    tma_store_4d(&p.tm_out, stg + ch * CH, ch * 64, g * G, i0 + t * T, b);
                 bulk_commit();
                 bulk_wait_all();
             } else {
@@ -346,29 +521,36 @@ __global__ void __launch_bounds__(kThreads, 1) global_attn_kernel(const __grid_c
     if (warp == 1) tmem_dealloc(tbase, 512);
 }
 
-template <int D, int G>
+template <int D, int G, bool F8>
 cudaError_t launch_t(const PrefillParams& p, cudaStream_t s) {
     constexpr int T = 128 / G;
     const long long rows = static_cast<long long>(p.B) * p.L * p.Hkv;
-    khat_kernel<D><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, s>>>(p);
+    if constexpr (F8) {
+        khat_e4m3_kernel<D><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, s>>>(p);
+        const dim3 vg(static_cast<unsigned>((p.vt_lp + 127) / 128), static_cast<unsigned>(p.Hkv),
+                      static_cast<unsigned>(p.B));
+        vt_e4m3_kernel<D><<<vg, 256, 0, s>>>(p, p.vt_ws, p.vt_lp);
+    } else {
+        khat_kernel<D><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, s>>>(p);
+    }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    auto k = global_attn_kernel<D, G>;
-    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Glb<D>::SMEM);
+    auto k = global_attn_kernel<D, G, F8>;
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Glb<D, F8>::SMEM);
     if (e != cudaSuccess) return e;
     const long long ctas = static_cast<long long>(p.B) * p.Hkv * ((p.L + 2 * T - 1) / (2 * T));
-    k<<<static_cast<unsigned>(ctas), kThreads, Glb<D>::SMEM, s>>>(p);
+    k<<<static_cast<unsigned>(ctas), kThreads, Glb<D, F8>::SMEM, s>>>(p);
     return cudaGetLastError();
 }
 
-template <int D>
+template <int D, bool F8>
 cudaError_t launch_d(const PrefillParams& p, cudaStream_t s) {
     switch (p.Hq / p.Hkv) {
-        case 1: return launch_t<D, 1>(p, s);
-        case 2: return launch_t<D, 2>(p, s);
-        case 4: return launch_t<D, 4>(p, s);
-        case 8: return launch_t<D, 8>(p, s);
-        case 16: return launch_t<D, 16>(p, s);
+        case 1: return launch_t<D, 1, F8>(p, s);
+        case 2: return launch_t<D, 2, F8>(p, s);
+        case 4: return launch_t<D, 4, F8>(p, s);
+        case 8: return launch_t<D, 8, F8>(p, s);
+        case 16: return launch_t<D, 16, F8>(p, s);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -380,7 +562,8 @@ int global_q_tile_tokens(int G) { return 128 / G; }
 
 cudaError_t launch_global_prefill(const PrefillParams& p, int d, cudaStream_t s) {
     if (p.Hkv <= 0 || p.Hq % p.Hkv || !global_supports(d, p.Hq / p.Hkv)) return cudaErrorInvalidValue;
-    return d == 128 ? launch_d<128>(p, s) : launch_d<64>(p, s);
+    if (p.fp8) return d == 128 ? launch_d<128, true>(p, s) : cudaErrorInvalidValue;
+    return d == 128 ? launch_d<128, false>(p, s) : launch_d<64, false>(p, s);
 }
 
 }  // namespace zg

@@ -26,14 +26,21 @@ struct RopeConsts {
 struct PrefillParams {
     CUtensorMap tm_q, tm_k, tm_v, tm_gate, tm_out;  // 4-D maps {d, heads, L, B}
     CUtensorMap tm_kh;                               // global prefill: fp16 k_hat workspace
-    const __nv_bfloat16* k_raw;                      // global prefill: raw keys [B, L, Hkv, d]
-    __half* khat;                                    // global prefill: k_hat workspace [B, L, Hkv, d]
+    const void* k_raw;                               // global prefill: raw keys [B, L, Hkv, d] (bf16 or E4M3)
+    void* khat;                                      // global prefill: k_hat workspace (fp16, or E4M3)
     const int32_t* pos;                              // [B, L]
     const float* wq;                                 // [d]
     const float* wk;                                 // [d]
     int B, L, Hq, Hkv, window;
     int n_ltiles;      // query tiles along L per (b, kv head)
     int pre;           // SWA: q, k already q_hat, k_hat (fp16) and gate already sigmoid(g) (bf16)
+    // global prefill over E4M3 inputs: q, k, v hold e4m3(x * scale); these undo the scales
+    int fp8;
+    const void* v_raw;                               // E4M3 values [B, L, Hkv, d] (transposed by the pre-pass)
+    CUtensorMap tm_vt;                               // V^T workspace {Lp, d, Hkv, B}
+    uint8_t* vt_ws;                                  // V^T workspace [B, Hkv, d, Lp] (E4M3)
+    int vt_lp;                                       // Lp: L rounded up to 16 (16-byte rows)
+    float in_dequant_q, in_dequant_k, in_dequant_v;  // 1 / scale of each input
     float scale_log2;  // log2(e) / sqrt(d)
     float eps;
     RopeConsts rope;

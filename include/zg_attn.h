@@ -233,6 +233,36 @@ zg_status zg_kv_cache_write_fp8(const zg_bf16 *k, const zg_bf16 *v, const int32_
                                 int ring, int rotary_dim, double theta, float eps, float k_scale, float v_scale,
                                 zg_stream stream);
 
+/* Bytes of workspace zg_global_prefill_fp8 needs: B * Hkv * d * (L + Lp), Lp = L rounded
+ * up to a multiple of 16 (0 for empty input). */
+size_t zg_global_prefill_fp8_workspace_bytes(int B, int L, int Hkv, int d);
+
+/*
+ * zg_global_prefill_fp8 -- zg_global_prefill with E4M3 (FP8) inputs and E4M3 tensor-core
+ * products.  The pages run the forward pass's matrix products in E4M3 ("ZGCM-1-7B 完全解説",
+ * section "学習の高速化 — FP8・Muon・TWEOが生む約4.2倍の効率"); here both attention
+ * products of the global layers take that format (tcgen05 kind::f8f6f4, fp32 accumulation).
+ *   q [B, L, Hq, d], k, v [B, L, Hkv, d]: one byte per element, E4M3, holding
+ *        e4m3(q * q_scale), e4m3(k * k_scale), e4m3(v * v_scale); the attention is that of
+ *        the dequantised inputs (stored / scale).  Scales finite and > 0, else ZG_ERR_SHAPE.
+ *   out [B, L, Hq, d] bf16, pos, wq, wk, rotary_dim, theta, eps: as zg_global_prefill.
+ *   Rounding: q_hat and k_hat (after RMSNorm and RoPE in fp32) are rounded to E4M3 times a
+ *        power-of-two scale that puts their bound sqrt(d) * max|w| just inside +-448 (the
+ *        scale is undone exactly in the softmax); the softmax weights P are rounded to
+ *        E4M3 (they are at most 2^8 there) and the row sums are those of the rounded
+ *        weights; V enters as stored.  Expect a relative error of a few per cent on the
+ *        output (three mantissa bits per operand), not the bf16 path's 1e-2.
+ *   workspace: device scratch of at least zg_global_prefill_fp8_workspace_bytes() bytes,
+ *        16-byte aligned, no initialisation; it receives k_hat in E4M3 and V transposed
+ *        to [B, Hkv, d, Lp] so that both operands of both products are K-major.
+ * Kernel shapes: d = 128 (one 128-byte row per head vector); Hq / Hkv in {1, 2, 4, 8, 16};
+ * ZG_ERR_UNSUPPORTED otherwise.  B == 0 or L == 0 is a no-op returning ZG_OK.
+ */
+zg_status zg_global_prefill_fp8(const uint8_t *q, const uint8_t *k, const uint8_t *v, const int32_t *pos,
+                                const float *wq, const float *wk, zg_bf16 *out, int B, int L, int Hq, int Hkv,
+                                int d, int rotary_dim, double theta, float eps, float q_scale, float k_scale,
+                                float v_scale, void *workspace, size_t workspace_bytes, zg_stream stream);
+
 /*
  * zg_hybrid_decode_noalloc -- the same decode step as zg_hybrid_decode, for
  * callers that cannot allocate device memory (no counterpart in the paper: it
