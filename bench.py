@@ -16,7 +16,8 @@ the inputs in pinned host memory, the host->device copies and the device->host
 copy of the output inside the timed region.  Outside the step, `parts` also
 times the other workloads one by one: the tiny gated SWA prefill (latency, L2
 flushed), the B=4 L=4096 gated SWA prefill (L2 flushed), the global prefill at
-L=262144, the decode step over E4M3 caches, the cache writer, the whole gated
+L=262144 (bf16, and with E4M3 inputs on the E4M3 tensor-core path), the decode
+step over E4M3 caches, the cache writer, the whole gated
 layer and the backward pass.  `cpu_baseline` times the fp64 oracle on a slice of
 the 256K workload, on the whole tiny configuration and on one decode step of one
 sequence, with the host CPU model and thread count.
@@ -629,7 +630,21 @@ def run_gpu(args):
                             "unit": "TFLOP/s", "frac": gf4 / g4_t / 1e12 / peaks["bf16_tflops"],
                             "frac_of_sustained": gf4 / g4_t / 1e12 / peaks["bf16_tflops_sustained"],
                             "traffic": None, "algorithmic_flops": gf4}}
-    del gbx, gb_out, gb_ws, flush
+    # the same workload with E4M3 inputs (e4m3(x * 1)) on the E4M3 tensor-core path
+    g8 = {n: workloads.to_e4m3(gbx[n], 1.0).view(torch.uint8) for n in ("q", "k", "v")}
+    del gb_ws
+    g8_ws = torch.empty(zg.global_prefill_fp8_workspace_bytes(G4b.B, G4b.L, G4b.Hkv, G4b.d), dtype=torch.uint8,
+                        device=dev)
+    g8_t = time_part(lambda: zg.global_prefill_fp8(g8["q"], g8["k"], g8["v"], gbx["pos"], gbx["wq"], gbx["wk"],
+                                                   rotary_dim=G4b.rotary_dim, theta=G4b.theta, eps=G4b.eps,
+                                                   out=gb_out, workspace=g8_ws), 2, warm=1)
+    fp8_peak = 2.0 * peaks["bf16_tflops"]  # measured bf16 peak x the nominal E4M3 : bf16 ratio (4.5 : 2.25)
+    glob256_fp8 = {"workload": f"{G4b.name} with E4M3 q, k, v", "ms": g8_t * 1e3, "tokens_per_s": G4b.tokens / g8_t,
+                   "roofline": {"bound": "tensor", "achieved": gf4 / g8_t / 1e12, "peak": fp8_peak,
+                                "unit": "TFLOP/s", "frac": gf4 / g8_t / 1e12 / fp8_peak,
+                                "peak_basis": "measured bf16 burst x 2 (nominal E4M3 : bf16 ratio)",
+                                "traffic": None, "algorithmic_flops": gf4}}
+    del gbx, gb_out, g8, g8_ws, flush
 
     # ---- the decode step over E4M3 caches (outside the step): the same workload, caches stored
     # as e4m3(k_hat * 1) and e4m3(v * 8)
@@ -720,6 +735,7 @@ def run_gpu(args):
             "tiny_swa_prefill": tiny,
             "swa_prefill_4k": swa4k,
             "global_prefill_256k": glob256,
+            "global_prefill_256k_fp8": glob256_fp8,
             "swa_prefill": {"workload": SWA.name, "ms": sw_t * 1e3, "tokens_per_s": SWA.tokens / sw_t,
                             "roofline": rl_swa},
             "hybrid_decode": {"workload": DEC.name, "us_per_step": dc_t * 1e6, "roofline": rl_dec},

@@ -40,6 +40,7 @@ constexpr uint32_t CH = 128 * 128;    // one 64-column chunk of 128 rows (16-bit
 constexpr int NBAR = 20;
 constexpr float kTau = 8.0f;
 constexpr int kThreads = 384;
+constexpr int kGroupCt = 128;  // CTAs of one (sequence, KV head) scheduled together on long sequences
 
 template <int D, bool F8 = false>
 struct Glb {
@@ -172,7 +173,9 @@ __global__ void __launch_bounds__(256) vt_e4m3_kernel(const __grid_constant__ Pr
         const int kr = idx / (D / 4), c4 = idx % (D / 4);
         const int j = j0 + kr;
         uint32_t w = 0u;
-        if (j < p.L) w = *reinterpret_cast<const uint32_t*>(v + ((static_cast<long long>(b) * p.L + j) * p.Hkv + g) * D + 4 * c4);
+        const long long src = ((static_cast<long long>(b) * p.L + j) * p.Hkv + g) * D + 4 * c4;
+        if (j < p.L && idx_ok(p.ctl, src + 3, static_cast<long long>(p.B) * p.L * p.Hkv * D, 66))
+            w = *reinterpret_cast<const uint32_t*>(v + src);
         *reinterpret_cast<uint32_t*>(&tile[kr][4 * c4]) = w;
     }
     __syncthreads();
@@ -182,7 +185,9 @@ __global__ void __launch_bounds__(256) vt_e4m3_kernel(const __grid_constant__ Pr
         if (j >= Lp) continue;
         const uint32_t w = uint32_t(tile[4 * k4][dim]) | uint32_t(tile[4 * k4 + 1][dim]) << 8 |
                            uint32_t(tile[4 * k4 + 2][dim]) << 16 | uint32_t(tile[4 * k4 + 3][dim]) << 24;
-        *reinterpret_cast<uint32_t*>(vt + ((static_cast<long long>(b) * p.Hkv + g) * D + dim) * Lp + j) = w;
+        const long long dst = ((static_cast<long long>(b) * p.Hkv + g) * D + dim) * Lp + j;
+        if (idx_ok(p.ctl, dst + 3, static_cast<long long>(p.B) * p.Hkv * D * Lp, 67))
+            *reinterpret_cast<uint32_t*>(vt + dst) = w;
     }
 }
 
@@ -215,9 +220,21 @@ __global__ void __launch_bounds__(kThreads, 1) global_attn_kernel(const __grid_c
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nbg = p.B * p.Hkv;
     const int n_ct = (p.L + 2 * T - 1) / (2 * T);
-    const int ct = n_ct - 1 - static_cast<int>(blockIdx.x / nbg);  // heaviest (longest key range) first
-    const int g = static_cast<int>(blockIdx.x % nbg) % p.Hkv;
-    const int b = static_cast<int>(blockIdx.x % nbg) / p.Hkv;
+    // Heaviest (longest key range) first.  Long sequences: in groups of kGroupCt CTAs of one (b, g),
+    // so that the CTAs resident together read the same K_hat / V blocks and share them in L2.
+    int ct, bg;
+    if (n_ct >= 2 * kGroupCt) {
+        const int q = static_cast<int>(blockIdx.x / (kGroupCt * nbg));  // group, heaviest first
+        const int r = static_cast<int>(blockIdx.x - static_cast<unsigned>(q * kGroupCt * nbg));
+        const int sz = min(kGroupCt, n_ct - q * kGroupCt);
+        bg = r / sz;
+        ct = n_ct - 1 - (q * kGroupCt + r % sz);
+    } else {
+        ct = n_ct - 1 - static_cast<int>(blockIdx.x / nbg);
+        bg = static_cast<int>(blockIdx.x % nbg);
+    }
+    const int g = bg % p.Hkv;
+    const int b = bg / p.Hkv;
     const int i0 = ct * 2 * T;
     const int nkb = (i0 + 2 * T + BK - 1) / BK;  // both tiles need the same key blocks
 
@@ -250,113 +267,118 @@ __global__ void __launch_bounds__(kThreads, 1) global_attn_kernel(const __grid_c
     const uint32_t sbase = smem_u32(smem);
     auto aborted = [&]() { return *abort_flag != 0; };
     auto fail = [&]() { *abort_flag = 1; };
-
-    if (warp == 0) {
-        // ------------------------------------------------------------ TMA
-        if (lane == 0 && !aborted()) {
-            tma_prefetch_desc(&p.tm_q);
-            tma_prefetch_desc(&p.tm_kh);
-            tma_prefetch_desc(F8 ? &p.tm_vt : &p.tm_v);
-            tma_prefetch_desc(&p.tm_out);
-            mbar_arrive_expect_tx(q_full, 2 * TILE);
-            for (int t = 0; t < 2; ++t)
-                for (int ch = 0; ch < NCH; ++ch)
-                    tma_load_4d(smem + OFF_Q + t * TILE + ch * CH, &p.tm_q, q_full, ch * 64, g * G, i0 + t * T, b);
-            bool ok = true;
-            for (int j = 0; j < nkb && ok && !aborted(); ++j) {
-                const int st = j & 1;
-                ok = mbar_wait(&k_empty[st], ((j >> 1) & 1) ^ 1, p.ctl, 51);
-                if (!ok) break;
-                mbar_arrive_expect_tx(&k_full[st], TILE);
-                for (int ch = 0; ch < NCH; ++ch)
-                    tma_load_4d(smem + OFF_K + st * TILE + ch * CH, &p.tm_kh, &k_full[st], ch * 64, g, j * BK, b);
-                ok = mbar_wait(&v_empty[st], ((j >> 1) & 1) ^ 1, p.ctl, 52);
-                if (!ok) break;
-                mbar_arrive_expect_tx(&v_full[st], TILE);
-                if constexpr (F8)  // V^T block: 128 key bytes per row, D rows
-                    tma_load_4d(smem + OFF_V + st * TILE, &p.tm_vt, &v_full[st], j * BK, 0, g, b);
-                else
+    // registers: the TMA / MMA warpgroup (warps 0-3) hands most of its share to the two softmax
+    // warpgroups, which hold a 128-score row each: 128 x 64 + 256 x 216 <= 384 x 168 (the launch's)
+    if (warp < 4) {
+        regs_dec<64>();
+        if (warp == 0) {
+            // ------------------------------------------------------------ TMA
+            if (lane == 0 && !aborted()) {
+                tma_prefetch_desc(&p.tm_q);
+                tma_prefetch_desc(&p.tm_kh);
+                tma_prefetch_desc(F8 ? &p.tm_vt : &p.tm_v);
+                tma_prefetch_desc(&p.tm_out);
+                mbar_arrive_expect_tx(q_full, 2 * TILE);
+                for (int t = 0; t < 2; ++t)
                     for (int ch = 0; ch < NCH; ++ch)
-                        tma_load_4d(smem + OFF_V + st * TILE + ch * CH, &p.tm_v, &v_full[st], ch * 64, g, j * BK, b);
+                        tma_load_4d(smem + OFF_Q + t * TILE + ch * CH, &p.tm_q, q_full, ch * 64, g * G, i0 + t * T, b);
+                bool ok = true;
+                for (int j = 0; j < nkb && ok && !aborted(); ++j) {
+                    const int st = j & 1;
+                    ok = mbar_wait(&k_empty[st], ((j >> 1) & 1) ^ 1, p.ctl, 51);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(&k_full[st], TILE);
+                    for (int ch = 0; ch < NCH; ++ch)
+                        tma_load_4d(smem + OFF_K + st * TILE + ch * CH, &p.tm_kh, &k_full[st], ch * 64, g, j * BK, b);
+                    ok = mbar_wait(&v_empty[st], ((j >> 1) & 1) ^ 1, p.ctl, 52);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(&v_full[st], TILE);
+                    if constexpr (F8)  // V^T block: 128 key bytes per row, D rows
+                        tma_load_4d(smem + OFF_V + st * TILE, &p.tm_vt, &v_full[st], j * BK, 0, g, b);
+                    else
+                        for (int ch = 0; ch < NCH; ++ch)
+                            tma_load_4d(smem + OFF_V + st * TILE + ch * CH, &p.tm_v, &v_full[st], ch * 64, g, j * BK, b);
+                }
+                if (!ok) fail();
             }
-            if (!ok) fail();
-        }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA
-        if (lane == 0 && !aborted()) {
-            auto qk = [&](int t, int j) {
-                constexpr uint32_t idesc = idesc_f16_f32(128, BK, false, false);  // fp16, or E4M3 (code 0)
-                const uint32_t kofs = OFF_K + (j & 1) * TILE;
-                if constexpr (F8) {
-#pragma unroll
-                    for (int ks = 0; ks < D / 32; ++ks)  // 32 E4M3 values = 32 bytes per k-step
-                        umma_f8(tbase + t * 128, sdesc(sbase + OFF_Q + t * TILE + ks * 32, 16, 1024, kSw128),
-                                sdesc(sbase + kofs + ks * 32, 16, 1024, kSw128), idesc, ks > 0);
-                } else {
-#pragma unroll
-                    for (int ks = 0; ks < D / 16; ++ks) {
-                        const uint32_t co = (ks >> 2) * CH + (ks & 3) * 32;
-                        umma_bf16(tbase + t * 128, sdesc(sbase + OFF_Q + t * TILE + co, 16, 1024, kSw128),
-                                  sdesc(sbase + kofs + co, 16, 1024, kSw128), idesc, ks > 0);
+        } else if (warp == 1) {
+            // ------------------------------------------------------------ MMA
+            if (lane == 0 && !aborted()) {
+                auto qk = [&](int t, int j) {
+                    constexpr uint32_t idesc = idesc_f16_f32(128, BK, false, false);  // fp16, or E4M3 (code 0)
+                    const uint32_t kofs = OFF_K + (j & 1) * TILE;
+                    if constexpr (F8) {
+    #pragma unroll
+                        for (int ks = 0; ks < D / 32; ++ks)  // 32 E4M3 values = 32 bytes per k-step
+                            umma_f8(tbase + t * 128, sdesc(sbase + OFF_Q + t * TILE + ks * 32, 16, 1024, kSw128),
+                                    sdesc(sbase + kofs + ks * 32, 16, 1024, kSw128), idesc, ks > 0);
+                    } else {
+    #pragma unroll
+                        for (int ks = 0; ks < D / 16; ++ks) {
+                            const uint32_t co = (ks >> 2) * CH + (ks & 3) * 32;
+                            umma_bf16(tbase + t * 128, sdesc(sbase + OFF_Q + t * TILE + co, 16, 1024, kSw128),
+                                      sdesc(sbase + kofs + co, 16, 1024, kSw128), idesc, ks > 0);
+                        }
                     }
+                    umma_commit(&s_full[t]);
+                };
+                auto pv = [&](int t, int j) {
+                    const uint32_t vofs = OFF_V + (j & 1) * TILE;
+                    if constexpr (F8) {
+                        // P (E4M3, four per TMEM column) times V^T (K-major: rows = dims, 128 key bytes each)
+                        constexpr uint32_t idesc = idesc_f16_f32(128, D, false, false);
+    #pragma unroll
+                        for (int ks = 0; ks < BK / 32; ++ks)
+                            umma_f8_tmem_a(tbase + 256 + t * 128, tbase + t * 128 + ks * 8,
+                                           sdesc(sbase + vofs + ks * 32, 16, 1024, kSw128), idesc,
+                                           (j > 0 || ks > 0) ? 1u : 0u);
+                    } else {
+                        constexpr uint32_t idesc = idesc_bf16_f32(128, D, false, true);
+    #pragma unroll
+                        for (int ks = 0; ks < BK / 16; ++ks)
+                            umma_tmem_a(tbase + 256 + t * 128, tbase + t * 128 + ks * 8,
+                                        sdesc(sbase + vofs + ks * 16 * 128, CH, 1024, kSw128), idesc,
+                                        (j > 0 || ks > 0) ? 1u : 0u);
+                    }
+                    umma_commit(&pv_done[t]);
+                };
+                bool ok = mbar_wait(&q_ready[0], 0, p.ctl, 53) && mbar_wait(&q_ready[1], 0, p.ctl, 53) &&
+                          mbar_wait(&k_full[0], 0, p.ctl, 54);
+                if (ok) {
+                    tc_fence_after();
+                    qk(0, 0);
+                    qk(1, 0);
+                    umma_commit(&k_empty[0]);
                 }
-                umma_commit(&s_full[t]);
-            };
-            auto pv = [&](int t, int j) {
-                const uint32_t vofs = OFF_V + (j & 1) * TILE;
-                if constexpr (F8) {
-                    // P (E4M3, four per TMEM column) times V^T (K-major: rows = dims, 128 key bytes each)
-                    constexpr uint32_t idesc = idesc_f16_f32(128, D, false, false);
-#pragma unroll
-                    for (int ks = 0; ks < BK / 32; ++ks)
-                        umma_f8_tmem_a(tbase + 256 + t * 128, tbase + t * 128 + ks * 8,
-                                       sdesc(sbase + vofs + ks * 32, 16, 1024, kSw128), idesc,
-                                       (j > 0 || ks > 0) ? 1u : 0u);
-                } else {
-                    constexpr uint32_t idesc = idesc_bf16_f32(128, D, false, true);
-#pragma unroll
-                    for (int ks = 0; ks < BK / 16; ++ks)
-                        umma_tmem_a(tbase + 256 + t * 128, tbase + t * 128 + ks * 8,
-                                    sdesc(sbase + vofs + ks * 16 * 128, CH, 1024, kSw128), idesc,
-                                    (j > 0 || ks > 0) ? 1u : 0u);
-                }
-                umma_commit(&pv_done[t]);
-            };
-            bool ok = mbar_wait(&q_ready[0], 0, p.ctl, 53) && mbar_wait(&q_ready[1], 0, p.ctl, 53) &&
-                      mbar_wait(&k_full[0], 0, p.ctl, 54);
-            if (ok) {
-                tc_fence_after();
-                qk(0, 0);
-                qk(1, 0);
-                umma_commit(&k_empty[0]);
-            }
-            for (int j = 0; j < nkb && ok && !aborted(); ++j) {
-                const bool more = j + 1 < nkb;
-                ok = mbar_wait(&v_full[j & 1], (j >> 1) & 1, p.ctl, 55) && mbar_wait(&p_ready[0], j & 1, p.ctl, 56);
-                if (!ok) break;
-                tc_fence_after();
-                pv(0, j);
-                if (more) {
-                    ok = mbar_wait(&k_full[(j + 1) & 1], ((j + 1) >> 1) & 1, p.ctl, 57);
+                for (int j = 0; j < nkb && ok && !aborted(); ++j) {
+                    const bool more = j + 1 < nkb;
+                    ok = mbar_wait(&v_full[j & 1], (j >> 1) & 1, p.ctl, 55) && mbar_wait(&p_ready[0], j & 1, p.ctl, 56);
                     if (!ok) break;
                     tc_fence_after();
-                    qk(0, j + 1);
+                    pv(0, j);
+                    if (more) {
+                        ok = mbar_wait(&k_full[(j + 1) & 1], ((j + 1) >> 1) & 1, p.ctl, 57);
+                        if (!ok) break;
+                        tc_fence_after();
+                        qk(0, j + 1);
+                    }
+                    ok = mbar_wait(&p_ready[1], j & 1, p.ctl, 58);
+                    if (!ok) break;
+                    tc_fence_after();
+                    pv(1, j);
+                    umma_commit(&v_empty[j & 1]);
+                    if (more) {
+                        qk(1, j + 1);
+                        umma_commit(&k_empty[(j + 1) & 1]);
+                    }
                 }
-                ok = mbar_wait(&p_ready[1], j & 1, p.ctl, 58);
-                if (!ok) break;
-                tc_fence_after();
-                pv(1, j);
-                umma_commit(&v_empty[j & 1]);
-                if (more) {
-                    qk(1, j + 1);
-                    umma_commit(&k_empty[(j + 1) & 1]);
-                }
+                if (!ok) fail();
+                umma_commit(drain);
+                (void)mbar_wait(drain, 0, p.ctl, 59);
             }
-            if (!ok) fail();
-            umma_commit(drain);
-            (void)mbar_wait(drain, 0, p.ctl, 59);
         }
-    } else if (warp >= 4) {
+    } else {
+        regs_inc<216>();
         // ------------------------------------------------------------ softmax / epilogue
         const int t = (warp - 4) >> 2;            // tile of this warpgroup
         const int row = threadIdx.x - 128 - t * 128;  // tile row = TMEM lane
@@ -402,9 +424,15 @@ __global__ void __launch_bounds__(kThreads, 1) global_attn_kernel(const __grid_c
                 for (int k = 0; k < 128; ++k)
                     if (k > kmax) r[k] = __float_as_uint(-INFINITY);
             }
-            float mx = __uint_as_float(r[0]);
+            // block maximum: eight independent chains of three-input maxima, then their maximum
+            float a8[8];
 #pragma unroll
-            for (int k = 1; k < 128; ++k) mx = fmaxf(mx, __uint_as_float(r[k]));
+            for (int i = 0; i < 8; ++i) a8[i] = fmaxf(__uint_as_float(r[i]), __uint_as_float(r[i + 8]));
+#pragma unroll
+            for (int k = 16; k < 128; k += 16)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) a8[i] = fmax3(a8[i], __uint_as_float(r[k + i]), __uint_as_float(r[k + 8 + i]));
+            const float mx = fmaxf(fmax3(fmax3(a8[0], a8[1], a8[2]), a8[3], a8[4]), fmax3(a8[5], a8[6], a8[7]));
             const float mb = mx * sc;
             float m_new = m_run;
             if (m_run == -INFINITY || mb > m_run + kTau) m_new = mb;

@@ -4,7 +4,7 @@ the access; an index out of range is recorded in the device error word and skipp
 
 The debug library runs in a child process (ZG_LIBRARY=debug selects it in the binding) on
 small, odd shapes through every instrumented kernel -- gated SWA and global prefill, the k_hat
-pre-pass, the decode step and its split merge (bf16 and E4M3 caches), the cache writer -- each
+pre-pass, the E4M3 global prefill and its pre-passes, the decode step and its split merge (bf16 and E4M3 caches), the cache writer -- each
 checked against the fp64 oracle with a clean error word.  Then the index check's own error
 path is exercised without a fault (zg_selftest_index_check) and the context is shown to be
 usable afterwards.  In the normal build the same self test records nothing."""
@@ -20,6 +20,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 CHILD = r'''
 import sys, torch
+import numpy as np
 sys.path.insert(0, "tests")
 import global_attention_fwd_b300 as zg
 import oracle, workloads
@@ -66,6 +67,26 @@ prefill(1, 170, 32, 2, 128, 128, 2)    # GQA 16
 prefill(1, 91, 2, 2, 128, 5, 3)        # MHA
 prefill(2, 77, 8, 2, 64, 0, 4)         # global, d = 64
 prefill(1, 130, 32, 8, 128, 0, 5)      # global, GQA 4
+
+def prefill_e4m3(B, L, Hq, Hkv, seed):  # global prefill on E4M3 inputs (k_hat and V^T pre-passes)
+    g = torch.Generator().manual_seed(seed)
+    st = {n: workloads.to_e4m3(rnd(B, L, h, 128, g=g), 1.0).view(torch.uint8) for n, h in (("q", Hq), ("k", Hkv), ("v", Hkv))}
+    deq = {n: st[n].view(torch.float8_e4m3fn).double() for n in st}
+    pos = torch.arange(L, dtype=torch.int32).repeat(B, 1).contiguous()
+    wq, wk = 0.5 + torch.rand(128, generator=g), 0.5 + torch.rand(128, generator=g)
+    out = zg.global_prefill_fp8(st["q"].cuda(), st["k"].cuda(), st["v"].cuda(), pos.cuda(), wq.cuda(), wk.cuda(),
+                                rotary_dim=42, theta=1e6)
+    torch.cuda.synchronize()
+    clean(f"e4m3 global prefill {B} {L} {Hq}/{Hkv}")
+    rows = list(range(B * L))
+    ref = oracle.prefill_rows(deq["q"], deq["k"], deq["v"], None, pos, wq, wk, window=0, rotary_dim=42, theta=1e6,
+                              eps=1e-6, rows=rows)
+    got = rows_of(out, rows)
+    err = float(np.linalg.norm(got - ref) / np.linalg.norm(ref))
+    assert err <= 0.10, err  # the E4M3 path's own bound
+
+prefill_e4m3(2, 45, 8, 2, 9)      # ragged: 45 keys, V^T padded to 48
+prefill_e4m3(1, 200, 16, 1, 10)   # GQA 16
 
 def decode(flags, B, Hq, Hkv, d, S, W, positions, seed, fp8):
     g = torch.Generator().manual_seed(seed)
