@@ -157,6 +157,8 @@ zg_status write_cache(const zg_bf16* k, const zg_bf16* v, const int32_t* pos, co
                       void* cv, int B, int L, int Hkv, int d, long long S, bool ring, int rotary_dim, double theta,
                       float eps, zg_stream stream, int fp8 = 0, float k_scale = 1.0f, float v_scale = 1.0f) {
     if (B == 0 || L == 0) return ZG_OK;
+    if (B > 65535 || static_cast<long long>(L) * Hkv >= (1ll << 31) || (ring && S >= (1ll << 31)))
+        return ZG_ERR_UNSUPPORTED;
     CacheParams c;
     std::memset(&c, 0, sizeof(c));
     if (!dev_ctl(c.ctl)) return ZG_ERR_CUDA;

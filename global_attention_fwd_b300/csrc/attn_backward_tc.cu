@@ -176,6 +176,9 @@ constexpr int kPrepRows = 4;
 
 __global__ void __launch_bounds__(256) bwd_tc_prep_kernel(const __grid_constant__ BackwardTcParams p) {
     __shared__ float buf[8][kPrepRows][D];
+    __shared__ float rope_f[2][kMaxRotHalf];  // read by lane-dependent index: staged out of the parameters
+    stage_rope(p.rope, rope_f[0], rope_f[1]);
+    __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long long nq = static_cast<long long>(p.B) * p.L * p.Hq, nk = static_cast<long long>(p.B) * p.L * p.Hkv;
     const long long row0 = (static_cast<long long>(blockIdx.x) * 8 + warp) * kPrepRows;
@@ -214,7 +217,7 @@ __global__ void __launch_bounds__(256) bwd_tc_prep_kernel(const __grid_constant_
 #pragma unroll
         for (int i = 0; i < kPrepRows; ++i) {
             float cs, sn;
-            rope_cos_sin(pos[i], p.rope.f_hi[j], p.rope.f_lo[j], cs, sn);
+            rope_cos_sin(pos[i], rope_f[0][j], rope_f[1][j], cs, sn);
             const float a = buf[warp][i][j], bb = buf[warp][i][j + p.rope.half];
             buf[warp][i][j] = a * cs - bb * sn;
             buf[warp][i][j + p.rope.half] = bb * cs + a * sn;

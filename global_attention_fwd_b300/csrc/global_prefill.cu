@@ -57,6 +57,10 @@ struct Glb {
 template <int D>
 __global__ void __launch_bounds__(256) khat_kernel(const __grid_constant__ PrefillParams p) {
     __shared__ __align__(16) float buf[8][D];
+    __shared__ float rope_f[2][kMaxRotHalf];
+    stage_rope(p.rope, rope_f[0], rope_f[1]);
+    __syncthreads();
+    constexpr int PER = D / 32;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long long row = static_cast<long long>(blockIdx.x) * 8 + warp;  // (b, j, g) flattened
     const long long nrows = static_cast<long long>(p.B) * p.L * p.Hkv;
@@ -64,11 +68,18 @@ __global__ void __launch_bounds__(256) khat_kernel(const __grid_constant__ Prefi
     const long long tok = row / p.Hkv;  // b * L + j
     if (!idx_ok(p.ctl, tok, static_cast<long long>(p.B) * p.L, 82)) return;
     const int pos = __ldg(p.pos + tok);
-    norm_rope_warp_d<D>(static_cast<const __nv_bfloat16*>(p.k_raw) + row * D, p.wk, p.eps, pos, p.rope, 1.0f,
-                        buf[warp]);
-    __half* kh = static_cast<__half*>(p.khat);
-    for (int e = 2 * lane; e < D; e += 64)
-        *reinterpret_cast<uint32_t*>(kh + row * D + e) = pack_half2(buf[warp][e], buf[warp][e + 1]);
+    const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(p.k_raw) + row * D + lane * PER;
+    float v[PER], wv[PER];
+#pragma unroll
+    for (int k = 0; k < PER; ++k) v[k] = __bfloat162float(x[k]);
+    norm_weights_lane<D>(p.wk, wv);
+    norm_rope_warp_vals<D>(v, wv, p.eps, pos, p.rope.half, rope_f[0], rope_f[1], 1.0f, buf[warp]);
+    __half* kh = static_cast<__half*>(p.khat) + row * D + lane * PER;
+    const float* y = buf[warp] + lane * PER;
+    if constexpr (PER == 4)
+        *reinterpret_cast<uint2*>(kh) = make_uint2(pack_half2(y[0], y[1]), pack_half2(y[2], y[3]));
+    else
+        *reinterpret_cast<uint32_t*>(kh) = pack_half2(y[0], y[1]);
 }
 
 // ---------------------------------------------------------------- E4M3 variant: pre-passes
@@ -133,6 +144,9 @@ __device__ __forceinline__ void qk_norm_rope_row_e4m3(uint8_t* tile, int row, co
 template <int D>
 __global__ void __launch_bounds__(256) khat_e4m3_kernel(const __grid_constant__ PrefillParams p) {
     __shared__ __align__(16) float buf[8][D];
+    __shared__ float rope_f[2][kMaxRotHalf];
+    stage_rope(p.rope, rope_f[0], rope_f[1]);
+    __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long long row = static_cast<long long>(blockIdx.x) * 8 + warp;  // (b, j, g)
     const long long nrows = static_cast<long long>(p.B) * p.L * p.Hkv;
@@ -154,7 +168,7 @@ __global__ void __launch_bounds__(256) khat_e4m3_kernel(const __grid_constant__ 
     for (int j = lane; j < p.rope.half; j += 32) {
         const float a = buf[warp][j], c = buf[warp][j + p.rope.half];
         float cs, sn;
-        rope_cos_sin(pos, p.rope.f_hi[j], p.rope.f_lo[j], cs, sn);
+        rope_cos_sin(pos, rope_f[0][j], rope_f[1][j], cs, sn);
         buf[warp][j] = a * cs - c * sn;
         buf[warp][j + p.rope.half] = c * cs + a * sn;
     }

@@ -64,7 +64,8 @@ struct Swa2 {
     static constexpr int NBAR = 4 * NQB + 5 * R + 2 * 3 + 2 + 3;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr uint32_t OFF_W = (OFF_MISC + 16 + 15) / 16 * 16;  // wq [D], wk [D] fp32
-    static constexpr uint32_t SMEM = OFF_W + 2 * D * 4;
+    static constexpr uint32_t OFF_R = OFF_W + 2 * D * 4;  // rotation frequencies: f_hi [64], f_lo [64] fp32
+    static constexpr uint32_t SMEM = OFF_R + 2 * kMaxRotHalf * 4;
     static constexpr int SCOLS = (NK + 31) / 32 * 32;  // TMEM columns of one S buffer
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr int O_COL = 2 * SCOLS;
@@ -153,6 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa2_kernel(const __grid_constant
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
     float* wq_s = reinterpret_cast<float*>(smem + C::OFF_W);
     float* wk_s = wq_s + D;
+    float* rf_s = reinterpret_cast<float*>(smem + C::OFF_R);  // [0, 64) f_hi, [64, 128) f_lo
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long long total = static_cast<long long>(p.B) * p.Hkv * p.n_ltiles;
@@ -191,6 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa2_kernel(const __grid_constant
         tmem_relinquish();
     }
     for (int e = threadIdx.x; e < 2 * D; e += kThreads) wq_s[e] = e < D ? __ldg(p.wq + e) : __ldg(p.wk + e - D);
+    stage_rope(p.rope, rf_s, rf_s + kMaxRotHalf);
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -419,9 +422,11 @@ __global__ void __launch_bounds__(kThreads, 1) swa2_kernel(const __grid_constant
             if constexpr (PRE)
                 (void)pos;
             else if constexpr (ROT > 0)
-                qk_norm_rope_row_pair_ct<D, 2 * G, ROT / 2>(qbuf0 + qb * C::QBUF, C::QCH, row, wq_s, p.eps, pos, p.rope);
+                qk_norm_rope_row_pair_ct<D, 2 * G, ROT / 2>(qbuf0 + qb * C::QBUF, C::QCH, row, wq_s, p.eps, pos, rf_s,
+                                                            rf_s + kMaxRotHalf);
             else
-                qk_norm_rope_row_pair<D, 2 * G>(qbuf0 + qb * C::QBUF, C::QCH, row, wq_s, p.eps, pos, p.rope);
+                qk_norm_rope_row_pair<D, 2 * G>(qbuf0 + qb * C::QBUF, C::QCH, row, wq_s, p.eps, pos, p.rope.half, rf_s,
+                                                rf_s + kMaxRotHalf);
             fence_async_smem();
             mbar_arrive(&q_ready[qb]);
             ++n;
@@ -455,10 +460,11 @@ __global__ void __launch_bounds__(kThreads, 1) swa2_kernel(const __grid_constant
                 if constexpr (PRE)
                     (void)pos;
                 else if constexpr (ROT > 0)
-                    qk_norm_rope_row_pair_ct<D, 2, ROT / 2>(kring, C::KCH, s * C::T + r, wk_s, p.eps, pos, p.rope,
+                    qk_norm_rope_row_pair_ct<D, 2, ROT / 2>(kring, C::KCH, s * C::T + r, wk_s, p.eps, pos, rf_s, rf_s + kMaxRotHalf,
                                                             active);
                 else
-                    qk_norm_rope_row_pair<D, 2>(kring, C::KCH, s * C::T + r, wk_s, p.eps, pos, p.rope, active);
+                    qk_norm_rope_row_pair<D, 2>(kring, C::KCH, s * C::T + r, wk_s, p.eps, pos, p.rope.half, rf_s,
+                                                    rf_s + kMaxRotHalf, active);
             }
             fence_async_smem();
             mbar_arrive(&k_ready[s]);

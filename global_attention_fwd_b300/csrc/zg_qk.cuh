@@ -178,10 +178,13 @@ __device__ __forceinline__ void qk_norm_rope_row_fast(uint8_t* base, uint32_t ch
 // lanes share one RoPE position (SL = 2 for key rows, 2G for the G query heads of a
 // token): each lane evaluates cos/sin for every SL-th frequency and they exchange them
 // with shuffles; the even lane of each row applies the rotations.  Every lane of the
-// warp must call this, with the same rc.half.  w_s: the D weights in shared memory.
+// warp must call this, with the same half.  w_s: the D weights, f_hi / f_lo: the rotation
+// frequencies, both in shared memory (read by lane-dependent index, which the kernel parameter
+// space would serve one address at a time).
 template <int D, int SL>
 __device__ __forceinline__ void qk_norm_rope_row_pair(uint8_t* base, uint32_t chunk_stride, int row, const float* w_s,
-                                                      float eps, int pos, const RopeConsts& rc, bool active = true) {
+                                                      float eps, int pos, int half, const float* f_hi,
+                                                      const float* f_lo, bool active = true) {
     constexpr int NC2 = D / 16;  // 16-byte chunks per half row
     const int lane = threadIdx.x & 31;
     const int part = lane & 1;
@@ -215,7 +218,6 @@ __device__ __forceinline__ void qk_norm_rope_row_pair(uint8_t* base, uint32_t ch
                                                        pack_half2(y2.x, y2.y), pack_half2(y3.x, y3.y));
     }
     __syncwarp();  // the odd lane's half is in shared memory before the even lane rotates
-    const int half = rc.half;
     const int mine = lane & (SL - 1);
     const int grp = lane & ~(SL - 1);
     constexpr int NI = (kMaxRotHalf + SL - 1) / SL;
@@ -224,7 +226,7 @@ __device__ __forceinline__ void qk_norm_rope_row_pair(uint8_t* base, uint32_t ch
         if (i * SL >= half) break;  // uniform over the warp
         const int jm = i * SL + mine;
         float cs = 1.f, sn = 0.f;
-        if (jm < half) rope_cos_sin(pos, rc.f_hi[jm], rc.f_lo[jm], cs, sn);
+        if (jm < half) rope_cos_sin(pos, f_hi[jm], f_lo[jm], cs, sn);
 #pragma unroll
         for (int h = 0; h < SL; ++h) {
             const float c2 = __shfl_sync(0xffffffffu, cs, grp | h);
@@ -246,8 +248,8 @@ __device__ __forceinline__ void qk_norm_rope_row_pair(uint8_t* base, uint32_t ch
 // them there, so no per-element shared-memory round trip is needed.
 template <int D, int SL, int HALF>
 __device__ __forceinline__ void qk_norm_rope_row_pair_ct(uint8_t* base, uint32_t chunk_stride, int row,
-                                                         const float* w_s, float eps, int pos, const RopeConsts& rc,
-                                                         bool active = true) {
+                                                         const float* w_s, float eps, int pos, const float* f_hi,
+                                                         const float* f_lo, bool active = true) {
     constexpr int NC2 = D / 16;
     constexpr int NR = (2 * HALF + 7) / 8;  // chunks holding rotated dims
     static_assert(NR <= NC2, "rotated dims must lie in the first half row");
@@ -299,7 +301,7 @@ __device__ __forceinline__ void qk_norm_rope_row_pair_ct(uint8_t* base, uint32_t
         const int jm = i * SL + mine;
         cj[i] = 1.f;
         sj[i] = 0.f;
-        if (jm < HALF) rope_cos_sin(pos, rc.f_hi[jm], rc.f_lo[jm], cj[i], sj[i]);
+        if (jm < HALF) rope_cos_sin(pos, f_hi[jm], f_lo[jm], cj[i], sj[i]);
     }
 #pragma unroll
     for (int j = 0; j < HALF; ++j) {
@@ -318,38 +320,69 @@ __device__ __forceinline__ void qk_norm_rope_row_pair_ct(uint8_t* base, uint32_t
     }
 }
 
-// RMSNorm + partial RoPE of one D-element head vector with one warp (x: bf16, global memory);
-// the result times `scale` goes to dst[D] (fp32, shared memory).  The decode step and the cache
-// writer both use it, so a key cached by a prefill and one cached by a decode step agree bit for bit.
+// RMSNorm + partial RoPE of one D-element head vector with one warp; lane l holds elements
+// l*D/32 .. l*D/32 + D/32 - 1 in v (fp32); the result times `scale` goes to dst[D] (fp32, shared
+// memory).  The decode step and the cache writer both use it, so a key cached by a prefill and
+// one cached by a decode step agree bit for bit.
+// The rotation frequencies come as pointers (f_hi[j], f_lo[j], j < half): a kernel that runs this
+// for many rows stages them in shared memory, because lane j reading element j straight from the
+// kernel parameters is a divergent constant-bank access, served one address at a time.
 template <int D>
-__device__ __forceinline__ void norm_rope_warp_d(const __nv_bfloat16* x, const float* w, float eps, int pos,
-                                                 const RopeConsts& rc, float scale, float* dst) {
+__device__ __forceinline__ void norm_rope_warp_vals(const float (&v)[D / 32], const float (&wv)[D / 32], float eps,
+                                                    int pos, int half, const float* f_hi, const float* f_lo,
+                                                    float scale, float* dst) {
     constexpr int PER = D / 32;
+    static_assert(PER == 2 || PER == 4, "head sizes 64 and 128");
     const int lane = threadIdx.x & 31;
-    float v[PER];
     float ss = 0.f;
 #pragma unroll
-    for (int k = 0; k < PER; ++k) {
-        v[k] = __bfloat162float(x[lane * PER + k]);
-        ss = fmaf(v[k], v[k], ss);
-    }
+    for (int k = 0; k < PER; ++k) ss = fmaf(v[k], v[k], ss);
 #pragma unroll
     for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
     const float inv = ss > 0.f || eps > 0.f ? rsqrtf(ss * (1.0f / D) + eps) : 0.f;
+    float o4[PER];
 #pragma unroll
-    for (int k = 0; k < PER; ++k) dst[lane * PER + k] = v[k] * inv * __ldg(w + lane * PER + k);
+    for (int k = 0; k < PER; ++k) o4[k] = v[k] * inv * wv[k];
+    if constexpr (PER == 4)  // one vector store per lane: no bank conflicts
+        *reinterpret_cast<float4*>(dst + lane * 4) = make_float4(o4[0], o4[1], o4[2], o4[3]);
+    else
+        *reinterpret_cast<float2*>(dst + lane * 2) = make_float2(o4[0], o4[1]);
     __syncwarp();
-    for (int j = lane; j < rc.half; j += 32) {
-        const float a = dst[j], b = dst[j + rc.half];
+    for (int j = lane; j < half; j += 32) {
+        const float a = dst[j], b = dst[j + half];
         float cs, sn;
-        rope_cos_sin(pos, rc.f_hi[j], rc.f_lo[j], cs, sn);
+        rope_cos_sin(pos, f_hi[j], f_lo[j], cs, sn);
         dst[j] = a * cs - b * sn;
-        dst[j + rc.half] = b * cs + a * sn;
+        dst[j + half] = b * cs + a * sn;
     }
     __syncwarp();
     if (scale != 1.0f)
         for (int e = lane; e < D; e += 32) dst[e] *= scale;
     __syncwarp();
+}
+// Copy the rotation frequencies of a launch into shared memory; every thread of the block calls
+// it, and a __syncthreads() follows before they are read.
+__device__ __forceinline__ void stage_rope(const RopeConsts& rc, float* s_hi, float* s_lo) {
+    for (int j = threadIdx.x; j < rc.half; j += blockDim.x) {
+        s_hi[j] = rc.f_hi[j];
+        s_lo[j] = rc.f_lo[j];
+    }
+}
+// the weights of lane l's elements, for norm_rope_warp_vals
+template <int D>
+__device__ __forceinline__ void norm_weights_lane(const float* w, float (&wv)[D / 32]) {
+#pragma unroll
+    for (int k = 0; k < D / 32; ++k) wv[k] = __ldg(w + (threadIdx.x & 31) * (D / 32) + k);
+}
+// the same with x (bf16) read from global memory
+template <int D>
+__device__ __forceinline__ void norm_rope_warp_d(const __nv_bfloat16* x, const float* w, float eps, int pos,
+                                                 const RopeConsts& rc, float scale, float* dst) {
+    float v[D / 32], wv[D / 32];
+#pragma unroll
+    for (int k = 0; k < D / 32; ++k) v[k] = __bfloat162float(x[(threadIdx.x & 31) * (D / 32) + k]);
+    norm_weights_lane<D>(w, wv);
+    norm_rope_warp_vals<D>(v, wv, eps, pos, rc.half, rc.f_hi, rc.f_lo, scale, dst);
 }
 
 // RMSNorm + partial RoPE of one 128-element head vector with one warp; x is bf16 in global memory.

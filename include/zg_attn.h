@@ -126,8 +126,9 @@ zg_status zg_global_prefill(const zg_bf16 *q, const zg_bf16 *k, const zg_bf16 *v
  *   consecutive positions do).  Other slots are left untouched.
  * zg_global_prefill_with_cache: k_cache, v_cache are one global layer's caches
  *   [B, Hkv, S_max, d] bf16; every token goes to slot pos[b,i], 0 <= pos < S_max.
- * Head sizes d = 64 and 128 (those of the decode step) are supported:
- * ZG_ERR_UNSUPPORTED otherwise.  The cache pointers must be 16-byte aligned and are written in place.
+ * Head sizes d = 64 and 128 (those of the decode step) are supported, with B <= 65535,
+ * L * Hkv < 2^31 and ring_slots < 2^31: ZG_ERR_UNSUPPORTED otherwise.  The cache pointers
+ * must be 16-byte aligned and are written in place.
  * A token whose position has no slot (negative, or >= S_max for a global cache) is
  * skipped and recorded on the device: zg_device_status() then returns
  * ZG_ERR_POSITION.  The pages define no interface; these calls follow the cache
