@@ -472,7 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1) global_attn_kernel(const __grid_c
             l_run *= corr;
             m_run = m_new;
             const float2 sc2 = make_float2(sc, sc), nm2 = make_float2(-m_run, -m_run);
-            float2 l2 = make_float2(0.f, 0.f);
+            float2 l2 = make_float2(0.f, 0.f), l3 = make_float2(0.f, 0.f);
 #pragma unroll
             for (int cb = 0; cb < 128; cb += 32) {
                 if constexpr (F8) {
@@ -500,12 +500,15 @@ __global__ void __launch_bounds__(kThreads, 1) global_attn_kernel(const __grid_c
                     for (int k = 0; k < 32; k += 2) {
                         const float2 x = fma2(make_float2(__uint_as_float(r[cb + k]), __uint_as_float(r[cb + k + 1])), sc2, nm2);
                         pk[k / 2] = pack_bf16x2(ex2_approx(x.x), ex2_approx(x.y));
-                        l2 = add2(l2, bf2f2(pk[k / 2]));
+                        if (k & 2)
+                            acc_bf16x2(pk[k / 2], l3.x, l3.y);
+                        else
+                            acc_bf16x2(pk[k / 2], l2.x, l2.y);
                     }
                     tmem_st16(s_addr + cb / 2, pk);  // P over S (these columns are already in registers)
                 }
             }
-            l_run += l2.x + l2.y;
+            l_run += (l2.x + l2.y) + (l3.x + l3.y);
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(&p_ready[t]);

@@ -543,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa2_kernel(const __grid_constant
                 mb = (m == -INFINITY ? 0.f : m) * p.scale_log2;
             }
             const float2 nm2 = make_float2(-mb, -mb);
-            float2 lacc = make_float2(0.f, 0.f);
+            float2 lacc = make_float2(0.f, 0.f), lacc2 = make_float2(0.f, 0.f);
             auto soft16 = [&](const uint32_t* r, int cb) {
                 uint32_t pk[8];
                 if (cb >= kr_lo && cb + 15 <= kr_hi) {
@@ -564,7 +564,10 @@ __global__ void __launch_bounds__(kThreads, 1) swa2_kernel(const __grid_constant
                 }
                 // row sums of the very bf16 P the PV product uses
 #pragma unroll
-                for (int k = 0; k < 8; ++k) lacc = add2(lacc, bf2f2(pk[k]));
+                for (int k = 0; k < 8; k += 2) {
+                    acc_bf16x2(pk[k], lacc.x, lacc.y);
+                    acc_bf16x2(pk[k + 1], lacc2.x, lacc2.y);
+                }
                 // P (keys cb..cb+15) -> TMEM columns cb/2 .. cb/2+7 of this S buffer (already read)
                 tmem_st8(s_addr + cb / 2, pk);
             };
@@ -583,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa2_kernel(const __grid_constant
             }
             {
                 uint32_t lv[8];
-                const float lsum = lacc.x + lacc.y;
+                const float lsum = (lacc.x + lacc.y) + (lacc2.x + lacc2.y);
 #pragma unroll
                 for (int k = 0; k < 8; ++k) lv[k] = __float_as_uint(lsum);
                 // l for the epilogue, four tiles deep: slot n & 3 is rewritten only by the

@@ -318,6 +318,13 @@ __device__ __forceinline__ float2 add2(float2 a, float2 b) {
     asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2_bits(a)), "l"(f2_bits(b)));
     return bits_f2(d);
 }
+// a += lo(u), b += hi(u) for a bf16 pair u, exactly (mixed-precision FMA: bf16 x bf16(1) + fp32)
+__device__ __forceinline__ void acc_bf16x2(uint32_t u, float& a, float& b) {
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, lo, %3, %0;\n\tfma.rn.f32.bf16 %1, hi, %3, %1;\n\t}"
+        : "+f"(a), "+f"(b)
+        : "r"(u), "h"(static_cast<unsigned short>(0x3F80)));
+}
 __device__ __forceinline__ float2 bf2f2(uint32_t u) { return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u)); }
 
 __device__ __forceinline__ float rcp_approx(float x) {  // hardware reciprocal
