@@ -592,8 +592,11 @@ zg_status zg_attention_backward(const zg_bf16* q, const zg_bf16* k, const zg_bf1
     const size_t need = backward_workspace_bytes(B, L, Hq, Hkv);
     if (!workspace || workspace_bytes < need || !aligned16(workspace)) return ZG_ERR_WORKSPACE;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const bool tc = backward_tc_supports(d, Hq, Hkv, window) && Hkv <= 65535 &&
-                    static_cast<long long>(B) * Hkv * ((L + 31) / 32) < (1ll << 31);
+    // the global layer (every earlier key, no gate) on the tensor cores too
+    const bool global_tc = !gated && (window <= 0 || window >= L) && backward_tc_global_supports(d, Hq, Hkv);
+    const bool tc = (backward_tc_supports(d, Hq, Hkv, window) || global_tc) && Hkv <= 65535 &&
+                    static_cast<long long>(B) * Hkv * ((L + 31) / 32) < (1ll << 31) &&
+                    static_cast<long long>(B) * L * (Hq + Hkv) < (1ll << 31);
     if (tc) {
         // tensor-core path (the ZGCM-1 local-layer shape)
         BackwardTcParams t;
@@ -631,7 +634,8 @@ zg_status zg_attention_backward(const zg_bf16* q, const zg_bf16* k, const zg_bf1
         t.L = L;
         t.Hq = Hq;
         t.Hkv = Hkv;
-        t.window = window;
+        t.global = global_tc ? 1 : 0;
+        t.window = global_tc ? L : window;
         t.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
         t.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
         t.eps = eps;

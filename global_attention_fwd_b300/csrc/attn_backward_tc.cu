@@ -180,27 +180,29 @@ __global__ void __launch_bounds__(256) bwd_tc_prep_kernel(const __grid_constant_
     stage_rope(p.rope, rope_f[0], rope_f[1]);
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const long long nq = static_cast<long long>(p.B) * p.L * p.Hq, nk = static_cast<long long>(p.B) * p.L * p.Hkv;
-    const long long row0 = (static_cast<long long>(blockIdx.x) * 8 + warp) * kPrepRows;
+    // row indices in 32-bit arithmetic: the host takes this path only for B * L * (Hq + Hkv) < 2^31
+    const unsigned nq = static_cast<unsigned>(p.B * p.L) * p.Hq, nk = static_cast<unsigned>(p.B * p.L) * p.Hkv;
+    const unsigned row0 = (blockIdx.x * 8u + warp) * kPrepRows;
     const bool gated = p.gate != nullptr;
     uint2 xr[kPrepRows], gr[kPrepRows], dr[kPrepRows];
     int pos[kPrepRows];
 #pragma unroll
     for (int i = 0; i < kPrepRows; ++i) {
-        const long long row = row0 + i;
+        const unsigned row = row0 + i;
         const bool is_q = row < nq;
-        const long long r = is_q ? row : row - nq;
+        const unsigned r = is_q ? row : row - nq;
         const bool valid = row < nq + nk;
-        xr[i] = valid ? *reinterpret_cast<const uint2*>((is_q ? p.q : p.k) + r * D + lane * 4) : make_uint2(0u, 0u);
-        pos[i] = valid ? __ldg(p.pos + r / (is_q ? p.Hq : p.Hkv)) : 0;
+        xr[i] = valid ? *reinterpret_cast<const uint2*>((is_q ? p.q : p.k) + static_cast<size_t>(r) * D + lane * 4)
+                      : make_uint2(0u, 0u);
+        pos[i] = valid ? __ldg(p.pos + r / static_cast<unsigned>(is_q ? p.Hq : p.Hkv)) : 0;
         if (valid && is_q && gated) {
-            gr[i] = *reinterpret_cast<const uint2*>(p.gate + r * D + lane * 4);
-            dr[i] = *reinterpret_cast<const uint2*>(p.dout + r * D + lane * 4);
+            gr[i] = *reinterpret_cast<const uint2*>(p.gate + static_cast<size_t>(r) * D + lane * 4);
+            dr[i] = *reinterpret_cast<const uint2*>(p.dout + static_cast<size_t>(r) * D + lane * 4);
         }
     }
 #pragma unroll
     for (int i = 0; i < kPrepRows; ++i) {
-        const long long row = row0 + i;
+        const unsigned row = row0 + i;
         const bool is_q = row < nq;
         const float4 w = __ldg(reinterpret_cast<const float4*>((is_q ? p.wq : p.wk) + lane * 4));
         const float v0 = bf16lo(xr[i].x), v1 = bf16hi(xr[i].x), v2 = bf16lo(xr[i].y), v3 = bf16hi(xr[i].y);
@@ -226,10 +228,10 @@ __global__ void __launch_bounds__(256) bwd_tc_prep_kernel(const __grid_constant_
     __syncwarp();
 #pragma unroll
     for (int i = 0; i < kPrepRows; ++i) {
-        const long long row = row0 + i;
+        const unsigned row = row0 + i;
         if (row >= nq + nk) break;
         const bool is_q = row < nq;
-        const long long r = is_q ? row : row - nq;
+        const size_t r = is_q ? row : row - nq;
         const float4 v = *reinterpret_cast<const float4*>(&buf[warp][i][lane * 4]);
         *reinterpret_cast<uint2*>((is_q ? p.qh : p.kh) + r * D + lane * 4) =
             make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
@@ -912,11 +914,316 @@ __global__ void __launch_bounds__(kKThreads, 1) bwd_kpass_kernel(const __grid_co
     if (warp == 8) tmem_dealloc(tbase, 512);
 }
 
+// ---------------------------------------------------------------- global layer: query pass
+// The global layer (every earlier key, no gate): the query tile of 32 tokens x 4 heads sees
+// the keys [0, t0 + 32), in blocks of 128, so its row statistics need every block first.
+//   loop 1, per block: S = Q_hat K_hat^T and dP = dA V^T into TMEM; each row keeps, per column
+//     half, a running maximum m (log2-scaled scores), l = sum of 2^(s c log2e - m) and
+//     D' = sum of the same weights times dP, rescaled when m moves; the halves merge into
+//     (m, 1 / l, D = D' / l) with D = rowsum(P dP) = rowsum(dA A), which go to the workspace in
+//     the windowed pass's format, for the key pass (run with window = L).
+//   loop 2, per block: S and dP again, P from the statistics, dS = P (dP - D) packed bf16 over
+//     dP, dQ_hat += dS K_hat in TMEM.
+//   dQ_hat then goes back through RoPE and RMSNorm into dq (fp32), as in the windowed pass.
+// Warps 0-7: rows (thread = row = TMEM lane; warp w has the lane quarter w & 3 and the column
+// half w >> 2 of every key block); warp 8: TMA (one thread); warp 9: MMA (one thread), TMEM.
+constexpr int kGThreads = 320;
+constexpr uint32_t GQ_Q = 0;                        // Q_hat tile
+constexpr uint32_t GQ_DA = GQ_Q + TILE128;          // dA tile
+constexpr uint32_t GQ_RING = GQ_DA + TILE128;       // 2 stages x (K_hat block, V block)
+constexpr uint32_t GQ_XCH = GQ_RING + 4 * TILE128;  // [2 halves][128 rows] float4 (m, l, D', 0)
+constexpr uint32_t GQ_W = GQ_XCH + 2 * 128 * 16;    // wq [D]
+constexpr uint32_t GQ_BAR = GQ_W + D * 4;
+constexpr uint32_t GQ_MISC = GQ_BAR + 16 * 8;
+constexpr uint32_t GQ_SMEM = GQ_MISC + 32;
+constexpr uint32_t GQ_DQ = GQ_RING;                 // dq staging (four fp32 boxes), ring free at the end
+constexpr uint32_t GQ_X = GQ_RING + 2 * TILE128;    // raw q tile, loaded into the free ring at the end
+static_assert(GQ_DQ + F32TILE <= GQ_X && GQ_X + TILE128 <= GQ_XCH, "staging inside the ring");
+static_assert(GQ_RING % 1024 == 0 && GQ_X % 1024 == 0, "swizzle atoms");
+static_assert(GQ_SMEM <= 227 * 1024, "shared memory");
+
+__global__ void __launch_bounds__(kGThreads, 1) bwd_qpass_global_kernel(const __grid_constant__ BackwardTcParams p) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + GQ_BAR);
+    uint64_t* q_full = bar + 0;
+    uint64_t* kv_full = bar + 1;   // [2]
+    uint64_t* kv_empty = bar + 3;  // [2]
+    uint64_t* s_full = bar + 5;
+    uint64_t* s_free = bar + 6;    // loop 1: the rows have S and dP in registers (256 arrivals)
+    uint64_t* ds_ready = bar + 7;  // loop 2: dS is in TMEM (256 arrivals)
+    uint64_t* dq_full = bar + 8;
+    uint64_t* x_full = bar + 9;
+    uint64_t* st_xch = bar + 10;   // both halves' statistics are in shared memory (256 arrivals)
+    uint64_t* dq_stg = bar + 11;   // dq staging written (128 arrivals)
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + GQ_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + GQ_MISC + 4);
+    float* w_s = reinterpret_cast<float*>(smem + GQ_W);
+    float4* xch = reinterpret_cast<float4*>(smem + GQ_XCH);
+    constexpr uint32_t C_S = 0, C_DP = 128, C_DQ = 256;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nbg = p.B * p.Hkv;
+    const int n_qt = (p.L + T - 1) / T;
+    const int t0 = (n_qt - 1 - static_cast<int>(blockIdx.x / nbg)) * T;  // heaviest (most key blocks) first
+    const int g = static_cast<int>(blockIdx.x % nbg) % p.Hkv;
+    const int b = static_cast<int>(blockIdx.x % nbg) / p.Hkv;
+    const int nblk = (t0 + T + BK - 1) / BK;  // key blocks [0, nblk), each visited by both loops
+
+    if (threadIdx.x == 0) {
+        *abort_flag = (smem_u32(smem) & 1023u) == 0 ? 0 : 1;
+        if (*abort_flag) report(p.ctl, 130, kErrAlign);
+        mbar_init(q_full, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&kv_full[i], 1);
+            mbar_init(&kv_empty[i], 1);
+        }
+        mbar_init(s_full, 1);
+        mbar_init(s_free, 256);
+        mbar_init(ds_ready, 256);
+        mbar_init(dq_full, 1);
+        mbar_init(x_full, 1);
+        mbar_init(st_xch, 256);
+        mbar_init(dq_stg, 128);
+        fence_barrier_init();
+    }
+    if (threadIdx.x < 32)
+        *reinterpret_cast<float4*>(w_s + lane * 4) = __ldg(reinterpret_cast<const float4*>(p.wq + lane * 4));
+    if (warp == 9) {
+        tmem_alloc(tslot, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tslot;
+    const uint32_t sbase = smem_u32(smem);
+    auto aborted = [&]() { return *abort_flag != 0; };
+    auto fail = [&]() { *abort_flag = 1; };
+
+    if (warp == 8) {
+        // ------------------------------------------------------------ TMA
+        if (lane == 0 && !aborted()) {
+            tma_prefetch_desc(&p.tm_qh);
+            tma_prefetch_desc(&p.tm_da);
+            tma_prefetch_desc(&p.tm_kk);
+            tma_prefetch_desc(&p.tm_vk);
+            tma_prefetch_desc(&p.tm_q);
+            mbar_arrive_expect_tx(q_full, 2 * TILE128);
+            for (int ch = 0; ch < 2; ++ch) {
+                tma_load_4d(smem + GQ_Q + ch * CH128, &p.tm_qh, q_full, ch * 64, g * G, t0, b);
+                tma_load_4d(smem + GQ_DA + ch * CH128, &p.tm_da, q_full, ch * 64, g * G, t0, b);
+            }
+            bool ok = true;
+            for (int n = 0; n < 2 * nblk && ok && !aborted(); ++n) {  // loop 1 then loop 2: blocks n mod nblk
+                const int st = n & 1, j = n % nblk;
+                ok = mbar_wait(&kv_empty[st], ((n >> 1) & 1) ^ 1, p.ctl, 131);
+                if (!ok) break;
+                uint8_t* dst = smem + GQ_RING + st * 2 * TILE128;
+                mbar_arrive_expect_tx(&kv_full[st], 2 * TILE128);
+                for (int ch = 0; ch < 2; ++ch) {
+                    tma_load_4d(dst + ch * CH128, &p.tm_kk, &kv_full[st], ch * 64, g, j * BK, b);
+                    tma_load_4d(dst + TILE128 + ch * CH128, &p.tm_vk, &kv_full[st], ch * 64, g, j * BK, b);
+                }
+            }
+            // the raw q rows for the RMSNorm backward, into the ring once every product is done
+            if (ok) ok = mbar_wait(dq_full, 0, p.ctl, 132);
+            if (ok) {
+                mbar_arrive_expect_tx(x_full, TILE128);
+                for (int ch = 0; ch < 2; ++ch)
+                    tma_load_4d(smem + GQ_X + ch * CH128, &p.tm_q, x_full, ch * 64, g * G, t0, b);
+            }
+            if (!ok) fail();
+        }
+    } else if (warp == 9) {
+        // ------------------------------------------------------------ MMA
+        if (lane == 0 && !aborted()) {
+            constexpr uint32_t id_s = idesc_bf16_f32(128, BK, false, false);  // S, dP: both operands K-major
+            constexpr uint32_t id_o = idesc_bf16_f32(128, D, false, true);    // dQ: K_hat block MN-major
+            bool ok = mbar_wait(q_full, 0, p.ctl, 133);
+            for (int n = 0; n < 2 * nblk && ok && !aborted(); ++n) {
+                const int st = n & 1;
+                const uint32_t kofs = GQ_RING + st * 2 * TILE128, vofs = kofs + TILE128;
+                ok = mbar_wait(&kv_full[st], (n >> 1) & 1, p.ctl, 134);
+                // loop 1 (and the first block of loop 2): S and dP of the previous block must be read;
+                // later in loop 2 the rows' dS hand-off below already implies it
+                if (ok && n > 0 && n <= nblk) ok = mbar_wait(s_free, (n - 1) & 1, p.ctl, 135);
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t co = (ks >> 2) * CH128 + (ks & 3) * 32;
+                    umma_bf16(tbase + C_S, sdesc(sbase + GQ_Q + co, 16, 1024, kSw128),
+                              sdesc(sbase + kofs + co, 16, 1024, kSw128), id_s, ks > 0);
+                }
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t co = (ks >> 2) * CH128 + (ks & 3) * 32;
+                    umma_bf16(tbase + C_DP, sdesc(sbase + GQ_DA + co, 16, 1024, kSw128),
+                              sdesc(sbase + vofs + co, 16, 1024, kSw128), id_s, ks > 0);
+                }
+                umma_commit(s_full);
+                if (n < nblk) {
+                    umma_commit(&kv_empty[st]);
+                    continue;
+                }
+                ok = mbar_wait(ds_ready, (n - nblk) & 1, p.ctl, 136);
+                if (!ok) break;
+                tc_fence_after();
+                // dQ_hat += dS K_hat: dS packed bf16, half h's 64 keys in the first 32 columns of its
+                // own 64-column part of the dP region
+#pragma unroll
+                for (int ks = 0; ks < BK / 16; ++ks)
+                    umma_tmem_a(tbase + C_DQ, tbase + C_DP + 64 * (ks >> 2) + 8 * (ks & 3),
+                                sdesc(sbase + kofs + ks * 16 * 128, CH128, 1024, kSw128), id_o,
+                                (n > nblk || ks > 0) ? 1u : 0u);
+                umma_commit(&kv_empty[st]);
+            }
+            umma_commit(dq_full);
+            if (!ok) fail();
+        }
+    } else {
+        // ------------------------------------------------------------ rows
+        const int q4 = warp & 3, hf = warp >> 2;
+        const int row = q4 * 32 + lane;
+        const uint32_t lane_addr = tbase + (static_cast<uint32_t>(q4 * 32) << 16);
+        const int t = t0 + row / G;
+        const bool valid_row = t < p.L;
+        const float sl = p.scale_log2;
+        float m = -INFINITY, l = 0.f, dsum = 0.f;  // this half's running max, weight sum, D'
+        bool ok = true;
+        auto load_block = [&](uint32_t (&s)[64], uint32_t (&dp)[64]) {
+            tmem_ld32(lane_addr + C_S + 64 * hf, s);
+            tmem_ld32(lane_addr + C_S + 64 * hf + 32, s + 32);
+            tmem_ld32(lane_addr + C_DP + 64 * hf, dp);
+            tmem_ld32(lane_addr + C_DP + 64 * hf + 32, dp + 32);
+            tmem_wait_ld();
+        };
+        for (int n = 0; n < nblk && ok; ++n) {
+            if (aborted() || !__all_sync(0xffffffffu, mbar_wait(s_full, n & 1, p.ctl, 137))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t s[64], dp[64];
+            load_block(s, dp);
+            tc_fence_before();
+            mbar_arrive(s_free);
+            const int kmax = t - (n * BK + 64 * hf);  // columns c <= kmax hold keys <= t
+            float bm = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 64; ++c)
+                if (c <= kmax) bm = fmaxf(bm, __uint_as_float(s[c]));
+            const float m_new = fmaxf(m, bm * sl);
+            if (m_new != -INFINITY) {
+                const float corr = ex2_approx(m - m_new);  // 0 while m is still -inf
+                float ls = 0.f, dl = 0.f;
+#pragma unroll
+                for (int c = 0; c < 64; ++c) {
+                    const float e = c <= kmax ? ex2_approx(fmaf(__uint_as_float(s[c]), sl, -m_new)) : 0.f;
+                    ls += e;
+                    dl = fmaf(e, __uint_as_float(dp[c]), dl);
+                }
+                l = fmaf(l, corr, ls);
+                dsum = fmaf(dsum, corr, dl);
+                m = m_new;
+            }
+        }
+        // merge the two column halves of every row
+        xch[hf * 128 + row] = make_float4(m, l, dsum, 0.f);
+        mbar_arrive(st_xch);
+        if (ok && !aborted()) ok = __all_sync(0xffffffffu, mbar_wait(st_xch, 0, p.ctl, 138));
+        const float4 o = xch[(1 - hf) * 128 + row];
+        float mm = fmaxf(m, o.x), lt = 0.f, dt = 0.f;
+        if (mm != -INFINITY) {
+            const float c0 = ex2_approx(m - mm), c1 = ex2_approx(o.x - mm);
+            lt = l * c0 + o.y * c1;
+            dt = dsum * c0 + o.z * c1;
+        } else {
+            mm = 0.f;
+        }
+        const float inv_l = lt > 0.f ? 1.0f / lt : 0.f;
+        const float dd = dt * inv_l;
+        if (hf == 0 && valid_row && ok)
+            p.stat[(static_cast<long long>(b) * p.L + t) * p.Hq + g * G + row % G] = make_float4(mm, inv_l, dd, 0.f);
+        for (int n = 0; n < nblk && ok; ++n) {
+            if (aborted() || !__all_sync(0xffffffffu, mbar_wait(s_full, (nblk + n) & 1, p.ctl, 139))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t s[64], dp[64];
+            load_block(s, dp);
+            const int kmax = t - (n * BK + 64 * hf);
+            uint32_t pk[32];
+#pragma unroll
+            for (int c = 0; c < 64; c += 2) {
+                float ds2[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const float pr = c + e <= kmax
+                                         ? ex2_approx(fmaf(__uint_as_float(s[c + e]), sl, -mm)) * inv_l
+                                         : 0.f;
+                    ds2[e] = pr * (__uint_as_float(dp[c + e]) - dd);
+                }
+                pk[c / 2] = pack_bf16x2(ds2[0], ds2[1]);
+            }
+            tmem_st16(lane_addr + C_DP + 64 * hf, pk);  // dS over dP (this half's columns, already read)
+            tmem_st16(lane_addr + C_DP + 64 * hf + 16, pk + 16);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(ds_ready);
+        }
+        if (!ok) fail();
+        if (hf == 0) {
+            // ---- epilogue (warps 0-3, thread = row): dQ_hat back through RoPE and RMSNorm into dq
+            if (ok && !aborted()) ok = __all_sync(0xffffffffu, mbar_wait(dq_full, 0, p.ctl, 140));
+            uint8_t* dq_t = smem + GQ_DQ;
+            if (ok) {
+                tc_fence_after();
+                tmem_row_to_tile(lane_addr + C_DQ, dq_t, row, p.scale);
+                if (!aborted()) ok = __all_sync(0xffffffffu, mbar_wait(x_full, 0, p.ctl, 141));
+            }
+            if (ok) {
+                if (valid_row) {
+                    const int pos = __ldg(p.pos + static_cast<long long>(b) * p.L + t);
+                    row_norm_rope_bwd(dq_t, row, smem + GQ_X, w_s, p.eps, p.rope.half, [&](int j) {
+                        float cs, sn;
+                        rope_cos_sin(pos, p.rope.f_hi[j], p.rope.f_lo[j], cs, sn);
+                        return make_float2(cs, sn);
+                    });
+                }
+                fence_async_smem();
+            }
+            mbar_arrive(dq_stg);
+            if (row == 0 && ok) {
+                if (mbar_wait(dq_stg, 0, p.ctl, 142)) {
+                    for (int k = 0; k < 4; ++k) tma_store_4d(&p.tm_dqf, dq_t + k * F32BOX, 32 * k, g * G, t0, b);
+                    bulk_commit();
+                    bulk_wait_all();
+                } else {
+                    ok = false;
+                }
+            }
+            if (!ok) fail();
+        }
+    }
+    __syncthreads();
+    if (aborted() && threadIdx.x == 0) {
+        const long long c0 = clock64();
+        while (clock64() - c0 < 4000000ll) {
+        }
+    }
+    tc_fence_after();
+    __syncthreads();
+    if (warp == 9) tmem_dealloc(tbase, 512);
+}
+
 }  // namespace
 
 bool backward_tc_supports(int d, int Hq, int Hkv, int window) {
     return d == D && Hkv > 0 && Hq == G * Hkv && window >= 1 && window <= 128;
 }
+bool backward_tc_global_supports(int d, int Hq, int Hkv) { return d == D && Hkv > 0 && Hq == G * Hkv; }
 
 size_t backward_tc_workspace_bytes(int B, int L, int Hq, int Hkv) {
     const size_t rq = static_cast<size_t>(B) * L * Hq, rk = static_cast<size_t>(B) * L * Hkv;
@@ -926,15 +1233,22 @@ size_t backward_tc_workspace_bytes(int B, int L, int Hq, int Hkv) {
 cudaError_t launch_backward_tc(const BackwardTcParams& p, cudaStream_t s) {
     const long long nq = static_cast<long long>(p.B) * p.L * p.Hq, nk = static_cast<long long>(p.B) * p.L * p.Hkv;
     if (nq == 0) return cudaSuccess;
+    if (nq + nk >= (1ll << 31)) return cudaErrorInvalidValue;  // the prep kernel indexes rows in 32 bits
     bwd_tc_prep_kernel<<<static_cast<unsigned>((nq + nk + 8 * kPrepRows - 1) / (8 * kPrepRows)), 256, 0, s>>>(p);
     cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(bwd_qpass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, QP_SMEM);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(bwd_kpass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, KP_SMEM);
     if (e != cudaSuccess) return e;
     const long long nbg = static_cast<long long>(p.B) * p.Hkv;
-    bwd_qpass_kernel<<<static_cast<unsigned>(nbg * ((p.L + T - 1) / T)), kQThreads, QP_SMEM, s>>>(p);
+    if (p.global) {  // every earlier key: statistics over all key blocks, then dq; the key pass with window = L
+        e = cudaFuncSetAttribute(bwd_qpass_global_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, GQ_SMEM);
+        if (e != cudaSuccess) return e;
+        bwd_qpass_global_kernel<<<static_cast<unsigned>(nbg * ((p.L + T - 1) / T)), kGThreads, GQ_SMEM, s>>>(p);
+    } else {
+        e = cudaFuncSetAttribute(bwd_qpass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, QP_SMEM);
+        if (e != cudaSuccess) return e;
+        bwd_qpass_kernel<<<static_cast<unsigned>(nbg * ((p.L + T - 1) / T)), kQThreads, QP_SMEM, s>>>(p);
+    }
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     bwd_kpass_kernel<<<static_cast<unsigned>(nbg * ((p.L + BK - 1) / BK)), kKThreads, KP_SMEM, s>>>(p);

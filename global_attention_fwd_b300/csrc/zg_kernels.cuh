@@ -176,11 +176,13 @@ struct BackwardTcParams {
     __nv_bfloat16* da;   // workspace: dA [B, L, Hq, d] (gated layers; dout itself otherwise)
     float4* stat;        // workspace: per query row (max of the log2-scaled scores, 1 / row sum, D, 0)
     int B, L, Hq, Hkv, window;
+    int global;  // 1: the global layer (every earlier key, no gate; window = L)
     float scale, scale_log2, eps;
     RopeConsts rope;
     DevCtl ctl;
 };
 bool backward_tc_supports(int d, int Hq, int Hkv, int window);
+bool backward_tc_global_supports(int d, int Hq, int Hkv);
 size_t backward_tc_workspace_bytes(int B, int L, int Hq, int Hkv);
 cudaError_t launch_backward_tc(const BackwardTcParams& p, cudaStream_t s);
 

@@ -2,8 +2,9 @@
 fp64 autograd oracle, every element of dq, dk, dv and dgate.
 
 Two paths.  The ZGCM-1 local-layer shape (d = 128, four query heads per KV head,
-window 1..128) runs on the tensor cores with bf16 MMA operands; every other shape
-runs in fp32 on the CUDA cores.
+window 1..128) and the ZGCM-1 global layer (the same heads, every earlier key, no gate)
+run on the tensor cores with bf16 MMA operands; every other shape runs in fp32 on the
+CUDA cores.
 
 Tolerance of the tensor-core path: the prefill's own bar, rel-L2 <= 1e-2 and max-abs
 <= 2e-2 relative to the gradient's largest element.  Its operands q_hat, k_hat, dA,
@@ -46,8 +47,10 @@ def zg():
 
 
 def _tc(c):
-    """the shapes the tensor-core path takes"""
-    return c.d == 128 and c.Hq == 4 * c.Hkv and 1 <= c.window <= 128
+    """the shapes the tensor-core path takes: the local layer (window 1..128) and the ungated
+    global layer (every earlier key), both with d = 128 and four query heads per KV head"""
+    glob = not c.gated and (c.window <= 0 or c.window >= c.L)
+    return c.d == 128 and c.Hq == 4 * c.Hkv and (1 <= c.window <= 128 or glob)
 
 
 def _close(got, ref, what, tc=False):
@@ -90,7 +93,10 @@ def _oracle(c, inp, sl=None):
 
 @pytest.mark.parametrize("B,L,Hq,Hkv,window,gated", [
     (2, 300, 8, 2, 128, True),    # the ZGCM-1 local layer: window 128, GQA 4:1, several windows and a tail
-    (1, 257, 8, 2, 0, False),     # global layer: every earlier key, no gate
+    (1, 257, 8, 2, 0, False),     # global layer: every earlier key, no gate (tensor cores: 3 key blocks)
+    (2, 300, 4, 1, 0, False),     # global layer, two sequences, ragged last query tile
+    (1, 33, 8, 2, 0, False),      # global layer shorter than one query tile
+    (1, 190, 4, 2, 0, False),     # global layer, GQA 2:1 (fp32 path)
     (1, 200, 4, 4, 64, True),     # no head sharing
     (2, 150, 8, 1, 200, True),    # window longer than the sequence, GQA 8:1
     (1, 70, 4, 1, 1, True),       # window 1: every query sees only itself (p = 1, dq = dk = 0)
@@ -130,3 +136,15 @@ def test_full_size_4k_training_shape_on_window_slices(zg):
         _close(dg[b, t0 + lo:t1], rg[0, lo:], f"dgate b{b} [{t0},{t1})", tc=True)
         _close(dk[b, t0 + lo:t0 + khi], rk[0, lo:khi], f"dk b{b} [{t0},{t1})", tc=True)
         _close(dv[b, t0 + lo:t0 + khi], rv[0, lo:khi], f"dv b{b} [{t0},{t1})", tc=True)
+
+
+def test_global_layer_at_the_4k_training_length(zg):
+    # the global layer at the pages' training length (4K): one sequence, one KV group of four
+    # query heads (the oracle's autograd over the full 4096 x 4096 score matrices stays within
+    # seconds); every element of dq, dk, dv; the global layer has no gate
+    c, inp = _case(1, 4096, 4, 1, 0, False, theta=1e6)
+    got = _gpu(zg, c, inp)
+    ref = _oracle(c, inp)
+    assert got[3] is None and ref[3] is None
+    for n, g, r in zip(("dq", "dk", "dv"), got[:3], ref[:3]):
+        _close(g, r, f"{c.name} {n}", tc=_tc(c))
