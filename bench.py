@@ -18,7 +18,8 @@ times the other workloads one by one: the tiny gated SWA prefill (latency, L2
 flushed), the B=4 L=4096 gated SWA prefill (L2 flushed), the global prefill at
 L=262144 (bf16, and with E4M3 inputs on the E4M3 tensor-core path), the decode
 step over E4M3 caches, the cache writer, the whole gated
-layer and the backward pass.  `cpu_baseline` times the fp64 oracle on a slice of
+layer and the backward pass (local layer, and the global layer at the 4K training
+shape).  `cpu_baseline` times the fp64 oracle on a slice of
 the 256K workload, on the whole tiny configuration and on one decode step of one
 sequence, with the host CPU model and thread count.
 
@@ -715,6 +716,23 @@ def run_gpu(args):
            "tensor": {"achieved_tflops": b_fl / b_t / 1e12, "peak": peaks["bf16_tflops"],
                       "frac": b_fl / b_t / 1e12 / peaks["bf16_tflops"], "algorithmic_flops": b_fl}}
 
+    # ---- backward of the global layer (outside the step): the 4K training shape, every earlier key
+    GB = workloads.PrefillCase("global_backward_B4_L4096_h32x8_d128", 4, 4, 4096, 32, 8, 128, 0, 42, 1e6, False)
+    gbx2 = workloads.prefill_inputs_device(GB, dev)
+    gdout = torch.randn(GB.B, GB.L, GB.Hq, GB.d, generator=gen, device=dev).to(torch.bfloat16)
+    gbws = torch.empty(zg.attention_backward_workspace_bytes(GB.B, GB.L, GB.Hq, GB.Hkv, GB.d), dtype=torch.uint8,
+                       device=dev)
+    gb_t = time_part(lambda: zg.attention_backward(gbx2["q"], gbx2["k"], gbx2["v"], None, gbx2["pos"], gbx2["wq"],
+                                                   gbx2["wk"], gdout, window=0, rotary_dim=GB.rotary_dim,
+                                                   theta=GB.theta, eps=GB.eps, workspace=gbws), 5)
+    gb_fl = backward_flops(GB)
+    bwd_glob = {"workload": f"{GB.name} backward (dq, dk, dv), three kernels per call", "ms": gb_t * 1e3,
+                "tokens_per_s": GB.tokens / gb_t,
+                "roofline": {"bound": "tensor", "achieved": gb_fl / gb_t / 1e12, "peak": peaks["bf16_tflops"],
+                             "unit": "TFLOP/s", "frac": gb_fl / gb_t / 1e12 / peaks["bf16_tflops"], "traffic": None,
+                             "algorithmic_flops": gb_fl}}
+    del gbx2, gdout, gbws
+
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
@@ -731,6 +749,7 @@ def run_gpu(args):
             "gated_swa_layer": lay,
             "kv_cache_write": kvc,
             "attention_backward": bwd,
+            "attention_backward_global": bwd_glob,
             "hybrid_decode_fp8": dec_fp8,
             "tiny_swa_prefill": tiny,
             "swa_prefill_4k": swa4k,

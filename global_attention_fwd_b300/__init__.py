@@ -32,7 +32,7 @@ EXPORTS = ("zg_swa_prefill", "zg_global_prefill_workspace_bytes", "zg_global_pre
            "zg_attention_backward_workspace_bytes", "zg_attention_backward",
            "zg_hybrid_decode_workspace_bytes", "zg_hybrid_decode", "zg_hybrid_decode_noalloc",
            "zg_hybrid_decode_fp8", "zg_kv_cache_write_fp8", "zg_global_prefill_fp8_workspace_bytes",
-           "zg_global_prefill_fp8",
+           "zg_global_prefill_fp8", "zg_swa_prefill_fp8",
            "zg_device_status", "zg_selftest_bounded_wait", "zg_selftest_index_check", "zg_debug_build",
            "zg_status_string")
 
@@ -83,6 +83,8 @@ def _load() -> ctypes.CDLL:
     lib.zg_global_prefill_fp8_workspace_bytes.restype = SZ
     lib.zg_global_prefill_fp8.argtypes = [P] * 7 + [I] * 6 + [D, F, F, F, F, P, SZ, P]
     lib.zg_global_prefill_fp8.restype = I
+    lib.zg_swa_prefill_fp8.argtypes = [P] * 8 + [I] * 7 + [D, F, F, F, F, P, SZ, P]
+    lib.zg_swa_prefill_fp8.restype = I
     lib.zg_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
     lib.zg_device_status.restype = I
     lib.zg_selftest_bounded_wait.argtypes = [U64, P]
@@ -200,6 +202,33 @@ def global_prefill_fp8(q, k, v, pos, wq, wk, *, q_scale=1.0, k_scale=1.0, v_scal
                                     B, L, Hq, Hkv, d, int(rotary_dim), float(theta), float(eps), float(q_scale),
                                     float(k_scale), float(v_scale), _ptr(workspace), ws_bytes, _stream(stream))
     _raise(st, "zg_global_prefill_fp8")
+    return out
+
+
+def swa_prefill_fp8(q, k, v, gate, pos, wq, wk, *, window=128, q_scale=1.0, k_scale=1.0, v_scale=1.0, rotary_dim,
+                    theta, eps=1e-6, out=None, workspace=None, stream=None):
+    """swa_prefill on E4M3 inputs: q [B,L,Hq,d], k, v [B,L,Hkv,d] uint8 holding e4m3(x * scale); gate
+    [B,L,Hq,d] bf16.  Products on the E4M3 tensor-core path.  Returns out [B,L,Hq,d] bf16."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, n, torch.uint8, 4)
+    _check(gate, "gate", torch.bfloat16, 4)
+    _check(pos, "pos", torch.int32, 2)
+    _check(wq, "wq", torch.float32)
+    _check(wk, "wk", torch.float32)
+    B, L, Hq, d = q.shape
+    Hkv = k.shape[2]
+    if out is None:
+        out = torch.empty(B, L, Hq, d, dtype=torch.bfloat16, device=q.device)
+    _check(out, "out", torch.bfloat16, 4)
+    need = global_prefill_fp8_workspace_bytes(B, L, Hkv, d)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = _lib.zg_swa_prefill_fp8(_ptr(q), _ptr(k), _ptr(v), _ptr(gate), _ptr(pos), _ptr(wq), _ptr(wk), _ptr(out),
+                                 B, L, Hq, Hkv, d, int(window), int(rotary_dim), float(theta), float(eps),
+                                 float(q_scale), float(k_scale), float(v_scale), _ptr(workspace), ws_bytes,
+                                 _stream(stream))
+    _raise(st, "zg_swa_prefill_fp8")
     return out
 
 

@@ -312,12 +312,16 @@ size_t zg_global_prefill_fp8_workspace_bytes(int B, int L, int Hkv, int d) {
     return static_cast<size_t>(B) * Hkv * d * (static_cast<size_t>(L) + lp);  // k_hat, then V^T
 }
 
-zg_status zg_global_prefill_fp8(const uint8_t* q, const uint8_t* k, const uint8_t* v, const int32_t* pos,
-                                const float* wq, const float* wk, zg_bf16* out, int B, int L, int Hq, int Hkv,
-                                int d, int rotary_dim, double theta, float eps, float q_scale, float k_scale,
-                                float v_scale, void* workspace, size_t workspace_bytes, zg_stream stream) {
-    zg_status st = check_prefill(q, k, v, nullptr, false, pos, wq, wk, out, B, L, Hq, Hkv, d, rotary_dim, theta, eps);
+// E4M3 prefill on the global pipeline: the global layer (gate NULL, every earlier key) or the gated
+// sliding-window layer (gate given, window >= 1)
+static zg_status prefill_fp8(const uint8_t* q, const uint8_t* k, const uint8_t* v, const zg_bf16* gate,
+                             const int32_t* pos, const float* wq, const float* wk, zg_bf16* out, int B, int L, int Hq,
+                             int Hkv, int d, int window, int rotary_dim, double theta, float eps, float q_scale,
+                             float k_scale, float v_scale, void* workspace, size_t workspace_bytes, zg_stream stream) {
+    const bool swa = gate != nullptr;
+    zg_status st = check_prefill(q, k, v, gate, swa, pos, wq, wk, out, B, L, Hq, Hkv, d, rotary_dim, theta, eps);
     if (st != ZG_OK) return st;
+    if (swa && window < 1) return ZG_ERR_SHAPE;
     if (!(std::isfinite(q_scale) && q_scale > 0.f && std::isfinite(k_scale) && k_scale > 0.f &&
           std::isfinite(v_scale) && v_scale > 0.f))
         return ZG_ERR_SHAPE;
@@ -337,9 +341,11 @@ zg_status zg_global_prefill_fp8(const uint8_t* q, const uint8_t* k, const uint8_
     std::memset(&p, 0, sizeof(p));
     if (!dev_ctl(p.ctl)) return ZG_ERR_CUDA;
     if (!make_map_u8(&p.tm_q, q, d, Hq, L, B, 128, G, T) || !make_map(&p.tm_out, out, d, Hq, L, B, G, T) ||
-        !make_map_u8(&p.tm_kh, kh, d, Hkv, L, B, 128, 1, 128) || !make_map_u8(&p.tm_vt, vt, lp, d, Hkv, B, 128, 128, 1))
+        !make_map_u8(&p.tm_kh, kh, d, Hkv, L, B, 128, 1, 128) || !make_map_u8(&p.tm_vt, vt, lp, d, Hkv, B, 128, 128, 1) ||
+        (swa && !make_map(&p.tm_gate, gate, d, Hq, L, B, G, T)))
         return ZG_ERR_CUDA;
     p.fp8 = 1;
+    p.swa = swa ? 1 : 0;
     p.k_raw = k;
     p.v_raw = v;
     p.khat = kh;
@@ -355,12 +361,29 @@ zg_status zg_global_prefill_fp8(const uint8_t* q, const uint8_t* k, const uint8_
     p.L = L;
     p.Hq = Hq;
     p.Hkv = Hkv;
-    p.window = L;
+    p.window = swa ? window : L;
     p.n_ltiles = static_cast<int>(n_lt);
     p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
     p.eps = eps;
     if (!rope_consts(p.rope, rotary_dim, theta)) return ZG_ERR_SHAPE;
     return launch_global_prefill(p, d, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? ZG_OK : ZG_ERR_CUDA;
+}
+
+zg_status zg_global_prefill_fp8(const uint8_t* q, const uint8_t* k, const uint8_t* v, const int32_t* pos,
+                                const float* wq, const float* wk, zg_bf16* out, int B, int L, int Hq, int Hkv,
+                                int d, int rotary_dim, double theta, float eps, float q_scale, float k_scale,
+                                float v_scale, void* workspace, size_t workspace_bytes, zg_stream stream) {
+    return prefill_fp8(q, k, v, nullptr, pos, wq, wk, out, B, L, Hq, Hkv, d, 0, rotary_dim, theta, eps, q_scale, k_scale,
+                       v_scale, workspace, workspace_bytes, stream);
+}
+
+zg_status zg_swa_prefill_fp8(const uint8_t* q, const uint8_t* k, const uint8_t* v, const zg_bf16* gate,
+                             const int32_t* pos, const float* wq, const float* wk, zg_bf16* out, int B, int L, int Hq,
+                             int Hkv, int d, int window, int rotary_dim, double theta, float eps, float q_scale,
+                             float k_scale, float v_scale, void* workspace, size_t workspace_bytes, zg_stream stream) {
+    if (!gate) return ZG_ERR_NULL;
+    return prefill_fp8(q, k, v, gate, pos, wq, wk, out, B, L, Hq, Hkv, d, window, rotary_dim, theta, eps, q_scale,
+                       k_scale, v_scale, workspace, workspace_bytes, stream);
 }
 
 zg_status zg_kv_cache_write(const zg_bf16* k, const zg_bf16* v, const int32_t* pos, const float* wk,

@@ -37,7 +37,7 @@ namespace {
 
 constexpr int BK = 128;               // keys per block
 constexpr uint32_t CH = 128 * 128;    // one 64-column chunk of 128 rows (16-bit elements)
-constexpr int NBAR = 20;
+constexpr int NBAR = 22;
 constexpr float kTau = 8.0f;
 constexpr int kThreads = 384;
 constexpr int kGroupCt = 128;  // CTAs of one (sequence, KV head) scheduled together on long sequences
@@ -207,7 +207,10 @@ __global__ void __launch_bounds__(256) vt_e4m3_kernel(const __grid_constant__ Pr
 
 // ---------------------------------------------------------------- kernel 2
 // F8: E4M3 inputs and products (see the pre-passes above); D = 128 only.
-template <int D, int G, bool F8>
+// SWA: the gated sliding-window layer on the same pipeline (used for E4M3 inputs): a CTA visits
+// only the key blocks that meet its queries' windows, masks both window edges, and multiplies the
+// output by sigmoid(gate) in the epilogue.
+template <int D, int G, bool F8, bool SWA = false>
 __global__ void __launch_bounds__(kThreads, 1) global_attn_kernel(const __grid_constant__ PrefillParams p) {
     constexpr int T = 128 / G;  // tokens per tile
     using C = Glb<D, F8>;
@@ -228,6 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1) global_attn_kernel(const __grid_c
     uint64_t* pv_done = bar + 15;  // [2] per tile
     uint64_t* out_bar = bar + 17;  // [2] per tile: the tile's output is in shared memory
     uint64_t* drain = bar + 19;
+    uint64_t* gate_full = bar + 20;  // [2] per tile (SWA): the gate tile is in the staging buffer
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
 
@@ -250,7 +254,10 @@ __global__ void __launch_bounds__(kThreads, 1) global_attn_kernel(const __grid_c
     const int g = bg % p.Hkv;
     const int b = bg / p.Hkv;
     const int i0 = ct * 2 * T;
-    const int nkb = (i0 + 2 * T + BK - 1) / BK;  // both tiles need the same key blocks
+    // key blocks jlo .. jlo + nkb - 1 (both tiles need the same blocks): from 0 for the global layer,
+    // from the block of the first key of the first query's window for SWA
+    const int jlo = SWA ? max(0, i0 - p.window + 1) / BK : 0;
+    const int nkb = (i0 + 2 * T + BK - 1) / BK - jlo;
 
     if (threadIdx.x == 0) {
         *abort_flag = (smem_u32(smem) & 1023u) == 0 ? 0 : 1;
@@ -266,6 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1) global_attn_kernel(const __grid_c
             mbar_init(&p_ready[i], 128);
             mbar_init(&pv_done[i], 1);
             mbar_init(&out_bar[i], 128);
+            mbar_init(&gate_full[i], 1);
         }
         mbar_init(drain, 1);
         fence_barrier_init();
@@ -303,15 +311,15 @@ __global__ void __launch_bounds__(kThreads, 1) global_attn_kernel(const __grid_c
                     if (!ok) break;
                     mbar_arrive_expect_tx(&k_full[st], TILE);
                     for (int ch = 0; ch < NCH; ++ch)
-                        tma_load_4d(smem + OFF_K + st * TILE + ch * CH, &p.tm_kh, &k_full[st], ch * 64, g, j * BK, b);
+                        tma_load_4d(smem + OFF_K + st * TILE + ch * CH, &p.tm_kh, &k_full[st], ch * 64, g, (jlo + j) * BK, b);
                     ok = mbar_wait(&v_empty[st], ((j >> 1) & 1) ^ 1, p.ctl, 52);
                     if (!ok) break;
                     mbar_arrive_expect_tx(&v_full[st], TILE);
                     if constexpr (F8)  // V^T block: 128 key bytes per row, D rows
-                        tma_load_4d(smem + OFF_V + st * TILE, &p.tm_vt, &v_full[st], j * BK, 0, g, b);
+                        tma_load_4d(smem + OFF_V + st * TILE, &p.tm_vt, &v_full[st], (jlo + j) * BK, 0, g, b);
                     else
                         for (int ch = 0; ch < NCH; ++ch)
-                            tma_load_4d(smem + OFF_V + st * TILE + ch * CH, &p.tm_v, &v_full[st], ch * 64, g, j * BK, b);
+                            tma_load_4d(smem + OFF_V + st * TILE + ch * CH, &p.tm_v, &v_full[st], ch * 64, g, (jlo + j) * BK, b);
                 }
                 if (!ok) fail();
             }
@@ -431,9 +439,13 @@ __global__ void __launch_bounds__(kThreads, 1) global_attn_kernel(const __grid_c
             tmem_ld32(s_addr + 64, r + 64);
             tmem_ld32(s_addr + 96, r + 96);
             tmem_wait_ld();
-            const bool diag = (j + 1) * BK - 1 > i0;  // the block reaches past the CTA's first query
-            const int kmax = iq - j * BK;  // last valid key column of this row in the block
-            if (diag) {
+            const int kmax = iq - (jlo + j) * BK;  // last valid key column of this row in the block
+            if constexpr (SWA) {
+                const int kmin = kmax - p.window + 1;  // first key column inside the window
+#pragma unroll
+                for (int k = 0; k < 128; ++k)
+                    if (k > kmax || k < kmin) r[k] = __float_as_uint(-INFINITY);
+            } else if ((jlo + j + 1) * BK - 1 > i0) {  // the block reaches past the CTA's first query
 #pragma unroll
                 for (int k = 0; k < 128; ++k)
                     if (k > kmax) r[k] = __float_as_uint(-INFINITY);
@@ -471,7 +483,9 @@ __global__ void __launch_bounds__(kThreads, 1) global_attn_kernel(const __grid_c
             }
             l_run *= corr;
             m_run = m_new;
-            const float2 sc2 = make_float2(sc, sc), nm2 = make_float2(-m_run, -m_run);
+            // a row whose window has not begun yet (SWA) has m_run = -inf and every score masked: P = 0
+            const float m_exp = m_run == -INFINITY ? 0.f : m_run;
+            const float2 sc2 = make_float2(sc, sc), nm2 = make_float2(-m_exp, -m_exp);
             float2 l2 = make_float2(0.f, 0.f), l3 = make_float2(0.f, 0.f);
 #pragma unroll
             for (int cb = 0; cb < 128; cb += 32) {
@@ -518,6 +532,14 @@ __global__ void __launch_bounds__(kThreads, 1) global_attn_kernel(const __grid_c
         // tile 0 and the V stages for tile 1, free once the tile's last product has completed.
         uint8_t* stg = F8 ? smem + (t == 0 ? OFF_K : OFF_V) : qt;
         if (ok && !aborted()) ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[t], (nkb - 1) & 1, p.ctl, 63));
+        if constexpr (SWA) {  // the gate tile (bf16) into the staging buffer, free now
+            if (ok && row == 0) {
+                mbar_arrive_expect_tx(&gate_full[t], (D / 64) * CH);
+                for (int ch = 0; ch < D / 64; ++ch)
+                    tma_load_4d(stg + ch * CH, &p.tm_gate, &gate_full[t], ch * 64, g * G, i0 + t * T, b);
+            }
+            if (ok && !aborted()) ok = __all_sync(0xffffffffu, mbar_wait(&gate_full[t], 0, p.ctl, 65));
+        }
         if (ok) {
             tc_fence_after();
             const float inv_l = l_run > 0.f ? (F8 ? p.in_dequant_v : 1.0f) / l_run : 0.f;
@@ -529,13 +551,24 @@ __global__ void __launch_bounds__(kThreads, 1) global_attn_kernel(const __grid_c
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) {
                     uint32_t ou[4];
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        ou[k] = pack_bf16x2(__uint_as_float(o[q4 * 8 + 2 * k]) * inv_l,
-                                            __uint_as_float(o[q4 * 8 + 2 * k + 1]) * inv_l);
                     const int e0 = cb + q4 * 8;
-                    *reinterpret_cast<uint4*>(stg + (e0 >> 6) * CH + sw128_off(row, (e0 & 63) >> 3)) =
-                        make_uint4(ou[0], ou[1], ou[2], ou[3]);
+                    uint4* dst = reinterpret_cast<uint4*>(stg + (e0 >> 6) * CH + sw128_off(row, (e0 & 63) >> 3));
+                    if constexpr (SWA) {  // out = A * sigmoid(gate), the gate read from the same place
+                        const uint4 gv = *dst;
+                        const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const float2 sg = sigmoid2_f32(bf2f2(gw[k]));
+                            ou[k] = pack_bf16x2(__uint_as_float(o[q4 * 8 + 2 * k]) * inv_l * sg.x,
+                                                __uint_as_float(o[q4 * 8 + 2 * k + 1]) * inv_l * sg.y);
+                        }
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            ou[k] = pack_bf16x2(__uint_as_float(o[q4 * 8 + 2 * k]) * inv_l,
+                                                __uint_as_float(o[q4 * 8 + 2 * k + 1]) * inv_l);
+                    }
+                    *dst = make_uint4(ou[0], ou[1], ou[2], ou[3]);
                 }
             }
             fence_async_smem();
@@ -566,7 +599,7 @@ __global__ void __launch_bounds__(kThreads, 1) global_attn_kernel(const __grid_c
     if (warp == 1) tmem_dealloc(tbase, 512);
 }
 
-template <int D, int G, bool F8>
+template <int D, int G, bool F8, bool SWA>
 cudaError_t launch_t(const PrefillParams& p, cudaStream_t s) {
     constexpr int T = 128 / G;
     const long long rows = static_cast<long long>(p.B) * p.L * p.Hkv;
@@ -580,7 +613,7 @@ cudaError_t launch_t(const PrefillParams& p, cudaStream_t s) {
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    auto k = global_attn_kernel<D, G, F8>;
+    auto k = global_attn_kernel<D, G, F8, SWA>;
     e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Glb<D, F8>::SMEM);
     if (e != cudaSuccess) return e;
     const long long ctas = static_cast<long long>(p.B) * p.Hkv * ((p.L + 2 * T - 1) / (2 * T));
@@ -588,14 +621,14 @@ cudaError_t launch_t(const PrefillParams& p, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-template <int D, bool F8>
+template <int D, bool F8, bool SWA = false>
 cudaError_t launch_d(const PrefillParams& p, cudaStream_t s) {
     switch (p.Hq / p.Hkv) {
-        case 1: return launch_t<D, 1, F8>(p, s);
-        case 2: return launch_t<D, 2, F8>(p, s);
-        case 4: return launch_t<D, 4, F8>(p, s);
-        case 8: return launch_t<D, 8, F8>(p, s);
-        case 16: return launch_t<D, 16, F8>(p, s);
+        case 1: return launch_t<D, 1, F8, SWA>(p, s);
+        case 2: return launch_t<D, 2, F8, SWA>(p, s);
+        case 4: return launch_t<D, 4, F8, SWA>(p, s);
+        case 8: return launch_t<D, 8, F8, SWA>(p, s);
+        case 16: return launch_t<D, 16, F8, SWA>(p, s);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -607,6 +640,7 @@ int global_q_tile_tokens(int G) { return 128 / G; }
 
 cudaError_t launch_global_prefill(const PrefillParams& p, int d, cudaStream_t s) {
     if (p.Hkv <= 0 || p.Hq % p.Hkv || !global_supports(d, p.Hq / p.Hkv)) return cudaErrorInvalidValue;
+    if (p.fp8 && p.swa) return d == 128 && p.window >= 1 ? launch_d<128, true, true>(p, s) : cudaErrorInvalidValue;
     if (p.fp8) return d == 128 ? launch_d<128, true>(p, s) : cudaErrorInvalidValue;
     return d == 128 ? launch_d<128, false>(p, s) : launch_d<64, false>(p, s);
 }

@@ -34,6 +34,7 @@ struct PrefillParams {
     int B, L, Hq, Hkv, window;
     int n_ltiles;      // query tiles along L per (b, kv head)
     int pre;           // SWA: q, k already q_hat, k_hat (fp16) and gate already sigmoid(g) (bf16)
+    int swa;           // E4M3 path: the gated sliding-window layer (window, gate map tm_gate) on the global pipeline
     // global prefill over E4M3 inputs: q, k, v hold e4m3(x * scale); these undo the scales
     int fp8;
     const void* v_raw;                               // E4M3 values [B, L, Hkv, d] (transposed by the pre-pass)

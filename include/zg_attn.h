@@ -265,6 +265,26 @@ zg_status zg_global_prefill_fp8(const uint8_t *q, const uint8_t *k, const uint8_
                                 float v_scale, void *workspace, size_t workspace_bytes, zg_stream stream);
 
 /*
+ * zg_swa_prefill_fp8 -- the gated sliding-window prefill (zg_swa_prefill's operation) with E4M3
+ * inputs and E4M3 tensor-core products, on the pipeline of zg_global_prefill_fp8: each query tile
+ * visits only the 128-key blocks that meet its queries' windows, masks both window edges, and
+ * multiplies by sigmoid(gate) (fp32, as zg_swa_prefill) before the bf16 store.
+ *   q, k, v: E4M3 as in zg_global_prefill_fp8 (scales likewise); gate [B, L, Hq, d] bf16 logits
+ *        (required: ZG_ERR_NULL if missing); window >= 1 (keys i - window + 1 .. i; ZG_ERR_SHAPE
+ *        otherwise; no upper bound: a window of L or more is the global layer with a gate).
+ *   workspace: the same size and use as zg_global_prefill_fp8's
+ *        (zg_global_prefill_fp8_workspace_bytes).
+ *   Rounding and expected error as zg_global_prefill_fp8.
+ * Kernel shapes: d = 128; Hq / Hkv in {1, 2, 4, 8, 16}; ZG_ERR_UNSUPPORTED otherwise.
+ * B == 0 or L == 0 is a no-op returning ZG_OK.
+ */
+zg_status zg_swa_prefill_fp8(const uint8_t *q, const uint8_t *k, const uint8_t *v, const zg_bf16 *gate,
+                             const int32_t *pos, const float *wq, const float *wk, zg_bf16 *out, int B, int L,
+                             int Hq, int Hkv, int d, int window, int rotary_dim, double theta, float eps,
+                             float q_scale, float k_scale, float v_scale, void *workspace, size_t workspace_bytes,
+                             zg_stream stream);
+
+/*
  * zg_hybrid_decode_noalloc -- the same decode step as zg_hybrid_decode, for
  * callers that cannot allocate device memory (no counterpart in the paper: it
  * exists for how the library is called, not for what it computes).
