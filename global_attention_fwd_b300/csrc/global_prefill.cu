@@ -136,45 +136,76 @@ __device__ __forceinline__ void qk_norm_rope_row_e4m3(uint8_t* tile, int row, co
         *at(j) = f_to_e4m3((a * cs - c * sn) * s_out);
         *at(j + rc.half) = f_to_e4m3((c * cs + a * sn) * s_out);
     }
-#pragma unroll 4
-    for (int e = 2 * rc.half; e < D; ++e) *at(e) = f_to_e4m3(e4m3_to_f(*at(e)) * f * __ldg(w + e) * s_out);
+    // the dims past the rotated ones: whole 16-byte chunks with paired conversions, the rest bytewise
+    const int c_first = (2 * rc.half + 15) / 16;  // chunks [c_first, D / 16) hold no rotated dim
+    for (int e = 2 * rc.half; e < 16 * c_first; ++e) *at(e) = f_to_e4m3(e4m3_to_f(*at(e)) * f * __ldg(w + e) * s_out);
+    const float fs = f * s_out;
+#pragma unroll 1
+    for (int c = c_first; c < D / 16; ++c) {
+        uint4* cp = reinterpret_cast<uint4*>(tile + sw128_off(row, c));
+        const uint4 v = *cp;
+        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float4 w4 = __ldg(reinterpret_cast<const float4*>(w + 16 * c + 4 * k));
+            const __half2_raw h01 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(u[k] & 0xFFFFu), __NV_E4M3);
+            const __half2_raw h23 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(u[k] >> 16), __NV_E4M3);
+            const float2 x01 = __half22float2(__half2(h01)), x23 = __half22float2(__half2(h23));
+            const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(x01.x * fs * w4.x, x01.y * fs * w4.y), __NV_SATFINITE,
+                                                         __NV_E4M3);
+            const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(x23.x * fs * w4.z, x23.y * fs * w4.w), __NV_SATFINITE,
+                                                         __NV_E4M3);
+            o[k] = lo | (hi << 16);
+        }
+        *cp = make_uint4(o[0], o[1], o[2], o[3]);
+    }
 }
 
-// k_hat in E4M3 (one warp per key row), from E4M3 keys
+// k_hat in E4M3 from E4M3 keys: one warp per key row at a time, four bytes per lane (lane l holds
+// elements 4l .. 4l + 3, the layout norm_rope_warp_vals takes)
 template <int D>
 __global__ void __launch_bounds__(256) khat_e4m3_kernel(const __grid_constant__ PrefillParams p) {
+    static_assert(D == 128, "one 128-byte row per head vector");
+    constexpr int kRows = 4;
     __shared__ __align__(16) float buf[8][D];
     __shared__ float rope_f[2][kMaxRotHalf];
     stage_rope(p.rope, rope_f[0], rope_f[1]);
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const long long row = static_cast<long long>(blockIdx.x) * 8 + warp;  // (b, j, g)
+    const long long row0 = (static_cast<long long>(blockIdx.x) * 8 + warp) * kRows;  // (b, j, g)
     const long long nrows = static_cast<long long>(p.B) * p.L * p.Hkv;
-    if (row >= nrows) return;
+    if (row0 >= nrows) return;
     const float s_kh = e4m3_hat_scale<D>(p.wk);
-    const long long tok = row / p.Hkv;
-    if (!idx_ok(p.ctl, tok, static_cast<long long>(p.B) * p.L, 94)) return;
-    const int pos = __ldg(p.pos + tok);
-    const uint8_t* kr = reinterpret_cast<const uint8_t*>(p.k_raw) + row * D;
-    for (int e = lane; e < D; e += 32) buf[warp][e] = e4m3_to_f(kr[e]) * p.in_dequant_k;
-    __syncwarp();
-    float ss = 0.f;
-    for (int e = lane; e < D; e += 32) ss = fmaf(buf[warp][e], buf[warp][e], ss);
+    float wv[4];
+    norm_weights_lane<D>(p.wk, wv);
+    uint32_t raw[kRows];
+    int pos[kRows];
 #pragma unroll
-    for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    const float inv = ss > 0.f || p.eps > 0.f ? rsqrtf(ss * (1.0f / D) + p.eps) : 0.f;
-    for (int e = lane; e < D; e += 32) buf[warp][e] *= inv * __ldg(p.wk + e);
-    __syncwarp();
-    for (int j = lane; j < p.rope.half; j += 32) {
-        const float a = buf[warp][j], c = buf[warp][j + p.rope.half];
-        float cs, sn;
-        rope_cos_sin(pos, rope_f[0][j], rope_f[1][j], cs, sn);
-        buf[warp][j] = a * cs - c * sn;
-        buf[warp][j + p.rope.half] = c * cs + a * sn;
+    for (int r = 0; r < kRows; ++r) {  // every load first
+        const long long row = row0 + r;
+        raw[r] = 0u;
+        pos[r] = 0;
+        if (row >= nrows) continue;
+        const long long tok = row / p.Hkv;
+        if (!idx_ok(p.ctl, tok, static_cast<long long>(p.B) * p.L, 94)) continue;
+        pos[r] = __ldg(p.pos + tok);
+        raw[r] = *reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint8_t*>(p.k_raw) + row * D + lane * 4);
     }
-    __syncwarp();
-    uint8_t* kh = reinterpret_cast<uint8_t*>(p.khat) + row * D;
-    for (int e = lane; e < D; e += 32) kh[e] = f_to_e4m3(buf[warp][e] * s_kh);
+#pragma unroll
+    for (int r = 0; r < kRows; ++r) {
+        const long long row = row0 + r;
+        if (row >= nrows) break;
+        float v[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) v[e] = e4m3_to_f((raw[r] >> (8 * e)) & 0xFFu) * p.in_dequant_k;
+        norm_rope_warp_vals<D>(v, wv, p.eps, pos[r], p.rope.half, rope_f[0], rope_f[1], 1.0f, buf[warp]);
+        const float4 y = *reinterpret_cast<const float4*>(buf[warp] + lane * 4);
+        const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(y.x * s_kh, y.y * s_kh), __NV_SATFINITE, __NV_E4M3);
+        const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(y.z * s_kh, y.w * s_kh), __NV_SATFINITE, __NV_E4M3);
+        *reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(p.khat) + row * D + lane * 4) = lo | (hi << 16);
+        __syncwarp();  // buf[warp] is reused by the next row
+    }
 }
 
 // V^T in E4M3: [B, Hkv, D, Lp] from [B, L, Hkv, D]; one CTA per 128 keys of one (b, KV head)
@@ -193,15 +224,24 @@ __global__ void __launch_bounds__(256) vt_e4m3_kernel(const __grid_constant__ Pr
         *reinterpret_cast<uint32_t*>(&tile[kr][4 * c4]) = w;
     }
     __syncthreads();
-    for (int idx = threadIdx.x; idx < D * 32; idx += 256) {
-        const int dim = idx / 32, k4 = idx % 32;  // keys 4 k4 .. 4 k4 + 3 of row `dim`
+    // 4 keys x 4 dims per thread: four 32-bit words of consecutive keys, transposed with byte permutes
+    for (int idx = threadIdx.x; idx < (D / 4) * 32; idx += 256) {
+        const int d4 = idx / 32, k4 = idx % 32;  // dims 4 d4 .. 4 d4 + 3, keys 4 k4 .. 4 k4 + 3
         const int j = j0 + 4 * k4;
         if (j >= Lp) continue;
-        const uint32_t w = uint32_t(tile[4 * k4][dim]) | uint32_t(tile[4 * k4 + 1][dim]) << 8 |
-                           uint32_t(tile[4 * k4 + 2][dim]) << 16 | uint32_t(tile[4 * k4 + 3][dim]) << 24;
-        const long long dst = ((static_cast<long long>(b) * p.Hkv + g) * D + dim) * Lp + j;
-        if (idx_ok(p.ctl, dst + 3, static_cast<long long>(p.B) * p.Hkv * D * Lp, 67))
-            *reinterpret_cast<uint32_t*>(vt + dst) = w;
+        uint32_t w[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) w[r] = *reinterpret_cast<const uint32_t*>(&tile[4 * k4 + r][4 * d4]);
+        const uint32_t t0 = __byte_perm(w[0], w[1], 0x5140), t1 = __byte_perm(w[2], w[3], 0x5140);
+        const uint32_t t2 = __byte_perm(w[0], w[1], 0x7362), t3 = __byte_perm(w[2], w[3], 0x7362);
+        const uint32_t o[4] = {__byte_perm(t0, t1, 0x5410), __byte_perm(t0, t1, 0x7632), __byte_perm(t2, t3, 0x5410),
+                               __byte_perm(t2, t3, 0x7632)};  // o[c]: dim 4 d4 + c of the four keys
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const long long dst = ((static_cast<long long>(b) * p.Hkv + g) * D + 4 * d4 + c) * Lp + j;
+            if (idx_ok(p.ctl, dst + 3, static_cast<long long>(p.B) * p.Hkv * D * Lp, 67))
+                *reinterpret_cast<uint32_t*>(vt + dst) = o[c];
+        }
     }
 }
 
@@ -604,7 +644,7 @@ cudaError_t launch_t(const PrefillParams& p, cudaStream_t s) {
     constexpr int T = 128 / G;
     const long long rows = static_cast<long long>(p.B) * p.L * p.Hkv;
     if constexpr (F8) {
-        khat_e4m3_kernel<D><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, s>>>(p);
+        khat_e4m3_kernel<D><<<static_cast<unsigned>((rows + 31) / 32), 256, 0, s>>>(p);  // four rows per warp
         const dim3 vg(static_cast<unsigned>((p.vt_lp + 127) / 128), static_cast<unsigned>(p.Hkv),
                       static_cast<unsigned>(p.B));
         vt_e4m3_kernel<D><<<vg, 256, 0, s>>>(p, p.vt_ws, p.vt_lp);
