@@ -16,7 +16,8 @@ the inputs in pinned host memory, the host->device copies and the device->host
 copy of the output inside the timed region.  Outside the step, `parts` also
 times the other workloads one by one: the tiny gated SWA prefill (latency, L2
 flushed), the B=4 L=4096 gated SWA prefill (L2 flushed), the global prefill at
-L=262144 (bf16, and with E4M3 inputs on the E4M3 tensor-core path), the decode
+L=262144 (bf16, and with E4M3 inputs on the E4M3 tensor-core path), the SWA
+prefill of the step with E4M3 inputs, the decode
 step over E4M3 caches, the cache writer, the whole gated
 layer and the backward pass (local layer, and the global layer at the 4K training
 shape).  `cpu_baseline` times the fp64 oracle on a slice of
@@ -647,6 +648,21 @@ def run_gpu(args):
                                 "traffic": None, "algorithmic_flops": gf4}}
     del gbx, gb_out, g8, g8_ws, flush
 
+    # the gated SWA prefill of the step's workload with E4M3 q, k, v (e4m3(x * 1)); gate and out bf16
+    sx = workloads.prefill_inputs_device(SWA, dev)
+    s8 = {n: workloads.to_e4m3(sx[n], 1.0).view(torch.uint8) for n in ("q", "k", "v")}
+    s8_out = torch.empty_like(sx["q"])
+    s8_ws = torch.empty(zg.global_prefill_fp8_workspace_bytes(SWA.B, SWA.L, SWA.Hkv, SWA.d), dtype=torch.uint8,
+                        device=dev)
+    s8_t = time_part(lambda: zg.swa_prefill_fp8(s8["q"], s8["k"], s8["v"], sx["gate"], sx["pos"], sx["wq"], sx["wk"],
+                                                window=SWA.window, rotary_dim=SWA.rotary_dim, theta=SWA.theta,
+                                                eps=SWA.eps, out=s8_out, workspace=s8_ws), 10)
+    s8_by = SWA.B * SWA.L * (SWA.Hq * SWA.d * (1 + 2 + 2) + 2 * SWA.Hkv * SWA.d)  # q, k, v E4M3; gate, out bf16
+    swa_fp8 = {"workload": f"{SWA.name} with E4M3 q, k, v", "ms": s8_t * 1e3, "tokens_per_s": SWA.tokens / s8_t,
+               "roofline": {"bound": "hbm", "achieved": s8_by / s8_t / 1e9, "peak": hbm, "unit": "GB/s",
+                            "frac": s8_by / s8_t / 1e9 / hbm, "traffic": None, "algorithmic_bytes": s8_by}}
+    del sx, s8, s8_out, s8_ws
+
     # ---- the decode step over E4M3 caches (outside the step): the same workload, caches stored
     # as e4m3(k_hat * 1) and e4m3(v * 8)
     f8 = {k: workloads.to_e4m3(v, 1.0 if k.startswith("k") else 8.0) for k, v in caches.items()}
@@ -755,6 +771,7 @@ def run_gpu(args):
             "swa_prefill_4k": swa4k,
             "global_prefill_256k": glob256,
             "global_prefill_256k_fp8": glob256_fp8,
+            "swa_prefill_fp8": swa_fp8,
             "swa_prefill": {"workload": SWA.name, "ms": sw_t * 1e3, "tokens_per_s": SWA.tokens / sw_t,
                             "roofline": rl_swa},
             "hybrid_decode": {"workload": DEC.name, "us_per_step": dc_t * 1e6, "roofline": rl_dec},
