@@ -839,6 +839,16 @@ def run_profile_case(args):
         def fn():
             zg.attention_backward(x["q"], x["k"], x["v"], x["gate"], x["pos"], x["wq"], x["wk"], dout, window=128,
                                   rotary_dim=c.rotary_dim, theta=c.theta, workspace=ws)
+    elif kind == "backward_global":
+        c = workloads.PrefillCase("global_backward_B1_L4096_profile", 4, 1, 4096, 32, 8, 128, 0, 42, 1e6, False)
+        x = workloads.prefill_inputs_device(c, dev)
+        dout = torch.randn(c.B, c.L, c.Hq, c.d, device=dev).to(torch.bfloat16)
+        ws = torch.empty(zg.attention_backward_workspace_bytes(c.B, c.L, c.Hq, c.Hkv, c.d), dtype=torch.uint8,
+                         device=dev)
+
+        def fn():
+            zg.attention_backward(x["q"], x["k"], x["v"], None, x["pos"], x["wq"], x["wk"], dout, window=0,
+                                  rotary_dim=c.rotary_dim, theta=c.theta, workspace=ws)
     elif kind == "decode8":
         c = workloads.DecodeCase("hybrid_decode_fp8_B1_p131071_profile", 5, 1, 32, (5, 11, 17, 23, 29), 32, 8, 128,
                                  131072, 128, 131071, 42, 1e6)
@@ -884,7 +894,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--step-only", action="store_true",
                     help="time the step alone: skip the parts measured outside it (for ncu launch lists)")
-    ap.add_argument("--profile-case", choices=["swa", "global", "global8", "decode", "kvcache", "backward", "decode8"], default=None,
+    ap.add_argument("--profile-case", choices=["swa", "global", "global8", "decode", "kvcache", "backward", "backward_global", "decode8"], default=None,
                     help="run only a small case of one kernel (for ncu captures)")
     args = ap.parse_args()
     if args.profile_case:

@@ -955,11 +955,14 @@ __global__ void __launch_bounds__(kGThreads, 1) bwd_qpass_global_kernel(const __
     uint64_t* x_full = bar + 9;
     uint64_t* st_xch = bar + 10;   // both halves' statistics are in shared memory (256 arrivals)
     uint64_t* dq_stg = bar + 11;   // dq staging written (128 arrivals)
+    uint64_t* dq_done = bar + 12;  // loop 2: the dQ product of a block has read its dS
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + GQ_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + GQ_MISC + 4);
     float* w_s = reinterpret_cast<float*>(smem + GQ_W);
     float4* xch = reinterpret_cast<float4*>(smem + GQ_XCH);
-    constexpr uint32_t C_S = 0, C_DP = 128, C_DQ = 256;
+    // TMEM: S, dP, dQ_hat (fp32, 128 columns each) and dS (bf16 packed, 64 columns: half h's keys in
+    // columns [32 h, 32 h + 32)), so the next block's S and dP products run while dS is formed
+    constexpr uint32_t C_S = 0, C_DP = 128, C_DQ = 256, C_DS = 384;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nbg = p.B * p.Hkv;
@@ -984,6 +987,7 @@ __global__ void __launch_bounds__(kGThreads, 1) bwd_qpass_global_kernel(const __
         mbar_init(x_full, 1);
         mbar_init(st_xch, 256);
         mbar_init(dq_stg, 128);
+        mbar_init(dq_done, 1);
         fence_barrier_init();
     }
     if (threadIdx.x < 32)
@@ -1040,13 +1044,23 @@ __global__ void __launch_bounds__(kGThreads, 1) bwd_qpass_global_kernel(const __
             constexpr uint32_t id_s = idesc_bf16_f32(128, BK, false, false);  // S, dP: both operands K-major
             constexpr uint32_t id_o = idesc_bf16_f32(128, D, false, true);    // dQ: K_hat block MN-major
             bool ok = mbar_wait(q_full, 0, p.ctl, 133);
+            // dQ_hat += dS K_hat for loop-2 block m (its K_hat in stage st_m)
+            auto issue_dq = [&](int m, int st_m) {
+                const uint32_t kofs = GQ_RING + st_m * 2 * TILE128;
+#pragma unroll
+                for (int ks = 0; ks < BK / 16; ++ks)
+                    umma_tmem_a(tbase + C_DQ, tbase + C_DS + 32 * (ks >> 2) + 8 * (ks & 3),
+                                sdesc(sbase + kofs + ks * 16 * 128, CH128, 1024, kSw128), id_o,
+                                (m > 0 || ks > 0) ? 1u : 0u);
+                umma_commit(dq_done);
+                umma_commit(&kv_empty[st_m]);
+            };
             for (int n = 0; n < 2 * nblk && ok && !aborted(); ++n) {
                 const int st = n & 1;
                 const uint32_t kofs = GQ_RING + st * 2 * TILE128, vofs = kofs + TILE128;
                 ok = mbar_wait(&kv_full[st], (n >> 1) & 1, p.ctl, 134);
-                // loop 1 (and the first block of loop 2): S and dP of the previous block must be read;
-                // later in loop 2 the rows' dS hand-off below already implies it
-                if (ok && n > 0 && n <= nblk) ok = mbar_wait(s_free, (n - 1) & 1, p.ctl, 135);
+                // S and dP of the previous block must be in the rows' registers
+                if (ok && n > 0) ok = mbar_wait(s_free, (n - 1) & 1, p.ctl, 135);
                 if (!ok) break;
                 tc_fence_after();
 #pragma unroll
@@ -1066,17 +1080,21 @@ __global__ void __launch_bounds__(kGThreads, 1) bwd_qpass_global_kernel(const __
                     umma_commit(&kv_empty[st]);
                     continue;
                 }
-                ok = mbar_wait(ds_ready, (n - nblk) & 1, p.ctl, 136);
-                if (!ok) break;
-                tc_fence_after();
-                // dQ_hat += dS K_hat: dS packed bf16, half h's 64 keys in the first 32 columns of its
-                // own 64-column part of the dP region
-#pragma unroll
-                for (int ks = 0; ks < BK / 16; ++ks)
-                    umma_tmem_a(tbase + C_DQ, tbase + C_DP + 64 * (ks >> 2) + 8 * (ks & 3),
-                                sdesc(sbase + kofs + ks * 16 * 128, CH128, 1024, kSw128), id_o,
-                                (n > nblk || ks > 0) ? 1u : 0u);
-                umma_commit(&kv_empty[st]);
+                // loop 2: the previous block's dQ once its dS is in TMEM (this block's S / dP run meanwhile)
+                const int m = n - nblk;
+                if (m > 0) {
+                    ok = mbar_wait(ds_ready, (m - 1) & 1, p.ctl, 136);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_dq(m - 1, (n - 1) & 1);
+                }
+            }
+            if (ok && !aborted()) {  // the last block's dQ
+                ok = mbar_wait(ds_ready, (nblk - 1) & 1, p.ctl, 143);
+                if (ok) {
+                    tc_fence_after();
+                    issue_dq(nblk - 1, (2 * nblk - 1) & 1);
+                }
             }
             umma_commit(dq_full);
             if (!ok) fail();
@@ -1153,6 +1171,8 @@ __global__ void __launch_bounds__(kGThreads, 1) bwd_qpass_global_kernel(const __
             tc_fence_after();
             uint32_t s[64], dp[64];
             load_block(s, dp);
+            tc_fence_before();
+            mbar_arrive(s_free);
             const int kmax = t - (n * BK + 64 * hf);
             uint32_t pk[32];
 #pragma unroll
@@ -1167,8 +1187,14 @@ __global__ void __launch_bounds__(kGThreads, 1) bwd_qpass_global_kernel(const __
                 }
                 pk[c / 2] = pack_bf16x2(ds2[0], ds2[1]);
             }
-            tmem_st16(lane_addr + C_DP + 64 * hf, pk);  // dS over dP (this half's columns, already read)
-            tmem_st16(lane_addr + C_DP + 64 * hf + 16, pk + 16);
+            // the dS columns are free once the previous block's dQ product has read them
+            if (n > 0 && (aborted() || !__all_sync(0xffffffffu, mbar_wait(dq_done, (n - 1) & 1, p.ctl, 144)))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            tmem_st16(lane_addr + C_DS + 32 * hf, pk);
+            tmem_st16(lane_addr + C_DS + 32 * hf + 16, pk + 16);
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(ds_ready);
