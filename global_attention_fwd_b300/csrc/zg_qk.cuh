@@ -101,77 +101,6 @@ __device__ __forceinline__ void qk_norm_rope_row(uint8_t* base, uint32_t chunk_s
     }
 }
 
-// Faster in-place RMSNorm + partial RoPE of one row of a swizzled smem tile, for warps
-// whose 32 lanes hold 32 consecutive rows.  w_s: the D weights in shared memory.
-// SHARE > 1: groups of SHARE consecutive lanes hold rows of the same token (the GQA
-// heads of one query), so each lane evaluates cos/sin for every SHARE-th frequency
-// and the group exchanges them with shuffles.  Every lane of the warp must call this.
-template <int D, int SHARE>
-__device__ __forceinline__ void qk_norm_rope_row_fast(uint8_t* base, uint32_t chunk_stride, int row, const float* w_s,
-                                                      float eps, int pos, const RopeConsts& rc) {
-    constexpr int NC = D / 8;
-    float2 ss2 = make_float2(0.f, 0.f);
-#pragma unroll 4
-    for (int c = 0; c < NC; ++c) {
-        const uint4 v = *reinterpret_cast<const uint4*>(base + (c >> 3) * chunk_stride + sw128_off(row, c & 7));
-        const float2 a = bf2f2(v.x), b = bf2f2(v.y), cc = bf2f2(v.z), d = bf2f2(v.w);
-        ss2 = fma2(a, a, ss2);
-        ss2 = fma2(b, b, ss2);
-        ss2 = fma2(cc, cc, ss2);
-        ss2 = fma2(d, d, ss2);
-    }
-    const float ss = ss2.x + ss2.y;
-    const float inv = ss > 0.f || eps > 0.f ? rsqrtf(ss * (1.0f / D) + eps) : 0.f;
-    const float2 inv2 = make_float2(inv, inv);
-#pragma unroll 4
-    for (int c = 0; c < NC; ++c) {
-        uint8_t* cp = base + (c >> 3) * chunk_stride + sw128_off(row, c & 7);
-        const uint4 v = *reinterpret_cast<const uint4*>(cp);
-        const float4 w0 = *reinterpret_cast<const float4*>(w_s + c * 8);
-        const float4 w1 = *reinterpret_cast<const float4*>(w_s + c * 8 + 4);
-        const float2 y0 = mul2(mul2(bf2f2(v.x), make_float2(w0.x, w0.y)), inv2);
-        const float2 y1 = mul2(mul2(bf2f2(v.y), make_float2(w0.z, w0.w)), inv2);
-        const float2 y2 = mul2(mul2(bf2f2(v.z), make_float2(w1.x, w1.y)), inv2);
-        const float2 y3 = mul2(mul2(bf2f2(v.w), make_float2(w1.z, w1.w)), inv2);
-        *reinterpret_cast<uint4*>(cp) = make_uint4(pack_half2(y0.x, y0.y), pack_half2(y1.x, y1.y),
-                                                   pack_half2(y2.x, y2.y), pack_half2(y3.x, y3.y));
-    }
-    const int half = rc.half;
-    auto rotate = [&](int j, float cs, float sn) {
-        __half* p1 = reinterpret_cast<__half*>(sw_elem(base, chunk_stride, row, j));
-        __half* p2 = reinterpret_cast<__half*>(sw_elem(base, chunk_stride, row, j + half));
-        const float x1 = __half2float(*p1), x2 = __half2float(*p2);
-        *p1 = __float2half_rn(x1 * cs - x2 * sn);
-        *p2 = __float2half_rn(x2 * cs + x1 * sn);
-    };
-    if constexpr (SHARE == 1) {
-#pragma unroll 1
-        for (int j = 0; j < half; ++j) {
-            float cs, sn;
-            rope_cos_sin(pos, rc.f_hi[j], rc.f_lo[j], cs, sn);
-            rotate(j, cs, sn);
-        }
-    } else {
-        const int lane = threadIdx.x & 31;
-        const int mine = lane & (SHARE - 1);
-        const int grp = lane & ~(SHARE - 1);
-        constexpr int NI = (kMaxRotHalf + SHARE - 1) / SHARE;
-#pragma unroll
-        for (int i = 0; i < NI; ++i) {
-            if (i * SHARE >= half) break;  // uniform over the warp
-            const int jm = i * SHARE + mine;
-            float cs = 1.f, sn = 0.f;
-            if (jm < half) rope_cos_sin(pos, rc.f_hi[jm], rc.f_lo[jm], cs, sn);
-#pragma unroll
-            for (int h = 0; h < SHARE; ++h) {
-                const float c2 = __shfl_sync(0xffffffffu, cs, grp | h);
-                const float s2 = __shfl_sync(0xffffffffu, sn, grp | h);
-                if (i * SHARE + h < half) rotate(i * SHARE + h, c2, s2);
-            }
-        }
-    }
-}
-
 // In-place RMSNorm + partial RoPE of one row of a swizzled smem tile with TWO lanes per
 // row: lanes 2i and 2i+1 of the warp own the same row, the even lane the first half of
 // the D values and the odd lane the second half.  SL (a power of two >= 2) consecutive
