@@ -544,23 +544,18 @@ __global__ void __launch_bounds__(kThreads, 1) swa2_kernel(const __grid_constant
             }
             const float2 nm2 = make_float2(-mb, -mb);
             float2 lacc = make_float2(0.f, 0.f), lacc2 = make_float2(0.f, 0.f);
+            // one code path for every 16-column group, with the window test per element: the kernel's
+            // six warp roles run concurrently, and a second (unmasked) copy of this body cost more in
+            // instruction fetch than the tests it saves
             auto soft16 = [&](const uint32_t* r, int cb) {
                 uint32_t pk[8];
-                if (cb >= kr_lo && cb + 15 <= kr_hi) {
 #pragma unroll
-                    for (int k = 0; k < 16; k += 2) {
-                        const float2 x = fma2(make_float2(__uint_as_float(r[k]), __uint_as_float(r[k + 1])), sc2, nm2);
-                        pk[k / 2] = pack_bf16x2(ex2_approx(x.x), ex2_approx(x.y));
-                    }
-                } else {
-#pragma unroll
-                    for (int k = 0; k < 16; k += 2) {
-                        const float2 x = fma2(make_float2(__uint_as_float(r[k]), __uint_as_float(r[k + 1])), sc2, nm2);
-                        const int kr = cb + k;
-                        const float e0 = (kr >= kr_lo && kr <= kr_hi) ? ex2_approx(x.x) : 0.f;
-                        const float e1 = (kr + 1 >= kr_lo && kr + 1 <= kr_hi) ? ex2_approx(x.y) : 0.f;
-                        pk[k / 2] = pack_bf16x2(e0, e1);
-                    }
+                for (int k = 0; k < 16; k += 2) {
+                    const float2 x = fma2(make_float2(__uint_as_float(r[k]), __uint_as_float(r[k + 1])), sc2, nm2);
+                    const int kr = cb + k;
+                    const float e0 = (kr >= kr_lo && kr <= kr_hi) ? ex2_approx(x.x) : 0.f;
+                    const float e1 = (kr + 1 >= kr_lo && kr + 1 <= kr_hi) ? ex2_approx(x.y) : 0.f;
+                    pk[k / 2] = pack_bf16x2(e0, e1);
                 }
                 // row sums of the very bf16 P the PV product uses
 #pragma unroll

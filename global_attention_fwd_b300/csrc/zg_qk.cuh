@@ -186,7 +186,7 @@ __device__ __forceinline__ void qk_norm_rope_row_pair_ct(uint8_t* base, uint32_t
     const int part = lane & 1;
     const int c0 = part * NC2;
     float2 ss2 = make_float2(0.f, 0.f);
-#pragma unroll
+#pragma unroll 2
     for (int c = 0; c < NC2; ++c) {
         const uint4 v =
             *reinterpret_cast<const uint4*>(base + ((c0 + c) >> 3) * chunk_stride + sw128_off(row, (c0 + c) & 7));
@@ -201,24 +201,40 @@ __device__ __forceinline__ void qk_norm_rope_row_pair_ct(uint8_t* base, uint32_t
     const float inv = ss > 0.f || eps > 0.f ? rsqrtf(ss * (1.0f / D) + eps) : 0.f;
     const float2 inv2 = make_float2(inv, inv);
     float y[NR * 8];  // even lane: normalised dims [0, 8*NR) before rotation
-#pragma unroll
-    for (int c = 0; c < NC2; ++c) {
+    // chunk c of this lane's half row: x * inv * w (kept for the rotation on the even lane's first NR
+    // chunks, stored otherwise)
+    auto chunk = [&](int c, float2 (&yy)[4]) {
         const int cg = c0 + c;
-        uint8_t* cp = base + (cg >> 3) * chunk_stride + sw128_off(row, cg & 7);
-        const uint4 v = *reinterpret_cast<const uint4*>(cp);
+        const uint4 v = *reinterpret_cast<const uint4*>(base + (cg >> 3) * chunk_stride + sw128_off(row, cg & 7));
         const float4 w0 = *reinterpret_cast<const float4*>(w_s + cg * 8);
         const float4 w1 = *reinterpret_cast<const float4*>(w_s + cg * 8 + 4);
-        const float2 y0 = mul2(mul2(bf2f2(v.x), make_float2(w0.x, w0.y)), inv2);
-        const float2 y1 = mul2(mul2(bf2f2(v.y), make_float2(w0.z, w0.w)), inv2);
-        const float2 y2 = mul2(mul2(bf2f2(v.z), make_float2(w1.x, w1.y)), inv2);
-        const float2 y3 = mul2(mul2(bf2f2(v.w), make_float2(w1.z, w1.w)), inv2);
-        if (c < NR) {  // kept for the rotation (meaningful on the even lane only)
-            y[c * 8 + 0] = y0.x; y[c * 8 + 1] = y0.y; y[c * 8 + 2] = y1.x; y[c * 8 + 3] = y1.y;
-            y[c * 8 + 4] = y2.x; y[c * 8 + 5] = y2.y; y[c * 8 + 6] = y3.x; y[c * 8 + 7] = y3.y;
+        yy[0] = mul2(mul2(bf2f2(v.x), make_float2(w0.x, w0.y)), inv2);
+        yy[1] = mul2(mul2(bf2f2(v.y), make_float2(w0.z, w0.w)), inv2);
+        yy[2] = mul2(mul2(bf2f2(v.z), make_float2(w1.x, w1.y)), inv2);
+        yy[3] = mul2(mul2(bf2f2(v.w), make_float2(w1.z, w1.w)), inv2);
+    };
+    auto store = [&](int c, const float2 (&yy)[4]) {
+        const int cg = c0 + c;
+        *reinterpret_cast<uint4*>(base + (cg >> 3) * chunk_stride + sw128_off(row, cg & 7)) =
+            make_uint4(pack_half2(yy[0].x, yy[0].y), pack_half2(yy[1].x, yy[1].y), pack_half2(yy[2].x, yy[2].y),
+                       pack_half2(yy[3].x, yy[3].y));
+    };
+#pragma unroll
+    for (int c = 0; c < NR; ++c) {
+        float2 yy[4];
+        chunk(c, yy);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            y[c * 8 + 2 * k] = yy[k].x;
+            y[c * 8 + 2 * k + 1] = yy[k].y;
         }
-        if (active && (part == 1 || c >= NR))
-            *reinterpret_cast<uint4*>(cp) = make_uint4(pack_half2(y0.x, y0.y), pack_half2(y1.x, y1.y),
-                                                       pack_half2(y2.x, y2.y), pack_half2(y3.x, y3.y));
+        if (active && part == 1) store(c, yy);
+    }
+#pragma unroll 1  // rolled: this helper runs beside the kernel's other roles, and code size costs fetch
+    for (int c = NR; c < NC2; ++c) {  // no rotated dims here (on either lane)
+        float2 yy[4];
+        chunk(c, yy);
+        if (active) store(c, yy);
     }
     // cos/sin: lane (grp | h) evaluates frequencies j = i*SL + h; everyone gathers them
     const int mine = lane & (SL - 1);
