@@ -566,18 +566,12 @@ __global__ void __launch_bounds__(kThreads, 1) swa2_kernel(const __grid_constant
                 // P (keys cb..cb+15) -> TMEM columns cb/2 .. cb/2+7 of this S buffer (already read)
                 tmem_st8(s_addr + cb / 2, pk);
             };
-            uint32_t ra[16], rb[16];
-            tmem_ld16(s_addr, ra);
-            tmem_wait_ld();
 #pragma unroll 1
-            for (int cb = 0; cb < C::NK; cb += 32) {
-                if (cb + 16 < C::NK) tmem_ld16(s_addr + cb + 16, rb);
+            for (int cb = 0; cb < C::NK; cb += 16) {
+                uint32_t ra[16];
+                tmem_ld16(s_addr + cb, ra);
+                tmem_wait_ld();
                 soft16(ra, cb);
-                tmem_wait_ld();
-                if (cb + 16 >= C::NK) break;
-                if (cb + 32 < C::NK) tmem_ld16(s_addr + cb + 32, ra);
-                soft16(rb, cb + 16);
-                tmem_wait_ld();
             }
             {
                 uint32_t lv[8];
