@@ -194,7 +194,8 @@ __global__ void __launch_bounds__(256) bwd_tc_prep_kernel(const __grid_constant_
         const bool valid = row < nq + nk;
         xr[i] = valid ? *reinterpret_cast<const uint2*>((is_q ? p.q : p.k) + static_cast<size_t>(r) * D + lane * 4)
                       : make_uint2(0u, 0u);
-        pos[i] = valid ? __ldg(p.pos + r / static_cast<unsigned>(is_q ? p.Hq : p.Hkv)) : 0;
+        const unsigned tok = r / static_cast<unsigned>(is_q ? p.Hq : p.Hkv);
+        pos[i] = valid && idx_ok(p.ctl, tok, static_cast<long long>(p.B) * p.L, 150) ? __ldg(p.pos + tok) : 0;
         if (valid && is_q && gated) {
             gr[i] = *reinterpret_cast<const uint2*>(p.gate + static_cast<size_t>(r) * D + lane * 4);
             dr[i] = *reinterpret_cast<const uint2*>(p.dout + static_cast<size_t>(r) * D + lane * 4);
@@ -515,7 +516,8 @@ __global__ void __launch_bounds__(kQThreads, 1) bwd_qpass_kernel(const __grid_co
             ok = __all_sync(0xffffffffu, ok);
         }
         const float Dd = Dp + exchange(2, make_float2(Dp, 0.f)).x;
-        if (ok && hf == 0 && valid_row) p.stat[qrow] = make_float4(m, il, Dd, 0.f);
+        if (ok && hf == 0 && valid_row && idx_ok(p.ctl, qrow, static_cast<long long>(p.B) * p.L * p.Hq, 152))
+            p.stat[qrow] = make_float4(m, il, Dd, 0.f);
         // ---- dS = P (dP - D) / l on this warp's 80 keys, packed bf16 over dP
         if (ok) {
 #pragma unroll 1
@@ -555,7 +557,8 @@ __global__ void __launch_bounds__(kQThreads, 1) bwd_qpass_kernel(const __grid_co
                                     __uint_as_float(v[4 * c + 2]) * p.scale, __uint_as_float(v[4 * c + 3]) * p.scale);
             }
             // cos / sin of this row's token: its eight threads (4 rows x 2 halves) share the pairs
-            const int pos = valid_row ? __ldg(p.pos + static_cast<long long>(b) * p.L + t) : 0;
+            const long long pi = static_cast<long long>(b) * p.L + t;
+            const int pos = valid_row && idx_ok(p.ctl, pi, static_cast<long long>(p.B) * p.L, 153) ? __ldg(p.pos + pi) : 0;
             for (int j = (row % G) * 2 + hf; j < p.rope.half; j += 2 * G) {
                 float cs, sn;
                 rope_cos_sin(pos, p.rope.f_hi[j], p.rope.f_lo[j], cs, sn);
@@ -815,8 +818,10 @@ __global__ void __launch_bounds__(kKThreads, 1) bwd_kpass_kernel(const __grid_co
             for (int i = 0; i < 2; ++i) {
                 const int c = 64 * h + lane + 32 * i;
                 const int u = u0 + c / G;
-                sts[lane + 32 * i] = u < p.L ? p.stat[(static_cast<long long>(b) * p.L + u) * p.Hq + g * G + c % G]
-                                             : make_float4(0.f, 0.f, 0.f, 0.f);
+                const long long si = (static_cast<long long>(b) * p.L + u) * p.Hq + g * G + c % G;
+                sts[lane + 32 * i] = u < p.L && idx_ok(p.ctl, si, static_cast<long long>(p.B) * p.L * p.Hq, 154)
+                                         ? p.stat[si]
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
             }
             __syncwarp();
             if (aborted() || !__all_sync(0xffffffffu, mbar_wait(&s_full[h], n & 1, p.ctl, 116))) {
@@ -881,7 +886,8 @@ __global__ void __launch_bounds__(kKThreads, 1) bwd_kpass_kernel(const __grid_co
             }
             if (ok) {
                 if (valid_key) {
-                    const int pos = __ldg(p.pos + static_cast<long long>(b) * p.L + kj);
+                    const long long pi = static_cast<long long>(b) * p.L + kj;
+                    const int pos = idx_ok(p.ctl, pi, static_cast<long long>(p.B) * p.L, 155) ? __ldg(p.pos + pi) : 0;
                     row_norm_rope_bwd(dk_t, row, smem + KP_X, w_s, p.eps, p.rope.half, [&](int j) {
                         float cs, sn;
                         rope_cos_sin(pos, p.rope.f_hi[j], p.rope.f_lo[j], cs, sn);
@@ -1161,8 +1167,9 @@ __global__ void __launch_bounds__(kGThreads, 1) bwd_qpass_global_kernel(const __
         }
         const float inv_l = lt > 0.f ? 1.0f / lt : 0.f;
         const float dd = dt * inv_l;
-        if (hf == 0 && valid_row && ok)
-            p.stat[(static_cast<long long>(b) * p.L + t) * p.Hq + g * G + row % G] = make_float4(mm, inv_l, dd, 0.f);
+        const long long si = (static_cast<long long>(b) * p.L + t) * p.Hq + g * G + row % G;
+        if (hf == 0 && valid_row && ok && idx_ok(p.ctl, si, static_cast<long long>(p.B) * p.L * p.Hq, 156))
+            p.stat[si] = make_float4(mm, inv_l, dd, 0.f);
         for (int n = 0; n < nblk && ok; ++n) {
             if (aborted() || !__all_sync(0xffffffffu, mbar_wait(s_full, (nblk + n) & 1, p.ctl, 139))) {
                 ok = false;
@@ -1211,7 +1218,8 @@ __global__ void __launch_bounds__(kGThreads, 1) bwd_qpass_global_kernel(const __
             }
             if (ok) {
                 if (valid_row) {
-                    const int pos = __ldg(p.pos + static_cast<long long>(b) * p.L + t);
+                    const long long pi = static_cast<long long>(b) * p.L + t;
+                    const int pos = idx_ok(p.ctl, pi, static_cast<long long>(p.B) * p.L, 157) ? __ldg(p.pos + pi) : 0;
                     row_norm_rope_bwd(dq_t, row, smem + GQ_X, w_s, p.eps, p.rope.half, [&](int j) {
                         float cs, sn;
                         rope_cos_sin(pos, p.rope.f_hi[j], p.rope.f_lo[j], cs, sn);

@@ -4,7 +4,8 @@ the access; an index out of range is recorded in the device error word and skipp
 
 The debug library runs in a child process (ZG_LIBRARY=debug selects it in the binding) on
 small, odd shapes through every instrumented kernel -- gated SWA and global prefill, the k_hat
-pre-pass, the E4M3 global prefill and its pre-passes, the decode step and its split merge (bf16 and E4M3 caches), the cache writer -- each
+pre-pass, the E4M3 global and sliding-window prefills and their pre-passes, the tensor-core
+backward (windowed and global), the decode step and its split merge (bf16 and E4M3 caches), the cache writer -- each
 checked against the fp64 oracle with a clean error word.  Then the index check's own error
 path is exercised without a fault (zg_selftest_index_check) and the context is shown to be
 usable afterwards.  In the normal build the same self test records nothing."""
@@ -87,6 +88,51 @@ def prefill_e4m3(B, L, Hq, Hkv, seed):  # global prefill on E4M3 inputs (k_hat a
 
 prefill_e4m3(2, 45, 8, 2, 9)      # ragged: 45 keys, V^T padded to 48
 prefill_e4m3(1, 200, 16, 1, 10)   # GQA 16
+
+def swa_e4m3(B, L, Hq, Hkv, W, seed):  # gated sliding window on E4M3 inputs (the global pipeline's window mode)
+    g = torch.Generator().manual_seed(seed)
+    st = {n: workloads.to_e4m3(rnd(B, L, h, 128, g=g), 1.0).view(torch.uint8) for n, h in (("q", Hq), ("k", Hkv), ("v", Hkv))}
+    deq = {n: st[n].view(torch.float8_e4m3fn).double() for n in st}
+    gate = rnd(B, L, Hq, 128, g=g)
+    pos = torch.arange(L, dtype=torch.int32).repeat(B, 1).contiguous()
+    wq, wk = 0.5 + torch.rand(128, generator=g), 0.5 + torch.rand(128, generator=g)
+    out = zg.swa_prefill_fp8(st["q"].cuda(), st["k"].cuda(), st["v"].cuda(), gate.cuda(), pos.cuda(), wq.cuda(), wk.cuda(),
+                             window=W, rotary_dim=42, theta=1e4)
+    torch.cuda.synchronize()
+    clean(f"e4m3 swa prefill {B} {L} {Hq}/{Hkv} W{W}")
+    rows = list(range(B * L))
+    ref = oracle.prefill_rows(deq["q"], deq["k"], deq["v"], gate.double(), pos, wq, wk, window=W, rotary_dim=42,
+                              theta=1e4, eps=1e-6, rows=rows)
+    got = rows_of(out, rows)
+    err = float(np.linalg.norm(got - ref) / np.linalg.norm(ref))
+    assert err <= 0.10, err
+
+swa_e4m3(2, 150, 8, 2, 37, 11)    # odd window, two sequences
+
+from oracle import backward as bw
+
+def backward(B, L, Hq, Hkv, W, gated, seed):  # the tensor-core backward (windowed, or the global layer for W = 0)
+    g = torch.Generator().manual_seed(seed)
+    x = dict(q=rnd(B, L, Hq, 128, g=g), k=rnd(B, L, Hkv, 128, g=g), v=rnd(B, L, Hkv, 128, g=g),
+             gate=rnd(B, L, Hq, 128, g=g) if gated else None, dout=rnd(B, L, Hq, 128, g=g),
+             pos=torch.arange(L, dtype=torch.int32).repeat(B, 1).contiguous(),
+             wq=0.5 + torch.rand(128, generator=g), wk=0.5 + torch.rand(128, generator=g))
+    d = {k: (v.cuda() if v is not None else None) for k, v in x.items()}
+    got = zg.attention_backward(d["q"], d["k"], d["v"], d["gate"], d["pos"], d["wq"], d["wk"], d["dout"], window=W,
+                                rotary_dim=42, theta=1e4)
+    torch.cuda.synchronize()
+    clean(f"backward {B} {L} {Hq}/{Hkv} W{W}")
+    ref = bw.gradients(x["q"], x["k"], x["v"], x["gate"], x["pos"], x["wq"], x["wk"], x["dout"], window=W, rotary_dim=42,
+                       theta=1e4, eps=1e-6)
+    for n, a, r in zip(("dq", "dk", "dv", "dgate"), got, ref):
+        if r is None:
+            continue
+        a = a.double().cpu().numpy(); r = r.detach().double().numpy()
+        rel = float(np.linalg.norm(a - r) / np.linalg.norm(r))
+        assert rel <= 1e-2, (n, rel)  # the tensor-core path's bar
+
+backward(1, 170, 8, 2, 128, True, 12)   # windowed, ragged last tile
+backward(1, 300, 4, 1, 0, False, 13)    # the global layer: three key blocks
 
 def decode(flags, B, Hq, Hkv, d, S, W, positions, seed, fp8):
     g = torch.Generator().manual_seed(seed)
