@@ -11,9 +11,10 @@ Inputs are drawn once on the device with seeded generators and stay resident in
 HBM; every input is larger than the 126 MB L2, so no flush is needed between
 steps.  `value` is the gated-SWA prefill throughput (tokens/s summed over all
 ranks, from CUDA events around that call); `parts` reports every call with its
-own roofline.  `e2e` repeats the SWA prefill through the same public API with
-the inputs in pinned host memory, the host->device copies and the device->host
-copy of the output inside the timed region.  Outside the step, `parts` also
+own roofline.  `e2e` runs the SWA prefill through the C-ABI call on host
+buffers (zg_swa_prefill_host): the inputs in pinned host memory, copied in and the
+output copied back inside the call and the timed region, chunk by chunk,
+overlapped with the kernel.  Outside the step, `parts` also
 times the other workloads one by one: the tiny gated SWA prefill (latency, L2
 flushed), the B=4 L=4096 gated SWA prefill (L2 flushed), the global prefill at
 L=262144 (bf16, and with E4M3 inputs on the E4M3 tensor-core path), the SWA
@@ -431,31 +432,49 @@ def run_gpu(args):
     roofline = dict(top, kernel=dominant, peak_source=f"{peak_kind} (MEASURED_PEAKS.json)" if peak_kind == "measured"
                     else "fallback")
 
-    # ---- e2e: SWA prefill through the public API with pinned host buffers
+    # ---- e2e: the SWA prefill through the C-ABI call on host buffers (zg_swa_prefill_host): the
+    # inputs in page-locked host memory, copied in and the output copied back inside the call, chunk
+    # by chunk, overlapped with the kernel
     e2e = None
     if not args.no_e2e:
         host = {k: v.cpu().pin_memory() for k, v in sx.items()}
         host_out = torch.empty(s_out.shape, dtype=s_out.dtype).pin_memory()
-        h2d = sum(v.numel() * v.element_size() for v in host.values())
+        chunk = 16384
+        hws = torch.empty(zg.swa_prefill_host_workspace_bytes(SWA.B, SWA.Hq, SWA.Hkv, SWA.d, SWA.window, chunk),
+                          dtype=torch.uint8, device=dev)
+        n_chunks = (SWA.L + chunk - 1) // chunk
+        halo = (n_chunks - 1) * ((SWA.window - 1 + 127) // 128 * 128)  # extra key / value / position rows copied
+        kv_row = SWA.Hkv * SWA.d * 2
+        h2d = (sum(host[k].numel() * host[k].element_size() for k in ("q", "k", "v", "gate", "pos", "wq", "wk")) +
+               SWA.B * halo * (2 * kv_row + 4))
         d2h = host_out.numel() * host_out.element_size()
+
+        def e2e_call():
+            zg.swa_prefill_host(host["q"], host["k"], host["v"], host["gate"], host["pos"], host["wq"], host["wk"],
+                                window=SWA.window, rotary_dim=SWA.rotary_dim, theta=SWA.theta, eps=SWA.eps,
+                                out=host_out, chunk_tokens=chunk, workspace=hws)
+
+        e2e_call()
         e_steps = max(1, min(args.steps, 3))
         barrier()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for _ in range(e_steps):
-            for k in ("q", "k", "v", "gate", "pos", "wq", "wk"):
-                sx[k].copy_(host[k], non_blocking=True)
-            swa()
-            host_out.copy_(s_out, non_blocking=True)
+            e2e_call()
         e1.record(stream)
         barrier()
         e_ms = e0.elapsed_time(e1)
         ev_ = torch.tensor([e_ms], dtype=torch.float64, device=dev)
         if ws > 1:
             torch.distributed.all_reduce(ev_, op=torch.distributed.ReduceOp.MAX)
+        st_, det_ = zg.device_status()
+        if st_ != 0:
+            raise RuntimeError(f"device status {st_} detail {det_:#x} after the host-buffer call")
         e2e = {"value": ws * SWA.tokens * e_steps / (ev_.item() * 1e-3), "unit": "tokens/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e_steps}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e_steps,
+               "call": f"zg_swa_prefill_host, pinned host buffers, chunks of {chunk} tokens"}
+        del hws
 
     # ---- CPU baseline: the oracle on a bounded sample (rank 0, N=1 only)
     cpu = None

@@ -26,7 +26,7 @@ STATUS = {
     -5: "ZG_ERR_POSITION", -6: "ZG_ERR_WORKSPACE", -7: "ZG_ERR_CUDA", -8: "ZG_ERR_DEVICE_TIMEOUT",
     -9: "ZG_ERR_UNIMPLEMENTED", -10: "ZG_ERR_DEVICE_INDEX",
 }
-EXPORTS = ("zg_swa_prefill", "zg_global_prefill_workspace_bytes", "zg_global_prefill",
+EXPORTS = ("zg_swa_prefill", "zg_swa_prefill_host_workspace_bytes", "zg_swa_prefill_host", "zg_global_prefill_workspace_bytes", "zg_global_prefill",
            "zg_swa_prefill_with_cache", "zg_global_prefill_with_cache", "zg_kv_cache_write",
            "zg_gated_swa_layer_workspace_bytes", "zg_gated_swa_layer", "zg_linear",
            "zg_attention_backward_workspace_bytes", "zg_attention_backward",
@@ -51,6 +51,10 @@ def _load() -> ctypes.CDLL:
                                 ctypes.c_size_t, ctypes.c_uint64)
     lib.zg_swa_prefill.argtypes = [P] * 8 + [I] * 7 + [D, F, P]
     lib.zg_swa_prefill.restype = I
+    lib.zg_swa_prefill_host_workspace_bytes.argtypes = [I] * 6
+    lib.zg_swa_prefill_host_workspace_bytes.restype = SZ
+    lib.zg_swa_prefill_host.argtypes = [P] * 8 + [I] * 7 + [D, F, I, P, SZ, P]
+    lib.zg_swa_prefill_host.restype = I
     lib.zg_global_prefill_workspace_bytes.argtypes = [I, I, I, I]
     lib.zg_global_prefill_workspace_bytes.restype = SZ
     lib.zg_global_prefill.argtypes = [P] * 7 + [I] * 6 + [D, F, P, SZ, P]
@@ -145,6 +149,50 @@ def swa_prefill(q, k, v, gate, pos, wq, wk, *, window=128, rotary_dim, theta, ep
     st = _lib.zg_swa_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(gate), _ptr(pos), _ptr(wq), _ptr(wk), _ptr(out),
                              B, L, Hq, Hkv, d, int(window), int(rotary_dim), float(theta), float(eps), _stream(stream))
     _raise(st, "zg_swa_prefill")
+    return out
+
+
+def swa_prefill_host_workspace_bytes(B, Hq, Hkv, d, window=128, chunk_tokens=16384) -> int:
+    return int(_lib.zg_swa_prefill_host_workspace_bytes(int(B), int(Hq), int(Hkv), int(d), int(window),
+                                                        int(chunk_tokens)))
+
+
+def _check_host(t, name, dtype, ndim=None):
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if t.is_cuda:
+        raise ValueError(f"{name} must be a host (CPU) tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {t.dim()}")
+
+
+def swa_prefill_host(q, k, v, gate, pos, wq, wk, *, window=128, rotary_dim, theta, eps=1e-6, out=None,
+                     chunk_tokens=16384, workspace=None, stream=None):
+    """swa_prefill on HOST tensors (pinned for overlap): the copies to and from the device happen inside the
+    call, chunk by chunk, overlapped with the kernel.  workspace: optional uint8 CUDA tensor of
+    >= swa_prefill_host_workspace_bytes() bytes.  Returns out (host, bf16)."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (gate, "gate")):
+        _check_host(t, n, torch.bfloat16, 4)
+    _check_host(pos, "pos", torch.int32, 2)
+    _check_host(wq, "wq", torch.float32)
+    _check_host(wk, "wk", torch.float32)
+    B, L, Hq, d = q.shape
+    Hkv = k.shape[2]
+    if out is None:
+        out = torch.empty(B, L, Hq, d, dtype=torch.bfloat16, pin_memory=True)
+    _check_host(out, "out", torch.bfloat16, 4)
+    need = swa_prefill_host_workspace_bytes(B, Hq, Hkv, d, window, chunk_tokens)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device="cuda")
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = _lib.zg_swa_prefill_host(_ptr(q), _ptr(k), _ptr(v), _ptr(gate), _ptr(pos), _ptr(wq), _ptr(wk), _ptr(out),
+                                  B, L, Hq, Hkv, d, int(window), int(rotary_dim), float(theta), float(eps),
+                                  int(chunk_tokens), _ptr(workspace), ws_bytes, _stream(stream))
+    _raise(st, "zg_swa_prefill_host")
     return out
 
 

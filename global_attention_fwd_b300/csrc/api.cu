@@ -1,5 +1,6 @@
 // api.cu -- the C ABI declared in include/zg_attn.h: argument checks, TMA
 // descriptors, RoPE constants, launches.  No device memory is allocated here.
+#include <algorithm>
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
@@ -413,6 +414,132 @@ zg_status zg_kv_cache_write_fp8(const zg_bf16* k, const zg_bf16* v, const int32_
     if (static_cast<long long>(B) * L * Hkv / 8 >= (1ll << 31)) return ZG_ERR_UNSUPPORTED;
     return write_cache(k, v, pos, wk, k_cache, v_cache, B, L, Hkv, d, S, ring != 0, rotary_dim, theta, eps, stream, 1,
                        k_scale, v_scale);
+}
+
+// ---- the gated SWA prefill from host buffers: chunks of tokens pipelined over three streams
+namespace {
+constexpr int kHostSlots = 2;  // device staging slots (chunk c uses slot c mod 2)
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+struct HostSlotLayout {
+    size_t q, k, v, gate, pos, out, bytes;  // offsets inside one slot, and its size
+};
+HostSlotLayout host_slot_layout(int B, int rows, int Hq, int Hkv, int d) {
+    HostSlotLayout s;
+    const size_t nq = static_cast<size_t>(B) * rows * Hq * d * 2, nk = static_cast<size_t>(B) * rows * Hkv * d * 2;
+    s.q = 0;
+    s.gate = s.q + align256(nq);
+    s.out = s.gate + align256(nq);
+    s.k = s.out + align256(nq);
+    s.v = s.k + align256(nk);
+    s.pos = s.v + align256(nk);
+    s.bytes = s.pos + align256(static_cast<size_t>(B) * rows * 4);
+    return s;
+}
+// halo of earlier keys a chunk carries: the window's W - 1 keys, rounded up to whole 128-token
+// blocks so the chunk's query tiles fall where they fall in one unchunked call
+int host_halo(int window) { return (window - 1 + 127) / 128 * 128; }
+}  // namespace
+
+size_t zg_swa_prefill_host_workspace_bytes(int B, int Hq, int Hkv, int d, int window, int chunk_tokens) {
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || window < 1 || chunk_tokens <= 0) return 0;
+    const int rows = chunk_tokens + host_halo(window);
+    return 256 + kHostSlots * host_slot_layout(B, rows, Hq, Hkv, d).bytes + 2 * static_cast<size_t>(d) * 4;
+}
+
+zg_status zg_swa_prefill_host(const zg_bf16* q, const zg_bf16* k, const zg_bf16* v, const zg_bf16* gate,
+                              const int32_t* pos, const float* wq, const float* wk, zg_bf16* out, int B, int L, int Hq,
+                              int Hkv, int d, int window, int rotary_dim, double theta, float eps, int chunk_tokens,
+                              void* workspace, size_t workspace_bytes, zg_stream stream) {
+    if (!q || !k || !v || !gate || !pos || !wq || !wk || !out) return ZG_ERR_NULL;
+    if (B < 0 || L < 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || Hq % Hkv || window < 1 || chunk_tokens <= 0)
+        return ZG_ERR_SHAPE;
+    if (B == 0 || L == 0) return ZG_OK;
+    const size_t need = zg_swa_prefill_host_workspace_bytes(B, Hq, Hkv, d, window, chunk_tokens);
+    if (!workspace || workspace_bytes < need || !aligned16(workspace)) return ZG_ERR_WORKSPACE;
+    const int halo = host_halo(window);
+    const int cap = chunk_tokens + halo;  // rows of one slot
+    const HostSlotLayout lay = host_slot_layout(B, cap, Hq, Hkv, d);
+    uint8_t* base = static_cast<uint8_t*>(workspace);
+    float* wq_d = reinterpret_cast<float*>(base + kHostSlots * lay.bytes);
+    float* wk_d = wq_d + d;
+    const size_t rq = static_cast<size_t>(Hq) * d * 2, rk = static_cast<size_t>(Hkv) * d * 2;  // bytes per token
+    cudaStream_t user = reinterpret_cast<cudaStream_t>(stream);
+    cudaStream_t s_in = nullptr, s_run = nullptr, s_out = nullptr;
+    cudaEvent_t ev[3 * kHostSlots + 2] = {};
+    zg_status st = ZG_OK;
+    auto ok = [&](cudaError_t e) {
+        if (e != cudaSuccess && st == ZG_OK) st = ZG_ERR_CUDA;
+        return st == ZG_OK;
+    };
+    bool good = ok(cudaStreamCreateWithFlags(&s_in, cudaStreamNonBlocking)) &&
+                ok(cudaStreamCreateWithFlags(&s_run, cudaStreamNonBlocking)) &&
+                ok(cudaStreamCreateWithFlags(&s_out, cudaStreamNonBlocking));
+    for (int i = 0; good && i < 3 * kHostSlots + 2; ++i) good = ok(cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming));
+    cudaEvent_t* ev_in = ev;                   // slot inputs copied
+    cudaEvent_t* ev_run = ev + kHostSlots;     // slot kernel done
+    cudaEvent_t* ev_out = ev + 2 * kHostSlots; // slot output copied back
+    cudaEvent_t ev_start = ev[3 * kHostSlots], ev_end = ev[3 * kHostSlots + 1];
+    if (good) {  // the internal streams start after the caller's earlier work
+        good = ok(cudaEventRecord(ev_start, user)) && ok(cudaStreamWaitEvent(s_in, ev_start, 0)) &&
+               ok(cudaStreamWaitEvent(s_run, ev_start, 0)) &&
+               ok(cudaMemcpyAsync(wq_d, wq, static_cast<size_t>(d) * 4, cudaMemcpyHostToDevice, s_in)) &&
+               ok(cudaMemcpyAsync(wk_d, wk, static_cast<size_t>(d) * 4, cudaMemcpyHostToDevice, s_in));
+    }
+    const int n_chunks = (L + chunk_tokens - 1) / chunk_tokens;
+    for (int c = 0; good && c < n_chunks; ++c) {
+        const int sl = c % kHostSlots;
+        uint8_t* sb = base + sl * lay.bytes;
+        const int t0 = c * chunk_tokens, t1 = std::min(L, t0 + chunk_tokens);
+        const int h = std::min(t0, halo), lc = (t1 - t0) + h;
+        auto* qd = reinterpret_cast<zg_bf16*>(sb + lay.q);
+        auto* gd = reinterpret_cast<zg_bf16*>(sb + lay.gate);
+        auto* od = reinterpret_cast<zg_bf16*>(sb + lay.out);
+        auto* kd = reinterpret_cast<zg_bf16*>(sb + lay.k);
+        auto* vd = reinterpret_cast<zg_bf16*>(sb + lay.v);
+        auto* pd = reinterpret_cast<int32_t*>(sb + lay.pos);
+        // inputs: keys, values and positions of the halo and the chunk; queries and gate of the chunk
+        // (the halo rows' outputs are computed and dropped); the slot's previous kernel must be done
+        if (c >= kHostSlots) good = ok(cudaStreamWaitEvent(s_in, ev_run[sl], 0));
+        const auto* kh = reinterpret_cast<const uint8_t*>(k);
+        const auto* vh = reinterpret_cast<const uint8_t*>(v);
+        const auto* qh = reinterpret_cast<const uint8_t*>(q);
+        const auto* gh = reinterpret_cast<const uint8_t*>(gate);
+        const auto* ph = reinterpret_cast<const uint8_t*>(pos);
+        good = good &&
+               ok(cudaMemcpy2DAsync(kd, lc * rk, kh + (t0 - h) * rk, L * rk, lc * rk, B, cudaMemcpyHostToDevice, s_in)) &&
+               ok(cudaMemcpy2DAsync(vd, lc * rk, vh + (t0 - h) * rk, L * rk, lc * rk, B, cudaMemcpyHostToDevice, s_in)) &&
+               ok(cudaMemcpy2DAsync(pd, static_cast<size_t>(lc) * 4, ph + static_cast<size_t>(t0 - h) * 4,
+                                    static_cast<size_t>(L) * 4, static_cast<size_t>(lc) * 4, B, cudaMemcpyHostToDevice,
+                                    s_in)) &&
+               ok(cudaMemcpy2DAsync(reinterpret_cast<uint8_t*>(qd) + h * rq, lc * rq, qh + t0 * rq, L * rq,
+                                    (t1 - t0) * rq, B, cudaMemcpyHostToDevice, s_in)) &&
+               ok(cudaMemcpy2DAsync(reinterpret_cast<uint8_t*>(gd) + h * rq, lc * rq, gh + t0 * rq, L * rq,
+                                    (t1 - t0) * rq, B, cudaMemcpyHostToDevice, s_in)) &&
+               ok(cudaEventRecord(ev_in[sl], s_in));
+        // the kernel, once the inputs are in and the slot's previous output has been copied out
+        good = good && ok(cudaStreamWaitEvent(s_run, ev_in[sl], 0)) &&
+               (c < kHostSlots || ok(cudaStreamWaitEvent(s_run, ev_out[sl], 0)));
+        if (good) {
+            const zg_status ks = zg_swa_prefill(qd, kd, vd, gd, pd, wq_d, wk_d, od, B, lc, Hq, Hkv, d, window,
+                                                rotary_dim, theta, eps, reinterpret_cast<zg_stream>(s_run));
+            if (ks != ZG_OK) {
+                st = ks;
+                good = false;
+            }
+        }
+        good = good && ok(cudaEventRecord(ev_run[sl], s_run)) && ok(cudaStreamWaitEvent(s_out, ev_run[sl], 0)) &&
+               ok(cudaMemcpy2DAsync(reinterpret_cast<uint8_t*>(out) + t0 * rq, L * rq,
+                                    reinterpret_cast<uint8_t*>(od) + h * rq, lc * rq, (t1 - t0) * rq, B,
+                                    cudaMemcpyDeviceToHost, s_out)) &&
+               ok(cudaEventRecord(ev_out[sl], s_out));
+    }
+    // the caller's stream continues after the last copy back (or after whatever was issued)
+    if (s_out && ev_end && cudaEventRecord(ev_end, s_out) == cudaSuccess) (void)cudaStreamWaitEvent(user, ev_end, 0);
+    for (auto& e : ev)
+        if (e) cudaEventDestroy(e);  // released once their work is done
+    for (cudaStream_t x : {s_in, s_run, s_out})
+        if (x) cudaStreamDestroy(x);
+    return st;
 }
 
 zg_status zg_swa_prefill_with_cache(const zg_bf16* q, const zg_bf16* k, const zg_bf16* v, const zg_bf16* gate,

@@ -95,6 +95,33 @@ zg_status zg_swa_prefill(const zg_bf16 *q, const zg_bf16 *k, const zg_bf16 *v, c
                          int B, int L, int Hq, int Hkv, int d, int window, int rotary_dim,
                          double theta, float eps, zg_stream stream);
 
+/* Bytes of device workspace zg_swa_prefill_host needs: two staging slots of
+ * chunk_tokens + the key halo (window - 1 rounded up to 128) tokens of every tensor, and the
+ * norm weights (0 for invalid sizes). */
+size_t zg_swa_prefill_host_workspace_bytes(int B, int Hq, int Hkv, int d, int window, int chunk_tokens);
+
+/*
+ * zg_swa_prefill_host -- zg_swa_prefill on HOST buffers, the copies overlapped with the work.
+ *   q, k, v, gate, pos, wq, wk, out: HOST pointers with zg_swa_prefill's layouts (out is
+ *        written).  Page-locked (pinned) memory lets the copies run asynchronously and overlap;
+ *        pageable memory gives the same result without the overlap.
+ *   The sequence is processed in chunks of chunk_tokens tokens (every sequence of the batch at
+ *   once): chunk c's inputs go to the device (its keys, values and positions with the window's
+ *   key halo before it), the prefill kernel runs on it, and its output rows come back, on three
+ *   internal streams, so that the copy of chunk c + 1 in, the kernel of chunk c and the copy of
+ *   chunk c - 1 out run at the same time.  The halo makes every output identical to one
+ *   zg_swa_prefill call over the whole sequence.
+ *   workspace: device scratch of at least zg_swa_prefill_host_workspace_bytes() bytes,
+ *        16-byte aligned (ZG_ERR_WORKSPACE otherwise); no initialisation.
+ *   stream: the work starts after the stream's earlier work and the stream waits for the last
+ *        copy back, so a synchronisation of the stream (or the device) completes the call.
+ * Errors as zg_swa_prefill (ZG_ERR_SHAPE also for chunk_tokens < 1), plus ZG_ERR_CUDA.
+ */
+zg_status zg_swa_prefill_host(const zg_bf16 *q, const zg_bf16 *k, const zg_bf16 *v, const zg_bf16 *gate,
+                              const int32_t *pos, const float *wq, const float *wk, zg_bf16 *out, int B, int L,
+                              int Hq, int Hkv, int d, int window, int rotary_dim, double theta, float eps,
+                              int chunk_tokens, void *workspace, size_t workspace_bytes, zg_stream stream);
+
 /* Bytes of workspace zg_global_prefill needs: B * L * Hkv * d * 2 (0 for empty input). */
 size_t zg_global_prefill_workspace_bytes(int B, int L, int Hkv, int d);
 
