@@ -785,6 +785,7 @@ zg_status zg_attention_backward(const zg_bf16* q, const zg_bf16* k, const zg_bf1
         t.Hq = Hq;
         t.Hkv = Hkv;
         t.global = global_tc ? 1 : 0;
+        t.fold = !global_tc && rotary_dim <= 64 ? 1 : 0;
         t.window = global_tc ? L : window;
         t.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
         t.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));

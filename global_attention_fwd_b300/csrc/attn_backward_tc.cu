@@ -182,7 +182,7 @@ __global__ void __launch_bounds__(256) bwd_tc_prep_kernel(const __grid_constant_
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // row indices in 32-bit arithmetic: the host takes this path only for B * L * (Hq + Hkv) < 2^31
     const unsigned nq = static_cast<unsigned>(p.B * p.L) * p.Hq, nk = static_cast<unsigned>(p.B * p.L) * p.Hkv;
-    const unsigned row0 = (blockIdx.x * 8u + warp) * kPrepRows;
+    const unsigned row0 = static_cast<unsigned>(p.prep_first) + (blockIdx.x * 8u + warp) * kPrepRows;
     const bool gated = p.gate != nullptr;
     uint2 xr[kPrepRows], gr[kPrepRows], dr[kPrepRows];
     int pos[kPrepRows];
@@ -253,7 +253,7 @@ __global__ void __launch_bounds__(256) bwd_tc_prep_kernel(const __grid_constant_
 // (max, sum, D, RMSNorm sums) through shared memory and a 64-arrival barrier per exchange.
 // Warp 8: TMA and MMA.
 constexpr int kQThreads = 288;
-constexpr int kNX = 6;  // pair exchanges per tile
+constexpr int kNX = 8;  // pair exchange slots per tile (0-5, and 7 for the RMSNorm sums of the q_hat fold)
 
 __global__ void __launch_bounds__(kQThreads, 1) bwd_qpass_kernel(const __grid_constant__ BackwardTcParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -267,6 +267,7 @@ __global__ void __launch_bounds__(kQThreads, 1) bwd_qpass_kernel(const __grid_co
     uint64_t* gd_full = bar + 6;   // gate and dout tiles (gated layers)
     uint64_t* stg_full = bar + 7;  // [2] dgate staging of a column half written (128 arrivals)
     uint64_t* dq_stg = bar + 9;    // dq staging written (256 arrivals)
+    uint64_t* qd_ready = bar + 10; // fold: q_hat and dA are in shared memory (256 arrivals)
     uint64_t* xbar = bar + 16;     // [kNX][4 quarters] pair exchanges (64 arrivals)
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + QP_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + QP_MISC + 4);
@@ -294,6 +295,7 @@ __global__ void __launch_bounds__(kQThreads, 1) bwd_qpass_kernel(const __grid_co
         mbar_init(&stg_full[0], 128);
         mbar_init(&stg_full[1], 128);
         mbar_init(dq_stg, 256);
+        mbar_init(qd_ready, 256);
         for (int i = 0; i < kNX * 4; ++i) mbar_init(&xbar[i], 64);
         fence_barrier_init();
     }
@@ -322,10 +324,14 @@ __global__ void __launch_bounds__(kQThreads, 1) bwd_qpass_kernel(const __grid_co
             tma_prefetch_desc(&p.tm_kq);
             tma_prefetch_desc(&p.tm_vq);
             tma_prefetch_desc(&p.tm_q);
-            mbar_arrive_expect_tx(ld_full, 3 * TILE128 + 2 * TILE160);
+            // fold: the gate (gated layers) and dout tiles instead of q_hat and dA, which the rows form
+            const bool q_tile = !p.fold || gated;
+            mbar_arrive_expect_tx(ld_full, (q_tile ? 3 : 2) * TILE128 + 2 * TILE160);
             for (int ch = 0; ch < 2; ++ch) {
-                tma_load_4d(smem + QP_Q + ch * CH128, &p.tm_qh, ld_full, ch * 64, g * G, t0, b);
-                tma_load_4d(smem + QP_DA + ch * CH128, &p.tm_da, ld_full, ch * 64, g * G, t0, b);
+                if (q_tile)
+                    tma_load_4d(smem + QP_Q + ch * CH128, p.fold ? &p.tm_gate : &p.tm_qh, ld_full, ch * 64, g * G, t0, b);
+                tma_load_4d(smem + QP_DA + ch * CH128, p.fold && gated ? &p.tm_dout : &p.tm_da, ld_full, ch * 64, g * G,
+                            t0, b);
                 tma_load_4d(smem + QP_K + ch * CH160, &p.tm_kq, ld_full, ch * 64, g, t0 - 128, b);
                 tma_load_4d(smem + QP_V + ch * CH160, &p.tm_vq, ld_full, ch * 64, g, t0 - 128, b);
                 tma_load_4d(smem + QP_X + ch * CH128, &p.tm_q, ld_full, ch * 64, g * G, t0, b);
@@ -333,6 +339,18 @@ __global__ void __launch_bounds__(kQThreads, 1) bwd_qpass_kernel(const __grid_co
             constexpr uint32_t id_s = idesc_bf16_f32(128, NKQ, false, false);
             constexpr uint32_t id_o = idesc_bf16_f32(128, D, false, true);
             bool ok = mbar_wait(ld_full, 0, p.ctl, 101);
+            if (ok && p.fold) {
+                // the rows' q_hat (and dA) go to the workspace for the key pass, read from shared memory
+                // beside the first products; dout is the caller's tensor and is never written
+                ok = mbar_wait(qd_ready, 0, p.ctl, 109);
+                if (ok) {
+                    for (int ch = 0; ch < 2; ++ch) {
+                        tma_store_4d(&p.tm_qh, smem + QP_Q + ch * CH128, ch * 64, g * G, t0, b);
+                        if (gated) tma_store_4d(&p.tm_da, smem + QP_DA + ch * CH128, ch * 64, g * G, t0, b);
+                    }
+                    bulk_commit();
+                }
+            }
             if (ok) {
                 tc_fence_after();
 #pragma unroll
@@ -352,6 +370,7 @@ __global__ void __launch_bounds__(kQThreads, 1) bwd_qpass_kernel(const __grid_co
                 umma_commit(s_full);
                 if (gated) {  // Q_hat and dA are read once the two products are done: reuse them
                     ok = mbar_wait(s_full, 0, p.ctl, 107);
+                    if (ok && p.fold) bulk_wait_all();  // and once their stores have read them
                     if (ok) {
                         mbar_arrive_expect_tx(gd_full, 2 * TILE128);
                         for (int ch = 0; ch < 2; ++ch) {
@@ -405,6 +424,88 @@ __global__ void __launch_bounds__(kQThreads, 1) bwd_qpass_kernel(const __grid_co
             if (ok && !aborted()) ok = __all_sync(0xffffffffu, mbar_wait(&xbar[k * 4 + q4], 0, p.ctl, 90 + k));
             return slot[(1 - hf) * 128 + row];
         };
+        if (p.fold) {
+            // ---- q_hat and dA formed here from the raw tiles (one pass less over HBM than a separate
+            // kernel): dA = dout * sigmoid(gate) in place over dout (gated layers), then
+            // q_hat = RoPE(RMSNorm(q) * wq) in bf16 over the gate tile.  Each thread owns the 64
+            // columns of its half row; the rotated pairs (j, j + half), half <= 32, lie in half 0.
+            if (!__all_sync(0xffffffffu, mbar_wait(ld_full, 0, p.ctl, 108))) ok = false;
+            uint8_t* qtile = smem + QP_Q;
+            uint8_t* dtile = smem + QP_DA;
+            const uint8_t* xtile = smem + QP_X;
+            if (ok && gated) {
+#pragma unroll 2
+                for (int c8 = 8 * hf; c8 < 8 * hf + 8; ++c8) {
+                    uint4* pd = reinterpret_cast<uint4*>(dtile + (c8 >> 3) * CH128 + sw128_off(row, c8 & 7));
+                    const uint4 dd = *pd;
+                    const uint4 go = ld_row8(qtile, row, c8);
+                    const uint32_t dw[4] = {dd.x, dd.y, dd.z, dd.w}, gw[4] = {go.x, go.y, go.z, go.w};
+                    uint32_t o[4];
+#pragma unroll
+                    for (int k2 = 0; k2 < 4; ++k2)  // the same arithmetic as the prep kernel's dA
+                        o[k2] = pack_bf16x2(bf16lo(dw[k2]) * sigmoid_f32(bf16lo(gw[k2])),
+                                            bf16hi(dw[k2]) * sigmoid_f32(bf16hi(gw[k2])));
+                    *pd = make_uint4(o[0], o[1], o[2], o[3]);
+                }
+            }
+            float ssq = 0.f;
+            if (ok) {
+#pragma unroll 2
+                for (int c8 = 8 * hf; c8 < 8 * hf + 8; ++c8) {
+                    const uint4 u = ld_row8(xtile, row, c8);
+                    const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                    for (int k2 = 0; k2 < 4; ++k2) {
+                        const float a = bf16lo(uw[k2]), c = bf16hi(uw[k2]);
+                        ssq = fmaf(a, a, fmaf(c, c, ssq));
+                    }
+                }
+            }
+            ssq += exchange(7, make_float2(ssq, 0.f)).x;
+            if (ok) {
+                const float inv = ssq > 0.f || p.eps > 0.f ? rsqrtf(ssq * (1.0f / D) + p.eps) : 0.f;
+                const int half = p.rope.half;
+                const int c_first = hf == 0 ? (2 * half + 7) / 8 : 8;  // chunks [c_first, 8 hf + 8) are not rotated
+                {
+                    // the rotated pairs are split between the row's two threads (after the exchange above,
+                    // both have read their gate columns, so either may write q_hat anywhere in half 0)
+                    const int pos = valid_row && idx_ok(p.ctl, static_cast<long long>(b) * p.L + t,
+                                                        static_cast<long long>(p.B) * p.L, 158)
+                                        ? __ldg(p.pos + static_cast<long long>(b) * p.L + t)
+                                        : 0;
+                    const int j_mid = (half + 1) / 2;
+#pragma unroll 1
+                    for (int j = hf == 0 ? 0 : j_mid; j < (hf == 0 ? j_mid : half); ++j) {
+                        const float a = ld_bf16(sw_elem(const_cast<uint8_t*>(xtile), CH128, row, j)) * inv * w_s[j];
+                        const float c = ld_bf16(sw_elem(const_cast<uint8_t*>(xtile), CH128, row, j + half)) * inv * w_s[j + half];
+                        float cs, sn;
+                        rope_cos_sin(pos, p.rope.f_hi[j], p.rope.f_lo[j], cs, sn);
+                        st_bf16(sw_elem(qtile, CH128, row, j), a * cs - c * sn);
+                        st_bf16(sw_elem(qtile, CH128, row, j + half), c * cs + a * sn);
+                    }
+                }
+                if (hf == 0) {
+#pragma unroll 1
+                    for (int e = 2 * half; e < 8 * c_first; ++e)
+                        st_bf16(sw_elem(qtile, CH128, row, e), ld_bf16(sw_elem(const_cast<uint8_t*>(xtile), CH128, row, e)) * inv * w_s[e]);
+                }
+#pragma unroll 1
+                for (int c8 = hf == 0 ? c_first : 8; c8 < 8 * hf + 8; ++c8) {
+                    const uint4 u = ld_row8(xtile, row, c8);
+                    const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
+                    const float* w = w_s + 8 * c8;
+                    uint32_t o[4];
+#pragma unroll
+                    for (int k2 = 0; k2 < 4; ++k2)
+                        o[k2] = pack_bf16x2(bf16lo(uw[k2]) * inv * w[2 * k2], bf16hi(uw[k2]) * inv * w[2 * k2 + 1]);
+                    *reinterpret_cast<uint4*>(qtile + (c8 >> 3) * CH128 + sw128_off(row, c8 & 7)) =
+                        make_uint4(o[0], o[1], o[2], o[3]);
+                }
+                fence_async_smem();
+            }
+            tc_fence_before();
+            mbar_arrive(qd_ready);
+        }
         float m = 0.f, l = 0.f;
         ok = __all_sync(0xffffffffu, mbar_wait(s_full, 0, p.ctl, 104));
         float mx = -INFINITY;
@@ -1268,7 +1369,10 @@ cudaError_t launch_backward_tc(const BackwardTcParams& p, cudaStream_t s) {
     const long long nq = static_cast<long long>(p.B) * p.L * p.Hq, nk = static_cast<long long>(p.B) * p.L * p.Hkv;
     if (nq == 0) return cudaSuccess;
     if (nq + nk >= (1ll << 31)) return cudaErrorInvalidValue;  // the prep kernel indexes rows in 32 bits
-    bwd_tc_prep_kernel<<<static_cast<unsigned>((nq + nk + 8 * kPrepRows - 1) / (8 * kPrepRows)), 256, 0, s>>>(p);
+    BackwardTcParams pp = p;
+    pp.prep_first = p.fold ? static_cast<int>(nq) : 0;  // fold: the query pass forms q_hat and dA, prep k_hat only
+    const long long prep_rows = nq + nk - pp.prep_first;
+    bwd_tc_prep_kernel<<<static_cast<unsigned>((prep_rows + 8 * kPrepRows - 1) / (8 * kPrepRows)), 256, 0, s>>>(pp);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(bwd_kpass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, KP_SMEM);

@@ -178,6 +178,8 @@ struct BackwardTcParams {
     float4* stat;        // workspace: per query row (max of the log2-scaled scores, 1 / row sum, D, 0)
     int B, L, Hq, Hkv, window;
     int global;  // 1: the global layer (every earlier key, no gate; window = L)
+    int fold;    // 1: the windowed query pass forms q_hat and dA itself (rotary_dim <= 64); prep does k_hat only
+    int prep_first;  // first row (q rows, then k rows) the prep kernel processes
     float scale, scale_log2, eps;
     RopeConsts rope;
     DevCtl ctl;
