@@ -302,7 +302,9 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * statistics.median(dts), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": SWA.name, "global_batch": SWA.B, "seq_len": SWA.L, "parallelism": "none (host)"},
+        # the GPU arm's config (its value is the gated-SWA prefill's tokens/s, as this arm's is)
+        "config": {"workload": f"{SWA.name} + {DEC.name} + {GLB.name}", "global_batch": SWA.B, "seq_len": SWA.L,
+                   "parallelism": "single GPU", "l2": "no flush: every input is larger than L2"},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": n, "cpu_model": cpu_model(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
