@@ -841,6 +841,16 @@ def run_profile_case(args):
         def fn():
             zg.global_prefill_fp8(x8["q"], x8["k"], x8["v"], x["pos"], x["wq"], x["wk"], rotary_dim=c.rotary_dim,
                                   theta=c.theta, out=out, workspace=ws)
+    elif kind == "swa8":
+        c = workloads.PrefillCase("swa_fp8_B1_L65536_profile", 3, 1, 65536, 32, 8, 128, 128, 42, 1e6, True, outliers=True)
+        x = workloads.prefill_inputs_device(c, dev)
+        x8 = {n: workloads.to_e4m3(x[n], 1.0).view(torch.uint8) for n in ("q", "k", "v")}
+        out = torch.empty_like(x["q"])
+        ws = torch.empty(zg.global_prefill_fp8_workspace_bytes(1, c.L, 8, 128), dtype=torch.uint8, device=dev)
+
+        def fn():
+            zg.swa_prefill_fp8(x8["q"], x8["k"], x8["v"], x["gate"], x["pos"], x["wq"], x["wk"], window=128,
+                               rotary_dim=c.rotary_dim, theta=c.theta, out=out, workspace=ws)
     elif kind == "kvcache":
         c = workloads.PrefillCase("kv_cache_B1_L65536_profile", 4, 1, 65536, 32, 8, 128, 0, 42, 1e6, False)
         x = workloads.prefill_inputs_device(c, dev)
@@ -915,7 +925,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--step-only", action="store_true",
                     help="time the step alone: skip the parts measured outside it (for ncu launch lists)")
-    ap.add_argument("--profile-case", choices=["swa", "global", "global8", "decode", "kvcache", "backward", "backward_global", "decode8"], default=None,
+    ap.add_argument("--profile-case", choices=["swa", "swa8", "global", "global8", "decode", "kvcache", "backward", "backward_global", "decode8"], default=None,
                     help="run only a small case of one kernel (for ncu captures)")
     args = ap.parse_args()
     if args.profile_case:

@@ -37,18 +37,19 @@ namespace {
 
 constexpr int BK = 128;               // keys per block
 constexpr uint32_t CH = 128 * 128;    // one 64-column chunk of 128 rows (16-bit elements)
-constexpr int NBAR = 22;
+constexpr int NBAR = 25;
 constexpr float kTau = 8.0f;
 constexpr int kThreads = 384;
 constexpr int kGroupCt = 128;  // CTAs of one (sequence, KV head) scheduled together on long sequences
 
-template <int D, bool F8 = false>
+template <int D, bool F8 = false, bool SWA = false>
 struct Glb {
     static constexpr uint32_t TILE = 128 * D * (F8 ? 1 : 2);  // one 128-row x D tile (16-bit: D/64 chunks)
     static constexpr uint32_t OFF_Q = 0;           // Q0, Q1
     static constexpr uint32_t OFF_K = 2 * TILE;    // 2 stages
     static constexpr uint32_t OFF_V = 4 * TILE;    // 2 stages
-    static constexpr uint32_t OFF_BAR = 6 * TILE;
+    static constexpr uint32_t OFF_G = 6 * TILE;    // SWA: gate / output staging, one bf16 tile per Q tile
+    static constexpr uint32_t OFF_BAR = OFF_G + (SWA ? 2 * 128 * D * 2 : 0);
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr uint32_t SMEM = OFF_MISC + 32;
 };
@@ -245,15 +246,31 @@ __global__ void __launch_bounds__(256) vt_e4m3_kernel(const __grid_constant__ Pr
     }
 }
 
+// Runs body(it, n) over this CTA's work items: blockIdx.x, + gridDim.x, ... while it returns true
+// (persistent CTAs), or blockIdx.x alone; n counts the items done before.
+template <bool MANY, class F>
+__device__ __forceinline__ void for_items(int n_items, F&& body) {
+    if constexpr (MANY) {
+        for (int it = static_cast<int>(blockIdx.x), n = 0; it < n_items; it += static_cast<int>(gridDim.x), ++n)
+            if (!body(it, n)) break;
+    } else {
+        (void)n_items;
+        body(static_cast<int>(blockIdx.x), 0);
+    }
+}
+
 // ---------------------------------------------------------------- kernel 2
 // F8: E4M3 inputs and products (see the pre-passes above); D = 128 only.
 // SWA: the gated sliding-window layer on the same pipeline (used for E4M3 inputs): a CTA visits
 // only the key blocks that meet its queries' windows, masks both window edges, and multiplies the
-// output by sigmoid(gate) in the epilogue.
+// output by sigmoid(gate) in the epilogue.  Its work items (two Q tiles of one KV head) are short,
+// so the CTAs are persistent: one per SM walks items blockIdx.x, + gridDim.x, ...; the TMA warp
+// fetches the next item's Q, K_hat / V^T blocks and gate tiles while the current one finishes, and
+// the gate tiles have their own staging buffer.  The global layer runs one item per CTA.
 template <int D, int G, bool F8, bool SWA = false>
 __global__ void __launch_bounds__(kThreads, 1) global_attn_kernel(const __grid_constant__ PrefillParams p) {
     constexpr int T = 128 / G;  // tokens per tile
-    using C = Glb<D, F8>;
+    using C = Glb<D, F8, SWA>;
     constexpr uint32_t TILE = C::TILE, OFF_Q = C::OFF_Q, OFF_K = C::OFF_K, OFF_V = C::OFF_V;
     constexpr uint32_t OFF_BAR = C::OFF_BAR, OFF_MISC = C::OFF_MISC;
     constexpr int NCH = F8 ? 1 : D / 64;  // TMA boxes per 128-row tile (128-byte box rows)
@@ -272,32 +289,44 @@ __global__ void __launch_bounds__(kThreads, 1) global_attn_kernel(const __grid_c
     uint64_t* out_bar = bar + 17;  // [2] per tile: the tile's output is in shared memory
     uint64_t* drain = bar + 19;
     uint64_t* gate_full = bar + 20;  // [2] per tile (SWA): the gate tile is in the staging buffer
+    uint64_t* q_empty = bar + 22;    // SWA: the item's score products are complete (Q buffer free)
+    uint64_t* stg_free = bar + 23;   // [2] per tile (SWA): the output store has read the staging buffer
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nbg = p.B * p.Hkv;
     const int n_ct = (p.L + 2 * T - 1) / (2 * T);
-    // Heaviest (longest key range) first.  Long sequences: in groups of kGroupCt CTAs of one (b, g),
-    // so that the CTAs resident together read the same K_hat / V blocks and share them in L2.
-    int ct, bg;
-    if (n_ct >= 2 * kGroupCt) {
-        const int q = static_cast<int>(blockIdx.x / (kGroupCt * nbg));  // group, heaviest first
-        const int r = static_cast<int>(blockIdx.x - static_cast<unsigned>(q * kGroupCt * nbg));
-        const int sz = min(kGroupCt, n_ct - q * kGroupCt);
-        bg = r / sz;
-        ct = n_ct - 1 - (q * kGroupCt + r % sz);
-    } else {
-        ct = n_ct - 1 - static_cast<int>(blockIdx.x / nbg);
-        bg = static_cast<int>(blockIdx.x % nbg);
-    }
-    const int g = bg % p.Hkv;
-    const int b = bg / p.Hkv;
-    const int i0 = ct * 2 * T;
-    // key blocks jlo .. jlo + nkb - 1 (both tiles need the same blocks): from 0 for the global layer,
-    // from the block of the first key of the first query's window for SWA
-    const int jlo = SWA ? max(0, i0 - p.window + 1) / BK : 0;
-    const int nkb = (i0 + 2 * T + BK - 1) / BK - jlo;
+    const int n_items = n_ct * nbg;
+    // One work item: Q tiles i0 .. i0 + 2T - 1 of KV head g of sequence b, and its key blocks
+    // jlo .. jlo + nkb - 1 (both tiles need the same blocks): from 0 for the global layer, from the
+    // block of the first key of the first query's window for SWA.
+    struct Item {
+        int g, b, i0, jlo, nkb;
+    };
+    auto item = [&](int it) {
+        // Heaviest (longest key range) first.  Long sequences: in groups of kGroupCt CTAs of one
+        // (b, g), so that the CTAs resident together read the same K_hat / V blocks and share them in L2.
+        int ct, bg;
+        if (n_ct >= 2 * kGroupCt) {
+            const int q = it / (kGroupCt * nbg);  // group, heaviest first
+            const int r = it - q * kGroupCt * nbg;
+            const int sz = min(kGroupCt, n_ct - q * kGroupCt);
+            bg = r / sz;
+            ct = n_ct - 1 - (q * kGroupCt + r % sz);
+        } else {
+            ct = n_ct - 1 - it / nbg;
+            bg = it % nbg;
+        }
+        Item w;
+        w.g = bg % p.Hkv;
+        w.b = bg / p.Hkv;
+        w.i0 = ct * 2 * T;
+        w.jlo = SWA ? max(0, w.i0 - p.window + 1) / BK : 0;
+        w.nkb = (w.i0 + 2 * T + BK - 1) / BK - w.jlo;
+        return w;
+    };
+    const Item w0 = item(static_cast<int>(blockIdx.x));  // the first (for the global layer, only) item
 
     if (threadIdx.x == 0) {
         *abort_flag = (smem_u32(smem) & 1023u) == 0 ? 0 : 1;
@@ -314,7 +343,9 @@ __global__ void __launch_bounds__(kThreads, 1) global_attn_kernel(const __grid_c
             mbar_init(&pv_done[i], 1);
             mbar_init(&out_bar[i], 128);
             mbar_init(&gate_full[i], 1);
+            mbar_init(&stg_free[i], 1);
         }
+        mbar_init(q_empty, 1);
         mbar_init(drain, 1);
         fence_barrier_init();
     }
@@ -340,35 +371,56 @@ __global__ void __launch_bounds__(kThreads, 1) global_attn_kernel(const __grid_c
                 tma_prefetch_desc(&p.tm_kh);
                 tma_prefetch_desc(F8 ? &p.tm_vt : &p.tm_v);
                 tma_prefetch_desc(&p.tm_out);
-                mbar_arrive_expect_tx(q_full, 2 * TILE);
-                for (int t = 0; t < 2; ++t)
-                    for (int ch = 0; ch < NCH; ++ch)
-                        tma_load_4d(smem + OFF_Q + t * TILE + ch * CH, &p.tm_q, q_full, ch * 64, g * G, i0 + t * T, b);
+                if constexpr (SWA) tma_prefetch_desc(&p.tm_gate);
                 bool ok = true;
-                for (int j = 0; j < nkb && ok && !aborted(); ++j) {
-                    const int st = j & 1;
-                    ok = mbar_wait(&k_empty[st], ((j >> 1) & 1) ^ 1, p.ctl, 51);
-                    if (!ok) break;
-                    mbar_arrive_expect_tx(&k_full[st], TILE);
-                    for (int ch = 0; ch < NCH; ++ch)
-                        tma_load_4d(smem + OFF_K + st * TILE + ch * CH, &p.tm_kh, &k_full[st], ch * 64, g, (jlo + j) * BK, b);
-                    ok = mbar_wait(&v_empty[st], ((j >> 1) & 1) ^ 1, p.ctl, 52);
-                    if (!ok) break;
-                    mbar_arrive_expect_tx(&v_full[st], TILE);
-                    if constexpr (F8)  // V^T block: 128 key bytes per row, D rows
-                        tma_load_4d(smem + OFF_V + st * TILE, &p.tm_vt, &v_full[st], (jlo + j) * BK, 0, g, b);
-                    else
+                int J = 0;  // key blocks of earlier items: the ring's position
+                for_items<SWA>(n_items, [&](int it, int n) {
+                    const Item w = n == 0 ? w0 : item(it);
+                    // the previous item's score products have read the Q buffer
+                    if (SWA && n > 0 && !(ok = mbar_wait(q_empty, (n - 1) & 1, p.ctl, 68))) return false;
+                    mbar_arrive_expect_tx(q_full, 2 * TILE);
+                    for (int t = 0; t < 2; ++t)
                         for (int ch = 0; ch < NCH; ++ch)
-                            tma_load_4d(smem + OFF_V + st * TILE + ch * CH, &p.tm_v, &v_full[st], ch * 64, g, (jlo + j) * BK, b);
-                }
+                            tma_load_4d(smem + OFF_Q + t * TILE + ch * CH, &p.tm_q, q_full, ch * 64, w.g * G, w.i0 + t * T, w.b);
+                    for (int j = 0; j < w.nkb && ok && !aborted(); ++j) {
+                        const int jj = J + j, st = jj & 1;
+                        ok = mbar_wait(&k_empty[st], ((jj >> 1) & 1) ^ 1, p.ctl, 51);
+                        if (!ok) break;
+                        mbar_arrive_expect_tx(&k_full[st], TILE);
+                        for (int ch = 0; ch < NCH; ++ch)
+                            tma_load_4d(smem + OFF_K + st * TILE + ch * CH, &p.tm_kh, &k_full[st], ch * 64, w.g,
+                                        (w.jlo + j) * BK, w.b);
+                        ok = mbar_wait(&v_empty[st], ((jj >> 1) & 1) ^ 1, p.ctl, 52);
+                        if (!ok) break;
+                        mbar_arrive_expect_tx(&v_full[st], TILE);
+                        if constexpr (F8)  // V^T block: 128 key bytes per row, D rows
+                            tma_load_4d(smem + OFF_V + st * TILE, &p.tm_vt, &v_full[st], (w.jlo + j) * BK, 0, w.g, w.b);
+                        else
+                            for (int ch = 0; ch < NCH; ++ch)
+                                tma_load_4d(smem + OFF_V + st * TILE + ch * CH, &p.tm_v, &v_full[st], ch * 64, w.g,
+                                            (w.jlo + j) * BK, w.b);
+                    }
+                    if constexpr (SWA) {  // the gate tiles (bf16), once the previous item's outputs are stored
+                        for (int t = 0; t < 2 && ok && !aborted(); ++t) {
+                            if (n > 0 && !(ok = mbar_wait(&stg_free[t], (n - 1) & 1, p.ctl, 69))) break;
+                            mbar_arrive_expect_tx(&gate_full[t], (D / 64) * CH);
+                            for (int ch = 0; ch < D / 64; ++ch)
+                                tma_load_4d(smem + C::OFF_G + t * (D / 64) * CH + ch * CH, &p.tm_gate, &gate_full[t],
+                                            ch * 64, w.g * G, w.i0 + t * T, w.b);
+                        }
+                    }
+                    J += w.nkb;
+                    return ok && !aborted();
+                });
                 if (!ok) fail();
             }
         } else if (warp == 1) {
             // ------------------------------------------------------------ MMA
             if (lane == 0 && !aborted()) {
-                auto qk = [&](int t, int j) {
+                // jj: the key block's place in the ring (counted over this CTA's items); j: within the item
+                auto qk = [&](int t, int jj) {
                     constexpr uint32_t idesc = idesc_f16_f32(128, BK, false, false);  // fp16, or E4M3 (code 0)
-                    const uint32_t kofs = OFF_K + (j & 1) * TILE;
+                    const uint32_t kofs = OFF_K + (jj & 1) * TILE;
                     if constexpr (F8) {
     #pragma unroll
                         for (int ks = 0; ks < D / 32; ++ks)  // 32 E4M3 values = 32 bytes per k-step
@@ -384,8 +436,8 @@ __global__ void __launch_bounds__(kThreads, 1) global_attn_kernel(const __grid_c
                     }
                     umma_commit(&s_full[t]);
                 };
-                auto pv = [&](int t, int j) {
-                    const uint32_t vofs = OFF_V + (j & 1) * TILE;
+                auto pv = [&](int t, int jj, int j) {
+                    const uint32_t vofs = OFF_V + (jj & 1) * TILE;
                     if constexpr (F8) {
                         // P (E4M3, four per TMEM column) times V^T (K-major: rows = dims, 128 key bytes each)
                         constexpr uint32_t idesc = idesc_f16_f32(128, D, false, false);
@@ -404,36 +456,46 @@ __global__ void __launch_bounds__(kThreads, 1) global_attn_kernel(const __grid_c
                     }
                     umma_commit(&pv_done[t]);
                 };
-                bool ok = mbar_wait(&q_ready[0], 0, p.ctl, 53) && mbar_wait(&q_ready[1], 0, p.ctl, 53) &&
-                          mbar_wait(&k_full[0], 0, p.ctl, 54);
-                if (ok) {
-                    tc_fence_after();
-                    qk(0, 0);
-                    qk(1, 0);
-                    umma_commit(&k_empty[0]);
-                }
-                for (int j = 0; j < nkb && ok && !aborted(); ++j) {
-                    const bool more = j + 1 < nkb;
-                    ok = mbar_wait(&v_full[j & 1], (j >> 1) & 1, p.ctl, 55) && mbar_wait(&p_ready[0], j & 1, p.ctl, 56);
-                    if (!ok) break;
-                    tc_fence_after();
-                    pv(0, j);
-                    if (more) {
-                        ok = mbar_wait(&k_full[(j + 1) & 1], ((j + 1) >> 1) & 1, p.ctl, 57);
+                bool ok = true;
+                int J = 0;
+                for_items<SWA>(n_items, [&](int it, int n) {
+                    const int nkb = n == 0 ? w0.nkb : item(it).nkb;
+                    ok = mbar_wait(&q_ready[0], n & 1, p.ctl, 53) && mbar_wait(&q_ready[1], n & 1, p.ctl, 53) &&
+                         mbar_wait(&k_full[J & 1], (J >> 1) & 1, p.ctl, 54);
+                    if (ok) {
+                        tc_fence_after();
+                        qk(0, J);
+                        qk(1, J);
+                        umma_commit(&k_empty[J & 1]);
+                        if (SWA && nkb == 1) umma_commit(q_empty);
+                    }
+                    for (int j = 0; j < nkb && ok && !aborted(); ++j) {
+                        const int jj = J + j;
+                        const bool more = j + 1 < nkb;
+                        ok = mbar_wait(&v_full[jj & 1], (jj >> 1) & 1, p.ctl, 55) && mbar_wait(&p_ready[0], jj & 1, p.ctl, 56);
                         if (!ok) break;
                         tc_fence_after();
-                        qk(0, j + 1);
+                        pv(0, jj, j);
+                        if (more) {
+                            ok = mbar_wait(&k_full[(jj + 1) & 1], ((jj + 1) >> 1) & 1, p.ctl, 57);
+                            if (!ok) break;
+                            tc_fence_after();
+                            qk(0, jj + 1);
+                        }
+                        ok = mbar_wait(&p_ready[1], jj & 1, p.ctl, 58);
+                        if (!ok) break;
+                        tc_fence_after();
+                        pv(1, jj, j);
+                        umma_commit(&v_empty[jj & 1]);
+                        if (more) {
+                            qk(1, jj + 1);
+                            umma_commit(&k_empty[(jj + 1) & 1]);
+                            if (SWA && j + 2 == nkb) umma_commit(q_empty);  // the item's last score products
+                        }
                     }
-                    ok = mbar_wait(&p_ready[1], j & 1, p.ctl, 58);
-                    if (!ok) break;
-                    tc_fence_after();
-                    pv(1, j);
-                    umma_commit(&v_empty[j & 1]);
-                    if (more) {
-                        qk(1, j + 1);
-                        umma_commit(&k_empty[(j + 1) & 1]);
-                    }
-                }
+                    J += nkb;
+                    return ok && !aborted();
+                });
                 if (!ok) fail();
                 umma_commit(drain);
                 (void)mbar_wait(drain, 0, p.ctl, 59);
@@ -449,183 +511,204 @@ __global__ void __launch_bounds__(kThreads, 1) global_attn_kernel(const __grid_c
         const uint32_t o_addr = lane_addr + 256 + t * 128;
         uint8_t* qt = smem + OFF_Q + t * TILE;
         const int tt = row / G;
-        const int iq = i0 + t * T + tt;
         // E4M3: q_hat and k_hat are stored times power-of-two scales (undone in the score scale)
         const float s_qh = F8 ? e4m3_hat_scale<D>(p.wq) : 1.f;
         const float s_kh = F8 ? e4m3_hat_scale<D>(p.wk) : 1.f;
-        bool ok = __all_sync(0xffffffffu, mbar_wait(q_full, 0, p.ctl, 60));
-        if (ok) {
-            const long long pi = static_cast<long long>(b) * p.L + iq;
-            const int pos = iq < p.L && idx_ok(p.ctl, pi, static_cast<long long>(p.B) * p.L, 83) ? __ldg(p.pos + pi) : 0;
-            if constexpr (F8)
-                qk_norm_rope_row_e4m3<D>(qt, row, p.wq, p.eps, pos, p.rope, p.in_dequant_q, s_qh);
-            else
-                qk_norm_rope_row<D>(qt, CH, row, p.wq, p.eps, pos, p.rope);
-            fence_async_smem();
-        }
-        mbar_arrive(&q_ready[t]);
-        if (!ok) fail();
-        float m_run = -INFINITY, l_run = 0.f;
         const float sc = F8 ? p.scale_log2 / (s_qh * s_kh) : p.scale_log2;
-        for (int j = 0; j < nkb && ok; ++j) {
-            if (aborted() || !__all_sync(0xffffffffu, mbar_wait(&s_full[t], j & 1, p.ctl, 61))) {
-                fail();
-                break;
+        // the position of this thread's query row in an item
+        auto pos_of = [&](const Item& w) {
+            const int iq = w.i0 + t * T + tt;
+            const long long pi = static_cast<long long>(w.b) * p.L + iq;
+            return iq < p.L && idx_ok(p.ctl, pi, static_cast<long long>(p.B) * p.L, 83) ? __ldg(p.pos + pi) : 0;
+        };
+        // q_hat of this thread's row of the n-th item, in place in the Q buffer
+        auto q_transform = [&](int n, int pos) {
+            const bool okq = __all_sync(0xffffffffu, mbar_wait(q_full, n & 1, p.ctl, 60));
+            if (okq) {
+                if constexpr (F8)
+                    qk_norm_rope_row_e4m3<D>(qt, row, p.wq, p.eps, pos, p.rope, p.in_dequant_q, s_qh);
+                else
+                    qk_norm_rope_row<D>(qt, CH, row, p.wq, p.eps, pos, p.rope);
+                fence_async_smem();
             }
-            tc_fence_after();
-            uint32_t r[128];
-            tmem_ld32(s_addr + 0, r);
-            tmem_ld32(s_addr + 32, r + 32);
-            tmem_ld32(s_addr + 64, r + 64);
-            tmem_ld32(s_addr + 96, r + 96);
-            tmem_wait_ld();
-            const int kmax = iq - (jlo + j) * BK;  // last valid key column of this row in the block
-            if constexpr (SWA) {
-                const int kmin = kmax - p.window + 1;  // first key column inside the window
-#pragma unroll
-                for (int k = 0; k < 128; ++k)
-                    if (k > kmax || k < kmin) r[k] = __float_as_uint(-INFINITY);
-            } else if ((jlo + j + 1) * BK - 1 > i0) {  // the block reaches past the CTA's first query
-#pragma unroll
-                for (int k = 0; k < 128; ++k)
-                    if (k > kmax) r[k] = __float_as_uint(-INFINITY);
-            }
-            // block maximum: eight independent chains of three-input maxima, then their maximum
-            float a8[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) a8[i] = fmaxf(__uint_as_float(r[i]), __uint_as_float(r[i + 8]));
-#pragma unroll
-            for (int k = 16; k < 128; k += 16)
-#pragma unroll
-                for (int i = 0; i < 8; ++i) a8[i] = fmax3(a8[i], __uint_as_float(r[k + i]), __uint_as_float(r[k + 8 + i]));
-            const float mx = fmaxf(fmax3(fmax3(a8[0], a8[1], a8[2]), a8[3], a8[4]), fmax3(a8[5], a8[6], a8[7]));
-            const float mb = mx * sc;
-            float m_new = m_run;
-            if (m_run == -INFINITY || mb > m_run + kTau) m_new = mb;
-            const float corr = m_run == -INFINITY ? 0.f : ex2_approx(m_run - m_new);
-            if (j > 0 && __any_sync(0xffffffffu, m_new != m_run)) {
-                // O(j-1) must be complete before it is scaled in place
-                if (!__all_sync(0xffffffffu, mbar_wait(&pv_done[t], (j - 1) & 1, p.ctl, 62))) {
+            mbar_arrive(&q_ready[t]);
+            if (!okq) fail();
+            return okq;
+        };
+        bool ok = true;
+        int J = 0;
+        for_items<SWA>(n_items, [&](int it, int n) {
+            const Item w = n == 0 ? w0 : item(it);
+            const int g = w.g, b = w.b, i0 = w.i0, jlo = w.jlo, nkb = w.nkb;
+            const int iq = i0 + t * T + tt;
+            ok = q_transform(n, pos_of(w));
+            float m_run = -INFINITY, l_run = 0.f;
+            for (int j = 0; j < nkb && ok; ++j) {
+                const int jj = J + j;
+                if (aborted() || !__all_sync(0xffffffffu, mbar_wait(&s_full[t], jj & 1, p.ctl, 61))) {
                     fail();
                     break;
                 }
                 tc_fence_after();
-#pragma unroll 1
+                uint32_t r[128];
+                tmem_ld32(s_addr + 0, r);
+                tmem_ld32(s_addr + 32, r + 32);
+                tmem_ld32(s_addr + 64, r + 64);
+                tmem_ld32(s_addr + 96, r + 96);
+                tmem_wait_ld();
+                const int kmax = iq - (jlo + j) * BK;  // last valid key column of this row in the block
+                if constexpr (SWA) {
+                    const int kmin = kmax - p.window + 1;  // first key column inside the window
+    #pragma unroll
+                    for (int k = 0; k < 128; ++k)
+                        if (k > kmax || k < kmin) r[k] = __float_as_uint(-INFINITY);
+                } else if ((jlo + j + 1) * BK - 1 > i0) {  // the block reaches past the CTA's first query
+    #pragma unroll
+                    for (int k = 0; k < 128; ++k)
+                        if (k > kmax) r[k] = __float_as_uint(-INFINITY);
+                }
+                // block maximum: eight independent chains of three-input maxima, then their maximum
+                float a8[8];
+    #pragma unroll
+                for (int i = 0; i < 8; ++i) a8[i] = fmaxf(__uint_as_float(r[i]), __uint_as_float(r[i + 8]));
+    #pragma unroll
+                for (int k = 16; k < 128; k += 16)
+    #pragma unroll
+                    for (int i = 0; i < 8; ++i) a8[i] = fmax3(a8[i], __uint_as_float(r[k + i]), __uint_as_float(r[k + 8 + i]));
+                const float mx = fmaxf(fmax3(fmax3(a8[0], a8[1], a8[2]), a8[3], a8[4]), fmax3(a8[5], a8[6], a8[7]));
+                const float mb = mx * sc;
+                float m_new = m_run;
+                if (m_run == -INFINITY || mb > m_run + kTau) m_new = mb;
+                const float corr = m_run == -INFINITY ? 0.f : ex2_approx(m_run - m_new);
+                if (j > 0 && __any_sync(0xffffffffu, m_new != m_run)) {
+                    // O(j-1) must be complete before it is scaled in place
+                    if (!__all_sync(0xffffffffu, mbar_wait(&pv_done[t], (jj - 1) & 1, p.ctl, 62))) {
+                        fail();
+                        break;
+                    }
+                    tc_fence_after();
+    #pragma unroll 1
+                    for (int cb = 0; cb < D; cb += 32) {
+                        uint32_t o[32];
+                        tmem_ld32(o_addr + cb, o);
+                        tmem_wait_ld();
+    #pragma unroll
+                        for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * corr);
+                        tmem_st32(o_addr + cb, o);
+                    }
+                    tmem_wait_st();
+                }
+                l_run *= corr;
+                m_run = m_new;
+                // a row whose window has not begun yet (SWA) has m_run = -inf and every score masked: P = 0
+                const float m_exp = m_run == -INFINITY ? 0.f : m_run;
+                const float2 sc2 = make_float2(sc, sc), nm2 = make_float2(-m_exp, -m_exp);
+                float2 l2 = make_float2(0.f, 0.f), l3 = make_float2(0.f, 0.f);
+    #pragma unroll
+                for (int cb = 0; cb < 128; cb += 32) {
+                    if constexpr (F8) {
+                        // P in E4M3 (at most 2^8 with the lazy maximum: inside the range), four per column.
+                        // The row sums add the rounded values the product uses: 16 per fp16 lane (at most
+                        // 2^12, so in range; relative rounding <= 9 * 2^-11, far below P's own 2^-4), then
+                        // once per 32 columns into fp32.
+                        uint32_t pk[8];
+                        __half2 hacc = __float2half2_rn(0.f);
+    #pragma unroll
+                        for (int k = 0; k < 32; k += 4) {
+                            const float2 x0 = fma2(make_float2(__uint_as_float(r[cb + k]), __uint_as_float(r[cb + k + 1])), sc2, nm2);
+                            const float2 x1 = fma2(make_float2(__uint_as_float(r[cb + k + 2]), __uint_as_float(r[cb + k + 3])), sc2, nm2);
+                            const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
+                                make_float2(ex2_approx(x0.x), ex2_approx(x0.y)), __NV_SATFINITE, __NV_E4M3);
+                            const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
+                                make_float2(ex2_approx(x1.x), ex2_approx(x1.y)), __NV_SATFINITE, __NV_E4M3);
+                            pk[k / 4] = uint32_t(lo) | (uint32_t(hi) << 16);
+                            const __half2_raw hl = __nv_cvt_fp8x2_to_halfraw2(lo, __NV_E4M3);
+                            const __half2_raw hh = __nv_cvt_fp8x2_to_halfraw2(hi, __NV_E4M3);
+                            hacc = __hadd2(hacc, __hadd2(__half2(hl), __half2(hh)));
+                        }
+                        l2 = add2(l2, __half22float2(hacc));
+                        tmem_st8(s_addr + cb / 4, pk);  // P over S (these columns are already in registers)
+                    } else {
+                        uint32_t pk[16];
+    #pragma unroll
+                        for (int k = 0; k < 32; k += 2) {
+                            const float2 x = fma2(make_float2(__uint_as_float(r[cb + k]), __uint_as_float(r[cb + k + 1])), sc2, nm2);
+                            pk[k / 2] = pack_bf16x2(ex2_approx(x.x), ex2_approx(x.y));
+                            if (k & 2)
+                                acc_bf16x2(pk[k / 2], l3.x, l3.y);
+                            else
+                                acc_bf16x2(pk[k / 2], l2.x, l2.y);
+                        }
+                        tmem_st16(s_addr + cb / 2, pk);  // P over S (these columns are already in registers)
+                    }
+                }
+                l_run += (l2.x + l2.y) + (l3.x + l3.y);
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(&p_ready[t]);
+            }
+            // ---- epilogue: O / l -> bf16 -> staging tile -> TMA store.  The staging tile is the tile's
+            // Q buffer, or (E4M3, whose Q buffer is half the size of the bf16 output) the K stages for
+            // tile 0 and the V stages for tile 1, free once the tile's last product has completed; SWA:
+            // the gate tile, which the output overwrites in place.
+            uint8_t* stg = SWA ? smem + C::OFF_G + t * (D / 64) * CH : F8 ? smem + (t == 0 ? OFF_K : OFF_V) : qt;
+            if (ok && !aborted()) ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[t], (J + nkb - 1) & 1, p.ctl, 63));
+            if (SWA && ok && !aborted()) ok = __all_sync(0xffffffffu, mbar_wait(&gate_full[t], n & 1, p.ctl, 65));
+            if (ok) {
+                tc_fence_after();
+                const float inv_l = l_run > 0.f ? (F8 ? p.in_dequant_v : 1.0f) / l_run : 0.f;
+    #pragma unroll 1
                 for (int cb = 0; cb < D; cb += 32) {
                     uint32_t o[32];
                     tmem_ld32(o_addr + cb, o);
                     tmem_wait_ld();
-#pragma unroll
-                    for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * corr);
-                    tmem_st32(o_addr + cb, o);
-                }
-                tmem_wait_st();
-            }
-            l_run *= corr;
-            m_run = m_new;
-            // a row whose window has not begun yet (SWA) has m_run = -inf and every score masked: P = 0
-            const float m_exp = m_run == -INFINITY ? 0.f : m_run;
-            const float2 sc2 = make_float2(sc, sc), nm2 = make_float2(-m_exp, -m_exp);
-            float2 l2 = make_float2(0.f, 0.f), l3 = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int cb = 0; cb < 128; cb += 32) {
-                if constexpr (F8) {
-                    // P in E4M3 (at most 2^8 with the lazy maximum: inside the range), four per column;
-                    // the row sums are those of the rounded values the product uses
-                    uint32_t pk[8];
-#pragma unroll
-                    for (int k = 0; k < 32; k += 4) {
-                        const float2 x0 = fma2(make_float2(__uint_as_float(r[cb + k]), __uint_as_float(r[cb + k + 1])), sc2, nm2);
-                        const float2 x1 = fma2(make_float2(__uint_as_float(r[cb + k + 2]), __uint_as_float(r[cb + k + 3])), sc2, nm2);
-                        const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
-                            make_float2(ex2_approx(x0.x), ex2_approx(x0.y)), __NV_SATFINITE, __NV_E4M3);
-                        const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
-                            make_float2(ex2_approx(x1.x), ex2_approx(x1.y)), __NV_SATFINITE, __NV_E4M3);
-                        pk[k / 4] = uint32_t(lo) | (uint32_t(hi) << 16);
-                        const __half2_raw hl = __nv_cvt_fp8x2_to_halfraw2(lo, __NV_E4M3);
-                        const __half2_raw hh = __nv_cvt_fp8x2_to_halfraw2(hi, __NV_E4M3);
-                        l2 = add2(l2, __half22float2(__half2(hl)));
-                        l2 = add2(l2, __half22float2(__half2(hh)));
-                    }
-                    tmem_st8(s_addr + cb / 4, pk);  // P over S (these columns are already in registers)
-                } else {
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int k = 0; k < 32; k += 2) {
-                        const float2 x = fma2(make_float2(__uint_as_float(r[cb + k]), __uint_as_float(r[cb + k + 1])), sc2, nm2);
-                        pk[k / 2] = pack_bf16x2(ex2_approx(x.x), ex2_approx(x.y));
-                        if (k & 2)
-                            acc_bf16x2(pk[k / 2], l3.x, l3.y);
-                        else
-                            acc_bf16x2(pk[k / 2], l2.x, l2.y);
-                    }
-                    tmem_st16(s_addr + cb / 2, pk);  // P over S (these columns are already in registers)
-                }
-            }
-            l_run += (l2.x + l2.y) + (l3.x + l3.y);
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(&p_ready[t]);
-        }
-        // ---- epilogue: O / l -> bf16 -> staging tile -> TMA store.  The staging tile is the tile's
-        // Q buffer, or (E4M3, whose Q buffer is half the size of the bf16 output) the K stages for
-        // tile 0 and the V stages for tile 1, free once the tile's last product has completed.
-        uint8_t* stg = F8 ? smem + (t == 0 ? OFF_K : OFF_V) : qt;
-        if (ok && !aborted()) ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[t], (nkb - 1) & 1, p.ctl, 63));
-        if constexpr (SWA) {  // the gate tile (bf16) into the staging buffer, free now
-            if (ok && row == 0) {
-                mbar_arrive_expect_tx(&gate_full[t], (D / 64) * CH);
-                for (int ch = 0; ch < D / 64; ++ch)
-                    tma_load_4d(stg + ch * CH, &p.tm_gate, &gate_full[t], ch * 64, g * G, i0 + t * T, b);
-            }
-            if (ok && !aborted()) ok = __all_sync(0xffffffffu, mbar_wait(&gate_full[t], 0, p.ctl, 65));
-        }
-        if (ok) {
-            tc_fence_after();
-            const float inv_l = l_run > 0.f ? (F8 ? p.in_dequant_v : 1.0f) / l_run : 0.f;
-#pragma unroll 1
-            for (int cb = 0; cb < D; cb += 32) {
-                uint32_t o[32];
-                tmem_ld32(o_addr + cb, o);
-                tmem_wait_ld();
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    uint32_t ou[4];
-                    const int e0 = cb + q4 * 8;
-                    uint4* dst = reinterpret_cast<uint4*>(stg + (e0 >> 6) * CH + sw128_off(row, (e0 & 63) >> 3));
-                    if constexpr (SWA) {  // out = A * sigmoid(gate), the gate read from the same place
-                        const uint4 gv = *dst;
-                        const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const float2 sg = sigmoid2_f32(bf2f2(gw[k]));
-                            ou[k] = pack_bf16x2(__uint_as_float(o[q4 * 8 + 2 * k]) * inv_l * sg.x,
-                                                __uint_as_float(o[q4 * 8 + 2 * k + 1]) * inv_l * sg.y);
+    #pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        uint32_t ou[4];
+                        const int e0 = cb + q4 * 8;
+                        uint4* dst = reinterpret_cast<uint4*>(stg + (e0 >> 6) * CH + sw128_off(row, (e0 & 63) >> 3));
+                        if constexpr (SWA) {  // out = A * sigmoid(gate), the gate read from the same place
+                            const uint4 gv = *dst;
+                            const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+    #pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                const float2 sg = sigmoid2_f32(bf2f2(gw[k]));
+                                ou[k] = pack_bf16x2(__uint_as_float(o[q4 * 8 + 2 * k]) * inv_l * sg.x,
+                                                    __uint_as_float(o[q4 * 8 + 2 * k + 1]) * inv_l * sg.y);
+                            }
+                        } else {
+    #pragma unroll
+                            for (int k = 0; k < 4; ++k)
+                                ou[k] = pack_bf16x2(__uint_as_float(o[q4 * 8 + 2 * k]) * inv_l,
+                                                    __uint_as_float(o[q4 * 8 + 2 * k + 1]) * inv_l);
                         }
-                    } else {
-#pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            ou[k] = pack_bf16x2(__uint_as_float(o[q4 * 8 + 2 * k]) * inv_l,
-                                                __uint_as_float(o[q4 * 8 + 2 * k + 1]) * inv_l);
+                        *dst = make_uint4(ou[0], ou[1], ou[2], ou[3]);
                     }
-                    *dst = make_uint4(ou[0], ou[1], ou[2], ou[3]);
                 }
+                fence_async_smem();
             }
-            fence_async_smem();
-        }
-        tc_fence_before();
-        mbar_arrive(&out_bar[t]);
-        if (row == 0 && ok && i0 + t * T < p.L) {  // a tile that starts past the end has nothing to store
-            if (mbar_wait(&out_bar[t], 0, p.ctl, 64)) {
-                for (int ch = 0; ch < D / 64; ++ch)
-                    tma_store_4d(&p.tm_out, stg + ch * CH, ch * 64, g * G, i0 + t * T, b);
-                bulk_commit();
-                bulk_wait_all();
-            } else {
-                fail();
+            tc_fence_before();
+            mbar_arrive(&out_bar[t]);
+            if (row == 0 && ok) {
+                if (!mbar_wait(&out_bar[t], n & 1, p.ctl, 64)) {
+                    fail();
+                } else if (i0 + t * T < p.L) {  // a tile that starts past the end has nothing to store
+                    for (int ch = 0; ch < D / 64; ++ch)
+                        tma_store_4d(&p.tm_out, stg + ch * CH, ch * 64, g * G, i0 + t * T, b);
+                    bulk_commit();
+                    if constexpr (SWA)
+                        bulk_wait_read_all();  // the next gate tile may land once the store has read this one
+                    else
+                        bulk_wait_all();
+                }
+                if (SWA) mbar_arrive(&stg_free[t]);
             }
-        }
-        if (!ok) fail();
+            if (!ok) fail();
+            J += nkb;
+            return ok && !aborted();
+        });
+        if constexpr (SWA)  // the outputs' stores complete before the CTA exits
+            if (row == 0) bulk_wait_all();
     }
     __syncthreads();
     if (aborted() && threadIdx.x == 0) {
@@ -654,10 +737,17 @@ cudaError_t launch_t(const PrefillParams& p, cudaStream_t s) {
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     auto k = global_attn_kernel<D, G, F8, SWA>;
-    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Glb<D, F8>::SMEM);
+    constexpr uint32_t smem = Glb<D, F8, SWA>::SMEM;
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    const long long ctas = static_cast<long long>(p.B) * p.Hkv * ((p.L + 2 * T - 1) / (2 * T));
-    k<<<static_cast<unsigned>(ctas), kThreads, Glb<D, F8>::SMEM, s>>>(p);
+    long long ctas = static_cast<long long>(p.B) * p.Hkv * ((p.L + 2 * T - 1) / (2 * T));
+    if constexpr (SWA) {  // persistent: one CTA per SM
+        int dev = 0, sms = 0;
+        if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+        if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+        ctas = ctas < sms ? ctas : sms;
+    }
+    k<<<static_cast<unsigned>(ctas), kThreads, smem, s>>>(p);
     return cudaGetLastError();
 }
 

@@ -108,6 +108,7 @@ def swa_e4m3(B, L, Hq, Hkv, W, seed):  # gated sliding window on E4M3 inputs (th
     assert err <= 0.10, err
 
 swa_e4m3(2, 150, 8, 2, 37, 11)    # odd window, two sequences
+swa_e4m3(2, 2500, 16, 4, 128, 12)  # 320 work items: two or three per persistent CTA
 
 from oracle import backward as bw
 
