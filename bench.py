@@ -681,7 +681,9 @@ def run_gpu(args):
     s8_by = SWA.B * SWA.L * (SWA.Hq * SWA.d * (1 + 2 + 2) + 2 * SWA.Hkv * SWA.d)  # q, k, v E4M3; gate, out bf16
     swa_fp8 = {"workload": f"{SWA.name} with E4M3 q, k, v", "ms": s8_t * 1e3, "tokens_per_s": SWA.tokens / s8_t,
                "roofline": {"bound": "hbm", "achieved": s8_by / s8_t / 1e9, "peak": hbm, "unit": "GB/s",
-                            "frac": s8_by / s8_t / 1e9 / hbm, "traffic": None, "algorithmic_bytes": s8_by}}
+                            "frac": s8_by / s8_t / 1e9 / hbm, "traffic": _traffic("swa_prefill_fp8_call"),
+                            "traffic_note": "k_hat and V^T pre-passes plus the attention kernel, one call",
+                            "algorithmic_bytes": s8_by}}
     del sx, s8, s8_out, s8_ws
 
     # ---- the decode step over E4M3 caches (outside the step): the same workload, caches stored
