@@ -557,11 +557,24 @@ __global__ void __launch_bounds__(kThreads, 1) global_attn_kernel(const __grid_c
                 tmem_ld32(s_addr + 96, r + 96);
                 tmem_wait_ld();
                 const int kmax = iq - (jlo + j) * BK;  // last valid key column of this row in the block
+                // SWA: the warp's 32 rows are 32 / G consecutive tokens, so most 32-column chunks lie
+                // wholly inside or wholly outside all their windows; `dead` marks the outside ones
+                // (left out of the maximum, P = 0 without exponentials), and only chunks that hold a
+                // window edge of some row are masked element by element
+                uint32_t dead = 0;
                 if constexpr (SWA) {
                     const int kmin = kmax - p.window + 1;  // first key column inside the window
     #pragma unroll
-                    for (int k = 0; k < 128; ++k)
-                        if (k > kmax || k < kmin) r[k] = __float_as_uint(-INFINITY);
+                    for (int c = 0; c < 4; ++c) {
+                        const int lo = 32 * c, hi = 32 * c + 31;
+                        if (__all_sync(0xffffffffu, lo > kmax || hi < kmin)) {
+                            dead |= 1u << c;
+                        } else if (__any_sync(0xffffffffu, hi > kmax || lo < kmin)) {
+    #pragma unroll
+                            for (int k = lo; k <= hi; ++k)
+                                if (k > kmax || k < kmin) r[k] = __float_as_uint(-INFINITY);
+                        }
+                    }
                 } else if ((jlo + j + 1) * BK - 1 > i0) {  // the block reaches past the CTA's first query
     #pragma unroll
                     for (int k = 0; k < 128; ++k)
@@ -569,12 +582,26 @@ __global__ void __launch_bounds__(kThreads, 1) global_attn_kernel(const __grid_c
                 }
                 // block maximum: eight independent chains of three-input maxima, then their maximum
                 float a8[8];
+                if constexpr (SWA) {
     #pragma unroll
-                for (int i = 0; i < 8; ++i) a8[i] = fmaxf(__uint_as_float(r[i]), __uint_as_float(r[i + 8]));
+                    for (int i = 0; i < 8; ++i) a8[i] = -INFINITY;
     #pragma unroll
-                for (int k = 16; k < 128; k += 16)
+                    for (int c = 0; c < 4; ++c) {
+                        if ((dead >> c) & 1u) continue;
     #pragma unroll
-                    for (int i = 0; i < 8; ++i) a8[i] = fmax3(a8[i], __uint_as_float(r[k + i]), __uint_as_float(r[k + 8 + i]));
+                        for (int k = 32 * c; k < 32 * c + 32; k += 16)
+    #pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                a8[i] = fmax3(a8[i], __uint_as_float(r[k + i]), __uint_as_float(r[k + 8 + i]));
+                    }
+                } else {
+    #pragma unroll
+                    for (int i = 0; i < 8; ++i) a8[i] = fmaxf(__uint_as_float(r[i]), __uint_as_float(r[i + 8]));
+    #pragma unroll
+                    for (int k = 16; k < 128; k += 16)
+    #pragma unroll
+                        for (int i = 0; i < 8; ++i) a8[i] = fmax3(a8[i], __uint_as_float(r[k + i]), __uint_as_float(r[k + 8 + i]));
+                }
                 const float mx = fmaxf(fmax3(fmax3(a8[0], a8[1], a8[2]), a8[3], a8[4]), fmax3(a8[5], a8[6], a8[7]));
                 const float mb = mx * sc;
                 float m_new = m_run;
@@ -606,6 +633,14 @@ __global__ void __launch_bounds__(kThreads, 1) global_attn_kernel(const __grid_c
                 float2 l2 = make_float2(0.f, 0.f), l3 = make_float2(0.f, 0.f);
     #pragma unroll
                 for (int cb = 0; cb < 128; cb += 32) {
+                    if (SWA && ((dead >> (cb / 32)) & 1u)) {  // outside every row's window: P = 0
+                        uint32_t z[16] = {};
+                        if constexpr (F8)
+                            tmem_st8(s_addr + cb / 4, z);
+                        else
+                            tmem_st16(s_addr + cb / 2, z);
+                        continue;
+                    }
                     if constexpr (F8) {
                         // P in E4M3 (at most 2^8 with the lazy maximum: inside the range), four per column.
                         // The row sums add the rounded values the product uses: 16 per fp16 lane (at most
