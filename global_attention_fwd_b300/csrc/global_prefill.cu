@@ -51,7 +51,8 @@ struct Glb {
     static constexpr uint32_t OFF_G = 6 * TILE;    // SWA: gate / output staging, one bf16 tile per Q tile
     static constexpr uint32_t OFF_BAR = OFF_G + (SWA ? 2 * 128 * D * 2 : 0);
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
-    static constexpr uint32_t SMEM = OFF_MISC + 32;
+    static constexpr uint32_t OFF_R = OFF_MISC + 32;  // E4M3: the rotation frequencies (hi, lo)
+    static constexpr uint32_t SMEM = OFF_R + (F8 ? 2 * kMaxRotHalf * 4 : 0);
 };
 
 // ---------------------------------------------------------------- kernel 1
@@ -143,6 +144,105 @@ __device__ __forceinline__ void qk_norm_rope_row_e4m3(uint8_t* tile, int row, co
     const float fs = f * s_out;
 #pragma unroll 1
     for (int c = c_first; c < D / 16; ++c) {
+        uint4* cp = reinterpret_cast<uint4*>(tile + sw128_off(row, c));
+        const uint4 v = *cp;
+        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float4 w4 = __ldg(reinterpret_cast<const float4*>(w + 16 * c + 4 * k));
+            const __half2_raw h01 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(u[k] & 0xFFFFu), __NV_E4M3);
+            const __half2_raw h23 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(u[k] >> 16), __NV_E4M3);
+            const float2 x01 = __half22float2(__half2(h01)), x23 = __half22float2(__half2(h23));
+            const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(x01.x * fs * w4.x, x01.y * fs * w4.y), __NV_SATFINITE,
+                                                         __NV_E4M3);
+            const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(x23.x * fs * w4.z, x23.y * fs * w4.w), __NV_SATFINITE,
+                                                         __NV_E4M3);
+            o[k] = lo | (hi << 16);
+        }
+        *cp = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
+// The same with the rotary width 2*HALF compiled in: the chunks holding rotated dims stay in
+// registers (no per-element shared-memory round trip), and the SL lanes that share a position (the
+// G query heads of a token sit in consecutive rows) split the cos/sin evaluations and exchange them
+// with shuffles.  f_hi / f_lo: the rotation frequencies in shared memory (read by lane-dependent
+// index).  Every lane of the warp calls it.
+template <int D, int SL, int HALF>
+__device__ __forceinline__ void qk_norm_rope_row_e4m3_ct(uint8_t* tile, int row, const float* w, float eps, int pos,
+                                                         const float* f_hi, const float* f_lo, float dq, float s_out) {
+    static_assert(D == 128, "one 128-byte swizzle row per head row");
+    constexpr int NR = (2 * HALF + 15) / 16;  // 16-byte chunks holding rotated dims
+    static_assert(NR <= D / 16, "rotary width above the head dimension");
+    float ss = 0.f;
+#pragma unroll
+    for (int c = 0; c < D / 16; ++c) {
+        const uint4 v = *reinterpret_cast<const uint4*>(tile + sw128_off(row, c));
+        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float a = e4m3_to_f(u[k] & 0xFF), b = e4m3_to_f((u[k] >> 8) & 0xFF);
+            const float c2 = e4m3_to_f((u[k] >> 16) & 0xFF), d2 = e4m3_to_f(u[k] >> 24);
+            ss = fmaf(a, a, fmaf(b, b, fmaf(c2, c2, fmaf(d2, d2, ss))));
+        }
+    }
+    ss *= dq * dq;
+    const float f = (ss > 0.f || eps > 0.f ? rsqrtf(ss * (1.0f / D) + eps) : 0.f) * dq;
+    const float fs = f * s_out;
+    // cos/sin: lane (grp | h) evaluates frequencies j = i*SL + h; everyone gathers them below
+    const int lane = threadIdx.x & 31;
+    const int mine = lane & (SL - 1), grp = lane & ~(SL - 1);
+    constexpr int NI = (HALF + SL - 1) / SL;
+    float cj[NI], sj[NI];
+#pragma unroll
+    for (int i = 0; i < NI; ++i) {
+        const int jm = i * SL + mine;
+        cj[i] = 1.f;
+        sj[i] = 0.f;
+        if (jm < HALF) rope_cos_sin(pos, f_hi[jm], f_lo[jm], cj[i], sj[i]);
+    }
+    // the chunks with rotated dims: x * w in registers, rotated, then times f * s_out
+    float y[NR * 16];
+#pragma unroll
+    for (int c = 0; c < NR; ++c) {
+        const uint4 v = *reinterpret_cast<const uint4*>(tile + sw128_off(row, c));
+        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float4 w4 = __ldg(reinterpret_cast<const float4*>(w + 16 * c + 4 * k));
+            const __half2_raw h01 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(u[k] & 0xFFFFu), __NV_E4M3);
+            const __half2_raw h23 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(u[k] >> 16), __NV_E4M3);
+            const float2 x01 = __half22float2(__half2(h01)), x23 = __half22float2(__half2(h23));
+            y[16 * c + 4 * k] = x01.x * w4.x;
+            y[16 * c + 4 * k + 1] = x01.y * w4.y;
+            y[16 * c + 4 * k + 2] = x23.x * w4.z;
+            y[16 * c + 4 * k + 3] = x23.y * w4.w;
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < HALF; ++j) {
+        const float cs = __shfl_sync(0xffffffffu, cj[j / SL], grp | (j % SL));
+        const float sn = __shfl_sync(0xffffffffu, sj[j / SL], grp | (j % SL));
+        const float a = y[j], b = y[j + HALF];
+        y[j] = a * cs - b * sn;
+        y[j + HALF] = b * cs + a * sn;
+    }
+#pragma unroll
+    for (int c = 0; c < NR; ++c) {
+        uint32_t o[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float* q4 = y + 16 * c + 4 * k;
+            const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(q4[0] * fs, q4[1] * fs), __NV_SATFINITE, __NV_E4M3);
+            const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(q4[2] * fs, q4[3] * fs), __NV_SATFINITE, __NV_E4M3);
+            o[k] = lo | (hi << 16);
+        }
+        *reinterpret_cast<uint4*>(tile + sw128_off(row, c)) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    // the chunks past the rotated dims, with paired conversions
+#pragma unroll 1
+    for (int c = NR; c < D / 16; ++c) {
         uint4* cp = reinterpret_cast<uint4*>(tile + sw128_off(row, c));
         const uint4 v = *cp;
         const uint32_t u[4] = {v.x, v.y, v.z, v.w};
@@ -267,7 +367,8 @@ __device__ __forceinline__ void for_items(int n_items, F&& body) {
 // so the CTAs are persistent: one per SM walks items blockIdx.x, + gridDim.x, ...; the TMA warp
 // fetches the next item's Q, K_hat / V^T blocks and gate tiles while the current one finishes, and
 // the gate tiles have their own staging buffer.  The global layer runs one item per CTA.
-template <int D, int G, bool F8, bool SWA = false>
+// ROT (E4M3): the rotary width compiled into the query transform, or 0 = any width.
+template <int D, int G, bool F8, bool SWA = false, int ROT = 0>
 __global__ void __launch_bounds__(kThreads, 1) global_attn_kernel(const __grid_constant__ PrefillParams p) {
     constexpr int T = 128 / G;  // tokens per tile
     using C = Glb<D, F8, SWA>;
@@ -292,6 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1) global_attn_kernel(const __grid_c
     uint64_t* q_empty = bar + 22;    // SWA: the item's score products are complete (Q buffer free)
     uint64_t* stg_free = bar + 23;   // [2] per tile (SWA): the output store has read the staging buffer
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
+    float* rf_s = reinterpret_cast<float*>(smem + C::OFF_R);  // E4M3: f_hi [kMaxRotHalf], f_lo [kMaxRotHalf]
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -349,6 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1) global_attn_kernel(const __grid_c
         mbar_init(drain, 1);
         fence_barrier_init();
     }
+    if constexpr (F8 && ROT > 0) stage_rope(p.rope, rf_s, rf_s + kMaxRotHalf);
     if (warp == 1) {
         tmem_alloc(tslot, 512);
         tmem_relinquish();
@@ -525,7 +628,10 @@ __global__ void __launch_bounds__(kThreads, 1) global_attn_kernel(const __grid_c
         auto q_transform = [&](int n, int pos) {
             const bool okq = __all_sync(0xffffffffu, mbar_wait(q_full, n & 1, p.ctl, 60));
             if (okq) {
-                if constexpr (F8)
+                if constexpr (F8 && ROT > 0)
+                    qk_norm_rope_row_e4m3_ct<D, G, ROT / 2>(qt, row, p.wq, p.eps, pos, rf_s, rf_s + kMaxRotHalf,
+                                                            p.in_dequant_q, s_qh);
+                else if constexpr (F8)
                     qk_norm_rope_row_e4m3<D>(qt, row, p.wq, p.eps, pos, p.rope, p.in_dequant_q, s_qh);
                 else
                     qk_norm_rope_row<D>(qt, CH, row, p.wq, p.eps, pos, p.rope);
@@ -757,7 +863,7 @@ __global__ void __launch_bounds__(kThreads, 1) global_attn_kernel(const __grid_c
     if (warp == 1) tmem_dealloc(tbase, 512);
 }
 
-template <int D, int G, bool F8, bool SWA>
+template <int D, int G, bool F8, bool SWA, int ROT>
 cudaError_t launch_t(const PrefillParams& p, cudaStream_t s) {
     constexpr int T = 128 / G;
     const long long rows = static_cast<long long>(p.B) * p.L * p.Hkv;
@@ -771,7 +877,7 @@ cudaError_t launch_t(const PrefillParams& p, cudaStream_t s) {
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    auto k = global_attn_kernel<D, G, F8, SWA>;
+    auto k = global_attn_kernel<D, G, F8, SWA, ROT>;
     constexpr uint32_t smem = Glb<D, F8, SWA>::SMEM;
     e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
@@ -786,14 +892,14 @@ cudaError_t launch_t(const PrefillParams& p, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-template <int D, bool F8, bool SWA = false>
+template <int D, bool F8, bool SWA = false, int ROT = 0>
 cudaError_t launch_d(const PrefillParams& p, cudaStream_t s) {
     switch (p.Hq / p.Hkv) {
-        case 1: return launch_t<D, 1, F8, SWA>(p, s);
-        case 2: return launch_t<D, 2, F8, SWA>(p, s);
-        case 4: return launch_t<D, 4, F8, SWA>(p, s);
-        case 8: return launch_t<D, 8, F8, SWA>(p, s);
-        case 16: return launch_t<D, 16, F8, SWA>(p, s);
+        case 1: return launch_t<D, 1, F8, SWA, ROT>(p, s);
+        case 2: return launch_t<D, 2, F8, SWA, ROT>(p, s);
+        case 4: return launch_t<D, 4, F8, SWA, ROT>(p, s);
+        case 8: return launch_t<D, 8, F8, SWA, ROT>(p, s);
+        case 16: return launch_t<D, 16, F8, SWA, ROT>(p, s);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -805,8 +911,16 @@ int global_q_tile_tokens(int G) { return 128 / G; }
 
 cudaError_t launch_global_prefill(const PrefillParams& p, int d, cudaStream_t s) {
     if (p.Hkv <= 0 || p.Hq % p.Hkv || !global_supports(d, p.Hq / p.Hkv)) return cudaErrorInvalidValue;
-    if (p.fp8 && p.swa) return d == 128 && p.window >= 1 ? launch_d<128, true, true>(p, s) : cudaErrorInvalidValue;
-    if (p.fp8) return d == 128 ? launch_d<128, true>(p, s) : cudaErrorInvalidValue;
+    // E4M3: the ZGCM-1 rotary width (42 of 128 dims) compiled in, any other through the general transform
+    constexpr int kRot = 42;
+    if (p.fp8 && p.swa) {
+        if (d != 128 || p.window < 1) return cudaErrorInvalidValue;
+        return 2 * p.rope.half == kRot ? launch_d<128, true, true, kRot>(p, s) : launch_d<128, true, true>(p, s);
+    }
+    if (p.fp8) {
+        if (d != 128) return cudaErrorInvalidValue;
+        return 2 * p.rope.half == kRot ? launch_d<128, true, false, kRot>(p, s) : launch_d<128, true>(p, s);
+    }
     return d == 128 ? launch_d<128, false>(p, s) : launch_d<64, false>(p, s);
 }
 

@@ -74,11 +74,12 @@ def test_fp8_small_lengths_all_rows(zg, B, L):
     _check(out, deq, extra, list(range(B * L)), 42, 1e6, f"fp8 global B{B} L{L}")
 
 
+@pytest.mark.parametrize("rot", [64, 42])  # the general query transform, and the one with 42 compiled in
 @pytest.mark.parametrize("Hq,Hkv,L", [(8, 8, 600), (4, 2, 530), (16, 2, 450), (32, 2, 300)])
-def test_fp8_gqa_ratios(zg, Hq, Hkv, L):
+def test_fp8_gqa_ratios(zg, Hq, Hkv, L, rot):
     stored, deq, extra = _inputs(1, L, Hq, Hkv, 128, seed=Hq * 7 + Hkv, scales=UNIT)
-    out = _run(zg, stored, extra, UNIT, 64, 1e4)
-    _check(out, deq, extra, list(range(L)), 64, 1e4, f"fp8 global {Hq}/{Hkv} L{L}")
+    out = _run(zg, stored, extra, UNIT, rot, 1e4)
+    _check(out, deq, extra, list(range(L)), rot, 1e4, f"fp8 global {Hq}/{Hkv} L{L} rotary {rot}")
 
 
 def test_fp8_scales_other_than_one(zg):

@@ -79,6 +79,13 @@ def test_fp8_swa_all_rows(zg, B, L, Hq, Hkv, window):
     _check(out, deq, extra, list(range(B * L)), window, f"fp8 swa B{B} L{L} {Hq}/{Hkv} W{window}")
 
 
+@pytest.mark.parametrize("rot", [0, 64, 128])  # widths other than 42 take the general query transform
+def test_fp8_swa_other_rotary_widths(zg, rot):
+    stored, deq, extra = _inputs(2, 350, 32, 8, seed=800 + rot, scales=UNIT)
+    out = _run(zg, stored, extra, UNIT, 128, rotary_dim=rot)
+    _check(out, deq, extra, list(range(2 * 350)), 128, f"fp8 swa rotary {rot}", rotary_dim=rot)
+
+
 def test_fp8_swa_scales_and_suppressing_gate(zg):
     """Per-tensor scales other than one, and gate logits ~ N(-3, 2^2) (most outputs suppressed)."""
     sc = dict(q=3.0, k=0.37, v=12.5)
