@@ -263,50 +263,66 @@ __device__ __forceinline__ void qk_norm_rope_row_e4m3_ct(uint8_t* tile, int row,
     }
 }
 
-// k_hat in E4M3 from E4M3 keys: one warp per key row at a time, four bytes per lane (lane l holds
-// elements 4l .. 4l + 3, the layout norm_rope_warp_vals takes)
-template <int D>
-__global__ void __launch_bounds__(256) khat_e4m3_kernel(const __grid_constant__ PrefillParams p) {
+// k_hat in E4M3 from E4M3 keys, one thread per key row: a CTA stages 128 rows (16 KB) in shared
+// memory with coalesced loads (128-byte swizzle), transforms each row in place with the query
+// transform's arithmetic (the key weights, the key hat scale), and writes the rows back
+// coalesced.  ROT: the rotary width compiled in (then SL lanes, a divisor of Hkv, share a position:
+// the KV heads of a token are consecutive rows), or 0 = any width.
+template <int D, int SL, int ROT>
+__global__ void __launch_bounds__(128) khat_e4m3_kernel(const __grid_constant__ PrefillParams p) {
     static_assert(D == 128, "one 128-byte row per head vector");
-    constexpr int kRows = 4;
-    __shared__ __align__(16) float buf[8][D];
-    __shared__ float rope_f[2][kMaxRotHalf];
-    stage_rope(p.rope, rope_f[0], rope_f[1]);
-    __syncthreads();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const long long row0 = (static_cast<long long>(blockIdx.x) * 8 + warp) * kRows;  // (b, j, g)
+    __shared__ __align__(1024) uint8_t tile[128 * D];
+    __shared__ float rf[2 * kMaxRotHalf];
     const long long nrows = static_cast<long long>(p.B) * p.L * p.Hkv;
-    if (row0 >= nrows) return;
+    const long long row0 = static_cast<long long>(blockIdx.x) * 128;
+    const uint8_t* src = reinterpret_cast<const uint8_t*>(p.k_raw);
+    uint8_t* dst = reinterpret_cast<uint8_t*>(p.khat);
+#pragma unroll
+    for (int k = 0; k < D / 16; ++k) {  // 16-byte piece i of the CTA's rows: row i / 8, chunk i % 8
+        const int i = threadIdx.x + 128 * k, r = i >> 3, c = i & 7;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (row0 + r < nrows) v = *reinterpret_cast<const uint4*>(src + (row0 + r) * D + c * 16);
+        *reinterpret_cast<uint4*>(tile + sw128_off(r, c)) = v;
+    }
+    if constexpr (ROT > 0) stage_rope(p.rope, rf, rf + kMaxRotHalf);
+    __syncthreads();
+    const int r = threadIdx.x;
+    const long long row = row0 + r;
+    const long long tok = row < nrows ? row / p.Hkv : 0;
+    const int pos =
+        row < nrows && idx_ok(p.ctl, tok, static_cast<long long>(p.B) * p.L, 94) ? __ldg(p.pos + tok) : 0;
     const float s_kh = e4m3_hat_scale<D>(p.wk);
-    float wv[4];
-    norm_weights_lane<D>(p.wk, wv);
-    uint32_t raw[kRows];
-    int pos[kRows];
+    if constexpr (ROT > 0)
+        qk_norm_rope_row_e4m3_ct<D, SL, ROT / 2>(tile, r, p.wk, p.eps, pos, rf, rf + kMaxRotHalf, p.in_dequant_k,
+                                                 s_kh);
+    else
+        qk_norm_rope_row_e4m3<D>(tile, r, p.wk, p.eps, pos, p.rope, p.in_dequant_k, s_kh);
+    __syncthreads();
 #pragma unroll
-    for (int r = 0; r < kRows; ++r) {  // every load first
-        const long long row = row0 + r;
-        raw[r] = 0u;
-        pos[r] = 0;
-        if (row >= nrows) continue;
-        const long long tok = row / p.Hkv;
-        if (!idx_ok(p.ctl, tok, static_cast<long long>(p.B) * p.L, 94)) continue;
-        pos[r] = __ldg(p.pos + tok);
-        raw[r] = *reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint8_t*>(p.k_raw) + row * D + lane * 4);
+    for (int k = 0; k < D / 16; ++k) {
+        const int i = threadIdx.x + 128 * k, rr = i >> 3, c = i & 7;
+        if (row0 + rr < nrows)
+            *reinterpret_cast<uint4*>(dst + (row0 + rr) * D + c * 16) =
+                *reinterpret_cast<const uint4*>(tile + sw128_off(rr, c));
     }
-#pragma unroll
-    for (int r = 0; r < kRows; ++r) {
-        const long long row = row0 + r;
-        if (row >= nrows) break;
-        float v[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) v[e] = e4m3_to_f((raw[r] >> (8 * e)) & 0xFFu) * p.in_dequant_k;
-        norm_rope_warp_vals<D>(v, wv, p.eps, pos[r], p.rope.half, rope_f[0], rope_f[1], 1.0f, buf[warp]);
-        const float4 y = *reinterpret_cast<const float4*>(buf[warp] + lane * 4);
-        const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(y.x * s_kh, y.y * s_kh), __NV_SATFINITE, __NV_E4M3);
-        const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(y.z * s_kh, y.w * s_kh), __NV_SATFINITE, __NV_E4M3);
-        *reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(p.khat) + row * D + lane * 4) = lo | (hi << 16);
-        __syncwarp();  // buf[warp] is reused by the next row
+}
+
+template <int D, int ROT>
+cudaError_t launch_khat_e4m3(const PrefillParams& p, long long rows, cudaStream_t s) {
+    const unsigned grid = static_cast<unsigned>((rows + 127) / 128);
+    if constexpr (ROT == 0) {
+        khat_e4m3_kernel<D, 1, 0><<<grid, 128, 0, s>>>(p);
+    } else {  // lanes sharing a position: the largest power of two <= 8 dividing Hkv
+        if (p.Hkv % 8 == 0)
+            khat_e4m3_kernel<D, 8, ROT><<<grid, 128, 0, s>>>(p);
+        else if (p.Hkv % 4 == 0)
+            khat_e4m3_kernel<D, 4, ROT><<<grid, 128, 0, s>>>(p);
+        else if (p.Hkv % 2 == 0)
+            khat_e4m3_kernel<D, 2, ROT><<<grid, 128, 0, s>>>(p);
+        else
+            khat_e4m3_kernel<D, 1, ROT><<<grid, 128, 0, s>>>(p);
     }
+    return cudaGetLastError();
 }
 
 // V^T in E4M3: [B, Hkv, D, Lp] from [B, L, Hkv, D]; one CTA per 128 keys of one (b, KV head)
@@ -868,7 +884,8 @@ cudaError_t launch_t(const PrefillParams& p, cudaStream_t s) {
     constexpr int T = 128 / G;
     const long long rows = static_cast<long long>(p.B) * p.L * p.Hkv;
     if constexpr (F8) {
-        khat_e4m3_kernel<D><<<static_cast<unsigned>((rows + 31) / 32), 256, 0, s>>>(p);  // four rows per warp
+        const cudaError_t ek = launch_khat_e4m3<D, ROT>(p, rows, s);
+        if (ek != cudaSuccess) return ek;
         const dim3 vg(static_cast<unsigned>((p.vt_lp + 127) / 128), static_cast<unsigned>(p.Hkv),
                       static_cast<unsigned>(p.B));
         vt_e4m3_kernel<D><<<vg, 256, 0, s>>>(p, p.vt_ws, p.vt_lp);
