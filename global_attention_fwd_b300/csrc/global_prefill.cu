@@ -37,7 +37,7 @@ namespace {
 
 constexpr int BK = 128;               // keys per block
 constexpr uint32_t CH = 128 * 128;    // one 64-column chunk of 128 rows (16-bit elements)
-constexpr int NBAR = 25;
+constexpr int NBAR = 27;
 constexpr float kTau = 8.0f;
 constexpr int kThreads = 384;
 constexpr int kGroupCt = 128;  // CTAs of one (sequence, KV head) scheduled together on long sequences
@@ -408,6 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1) global_attn_kernel(const __grid_c
     uint64_t* gate_full = bar + 20;  // [2] per tile (SWA): the gate tile is in the staging buffer
     uint64_t* q_empty = bar + 22;    // SWA: the item's score products are complete (Q buffer free)
     uint64_t* stg_free = bar + 23;   // [2] per tile (SWA): the output store has read the staging buffer
+    uint64_t* sig_ready = bar + 25;  // [2] per tile (SWA): the staging buffer holds sigmoid(gate)
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
     float* rf_s = reinterpret_cast<float*>(smem + C::OFF_R);  // E4M3: f_hi [kMaxRotHalf], f_lo [kMaxRotHalf]
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
@@ -462,6 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1) global_attn_kernel(const __grid_c
             mbar_init(&out_bar[i], 128);
             mbar_init(&gate_full[i], 1);
             mbar_init(&stg_free[i], 1);
+            mbar_init(&sig_ready[i], 64);
         }
         mbar_init(q_empty, 1);
         mbar_init(drain, 1);
@@ -619,6 +621,30 @@ __global__ void __launch_bounds__(kThreads, 1) global_attn_kernel(const __grid_c
                 umma_commit(drain);
                 (void)mbar_wait(drain, 0, p.ctl, 59);
             }
+        } else if constexpr (SWA) {
+            // ------------------------------------------------------------ sigmoid(gate) (warps 2, 3)
+            // each gate tile, once landed, becomes sigmoid(gate) in place (fp32, rounded to bf16:
+            // 2^-9 relative at every magnitude), so that the epilogue only multiplies
+            const int tid = static_cast<int>(threadIdx.x) - 64;
+            bool ok = true;
+            for_items<SWA>(n_items, [&](int, int n) {
+                for (int t = 0; t < 2 && ok; ++t) {
+                    ok = __all_sync(0xffffffffu, mbar_wait(&gate_full[t], n & 1, p.ctl, 70));
+                    if (!ok) break;
+                    uint4* g4 = reinterpret_cast<uint4*>(smem + C::OFF_G + t * (D / 64) * CH);
+#pragma unroll 4
+                    for (int i = tid; i < 128 * D / 8; i += 64) {
+                        const uint4 v = g4[i];
+                        const float2 a = sigmoid2_f32(bf2f2(v.x)), b = sigmoid2_f32(bf2f2(v.y));
+                        const float2 c = sigmoid2_f32(bf2f2(v.z)), d = sigmoid2_f32(bf2f2(v.w));
+                        g4[i] = make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(b.x, b.y), pack_bf16x2(c.x, c.y),
+                                           pack_bf16x2(d.x, d.y));
+                    }
+                    mbar_arrive(&sig_ready[t]);
+                }
+                return ok && !aborted();
+            });
+            if (!ok) fail();
         }
     } else {
         regs_inc<216>();
@@ -807,10 +833,10 @@ __global__ void __launch_bounds__(kThreads, 1) global_attn_kernel(const __grid_c
             // ---- epilogue: O / l -> bf16 -> staging tile -> TMA store.  The staging tile is the tile's
             // Q buffer, or (E4M3, whose Q buffer is half the size of the bf16 output) the K stages for
             // tile 0 and the V stages for tile 1, free once the tile's last product has completed; SWA:
-            // the gate tile, which the output overwrites in place.
+            // the gate tile, turned into sigmoid(gate) by warps 2 and 3, which the output overwrites in place.
             uint8_t* stg = SWA ? smem + C::OFF_G + t * (D / 64) * CH : F8 ? smem + (t == 0 ? OFF_K : OFF_V) : qt;
             if (ok && !aborted()) ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[t], (J + nkb - 1) & 1, p.ctl, 63));
-            if (SWA && ok && !aborted()) ok = __all_sync(0xffffffffu, mbar_wait(&gate_full[t], n & 1, p.ctl, 65));
+            if (SWA && ok && !aborted()) ok = __all_sync(0xffffffffu, mbar_wait(&sig_ready[t], n & 1, p.ctl, 65));
             if (ok) {
                 tc_fence_after();
                 const float inv_l = l_run > 0.f ? (F8 ? p.in_dequant_v : 1.0f) / l_run : 0.f;
@@ -824,12 +850,12 @@ __global__ void __launch_bounds__(kThreads, 1) global_attn_kernel(const __grid_c
                         uint32_t ou[4];
                         const int e0 = cb + q4 * 8;
                         uint4* dst = reinterpret_cast<uint4*>(stg + (e0 >> 6) * CH + sw128_off(row, (e0 & 63) >> 3));
-                        if constexpr (SWA) {  // out = A * sigmoid(gate), the gate read from the same place
+                        if constexpr (SWA) {  // out = A * sigmoid(gate), sigmoid(gate) read from the same place
                             const uint4 gv = *dst;
                             const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
     #pragma unroll
                             for (int k = 0; k < 4; ++k) {
-                                const float2 sg = sigmoid2_f32(bf2f2(gw[k]));
+                                const float2 sg = bf2f2(gw[k]);
                                 ou[k] = pack_bf16x2(__uint_as_float(o[q4 * 8 + 2 * k]) * inv_l * sg.x,
                                                     __uint_as_float(o[q4 * 8 + 2 * k + 1]) * inv_l * sg.y);
                             }
