@@ -277,8 +277,8 @@ size_t zg_global_prefill_fp8_workspace_bytes(int B, int L, int Hkv, int d);
  *   Rounding: q_hat and k_hat (after RMSNorm and RoPE in fp32) are rounded to E4M3 times a
  *        power-of-two scale that puts their bound sqrt(d) * max|w| just inside +-448 (the
  *        scale is undone exactly in the softmax); the softmax weights P are rounded to
- *        E4M3 (they are at most 2^8 there) and the row sums are those of the rounded
- *        weights; V enters as stored.  Expect a relative error of a few per cent on the
+ *        E4M3 (they are at most 2^8 there) and the row sums add the rounded weights (16 per
+ *        fp16 lane, then fp32: relative rounding <= 9 * 2^-11); V enters as stored.  Expect a relative error of a few per cent on the
  *        output (three mantissa bits per operand), not the bf16 path's 1e-2.
  *   workspace: device scratch of at least zg_global_prefill_fp8_workspace_bytes() bytes,
  *        16-byte aligned, no initialisation; it receives k_hat in E4M3 and V transposed
@@ -293,9 +293,11 @@ zg_status zg_global_prefill_fp8(const uint8_t *q, const uint8_t *k, const uint8_
 
 /*
  * zg_swa_prefill_fp8 -- the gated sliding-window prefill (zg_swa_prefill's operation) with E4M3
- * inputs and E4M3 tensor-core products, on the pipeline of zg_global_prefill_fp8: each query tile
- * visits only the 128-key blocks that meet its queries' windows, masks both window edges, and
- * multiplies by sigmoid(gate) (fp32, as zg_swa_prefill) before the bf16 store.
+ * inputs and E4M3 tensor-core products, on the pipeline of zg_global_prefill_fp8 (one persistent
+ * CTA per SM walking pairs of query tiles): each query tile visits only the 128-key blocks that
+ * meet its queries' windows, masks both window edges, and multiplies by sigmoid(gate) before the
+ * bf16 store; sigmoid(gate) is evaluated in fp32 and rounded to bf16 (2^-9 relative at every
+ * magnitude) first.
  *   q, k, v: E4M3 as in zg_global_prefill_fp8 (scales likewise); gate [B, L, Hq, d] bf16 logits
  *        (required: ZG_ERR_NULL if missing); window >= 1 (keys i - window + 1 .. i; ZG_ERR_SHAPE
  *        otherwise; no upper bound: a window of L or more is the global layer with a gate).
