@@ -82,6 +82,15 @@ def test_fp8_gqa_ratios(zg, Hq, Hkv, L, rot):
     _check(out, deq, extra, list(range(L)), rot, 1e4, f"fp8 global {Hq}/{Hkv} L{L} rotary {rot}")
 
 
+@pytest.mark.parametrize("Hq,Hkv", [(16, 4), (12, 3)])  # KV heads per token not a multiple of 8
+def test_fp8_kv_head_counts(zg, Hq, Hkv):
+    """The k_hat pre-pass shares each token's rotation among its consecutive KV-head rows (4 lanes
+    here, or none for 3 heads); the whole output against the oracle."""
+    stored, deq, extra = _inputs(2, 333, Hq, Hkv, 128, seed=40 + Hkv, scales=UNIT)
+    out = _run(zg, stored, extra, UNIT, 42, 1e6)
+    _check(out, deq, extra, list(range(2 * 333)), 42, 1e6, f"fp8 global {Hq}/{Hkv}")
+
+
 def test_fp8_scales_other_than_one(zg):
     """Per-tensor scales (not powers of two) are divided out: the same attention as unit scales
     of the same dequantised values, within the tolerance."""

@@ -72,6 +72,8 @@ def _check(out, deq, extra, rows, window, what, rotary_dim=42, theta=1e4):
     (1, 200, 32, 8, 1),       # window 1: each query sees only itself
     (2, 3000, 32, 8, 128),    # 752 work items: several per persistent CTA, every row checked
     (1, 5000, 8, 8, 200),     # MHA, up to four key blocks per item, 160 items (some CTAs take two)
+    (2, 700, 12, 3, 128),     # three KV heads: no rotation shared across k_hat rows
+    (2, 700, 16, 4, 96),      # four KV heads
 ])
 def test_fp8_swa_all_rows(zg, B, L, Hq, Hkv, window):
     stored, deq, extra = _inputs(B, L, Hq, Hkv, seed=700 + L + window, scales=UNIT)
