@@ -325,30 +325,42 @@ cudaError_t launch_khat_e4m3(const PrefillParams& p, long long rows, cudaStream_
     return cudaGetLastError();
 }
 
-// V^T in E4M3: [B, Hkv, D, Lp] from [B, L, Hkv, D]; one CTA per 128 keys of one (b, KV head)
+// V^T in E4M3: [B, Hkv, D, Lp] from [B, L, Hkv, D]; one CTA per 128 keys of one (b, KV head).
+// 16-byte loads of the key rows into a 132-byte-stride tile (four 4-byte stores each, on distinct
+// banks); then each thread transposes blocks of 4 keys x 4 dims with byte permutes, a warp taking
+// 32 keys x 16 dims so that its tile reads hit 32 distinct banks and its stores fill whole 32-byte
+// sectors of four V^T rows.
 template <int D>
 __global__ void __launch_bounds__(256) vt_e4m3_kernel(const __grid_constant__ PrefillParams p, uint8_t* vt, int Lp) {
-    __shared__ uint8_t tile[128][D + 4];
+    static_assert(D == 128, "one 128-byte row per head vector");
+    __shared__ uint32_t tile[128][D / 4 + 1];
     const int j0 = blockIdx.x * 128, g = blockIdx.y, b = blockIdx.z;
     const uint8_t* v = reinterpret_cast<const uint8_t*>(p.v_raw);
-    for (int idx = threadIdx.x; idx < 128 * (D / 4); idx += 256) {
-        const int kr = idx / (D / 4), c4 = idx % (D / 4);
+#pragma unroll
+    for (int k = 0; k < 128 * D / 16 / 256; ++k) {  // 16-byte piece i: key row i / 8, piece i % 8
+        const int i = threadIdx.x + 256 * k, kr = i >> 3, c = i & 7;
         const int j = j0 + kr;
-        uint32_t w = 0u;
-        const long long src = ((static_cast<long long>(b) * p.L + j) * p.Hkv + g) * D + 4 * c4;
-        if (j < p.L && idx_ok(p.ctl, src + 3, static_cast<long long>(p.B) * p.L * p.Hkv * D, 66))
-            w = *reinterpret_cast<const uint32_t*>(v + src);
-        *reinterpret_cast<uint32_t*>(&tile[kr][4 * c4]) = w;
+        uint4 w = make_uint4(0u, 0u, 0u, 0u);
+        const long long src = ((static_cast<long long>(b) * p.L + j) * p.Hkv + g) * D + 16 * c;
+        if (j < p.L && idx_ok(p.ctl, src + 15, static_cast<long long>(p.B) * p.L * p.Hkv * D, 66))
+            w = *reinterpret_cast<const uint4*>(v + src);
+        tile[kr][4 * c] = w.x;
+        tile[kr][4 * c + 1] = w.y;
+        tile[kr][4 * c + 2] = w.z;
+        tile[kr][4 * c + 3] = w.w;
     }
     __syncthreads();
-    // 4 keys x 4 dims per thread: four 32-bit words of consecutive keys, transposed with byte permutes
-    for (int idx = threadIdx.x; idx < (D / 4) * 32; idx += 256) {
-        const int d4 = idx / 32, k4 = idx % 32;  // dims 4 d4 .. 4 d4 + 3, keys 4 k4 .. 4 k4 + 3
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int blk = warp * 4 + k;                        // 32 blocks of 32 keys x 16 dims
+        const int k4 = (blk & 3) * 8 + (lane >> 2);          // keys 4 k4 .. 4 k4 + 3
+        const int d4 = (blk >> 2) * 4 + (lane & 3);          // dims 4 d4 .. 4 d4 + 3
         const int j = j0 + 4 * k4;
         if (j >= Lp) continue;
         uint32_t w[4];
 #pragma unroll
-        for (int r = 0; r < 4; ++r) w[r] = *reinterpret_cast<const uint32_t*>(&tile[4 * k4 + r][4 * d4]);
+        for (int r = 0; r < 4; ++r) w[r] = tile[4 * k4 + r][d4];
         const uint32_t t0 = __byte_perm(w[0], w[1], 0x5140), t1 = __byte_perm(w[2], w[3], 0x5140);
         const uint32_t t2 = __byte_perm(w[0], w[1], 0x7362), t3 = __byte_perm(w[2], w[3], 0x7362);
         const uint32_t o[4] = {__byte_perm(t0, t1, 0x5410), __byte_perm(t0, t1, 0x7632), __byte_perm(t2, t3, 0x5410),
