@@ -93,6 +93,10 @@ def swa_bytes(c):  # algorithmic HBM bytes: read q, gate, k, v once, write out o
     return c.B * c.L * (3 * c.Hq * c.d * 2 + 2 * c.Hkv * c.d * 2)
 
 
+def swa_fp8_bytes(c):  # the same with E4M3 q, k, v (one byte per element); gate and out stay bf16
+    return c.B * c.L * (c.Hq * c.d * (1 + 2 + 2) + 2 * c.Hkv * c.d)
+
+
 def global_flops(c):  # 2 matmuls x 2 flop x d per unmasked (row, key, head)
     return 4.0 * c.d * c.Hq * c.B * (c.L * (c.L + 1) / 2)
 
@@ -678,7 +682,7 @@ def run_gpu(args):
     s8_t = time_part(lambda: zg.swa_prefill_fp8(s8["q"], s8["k"], s8["v"], sx["gate"], sx["pos"], sx["wq"], sx["wk"],
                                                 window=SWA.window, rotary_dim=SWA.rotary_dim, theta=SWA.theta,
                                                 eps=SWA.eps, out=s8_out, workspace=s8_ws), 10)
-    s8_by = SWA.B * SWA.L * (SWA.Hq * SWA.d * (1 + 2 + 2) + 2 * SWA.Hkv * SWA.d)  # q, k, v E4M3; gate, out bf16
+    s8_by = swa_fp8_bytes(SWA)
     swa_fp8 = {"workload": f"{SWA.name} with E4M3 q, k, v", "ms": s8_t * 1e3, "tokens_per_s": SWA.tokens / s8_t,
                "roofline": {"bound": "hbm", "achieved": s8_by / s8_t / 1e9, "peak": hbm, "unit": "GB/s",
                             "frac": s8_by / s8_t / 1e9 / hbm, "traffic": _traffic("swa_prefill_fp8_call"),

@@ -23,6 +23,31 @@ def test_swa_bytes_are_the_tensors_read_and_written_once():
     assert bench.swa_bytes(c) == q_gate_out + k_v
 
 
+def test_swa_fp8_bytes_count_one_byte_per_qkv_element():
+    c = workloads.SWA_256K
+    q = _numel(c.B, c.L, c.Hq, c.d)            # E4M3: one byte each
+    gate_out = 2 * _numel(c.B, c.L, c.Hq, c.d) * BF16
+    k_v = 2 * _numel(c.B, c.L, c.Hkv, c.d)      # E4M3
+    assert bench.swa_fp8_bytes(c) == q + gate_out + k_v
+    assert bench.swa_fp8_bytes(c) < bench.swa_bytes(c)
+
+
+def test_traffic_is_reported_only_for_the_sources_it_was_measured_on(tmp_path, monkeypatch):
+    """A per-launch DRAM figure from the committed ncu summary counts only while the kernel sources
+    hash to the value recorded beside it; any other hash (sources changed since) gives None."""
+    import json
+    path = tmp_path / "traffic.json"
+    monkeypatch.setattr(bench, "TRAFFIC_PATH", str(path))
+    path.write_text(json.dumps({"kernel_source_hash": bench.kernel_source_hash(),
+                                "per_launch_bytes": {"k": 123, "n": None}}))
+    assert bench._traffic("k") == 123
+    assert bench._traffic("n") is None and bench._traffic("missing") is None
+    path.write_text(json.dumps({"kernel_source_hash": "0" * 16, "per_launch_bytes": {"k": 123}}))
+    assert bench._traffic("k") is None
+    path.unlink()
+    assert bench._traffic("k") is None
+
+
 def test_window_pairs_by_enumeration():
     for L, W in ((1, 128), (100, 128), (300, 128), (4096, 128), (50, 1), (257, 0)):
         c = workloads.PrefillCase("t", 0, 1, L, 4, 1, 128, W, 42, 1e4, True)
