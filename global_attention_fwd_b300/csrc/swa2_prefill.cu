@@ -609,9 +609,13 @@ __global__ void __launch_bounds__(kThreads, 1) swa2_kernel(const __grid_constant
             tmem_ld16(lane_addr + C::O_COL, ra);
             tmem_wait_ld();
             const float lsum = __uint_as_float(lraw);
-            // out = O / l * sigmoid(g), the sigmoid in fp32 (sigmoid2_f32: no cancellation for g < 0)
+            // out = O / l * sigmoid(g) in fp32, as O / (l (1 + 2^(-g log2 e))): one reciprocal per
+            // element for 1/l and the sigmoid together, with no cancellation for g < 0; a row with
+            // l = 0 has O = 0, and l = 1 there keeps the product finite.  PRE: sigmoid(g) is given.
             const float c = lsum > 0.f ? 1.0f / lsum : 0.f;
             const float2 c2 = make_float2(c, c);
+            const float ls = lsum > 0.f ? lsum : 1.f;
+            const float2 l2 = make_float2(ls, ls);
             uint8_t* buf = qbuf0 + qb * C::QBUF;
             auto epi16 = [&](const uint32_t* r, int cb) {
 #pragma unroll
@@ -623,10 +627,15 @@ __global__ void __launch_bounds__(kThreads, 1) swa2_kernel(const __grid_constant
                     uint32_t ou[4];
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
-                        const float2 sg = PRE ? bf2f2(gu[k]) : sigmoid2_f32(bf2f2(gu[k]));
-                        const float2 oc = mul2(
-                            make_float2(__uint_as_float(r[q2 * 8 + 2 * k]), __uint_as_float(r[q2 * 8 + 2 * k + 1])), c2);
-                        const float2 o = mul2(oc, sg);
+                        const float2 rr = make_float2(__uint_as_float(r[q2 * 8 + 2 * k]), __uint_as_float(r[q2 * 8 + 2 * k + 1]));
+                        float2 o;
+                        if constexpr (PRE) {
+                            o = mul2(mul2(rr, c2), bf2f2(gu[k]));
+                        } else {
+                            const float2 t = mul2(bf2f2(gu[k]), make_float2(-kLog2e, -kLog2e));
+                            const float2 d = fma2(make_float2(ex2_approx(t.x), ex2_approx(t.y)), l2, l2);
+                            o = mul2(rr, make_float2(rcp_approx(d.x), rcp_approx(d.y)));
+                        }
                         ou[k] = pack_bf16x2(o.x, o.y);
                     }
                     *reinterpret_cast<uint4*>(gp) = make_uint4(ou[0], ou[1], ou[2], ou[3]);
